@@ -1,0 +1,220 @@
+"""Plain fp64 CPU oracle for jagged (packed, padding-free) softmax attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: it exists so that tests, the smoke check and the timed
+CPU baseline of the benchmark can check the CUDA library against an obviously
+correct definition.  It shares no code, constants or helpers with the CUDA
+path; both sides only read the same seeded inputs.
+
+What is computed (sources, by page title and section):
+
+* "Optimizing Jagged Flash Attention with TLX" (pytorch.org), Introduction:
+  sequences are packed back to back and their boundaries live in an offsets
+  tensor; attention runs over the packed tensors without padded tokens.
+* Same page, section 1 ("The Challenge"): in broadcast-Q mode one dense Q is
+  shared by every sequence and dQ is summed over the whole batch.
+* "cuTile Kernels - FMHA Implementation" (build.nvidia.com), "Attention
+  Basics": Attention(Q, K, V) = softmax(Q K^T * scale) V, with causal masking
+  setting future scores to -inf before the softmax.
+* Same page, "Flash Attention Algorithm": the tiled online softmax reaches
+  exactly this result (up to rounding order), so the oracle is the plain
+  definition written out, one (sequence, head) at a time, with no tiling.
+* "Optimizing Jagged Flash Attention with TLX", "2-CTA collaborative MMA":
+  the backward needs dQ, dK and dV (five products per K/V block).  The pages
+  do not print the backward formulas; the oracle uses the gradient of the
+  definition above, which is what those five products compute:
+      dV = P^T dO,  dP = dO V^T,  Delta_i = sum_j P_ij dP_ij,
+      dS = P * (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
+
+Readings where the pages are silent (each listed in the design notes):
+
+* Layouts: self-attention q, k, v, out are [T, H, D] with T = offsets[B];
+  lse is [H, T].  Broadcast-Q: q and dq are [Lq, H, D], k, v, dk, dv are
+  [T, H, D], out and dout are [B, Lq, H, D], lse is [B, H, Lq].
+* LSE is the natural-log log-sum-exp of the scaled scores of each query row.
+* Causal (self-attention only) keeps key j for query i iff j <= i, both
+  counted from the start of their sequence.
+* A sequence of length 0 contributes no rows in self-attention; in broadcast
+  mode it yields O = 0, LSE = -inf and no dQ contribution.
+
+Parity pins (tests/test_oracle_pins.py): closed forms (length 1, constant V,
+a hand-derived two-key example in tests/golden), row-stochasticity, LSE by a
+direct sum, padded-dense equality against torch's float64 SDPA on CPU (a
+library special case), float64 autograd of that library route, central finite
+differences of the gradients, broadcast = stacked per-sequence attention, and
+permutation invariants.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ROW_CHUNK = 1024  # query rows per dense score block, so 8192-long rows fit
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _seq_bounds(offsets):
+    off = np.asarray(offsets, dtype=np.int64)
+    if off.ndim != 1 or off.size < 1 or off[0] != 0 or np.any(np.diff(off) < 0):
+        raise ValueError("offsets must be 1-D, start at 0 and be non-decreasing")
+    return off
+
+
+def _scores(qc, kb, scale, causal, row0):
+    """Scaled scores of query rows [row0, row0+len(qc)) against all keys.
+
+    Causal masking follows "cuTile Kernels - FMHA Implementation",
+    "Attention Basics": future keys (j > i) get -inf before the softmax.
+    """
+    s = scale * (qc @ kb.T)
+    if causal:
+        i = np.arange(row0, row0 + qc.shape[0])[:, None]
+        j = np.arange(kb.shape[0])[None, :]
+        s = np.where(j > i, -np.inf, s)
+    return s
+
+
+def _lse_rows(s):
+    """Natural log-sum-exp per row; -inf for a row with no admissible key."""
+    m = np.max(s, axis=1)
+    finite = np.isfinite(m)
+    m0 = np.where(finite, m, 0.0)
+    with np.errstate(divide="ignore"):
+        lse = m0 + np.log(np.sum(np.exp(s - m0[:, None]), axis=1))
+    return np.where(finite, lse, -np.inf)
+
+
+def _probs(s, lse):
+    out = np.zeros_like(s)
+    ok = np.isfinite(lse)
+    out[ok] = np.exp(s[ok] - lse[ok, None])
+    return out
+
+
+def _grad_scores(p, dp):
+    """dS = P * (dP - Delta) with Delta_i = sum_j P_ij dP_ij: the gradient of
+    sum(O * dO) with respect to the scaled scores, row by row."""
+    delta = np.sum(p * dp, axis=1)
+    return p * (dp - delta[:, None])
+
+
+def _pairs(B, H, seqs, heads):
+    bs = range(B) if seqs is None else seqs
+    hs = range(H) if heads is None else heads
+    return [(b, h) for b in bs for h in hs]
+
+
+def forward(q, k, v, offsets, scale, causal=False, broadcast_q=False,
+            seqs=None, heads=None):
+    """Attention forward over packed sequences.
+
+    Returns (out, lse) in the layouts given in the module docstring.  With
+    `seqs` / `heads` only those (sequence, head) pairs are computed; the other
+    entries are NaN (used to sample outputs of large workloads).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    off = _seq_bounds(offsets)
+    B = off.size - 1
+    T, H, D = k.shape
+    if v.shape != k.shape or off[-1] != T:
+        raise ValueError("k, v must be [T, H, D] with T = offsets[B]")
+    if broadcast_q and causal:
+        raise ValueError("causal masking is defined for self-attention only")
+    if broadcast_q:
+        Lq = q.shape[0]
+        out = np.full((B, Lq, H, D), np.nan)
+        lse = np.full((B, H, Lq), np.nan)
+    else:
+        if q.shape != k.shape:
+            raise ValueError("self-attention q must be [T, H, D]")
+        out = np.full((T, H, D), np.nan)
+        lse = np.full((H, T), np.nan)
+    for b, h in _pairs(B, H, seqs, heads):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        kb, vb = k[s0:s1, h, :], v[s0:s1, h, :]
+        qb = q[:, h, :] if broadcast_q else q[s0:s1, h, :]
+        nq = qb.shape[0]
+        ob = np.zeros((nq, D))
+        lb = np.full(nq, -np.inf)
+        if s1 > s0:
+            for r0 in range(0, nq, ROW_CHUNK):
+                r1 = min(nq, r0 + ROW_CHUNK)
+                s = _scores(qb[r0:r1], kb, scale, causal, r0)
+                l = _lse_rows(s)
+                ob[r0:r1] = _probs(s, l) @ vb
+                lb[r0:r1] = l
+        if broadcast_q:
+            out[b, :, h, :] = ob
+            lse[b, h, :] = lb
+        else:
+            out[s0:s1, h, :] = ob
+            lse[h, s0:s1] = lb
+    return out, lse
+
+
+def backward(q, k, v, offsets, dout, scale, causal=False, broadcast_q=False,
+             seqs=None, heads=None):
+    """Gradients (dq, dk, dv) of sum(out * dout) for the forward above.
+
+    In broadcast-Q mode dq is the sum over all sequences of the per-sequence
+    dQ_b, as the TLX JFA page (section 1) describes; sampling with `seqs`
+    then sums only the sampled sequences.  Entries of unsampled pairs are NaN
+    in dk / dv (and in dq for self-attention).
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    off = _seq_bounds(offsets)
+    B = off.size - 1
+    T, H, D = k.shape
+    if broadcast_q and causal:
+        raise ValueError("causal masking is defined for self-attention only")
+    dk = np.full((T, H, D), np.nan)
+    dv = np.full((T, H, D), np.nan)
+    if broadcast_q:
+        dq = np.zeros_like(q)
+        if heads is not None:
+            dq[:] = np.nan
+            for h in heads:
+                dq[:, h, :] = 0.0
+    else:
+        dq = np.full((T, H, D), np.nan)
+    for b, h in _pairs(B, H, seqs, heads):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        kb, vb = k[s0:s1, h, :], v[s0:s1, h, :]
+        if broadcast_q:
+            qb, dob = q[:, h, :], dout[b, :, h, :]
+        else:
+            qb, dob = q[s0:s1, h, :], dout[s0:s1, h, :]
+        nq = qb.shape[0]
+        dqb = np.zeros((nq, D))
+        dkb = np.zeros((s1 - s0, D))
+        dvb = np.zeros((s1 - s0, D))
+        if s1 > s0:
+            for r0 in range(0, nq, ROW_CHUNK):
+                r1 = min(nq, r0 + ROW_CHUNK)
+                s = _scores(qb[r0:r1], kb, scale, causal, r0)
+                p = _probs(s, _lse_rows(s))
+                dp = dob[r0:r1] @ vb.T
+                ds = _grad_scores(p, dp)
+                dqb[r0:r1] = scale * (ds @ kb)
+                dkb += scale * (ds.T @ qb[r0:r1])
+                dvb += p.T @ dob[r0:r1]
+        if broadcast_q:
+            dq[:, h, :] += dqb
+        else:
+            dq[s0:s1, h, :] = dqb
+        dk[s0:s1, h, :] = dkb
+        dv[s0:s1, h, :] = dvb
+    return dq, dk, dv
+
+
+def delta_rowsum(out, dout, broadcast_q=False):
+    """Delta = rowsum(dO * O), the backward pre-pass quantity, in fp64.
+
+    For the exact O of the forward this equals sum_j P_ij dP_ij (used by
+    `backward`); layout is that of lse ([H, T], or [B, H, Lq] in broadcast).
+    """
+    o, do = _as64(out), _as64(dout)
+    d = np.sum(o * do, axis=-1)
+    return np.moveaxis(d, -1, -2) if broadcast_q else d.T.copy()
