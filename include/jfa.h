@@ -1,0 +1,116 @@
+/*
+ * jfa.h - C ABI of the GB300 (sm_103a) jagged flash attention library.
+ *
+ * Exact softmax attention, forward and backward, over packed, padding-free
+ * bf16 Q/K/V whose sequence boundaries are given by an int32 offsets array
+ * ("Optimizing Jagged Flash Attention with TLX", pytorch.org, Introduction:
+ * sequences are packed contiguously and their boundaries recorded in an
+ * offsets tensor; the attention never materialises padded tokens).  The
+ * broadcast-Q mode, where one dense Q is shared by every sequence and dQ is
+ * summed over the batch, follows section 1 of the same page ("The
+ * Challenge", broadcast_q=True).  The per-row math is the softmax attention
+ * of "cuTile Kernels - FMHA Implementation" (build.nvidia.com), "Attention
+ * Basics" and "Flash Attention Algorithm".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers on the current CUDA device, row
+ *   major and contiguous, 16-byte aligned.  q, k, v, out, dout, dq, dk, dv
+ *   hold bf16 (IEEE bfloat16); lse holds fp32; offsets holds int32.
+ * - offsets: device int32[B+1], offsets[0] = 0, non-decreasing; sequence b
+ *   owns packed rows [offsets[b], offsets[b+1]) of k and v (and of q in
+ *   self-attention).  T = offsets[B].  Every length must be <= max_len.
+ *   The host never reads offsets; a violation found on the device sets the
+ *   device error word (see jfa_sync_and_check) and no output is written.
+ * - Self-attention layouts: q, k, v, out, dout, dq, dk, dv are [T, H, D];
+ *   lse is [H, T].
+ * - Broadcast-Q layouts: q and dq are [q_len, H, D]; k, v, dk, dv are
+ *   [T, H, D]; out and dout are [B, q_len, H, D]; lse is [B, H, q_len].
+ * - lse is the natural-log log-sum-exp of the scaled scores of each query
+ *   row.  A broadcast sequence of length 0 gives out = 0 and lse = -inf and
+ *   adds nothing to dq.
+ * - causal (self-attention only): query i attends to key j iff j <= i, both
+ *   counted from the start of their own sequence.
+ * - scale: positive finite softmax scale (normally 1/sqrt(D)).
+ * - D must be 64 or 128.
+ * - Inputs must be finite.  Rows of neighbouring sequences are read into a
+ *   tile's padding and then multiplied by an exact zero, so a non-finite
+ *   value in one sequence can leak into its neighbours.
+ * - Ownership: the caller owns every buffer.  The library keeps no pointer
+ *   after the call returns.  Scratch memory is taken stream-ordered from a
+ *   library-owned CUDA memory pool (cudaMallocAsync / cudaFreeAsync on
+ *   `stream`), so calls are asynchronous and capturable in a CUDA graph.
+ * - Errors: a non-OK status means nothing was enqueued; jfa_last_error()
+ *   gives the reason (thread-local).  Errors found by the device (bad
+ *   offsets, a bounded wait that ran out) are reported by
+ *   jfa_sync_and_check().  With the environment variable JFA_VALIDATE=1
+ *   every call synchronises and checks before returning.
+ * - Thread safety: calls on different streams may run concurrently.
+ */
+#ifndef JFA_H_
+#define JFA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or offsets */
+  JFA_ERR_UNSUPPORTED = 2, /* D not in {64,128}; causal with broadcast_q */
+  JFA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  JFA_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out */
+  JFA_ERR_WORKSPACE = 5    /* scratch allocation failed */
+} jfa_status;
+
+/* Forward pass, self-attention (broadcast_q must be 0; use jfa_fwd_bq for
+ * broadcast-Q, which needs the dense Q length).  Writes out and lse.
+ * Follows "Optimizing Jagged Flash Attention with TLX", section 2.1
+ * (persistent, warp-specialised forward) and "cuTile Kernels - FMHA
+ * Implementation", "Flash Attention Algorithm" (online softmax). */
+jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                   int H, int D, int max_len, int broadcast_q, int causal, float scale, void* out,
+                   float* lse, cudaStream_t stream);
+
+/* Backward pass, self-attention: given out, lse from jfa_fwd and dout,
+ * writes dq, dk, dv (gradients of sum(out * dout)).  Five products per K/V
+ * block, as in "Optimizing Jagged Flash Attention with TLX", section
+ * "2-CTA collaborative MMA", with the Delta = rowsum(dout * out) pre-pass
+ * and an fp32 dq accumulator ("Multi-stage dQ staging"). */
+jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                   int H, int D, int max_len, int broadcast_q, int causal, float scale,
+                   const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                   void* dv, cudaStream_t stream);
+
+/* Same as jfa_fwd / jfa_bwd with the dense Q length `q_len` (>= 1) added.
+ * Required when broadcast_q = 1 (q_len is then the row count of q); with
+ * broadcast_q = 0 q_len is ignored.  Broadcast-Q: section 1 of "Optimizing
+ * Jagged Flash Attention with TLX"; dq is summed over all B sequences. */
+jfa_status jfa_fwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      float scale, void* out, float* lse, cudaStream_t stream);
+jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      float scale, const void* out, const float* lse, const void* dout, void* dq,
+                      void* dk, void* dv, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device.  Returns JFA_ERR_INVALID_ARG for offsets found invalid on
+ * the device, JFA_ERR_TIMEOUT for a bounded wait that ran out,
+ * JFA_ERR_CUDA if the stream reported an error, JFA_OK otherwise. */
+jfa_status jfa_sync_and_check(cudaStream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* jfa_last_error(void);
+
+/* Library version string. */
+const char* jfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H_ */

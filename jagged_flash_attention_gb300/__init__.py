@@ -1,0 +1,151 @@
+"""GB300 (sm_103a) jagged flash attention: a thin Python binding of libjfa.so.
+
+The binding only marshals arguments (pointers, sizes, the current CUDA
+stream) into the C ABI of include/jfa.h; every step of the computation runs
+in the library's CUDA kernels.  PyTorch supplies device memory and streams.
+There is no fallback: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .build import LIB_PATH
+
+__all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq",
+           "jfa_sync_and_check", "forward", "backward", "STATUS"]
+
+STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_CUDA",
+          4: "JFA_ERR_TIMEOUT", 5: "JFA_ERR_WORKSPACE"}
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+class JfaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libjfa.so (built by jagged_flash_attention_gb300.build)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run jagged_flash_attention_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        fwd = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]
+        bwd = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]
+        L.jfa_fwd.argtypes = fwd
+        L.jfa_bwd.argtypes = bwd
+        L.jfa_fwd_bq.argtypes = fwd[:8] + [_I] + fwd[8:]
+        L.jfa_bwd_bq.argtypes = bwd[:8] + [_I] + bwd[8:]
+        for f in (L.jfa_fwd, L.jfa_bwd, L.jfa_fwd_bq, L.jfa_bwd_bq):
+            f.restype = _I
+        L.jfa_sync_and_check.argtypes = [_P]
+        L.jfa_sync_and_check.restype = _I
+        L.jfa_last_error.restype = ctypes.c_char_p
+        L.jfa_version.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != 0:
+        raise JfaError(status, lib().jfa_last_error().decode())
+
+
+def jfa_fwd(q, k, v, offsets, B, H, D, max_len, broadcast_q, causal, scale, out, lse, stream=None):
+    _check(lib().jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, D, max_len,
+                         int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse),
+                         _stream(stream)))
+
+
+def jfa_bwd(q, k, v, offsets, B, H, D, max_len, broadcast_q, causal, scale, out, lse, dout,
+            dq, dk, dv, stream=None):
+    _check(lib().jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, D, max_len,
+                         int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse),
+                         _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
+
+
+def jfa_fwd_bq(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale, out, lse,
+               stream=None):
+    _check(lib().jfa_fwd_bq(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, D, max_len, q_len,
+                            int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse),
+                            _stream(stream)))
+
+
+def jfa_bwd_bq(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale, out, lse,
+               dout, dq, dk, dv, stream=None):
+    _check(lib().jfa_bwd_bq(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, D, max_len, q_len,
+                            int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse),
+                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
+
+
+def jfa_sync_and_check(stream=None):
+    _check(lib().jfa_sync_and_check(_stream(stream)))
+
+
+def _shapes(q, k, offsets, broadcast_q):
+    T, H, D = k.shape
+    B = offsets.numel() - 1
+    return B, H, D, (q.shape[0] if broadcast_q else 0)
+
+
+def forward(q, k, v, offsets, max_len, causal=False, broadcast_q=False, scale=None, out=None,
+            lse=None, stream=None):
+    """Allocate out / lse with torch and call the C ABI.  Tensors are CUDA
+    tensors in the layouts of include/jfa.h; offsets is int32 [B+1]."""
+    import torch
+    B, H, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if out is None:
+        out = torch.empty((B, Lq, H, D) if broadcast_q else tuple(q.shape), dtype=q.dtype,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Lq) if broadcast_q else (H, k.shape[0]), dtype=torch.float32,
+                          device=q.device)
+    if broadcast_q:
+        jfa_fwd_bq(q, k, v, offsets, B, H, D, max_len, Lq, 1, causal, scale, out, lse, stream)
+    else:
+        jfa_fwd(q, k, v, offsets, B, H, D, max_len, 0, causal, scale, out, lse, stream)
+    return out, lse
+
+
+def backward(q, k, v, offsets, max_len, out, lse, dout, causal=False, broadcast_q=False,
+             scale=None, dq=None, dk=None, dv=None, stream=None):
+    """Allocate dq / dk / dv with torch and call the C ABI."""
+    import torch
+    B, H, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if broadcast_q:
+        jfa_bwd_bq(q, k, v, offsets, B, H, D, max_len, Lq, 1, causal, scale, out, lse, dout,
+                   dq, dk, dv, stream)
+    else:
+        jfa_bwd(q, k, v, offsets, B, H, D, max_len, 0, causal, scale, out, lse, dout, dq, dk, dv,
+                stream)
+    return dq, dk, dv

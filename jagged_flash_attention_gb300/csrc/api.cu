@@ -1,0 +1,434 @@
+// Host side of the C ABI declared in include/jfa.h: argument validation,
+// stream-ordered scratch memory, TMA tensor-map encoding and the launch
+// sequence of the forward and backward passes.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "jfa.h"
+
+namespace jfa {
+// Device error word, OR-ed by the kernels (bits in ptx.cuh).
+__device__ int g_device_error;
+}  // namespace jfa
+
+namespace {
+
+using namespace jfa;
+
+thread_local std::string t_last_error;
+
+jfa_status fail(jfa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  cudaMemPool_t pool = nullptr;
+  int* err = nullptr;  // device address of g_device_error
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool validate_mode() {
+  static const bool v = [] {
+    const char* e = std::getenv("JFA_VALIDATE");
+    return e && e[0] == '1';
+  }();
+  return v;
+}
+
+jfa_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(JFA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(JFA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess)
+      return fail(JFA_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+    s.sms = prop.multiProcessorCount;
+    s.cc_major = prop.major;
+    s.cc_minor = prop.minor;
+    if (!(prop.major == 10 && prop.minor == 3))
+      return fail(JFA_ERR_UNSUPPORTED, "device %s is sm_%d%d; this library is built for sm_103a",
+                  prop.name, prop.major, prop.minor);
+    cudaMemPoolProps pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.allocType = cudaMemAllocationTypePinned;
+    pp.location.type = cudaMemLocationTypeDevice;
+    pp.location.id = dev;
+    e = cudaMemPoolCreate(&s.pool, &pp);
+    if (e != cudaSuccess) return fail(JFA_ERR_CUDA, "cudaMemPoolCreate: %s", cudaGetErrorString(e));
+    uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool between calls
+    cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_device_error);
+    if (e != cudaSuccess)
+      return fail(JFA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess)
+        return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return JFA_OK;
+}
+
+// [rows, H, D] bf16 tensor viewed as a 3-D map (D, H, rows), box 64 x 1 x 128,
+// 128-byte swizzle: one TMA copy fills one 16 KB swizzle-atom slab.
+jfa_status map_rows(CUtensorMap* m, const void* ptr, int D, int H, long long rows, const char* nm) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(JFA_ERR_CUDA, "tensor map for %s failed (%d)", nm, (int)r);
+  return JFA_OK;
+}
+
+// [B, Lq, H, D] bf16 tensor as a 4-D map (D, H, Lq, B), box 64 x 1 x 128 x 1.
+jfa_status map_bq(CUtensorMap* m, const void* ptr, int D, int H, int Lq, int B, const char* nm) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Lq, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)Lq * H * D * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(JFA_ERR_CUDA, "tensor map for %s failed (%d)", nm, (int)r);
+  return JFA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long cdivll(long long a, long long b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Shape {
+  int B, H, D, max_len, Lq, broadcast, causal;
+  float scale;
+  long long Tcap;  // upper bound of T used to size scratch and tensor maps
+};
+
+jfa_status check_common(const Shape& s, const void* q, const void* k, const void* v,
+                        const int32_t* offsets) {
+  if (s.B < 1) return fail(JFA_ERR_INVALID_ARG, "B must be >= 1 (got %d)", s.B);
+  if (s.H < 1 || s.H > 65535) return fail(JFA_ERR_INVALID_ARG, "H must be in [1, 65535] (got %d)", s.H);
+  if (s.D != 64 && s.D != 128) return fail(JFA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", s.D);
+  if (s.max_len < 0) return fail(JFA_ERR_INVALID_ARG, "max_len must be >= 0");
+  if (cdivll(s.max_len, kBN) > 65535 || cdivll(s.Lq, kBM) > 65535)
+    return fail(JFA_ERR_INVALID_ARG, "sequence length too large");
+  if ((long long)s.B * s.max_len >= (1LL << 31))
+    return fail(JFA_ERR_INVALID_ARG, "B * max_len must be < 2^31");
+  if (!std::isfinite(s.scale) || !(s.scale > 0.f))
+    return fail(JFA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (s.broadcast && s.causal)
+    return fail(JFA_ERR_UNSUPPORTED, "causal masking is supported for self-attention only");
+  if (s.broadcast && s.Lq < 1) return fail(JFA_ERR_INVALID_ARG, "q_len must be >= 1 in broadcast mode");
+  if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "offsets must be a non-null, 4-byte aligned device pointer");
+  if (!q || !k || !v) return fail(JFA_ERR_INVALID_ARG, "q, k, v must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(JFA_ERR_INVALID_ARG, "q, k, v must be 16-byte aligned");
+  return JFA_OK;
+}
+
+jfa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(JFA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+jfa_status finish(DeviceState* ds, cudaStream_t stream) {
+  if (!validate_mode()) return JFA_OK;
+  (void)ds;
+  return jfa_sync_and_check(stream);
+}
+
+jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
+                  const int32_t* offsets, void* out, float* lse, cudaStream_t stream) {
+  jfa_status st = check_common(s, q, k, v, offsets);
+  if (st != JFA_OK) return st;
+  if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "lse must be non-null, 4-byte aligned");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != JFA_OK) return st;
+  cudaError_t e;
+  if (s.max_len == 0) {  // every sequence is empty
+    if (s.broadcast) {
+      e = launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H, s.D,
+                            stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+    }
+    return finish(ds, stream);
+  }
+  const long long qt = s.broadcast ? cdivll(s.Lq, kBM) : cdivll(s.max_len, kBM);
+  const long long cap = (long long)s.H * s.B * qt;
+  if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  const size_t items_off = 256;
+  const size_t bytes = align256(items_off + cap * sizeof(Item));
+  CUtensorMap tq, tk, tv;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  void* scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
+  Item* items = reinterpret_cast<Item*>(base + items_off);
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0,
+                 items, (int)cap, hdr, ds->err};
+  e = launch_sched(sp, stream);
+  if (e == cudaSuccess) {
+    FwdParams fp;
+    fp.offsets = offsets;
+    fp.B = s.B;
+    fp.H = s.H;
+    fp.Lq = s.Lq;
+    fp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.lse = lse;
+    fp.items = items;
+    fp.hdr = hdr;
+    fp.err = ds->err;
+    const int grid = (int)std::min<long long>(ds->sms, cap);
+    e = launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+  }
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(ds, stream);
+}
+
+jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
+                  const int32_t* offsets, const void* out, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, cudaStream_t stream) {
+  jfa_status st = check_common(s, q, k, v, offsets);
+  if (st != JFA_OK) return st;
+  if (!out || !dout || !dq || !dk || !dv)
+    return fail(JFA_ERR_INVALID_ARG, "out, dout, dq, dk, dv must be non-null");
+  if (!aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(JFA_ERR_INVALID_ARG, "out, dout, dq, dk, dv must be 16-byte aligned");
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "lse must be non-null, 4-byte aligned");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != JFA_OK) return st;
+  cudaError_t e;
+  if (s.max_len == 0) {
+    if (s.broadcast) {  // no keys anywhere: dq = 0
+      e = launch_fill_empty(static_cast<__nv_bfloat16*>(dq), nullptr, (long long)s.Lq * s.H, s.D,
+                            stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+    }
+    return finish(ds, stream);
+  }
+  const long long cap = (long long)s.H * s.B * cdivll(s.max_len, kBN);
+  if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  const int grid = (int)std::min<long long>(ds->sms, cap);
+  const int shards = s.broadcast ? std::min(16, grid) : 1;
+  const long long shard_elems = (long long)s.Lq * s.H * s.D;
+  const long long delta_elems = s.broadcast ? (long long)s.B * s.H * s.Lq : (long long)s.H * s.Tcap;
+  const long long acc_elems =
+      s.broadcast ? shards * shard_elems : s.Tcap * (long long)s.H * s.D;
+  size_t off = 256;
+  const size_t items_off = off;
+  off = align256(off + cap * sizeof(Item));
+  const size_t delta_off = off;
+  off = align256(off + delta_elems * sizeof(float));
+  const size_t acc_off = off;
+  off = align256(off + acc_elems * sizeof(float));
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if (s.broadcast)
+    st = map_bq(&tdo, dout, s.D, s.H, s.Lq, s.B, "dout");
+  else
+    st = map_rows(&tdo, dout, s.D, s.H, s.Tcap, "dout");
+  if (st != JFA_OK) return st;
+  void* scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
+  Item* items = reinterpret_cast<Item*>(base + items_off);
+  float* delta = reinterpret_cast<float*>(base + delta_off);
+  float* acc = reinterpret_cast<float*>(base + acc_off);
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1,
+                 items, (int)cap, hdr, ds->err};
+  e = launch_sched(sp, stream);
+  if (e == cudaSuccess) {
+    PrepParams pp;
+    pp.out = static_cast<const __nv_bfloat16*>(out);
+    pp.dout = static_cast<const __nv_bfloat16*>(dout);
+    pp.delta = delta;
+    pp.dq_acc = acc;
+    pp.dq_acc_elems_bcast = s.broadcast ? acc_elems : 0;
+    pp.B = s.B;
+    pp.H = s.H;
+    pp.D = s.D;
+    pp.Lq = s.Lq;
+    pp.broadcast = s.broadcast;
+    pp.hdr = hdr;
+    e = launch_prep(pp, ds->sms, stream);
+  }
+  if (e == cudaSuccess) {
+    BwdParams bp;
+    bp.offsets = offsets;
+    bp.B = s.B;
+    bp.H = s.H;
+    bp.Lq = s.Lq;
+    bp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+    bp.scale = s.scale;
+    bp.lse = lse;
+    bp.delta = delta;
+    bp.dq_acc = acc;
+    bp.dq_shards = shards;
+    bp.shard_stride = shard_elems;
+    bp.dk = static_cast<__nv_bfloat16*>(dk);
+    bp.dv = static_cast<__nv_bfloat16*>(dv);
+    bp.items = items;
+    bp.hdr = hdr;
+    bp.err = ds->err;
+    e = launch_bwd(s.D, s.causal, s.broadcast, tq, tk, tv, tdo, bp, grid, stream);
+  }
+  if (e == cudaSuccess) {
+    FinParams fp;
+    fp.dq_acc = acc;
+    fp.dq = static_cast<__nv_bfloat16*>(dq);
+    fp.scale = s.scale;
+    fp.H = s.H;
+    fp.D = s.D;
+    fp.Lq = s.Lq;
+    fp.broadcast = s.broadcast;
+    fp.shards = shards;
+    fp.shard_stride = shard_elems;
+    fp.hdr = hdr;
+    e = launch_finalize(fp, ds->sms, stream);
+  }
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(ds, stream);
+}
+
+Shape make_shape(int B, int H, int D, int max_len, int q_len, int broadcast_q, int causal,
+                 float scale) {
+  Shape s;
+  s.B = B;
+  s.H = H;
+  s.D = D;
+  s.max_len = max_len;
+  s.Lq = broadcast_q ? q_len : 0;
+  s.broadcast = broadcast_q ? 1 : 0;
+  s.causal = causal ? 1 : 0;
+  s.scale = scale;
+  s.Tcap = (long long)(B > 0 ? B : 0) * (max_len > 0 ? max_len : 0);
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                   int H, int D, int max_len, int broadcast_q, int causal, float scale, void* out,
+                   float* lse, cudaStream_t stream) {
+  if (broadcast_q)
+    return fail(JFA_ERR_INVALID_ARG,
+                "broadcast_q=1 needs the dense Q length: call jfa_fwd_bq with q_len");
+  t_last_error.clear();
+  return do_fwd(make_shape(B, H, D, max_len, 0, 0, causal, scale), q, k, v, offsets, out, lse,
+                stream);
+}
+
+jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                   int H, int D, int max_len, int broadcast_q, int causal, float scale,
+                   const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                   void* dv, cudaStream_t stream) {
+  if (broadcast_q)
+    return fail(JFA_ERR_INVALID_ARG,
+                "broadcast_q=1 needs the dense Q length: call jfa_bwd_bq with q_len");
+  t_last_error.clear();
+  return do_bwd(make_shape(B, H, D, max_len, 0, 0, causal, scale), q, k, v, offsets, out, lse,
+                dout, dq, dk, dv, stream);
+}
+
+jfa_status jfa_fwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      float scale, void* out, float* lse, cudaStream_t stream) {
+  t_last_error.clear();
+  return do_fwd(make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale), q, k, v, offsets,
+                out, lse, stream);
+}
+
+jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      float scale, const void* out, const float* lse, const void* dout, void* dq,
+                      void* dk, void* dv, cudaStream_t stream) {
+  t_last_error.clear();
+  return do_bwd(make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale), q, k, v, offsets,
+                out, lse, dout, dq, dk, dv, stream);
+}
+
+jfa_status jfa_sync_and_check(cudaStream_t stream) {
+  DeviceState* ds = nullptr;
+  jfa_status st = device_state(&ds);
+  if (st != JFA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (word & kErrTimeout)
+      return fail(JFA_ERR_TIMEOUT, "a device-side bounded wait ran out (error bits 0x%x)", word);
+    if (word & kErrBadOffsets)
+      return fail(JFA_ERR_INVALID_ARG,
+                  "offsets failed device checks: offsets[0] != 0, decreasing, or a length above "
+                  "max_len (error bits 0x%x)",
+                  word);
+    return fail(JFA_ERR_CUDA, "device error bits 0x%x", word);
+  }
+  return JFA_OK;
+}
+
+const char* jfa_last_error(void) { return t_last_error.c_str(); }
+
+const char* jfa_version(void) { return "jfa-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

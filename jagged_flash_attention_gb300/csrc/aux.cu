@@ -1,0 +1,236 @@
+// Device work-list scheduler, backward pre-pass (Delta = rowsum(dO * O) and
+// zeroing of the fp32 dQ accumulator), dQ finalisation, and a fill kernel
+// for the all-empty broadcast case.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace jfa {
+
+namespace {
+
+constexpr int kSchedThreads = 1024;
+constexpr int kMaxBuckets = 1024;
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Tiles of sequence b that become work items (one item per head and tile).
+//  forward:  query tiles (self: of the sequence; broadcast: of the dense Q)
+//  backward: key/value blocks of the sequence
+__device__ __forceinline__ int n_tiles(const SchedParams& p, int L) {
+  if (p.backward) return cdiv(L, kBN);
+  // broadcast: every sequence, even an empty one, owns its output rows
+  return p.broadcast ? cdiv(p.Lq, kBM) : cdiv(L, kBM);
+}
+
+// Cost bucket of sequence b: work of its longest item, in tile units.
+//  forward:  key tiles a query tile visits (causal: the last query tile's)
+//  backward: query tiles a key block visits (broadcast: all equal)
+__device__ __forceinline__ int bucket_of(const SchedParams& p, int L) {
+  int c = p.backward ? (p.broadcast ? 0 : cdiv(L, kBM)) : cdiv(L, kBN);
+  return c < kMaxBuckets ? c : kMaxBuckets - 1;
+}
+
+// Block-wide exclusive scan over the buckets in DESCENDING bucket order:
+// base[k] = sum of hist[k'] for k' > k.
+__device__ void scan_desc(const int* hist, int* base, int* warp_tot) {
+  const int tid = threadIdx.x;
+  const int k = kMaxBuckets - 1 - tid;  // thread tid handles bucket k
+  int v = hist[k];
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if ((tid & 31) >= o) x += y;
+  }
+  if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
+  __syncthreads();
+  if (tid < 32) {
+    int w = warp_tot[tid];
+    int z = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (tid >= o) z += y;
+    }
+    warp_tot[tid] = z - w;  // exclusive warp prefix
+  }
+  __syncthreads();
+  base[k] = warp_tot[tid >> 5] + x - v;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) {
+  __shared__ int hist[kMaxBuckets];
+  __shared__ int base[kMaxBuckets];
+  __shared__ int cursor[kMaxBuckets];
+  __shared__ int warp_tot[32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kMaxBuckets; i += blockDim.x) hist[i] = 0, cursor[i] = 0;
+  if (tid == 0) s_bad = (p.offsets[0] != 0);
+  __syncthreads();
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int L = p.offsets[b + 1] - p.offsets[b];
+    if (L < 0 || L > p.max_len) {
+      s_bad = 1;
+      continue;
+    }
+    const int nt = n_tiles(p, L);
+    if (nt > 0) atomicAdd(&hist[bucket_of(p, L)], p.H * nt);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      p.hdr->n_items = 0;
+      p.hdr->T = 0;
+      p.hdr->ticket = 0;
+      p.hdr->valid = 0;
+      atomicOr(p.err, kErrBadOffsets);
+    }
+    return;
+  }
+  scan_desc(hist, base, warp_tot);
+  __syncthreads();
+  const int total = base[0] + hist[0];
+  if (total > p.capacity) {
+    if (tid == 0) {
+      p.hdr->n_items = 0;
+      p.hdr->T = 0;
+      p.hdr->ticket = 0;
+      p.hdr->valid = 0;
+      atomicOr(p.err, kErrCapacity);
+    }
+    return;
+  }
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int L = p.offsets[b + 1] - p.offsets[b];
+    const int nt = n_tiles(p, L);
+    if (nt == 0) continue;
+    const int key = bucket_of(p, L);
+    int pos = base[key] + atomicAdd(&cursor[key], p.H * nt);
+    // Heads outer, tiles inner, so that consecutive items share K/V (or Q)
+    // in L2.  Forward causal: longest query tile first.
+    const bool reverse = !p.backward && p.causal;
+    for (int h = 0; h < p.H; ++h)
+      for (int t = 0; t < nt; ++t) {
+        const int tt = reverse ? nt - 1 - t : t;
+        p.items[pos++] = make_int2(b, (h << 16) | tt);
+      }
+  }
+  if (tid == 0) {
+    p.hdr->n_items = total;
+    p.hdr->T = p.offsets[p.B];
+    p.hdr->ticket = 0;
+    p.hdr->valid = 1;
+  }
+}
+
+// Delta[row] = sum_d dO[row, d] * O[row, d] in fp32; 16 threads per row of
+// D=128 (8 for D=64), each reading 16 bytes of both tensors.
+__global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
+  const int T = p.hdr->T;
+  const bool ok = p.hdr->valid != 0;
+  const int tpr = p.D / 8;  // threads per row
+  const long long rows = p.broadcast ? (long long)p.B * p.Lq * p.H : (long long)T * p.H;
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  if (ok) {
+    // Warp-uniform loop: each warp owns 32/tpr consecutive rows per step.
+    const int lane = threadIdx.x & 31;
+    const int rows_per_warp = 32 / tpr;
+    const long long wid = gtid >> 5, nwarps = nthreads >> 5;
+    for (long long r0 = wid * rows_per_warp; r0 < rows; r0 += nwarps * rows_per_warp) {
+      const long long row = r0 + lane / tpr;
+      const int part = lane % tpr;
+      const bool valid = row < rows;
+      float acc = 0.f;
+      if (valid) {
+        const uint4 o = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
+        const uint4 g = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 a = __bfloat1622float2(o2[i]);
+          const float2 c = __bfloat1622float2(g2[i]);
+          acc = fmaf(a.x, c.x, acc);
+          acc = fmaf(a.y, c.y, acc);
+        }
+      }
+      for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (valid && part == 0) {
+        long long di;
+        if (p.broadcast) {
+          const long long h = row % p.H;
+          const long long bi = row / p.H;  // b * Lq + i
+          const long long b = bi / p.Lq, i = bi % p.Lq;
+          di = (b * p.H + h) * p.Lq + i;
+        } else {
+          const long long h = row % p.H, t = row / p.H;
+          di = h * T + t;
+        }
+        p.delta[di] = acc;
+      }
+    }
+  }
+  // zero the fp32 dQ accumulator
+  const long long n = p.broadcast ? p.dq_acc_elems_bcast : (ok ? (long long)T * p.H * p.D : 0);
+  float4* z = reinterpret_cast<float4*>(p.dq_acc);
+  for (long long i = gtid; i < n / 4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dq = bf16(scale * sum over shards of the fp32 accumulator)
+__global__ void __launch_bounds__(256) finalize_kernel(FinParams p) {
+  const long long n = p.broadcast ? (long long)p.Lq * p.H * p.D
+                                  : (p.hdr->valid ? (long long)p.hdr->T * p.H * p.D : 0);
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = gtid; i < n / 4; i += nthreads) {
+    float4 a = reinterpret_cast<const float4*>(p.dq_acc)[i];
+    for (int s = 1; s < p.shards; ++s) {
+      const float4 c = reinterpret_cast<const float4*>(p.dq_acc + s * p.shard_stride)[i];
+      a.x += c.x, a.y += c.y, a.z += c.z, a.w += c.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * p.scale, a.y * p.scale);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * p.scale, a.w * p.scale);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p.dq)[i] = v;
+  }
+}
+
+// out[rows, D] = 0 (bf16), lse[rows] = -inf: outputs of a broadcast batch
+// whose sequences are all empty.
+__global__ void fill_empty_kernel(__nv_bfloat16* out, float* lse, long long rows, int D) {
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = gtid; i < rows * D / 8; i += nthreads)
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+  if (lse)
+    for (long long i = gtid; i < rows; i += nthreads) lse[i] = -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_sched(const SchedParams& p, cudaStream_t s) {
+  sched_kernel<<<1, kSchedThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepParams& p, int sms, cudaStream_t s) {
+  prep_kernel<<<sms * 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s) {
+  finalize_kernel<<<sms * 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
+                              cudaStream_t s) {
+  fill_empty_kernel<<<256, 256, 0, s>>>(out, lse, rows, D);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

@@ -1,0 +1,526 @@
+// Jagged flash attention backward (dK/dV main loop + dQ reduction) for sm_103a.
+//
+// Method: "Optimizing Jagged Flash Attention with TLX" (pytorch.org):
+//  * "Scheduling jagged tiles across SMs": the backward loops over K/V
+//    blocks on the outside and Q tiles on the inside; work items are the
+//    valid (sequence, head, K/V block) tiles, block-innermost.
+//  * "2-CTA collaborative MMA": five GEMMs per K/V block produce dQ, dK, dV.
+//  * "Multi-stage dQ staging": dQ partials of every K/V block are summed in
+//    fp32 across CTAs (broadcast-Q: across the whole batch); here each CTA
+//    adds into one of several fp32 shards with vector red.global.add and a
+//    separate kernel sums the shards and casts to bf16.
+//  * "Loop peeling": masks cost nothing on interior tiles; invalid query
+//    columns are removed through an LSE of +inf and invalid key rows through
+//    a per-thread predicate, so only causal diagonal tiles test elements.
+//
+// Per K/V block (128 keys) and Q tile (128 queries), with scores kept
+// transposed (keys on TMEM lanes) so that P^T and dS^T can feed the next
+// MMAs straight from tensor memory:
+//   S^T  = K Q^T            (SS, K-major / K-major)
+//   dP^T = V dO^T           (SS)
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e),  dS^T = P^T (dP^T - Delta)
+//   dV  += P^T dO           (TS: A = P^T in TMEM, B = dO MN-major)
+//   dK  += dS^T Q           (TS: A = dS^T in TMEM, B = Q MN-major)
+//   dQ   = dS K             (SS: A = dS MN-major from SMEM, B = K MN-major)
+// CTA = 6 warps: warps 0-3 score/gradient math, dQ drain and dK/dV epilogue
+// (thread r owns TMEM lane r), warp 4 TMA producer, warp 5 MMA issuer.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NSQ = 2;              // Q / dO ring depth
+  static constexpr int kTile = kBM * D * 2;  // bytes of a 128-row bf16 tile
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kK = 0;
+  static constexpr int kV = kTile;
+  static constexpr int kQ = 2 * kTile;
+  static constexpr int kDO = kQ + NSQ * kTile;
+  static constexpr int kDS = kDO + NSQ * kTile;  // dS: [128 keys][128 queries] bf16
+  static constexpr int kStat = kDS + 32768;     // LSE*log2e and Delta, 2 buffers
+  static constexpr int kCtl = kStat + 2 * 2 * kBM * 4;
+  static constexpr int kSmem = kCtl + 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128;
+  static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kColDQ = (D == 128) ? 0 : 384;  // D=128: reuses S
+};
+
+struct BwdCtl {
+  uint64_t kv_full, kv_empty;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t st_full, ds_full;
+  uint64_t dq_full, dq_empty;
+  uint64_t dkdv_full, dkdv_empty;
+  uint64_t tmp;
+  uint64_t stat_full;  // LSE/Delta of the current Q tile staged by all 128 threads
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  int item_slot[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct RowBox {
+  int row, shift, n;  // TMA row coordinate, rows moved back, valid rows
+};
+// 128-row box starting at packed row `start` of a sequence of `len` rows
+// remaining; moved back so it never reads past row T.
+__device__ __forceinline__ RowBox row_box(int start, int remaining, int T) {
+  RowBox r;
+  r.shift = max(0, start + 128 - T);
+  r.row = start - r.shift;
+  r.n = min(128, remaining);
+  return r;
+}
+
+struct BwdTile {
+  int b, h, kb;
+  int off0, L;
+  RowBox kt;   // keys of this block
+  int t0, nt;  // first query tile and count
+};
+
+template <bool BCAST, bool CAUSAL>
+__device__ __forceinline__ BwdTile decode(const BwdParams& p, int idx, int T) {
+  BwdTile f;
+  const Item it = p.items[idx];
+  f.b = it.x;
+  f.h = it.y >> 16;
+  f.kb = it.y & 0xffff;
+  f.off0 = p.offsets[f.b];
+  f.L = p.offsets[f.b + 1] - f.off0;
+  f.kt = row_box(f.off0 + f.kb * kBN, f.L - f.kb * kBN, T);
+  if (BCAST) {
+    f.t0 = 0;
+    f.nt = cdiv(p.Lq, kBM);
+  } else {
+    f.t0 = CAUSAL ? (f.kb * kBN) / kBM : 0;
+    f.nt = cdiv(f.L, kBM) - f.t0;
+  }
+  return f;
+}
+
+// Query tile t of the item: box (self) and local index of its row 0.
+template <bool BCAST>
+__device__ __forceinline__ RowBox q_box(const BwdParams& p, const BwdTile& f, int t, int T) {
+  if (BCAST) {
+    RowBox r;
+    r.row = t * kBM;
+    r.shift = 0;
+    r.n = min(kBM, p.Lq - t * kBM);
+    return r;
+  }
+  return row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > JFA_WAIT_LIMIT_CYCLES) {
+      atomicOr(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// Item queue consumer: returns the item index or -1 at the end.  `warp`:
+// called by a whole warp (lane 0 arrives) rather than by a single thread.
+__device__ __forceinline__ int next_item(BwdCtl* c, uint32_t n, bool warp, bool* ok, int* err) {
+  const int slot = n & 1;
+  const bool got = warp ? mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)
+                        : mbar_wait(&c->item_full[slot], (n >> 1) & 1, &c->abort, err);
+  if (!got) {
+    *ok = false;
+    return -1;
+  }
+  const int idx = c->item_slot[slot];
+  if (warp) __syncwarp();
+  if (!warp || (threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  return idx;
+}
+
+template <int D, bool CAUSAL, bool BCAST>
+__device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                              const CUtensorMap* tdo, const BwdParams& p, uint8_t* smem,
+                              BwdCtl* c) {
+  using C = BwdCfg<D>;
+  const int n_items = p.hdr->n_items;
+  const int T = p.hdr->T;
+  uint32_t it = 0, gq = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    const int slot = n & 1;
+    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
+    const int idx = atomicAdd(&p.hdr->ticket, 1);
+    c->item_slot[slot] = idx < n_items ? idx : -1;
+    mbar_arrive(&c->item_full[slot]);
+    if (idx >= n_items) break;
+    const BwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
+    if (!mbar_wait(&c->kv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
+    mbar_arrive_expect_tx(&c->kv_full, 2 * C::kTile);
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) {
+      tma_load_3d(smem + C::kK + s * 16384, tk, &c->kv_full, s * 64, f.h, f.kt.row);
+      tma_load_3d(smem + C::kV + s * 16384, tv, &c->kv_full, s * 64, f.h, f.kt.row);
+    }
+    ++it;
+    for (int i = 0; i < f.nt; ++i) {
+      const uint32_t g = gq;
+      const int st = g % C::NSQ;
+      if (!mbar_wait(&c->qdo_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
+      const int t = f.t0 + i;
+      const RowBox qb = q_box<BCAST>(p, f, t, T);
+      mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile);
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s) {
+        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->qdo_full[st], s * 64, f.h,
+                    qb.row);
+        if (BCAST)
+          tma_load_4d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->qdo_full[st], s * 64,
+                      f.h, qb.row, f.b);
+        else
+          tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->qdo_full[st], s * 64,
+                      f.h, qb.row);
+      }
+      ++gq;
+    }
+  }
+  if (it > 0) drain_wait(&c->kv_full, (it - 1) & 1, p.err);
+  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
+    drain_wait(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
+}
+
+template <int D, bool CAUSAL, bool BCAST>
+__device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t tbase) {
+  using C = BwdCfg<D>;
+  const int T = p.hdr->T;
+  const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+  const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
+  const uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS MN-major)
+  const uint32_t sk = smem_addr(smem + C::kK), sv = smem_addr(smem + C::kV);
+  const uint32_t sds = smem_addr(smem + C::kDS);
+  uint32_t it = 0, gq = 0;
+  bool ok = true, issued = false;
+  for (uint32_t n = 0; ok; ++n) {
+    const int idx = next_item(c, n, false, &ok, p.err);
+    if (idx < 0) break;
+    const BwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
+    if (!mbar_wait(&c->kv_full, it & 1, &c->abort, p.err)) break;
+    for (int i = 0; i < f.nt; ++i, ++gq) {
+      const uint32_t g = gq;
+      const int st = g % C::NSQ;
+      const uint32_t sq = smem_addr(smem + C::kQ + st * C::kTile);
+      const uint32_t sdo = smem_addr(smem + C::kDO + st * C::kTile);
+      if (!mbar_wait(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
+      // D=128: dQ_{g-1} lives in the S columns; it must be drained first.
+      if (D == 128 && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+        mma_ss(tmem_at(tbase, 0, C::kColS), smem_desc_sw128(sk + off, 16, 1024),
+               smem_desc_sw128(sq + off, 16, 1024), id_st, k > 0);
+      }
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+        mma_ss(tmem_at(tbase, 0, C::kColDP), smem_desc_sw128(sv + off, 16, 1024),
+               smem_desc_sw128(sdo + off, 16, 1024), id_st, k > 0);
+      }
+      mma_commit(&c->st_full);
+      issued = true;
+      if (!mbar_wait(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      if (i == 0 && !mbar_wait(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kBM / 16; ++k) {
+        mma_ts(tmem_at(tbase, 0, C::kColDV), tmem_at(tbase, 0, C::kColS + k * 8),
+               smem_desc_sw128(sdo + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+      }
+#pragma unroll
+      for (int k = 0; k < kBM / 16; ++k) {
+        mma_ts(tmem_at(tbase, 0, C::kColDK), tmem_at(tbase, 0, C::kColDP + k * 8),
+               smem_desc_sw128(sq + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+      }
+      mma_commit(&c->qdo_empty[st]);
+      if (D == 128) {
+        // dQ overwrites the S columns that the dV MMA reads P^T from.
+        mma_commit(&c->tmp);
+        if (!mbar_wait(&c->tmp, g & 1, &c->abort, p.err)) { ok = false; break; }
+      } else if (g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kBN / 16; ++k) {
+        mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sds + k * 2048, 16384, 1024),
+               smem_desc_sw128(sk + k * 2048, 16384, 1024), id_dq, k > 0);
+      }
+      mma_commit(&c->dq_full);
+    }
+    if (!ok) break;
+    mma_commit(&c->dkdv_full);
+    mma_commit(&c->kv_empty);
+    ++it;
+  }
+  if (issued) {
+    mma_commit(&c->drain);
+    drain_wait(&c->drain, 0, p.err);
+  }
+}
+
+template <int D, bool CAUSAL, bool BCAST>
+__device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t tbase) {
+  using C = BwdCfg<D>;
+  const int r = threadIdx.x;  // TMEM lane: key row for S/dP/dK/dV, query row for dQ
+  const int warp = r >> 5;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const int T = p.hdr->T;
+  const float sl2 = p.scale_log2;
+  float* s_lse = reinterpret_cast<float*>(smem + C::kStat);  // [2][128]
+  float* s_dlt = s_lse + 2 * kBM;                            // [2][128]
+  uint8_t* sds = smem + C::kDS;
+  const int shard = BCAST ? static_cast<int>(blockIdx.x % p.dq_shards) : 0;
+  uint32_t it = 0, gq = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    const int idx = next_item(c, n, true, &ok, p.err);
+    if (idx < 0) break;
+    const BwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
+    const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
+    const bool key_ok = r >= f.kt.shift && r < f.kt.shift + f.kt.n;
+    for (int i = 0; i < f.nt; ++i, ++gq) {
+      const uint32_t g = gq;
+      const int t = f.t0 + i;
+      const RowBox qb = q_box<BCAST>(p, f, t, T);
+      const int q0 = t * kBM - qb.shift;  // local query index of column 0
+      // Stage LSE*log2e and Delta of this Q tile's rows (thread r: row r).
+      {
+        const int qi = q0 + r;
+        const bool q_ok = r >= qb.shift && r < qb.shift + qb.n;
+        float lv = INFINITY, dv = 0.f;
+        if (q_ok) {
+          const long long si = BCAST ? (static_cast<long long>(f.b) * p.H + f.h) * p.Lq + qi
+                                     : static_cast<long long>(f.h) * T + f.off0 + qi;
+          lv = p.lse[si] * kLog2e;
+          dv = p.delta[si];
+        }
+        s_lse[(g & 1) * kBM + r] = lv;
+        s_dlt[(g & 1) * kBM + r] = dv;
+      }
+      mbar_arrive(&c->stat_full);
+      if (!mbar_wait_warp(&c->stat_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      const float* lse_t = s_lse + (g & 1) * kBM;
+      const float* dlt_t = s_dlt + (g & 1) * kBM;
+      if (!mbar_wait_warp(&c->st_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      // Causal: key > query is masked; column c is admissible iff c >= c_min.
+      const int c_min = CAUSAL ? key - q0 : -1;
+      const bool diag = CAUSAL && __any_sync(0xffffffffu, c_min > 0);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sraw[32], praw[32];
+        tmem_ld32(tbase + lane_base + C::kColS + ch * 32, sraw);
+        tmem_ld32(tbase + lane_base + C::kColDP + ch * 32, praw);
+        tmem_wait_ld();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 2) {
+          const int col = ch * 32 + cc;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -lse_t[col]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sraw[cc + 1]), sl2, -lse_t[col + 1]));
+          if (!key_ok) p0 = 0.f, p1 = 0.f;
+          if (diag) {
+            p0 = col >= c_min ? p0 : 0.f;
+            p1 = col + 1 >= c_min ? p1 : 0.f;
+          }
+          const float d0 = p0 * (__uint_as_float(praw[cc]) - dlt_t[col]);
+          const float d1 = p1 * (__uint_as_float(praw[cc + 1]) - dlt_t[col + 1]);
+          pk[cc / 2] = pack_bf16x2(p0, p1);
+          dk[cc / 2] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tbase + lane_base + C::kColS + ch * 16, pk);
+        tmem_st16(tbase + lane_base + C::kColDP + ch * 16, dk);
+        // dS row r (queries ch*32 .. ch*32+31) into the swizzled SMEM tile.
+        uint8_t* slab = sds + (ch >> 1) * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (ch & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(slab + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&c->ds_full);
+      // dQ drain: lane r is query row r of dQ = dS K.
+      if (!mbar_wait_warp(&c->dq_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const int qi = q0 + r;
+        const bool q_ok = r >= qb.shift && r < qb.shift + qb.n;
+        float* dst = BCAST ? p.dq_acc + shard * p.shard_stride +
+                                 (static_cast<long long>(qi) * p.H + f.h) * D
+                           : p.dq_acc + (static_cast<long long>(f.off0 + qi) * p.H + f.h) * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t q[32];
+          tmem_ld32(tbase + lane_base + C::kColDQ + ch * 32, q);
+          tmem_wait_ld();
+          if (q_ok) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              atomicAdd(reinterpret_cast<float4*>(dst + ch * 32 + 4 * u),
+                        make_float4(__uint_as_float(q[4 * u]), __uint_as_float(q[4 * u + 1]),
+                                    __uint_as_float(q[4 * u + 2]), __uint_as_float(q[4 * u + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&c->dq_empty);
+    }
+    if (!ok) break;
+    // Item epilogue: dV and scale * dK rows of this K/V block.
+    if (!mbar_wait_warp(&c->dkdv_full, it & 1, &c->abort, p.err)) break;
+    tc_fence_after();
+    const long long row = (static_cast<long long>(f.off0) + key) * p.H + f.h;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+      const float mul = which == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_base + col + ch * 32, v);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2)
+          w[i2] = pack_bf16x2(__uint_as_float(v[2 * i2]) * mul, __uint_as_float(v[2 * i2 + 1]) * mul);
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&c->dkdv_empty);
+    ++it;
+  }
+}
+
+template <int D, bool CAUSAL, bool BCAST>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+               const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  BwdCtl* c = reinterpret_cast<BwdCtl*>(smem + C::kCtl);
+  const int warp = warp_id(), lane = lane_id();
+  if ((smem_addr(smem) & 1023) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&c->kv_full, 1);
+    mbar_init(&c->kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->qdo_full[i], 1);
+      mbar_init(&c->qdo_empty[i], 1);
+      mbar_init(&c->item_full[i], 1);
+      mbar_init(&c->item_empty[i], 5);
+    }
+    mbar_init(&c->st_full, 1);
+    mbar_init(&c->ds_full, kBM);
+    mbar_init(&c->dq_full, 1);
+    mbar_init(&c->dq_empty, kBM);
+    mbar_init(&c->dkdv_full, 1);
+    mbar_init(&c->dkdv_empty, kBM);
+    mbar_init(&c->tmp, 1);
+    mbar_init(&c->stat_full, kBM);
+    mbar_init(&c->drain, 1);
+    c->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&c->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = c->tmem_base;
+  if (warp < 4) {
+    math_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
+  } else {
+    if (lane == 0) mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool BCAST>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  static_assert(C::kSmem <= 232448, "shared memory budget");
+  static_assert(sizeof(BwdCtl) <= 512, "control block");
+  auto kern = bwd_kernel<D, CAUSAL, BCAST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kBwdThreads, C::kSmem, s>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdParams& p, int grid, cudaStream_t s) {
+  if (D == 128) {
+    if (bcast) return launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, grid, s);
+    if (causal) return launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, grid, s);
+    return launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, grid, s);
+  }
+  if (bcast) return launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, grid, s);
+  if (causal) return launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, grid, s);
+  return launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, grid, s);
+}
+
+}  // namespace jfa

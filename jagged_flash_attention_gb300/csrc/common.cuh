@@ -1,0 +1,101 @@
+// Shared definitions of the jagged flash attention kernels: tile sizes, the
+// device work-list header, kernel parameter blocks and the host-side launch
+// entry points implemented in the .cu files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "errbits.cuh"
+
+namespace jfa {
+
+constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
+constexpr int kBN = 128;  // keys per tile
+
+// Small header at the start of every scratch block, written by the
+// scheduler kernel and read by the kernels that follow it on the stream.
+struct WorkHeader {
+  int n_items;  // number of work items in the list
+  int T;        // offsets[B], total packed tokens
+  int ticket;   // dynamic work counter of the persistent kernels
+  int valid;    // 1 if offsets passed the device checks
+  int pad[4];
+};
+
+// A work item: x = sequence b, y = (head << 16) | tile.
+using Item = int2;
+
+struct SchedParams {
+  const int32_t* offsets;
+  int B, H, Lq, max_len;
+  int causal, broadcast, backward;
+  Item* items;
+  int capacity;
+  WorkHeader* hdr;
+  int* err;
+};
+
+struct FwdParams {
+  const int32_t* offsets;
+  int B, H, Lq;
+  float scale_log2;  // scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  const Item* items;
+  WorkHeader* hdr;
+  int* err;
+};
+
+struct BwdParams {
+  const int32_t* offsets;
+  int B, H, Lq;
+  float scale_log2;
+  float scale;
+  const float* lse;    // caller's LSE (natural log)
+  const float* delta;  // rowsum(dO * O), same layout as lse
+  float* dq_acc;       // fp32 accumulator: self [Tcap,H,D]; broadcast [shards,Lq,H,D]
+  int dq_shards;       // broadcast only
+  long long shard_stride;  // elements per shard
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const Item* items;
+  WorkHeader* hdr;
+  int* err;
+};
+
+struct PrepParams {
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  float* delta;
+  float* dq_acc;
+  long long dq_acc_elems_bcast;  // broadcast: elements to zero; self: 0 (uses T)
+  int B, H, D, Lq, broadcast;
+  const WorkHeader* hdr;
+};
+
+struct FinParams {
+  const float* dq_acc;
+  __nv_bfloat16* dq;
+  float scale;
+  int H, D, Lq, broadcast, shards;
+  long long shard_stride;
+  const WorkHeader* hdr;
+};
+
+// Host-side launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
+cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_prep(const PrepParams& p, int sms, cudaStream_t s);
+cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s);
+cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
+                              cudaStream_t s);
+cudaError_t prepare_kernels(int device);
+
+}  // namespace jfa

@@ -1,0 +1,93 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+entry point declared in include/jfa.h, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from jagged_flash_attention_gb300 import build, lib
+    build.build()
+    return lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "jfa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(jfa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq", "jfa_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version(L):
+    assert b"sm_103a" in L.jfa_version()
+
+
+def _fwd(L, **kw):
+    a = dict(q=16, k=16, v=16, off=16, B=2, H=2, D=128, max_len=10, bq=0, causal=0, scale=0.1,
+             out=16, lse=16)
+    a.update(kw)
+    return L.jfa_fwd(a["q"], a["k"], a["v"], a["off"], a["B"], a["H"], a["D"], a["max_len"],
+                     a["bq"], a["causal"], a["scale"], a["out"], a["lse"], 0)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(D=96), 2, "D must be 64 or 128"),
+    (dict(bq=1), 1, "jfa_fwd_bq"),
+    (dict(B=0), 1, "B must be"),
+    (dict(H=0), 1, "H must be"),
+    (dict(scale=float("nan")), 1, "scale"),
+    (dict(scale=-1.0), 1, "scale"),
+    (dict(q=0), 1, "non-null"),
+    (dict(k=24), 1, "16-byte aligned"),
+    (dict(off=0), 1, "offsets"),
+    (dict(out=8), 1, "out must be"),
+    (dict(lse=0), 1, "lse must be"),
+    (dict(max_len=-1), 1, "max_len"),
+])
+def test_host_argument_errors(L, kw, status, needle):
+    assert _fwd(L, **kw) == status
+    assert needle in L.jfa_last_error().decode()
+
+
+def test_causal_broadcast_unsupported(L):
+    st = L.jfa_fwd_bq(16, 16, 16, 16, 2, 2, 128, 10, 64, 1, 1, 0.1, 16, 16, 0)
+    assert st == 2 and b"self-attention only" in L.jfa_last_error()
+    st = L.jfa_bwd_bq(16, 16, 16, 16, 2, 2, 128, 10, 0, 1, 0, 0.1, 16, 16, 16, 16, 16, 16, 0)
+    assert st == 1 and b"q_len" in L.jfa_last_error()
+
+
+def test_bwd_argument_errors(L):
+    st = L.jfa_bwd(16, 16, 16, 16, 2, 2, 128, 10, 0, 0, 0.1, 16, 16, 16, 0, 16, 16, 0)
+    assert st == 1 and b"non-null" in L.jfa_last_error()
+    st = L.jfa_bwd(16, 16, 16, 16, 2, 2, 64, 10, 0, 0, 0.1, 16, 16, 16, 16, 16, 40, 0)
+    assert st == 1 and b"16-byte" in L.jfa_last_error()
+
+
+def test_product_path_does_not_touch_oracle():
+    """The package and the CUDA sources never reference the oracle."""
+    pkg = os.path.join(ROOT, "jagged_flash_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in txt.lower(), f
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import jagged_flash_attention_gb300 as jfa
+    monkeypatch.setattr(jfa, "_LIB", None)
+    monkeypatch.setattr(jfa, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        jfa.lib()

@@ -1,0 +1,42 @@
+"""The seeded workload generators: deterministic, and with the length
+distributions each workload names."""
+import numpy as np
+
+import jfa_workloads as W
+
+
+def test_lengths_are_deterministic_and_in_range():
+    for name in W.ORDER:
+        w = W.WORKLOADS[name]
+        a, b = W.sample_lengths(w), W.sample_lengths(w)
+        np.testing.assert_array_equal(a, b)
+        assert a.size == w.B and a.min() >= 1
+    L = W.sample_lengths(W.WORKLOADS["tiny_self"])
+    assert L.max() <= 64
+    L = W.sample_lengths(W.WORKLOADS["jagged_self"])
+    assert L.min() >= 16 and L.max() <= 2048 and abs(L.mean() - 1032) < 150
+    L = W.sample_lengths(W.WORKLOADS["broadcast_q"])
+    assert L.max() <= 4096 and 380 < np.median(L) < 680
+    L = W.sample_lengths(W.WORKLOADS["causal_self"])
+    assert L.min() >= 256 and L.max() <= 8192
+    L = W.sample_lengths(W.WORKLOADS["skewed_broadcast_q"])
+    assert (L == 8192).sum() >= 41 and L.max() <= 8192 and 170 < L[L < 8192].mean() < 230
+
+
+def test_offsets_and_pairs():
+    off = W.offsets_from_lengths([3, 0, 5])
+    assert off.dtype == np.int32 and list(off) == [0, 3, 3, 8]
+    assert W.pairs([3, 0, 5]) == 9 + 25
+    assert W.pairs([3, 5], causal=True) == 6 + 15
+    assert W.pairs([3, 5], q_len=7, broadcast_q=True) == 56
+
+
+def test_values_deterministic_bf16():
+    import torch
+    x = W.make_inputs(W.WORKLOADS["tiny_self"])
+    y = W.make_inputs(W.WORKLOADS["tiny_self"])
+    assert x["q"].dtype == torch.bfloat16
+    assert torch.equal(x["q"], y["q"]) and torch.equal(x["dout"], y["dout"])
+    assert x["q"].shape == (x["T"], 2, 64)
+    b = W.make_inputs(W.WORKLOADS["broadcast_q"], lengths=[3, 4])
+    assert b["q"].shape == (256, 4, 128) and b["dout"].shape == (2, 256, 4, 128)
