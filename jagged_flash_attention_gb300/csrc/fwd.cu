@@ -190,6 +190,17 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
   const uint32_t sq = smem_addr(smem + C::kQ);
   uint32_t it = 0, kv = 0;
+  // PV completions observed so far through o_ready.  A parity wait is only
+  // valid while the barrier is at most one phase ahead of the waiter, so PV_x
+  // is issued only after PV_{x-1} has been observed (free in steady state:
+  // the softmax warps waited for PV_{x-1} before releasing P_x).
+  uint32_t pv_seen = 0;
+  auto wait_pv = [&](uint32_t x) -> bool {
+    if (x < pv_seen) return true;
+    if (!mbar_wait(&c->o_ready, x & 1, &c->abort, p.err)) return false;
+    pv_seen = x + 1;
+    return true;
+  };
   bool ok = true;
   bool issued = false;
   for (uint32_t n = 0; ok; ++n) {
@@ -205,7 +216,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
         const uint32_t buf = g & 1;
         if (!mbar_wait(&c->k_full[st], (g / C::NS) & 1, &c->abort, p.err)) { ok = false; break; }
         // S buffer `buf` last held P_{g-2}; its PV must have finished reading it.
-        if (g >= 2 && !mbar_wait(&c->o_ready, (g - 2) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (g >= 2 && !wait_pv(g - 2)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + C::kK + st * C::kTile);
 #pragma unroll
@@ -226,6 +237,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
         if (!mbar_wait(&c->p_full[buf], (g >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
         if (!mbar_wait(&c->v_full[st], (g / C::NS) & 1, &c->abort, p.err)) { ok = false; break; }
         if (j == 1 && !mbar_wait(&c->o_free, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        if (g >= 1 && !wait_pv(g - 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sv = smem_addr(smem + C::kV + st * C::kTile);
 #pragma unroll
