@@ -97,6 +97,28 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
                       float scale, const void* out, const float* lse, const void* dout, void* dq,
                       void* dk, void* dv, cudaStream_t stream);
 
+/* Allocation-free forward pass.  The pages have no counterpart: this entry
+ * point exists for callers that must not allocate device memory while the
+ * library runs (memory owned and pre-partitioned by a host framework, for
+ * example an inference server or plugin host that forbids allocation during
+ * execution, or a real-time loop that cannot risk an out-of-memory failure).
+ * Same arguments and results as jfa_fwd_bq (broadcast_q = 0 gives
+ * self-attention and ignores q_len).  It calls no cudaMalloc, cudaFree or
+ * allocating routine: its scratch lives in one 1 MiB device array inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.  Limit: H * B * ceil(L / 128) <= 131040 work items, with L = max_len
+ * (self-attention) or q_len (broadcast); larger problems return
+ * JFA_ERR_WORKSPACE with nothing enqueued.  The first call on each device
+ * looks up the device addresses it needs (no allocation); make that first
+ * call before capturing a stream into a CUDA graph.  All calls share the one
+ * array, so calls whose GPU work overlaps (different streams, or different
+ * host threads) race and give wrong results: serialise them.  Device-side
+ * errors set the same device error word that jfa_sync_and_check reads. */
+jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const int32_t* offsets,
+                              int B, int H, int D, int max_len, int q_len, int broadcast_q,
+                              int causal, float scale, void* out, float* lse,
+                              cudaStream_t stream);
+
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device.  Returns JFA_ERR_INVALID_ARG for offsets found invalid on
  * the device, JFA_ERR_TIMEOUT for a bounded wait that ran out,

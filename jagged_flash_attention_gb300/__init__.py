@@ -103,6 +103,20 @@ def jfa_bwd_bq(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, s
                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
+def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale,
+                       out, lse, stream=None):
+    """Allocation-free forward (see include/jfa.h): for callers that must not
+    allocate device memory during the call.  The caller passes every buffer;
+    the library's scratch is a fixed 1 MiB device array."""
+    L = lib()
+    fn = L.jfa_fwd_bq_noalloc
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, D, max_len, q_len,
+              int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse), _stream(stream)))
+
+
 def jfa_sync_and_check(stream=None):
     _check(lib().jfa_sync_and_check(_stream(stream)))
 

@@ -432,3 +432,147 @@ const char* jfa_last_error(void) { return t_last_error.c_str(); }
 const char* jfa_version(void) { return "jfa-gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward entry point.
+//
+// Some callers may not allocate device memory at all while they run this
+// library: code whose memory is entirely owned and pre-partitioned by a host
+// framework (inference servers and plugin hosts that hand a library fixed
+// buffers and forbid allocations during execution), real-time loops that
+// must not take the allocator's locks or risk an out-of-memory failure
+// mid-run, and code running where the caller has made allocation illegal.
+// For them the forward pass keeps its scratch (the work-list header and the
+// work items) in the file-scope device array below instead of a pool.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Maximum scratch of the allocation-free forward: 256 B header plus 8 B per
+// work item, i.e. at most (1 MiB - 256 B) / 8 = 131040 items, where items =
+// H * B * ceil(max_len / 128) (self-attention) or H * B * ceil(q_len / 128)
+// (broadcast-Q).  Every GPU that loads the library holds this array until
+// the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;          // device address of the error word
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// Once per device, with that device current: resolve the device addresses of
+// the scratch array and of the error word.  In host code the array's name is
+// only a host-side stand-in, so its address must come from
+// cudaGetSymbolAddress.  Nothing here allocates memory.
+jfa_status noalloc_device(NoAllocDevice** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(JFA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(JFA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess)
+      return fail(JFA_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+    if (!(prop.major == 10 && prop.minor == 3))
+      return fail(JFA_ERR_UNSUPPORTED, "device %s is sm_%d%d; this library is built for sm_103a",
+                  prop.name, prop.major, prop.minor);
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(JFA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    void* err = nullptr;
+    e = cudaGetSymbolAddress(&err, g_device_error);
+    if (e != cudaSuccess || err == nullptr)
+      return fail(JFA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess)
+        return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.sms = prop.multiProcessorCount;
+    d.scratch = static_cast<uint8_t*>(ptr);
+    d.err = static_cast<int*>(err);
+    d.ready = true;
+  }
+  *out = &d;
+  return JFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const int32_t* offsets,
+                              int B, int H, int D, int max_len, int q_len, int broadcast_q,
+                              int causal, float scale, void* out, float* lse,
+                              cudaStream_t stream) {
+  t_last_error.clear();
+  const Shape s = make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale);
+  jfa_status st = check_common(s, q, k, v, offsets);
+  if (st != JFA_OK) return st;
+  if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "lse must be non-null, 4-byte aligned");
+  const long long qt = s.broadcast ? cdivll(s.Lq, kBM) : cdivll(s.max_len, kBM);
+  const long long cap = (long long)s.H * s.B * qt;
+  const size_t items_off = 256;
+  const long long max_items = (long long)((kNoAllocScratchBytes - items_off) / sizeof(Item));
+  if (cap > max_items)
+    return fail(JFA_ERR_WORKSPACE,
+                "jfa_fwd_bq_noalloc: this problem needs up to %lld work items (H * B * "
+                "ceil(len / 128)) but the static scratch array (%zu bytes) holds at most %lld; "
+                "use jfa_fwd / jfa_fwd_bq",
+                cap, kNoAllocScratchBytes, max_items);
+  NoAllocDevice* d = nullptr;
+  if ((st = noalloc_device(&d)) != JFA_OK) return st;
+  cudaError_t e;
+  if (s.max_len == 0) {
+    if (s.broadcast) {
+      e = launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H,
+                            s.D, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+    }
+    return JFA_OK;
+  }
+  CUtensorMap tq, tk, tv;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(d->scratch);
+  Item* items = reinterpret_cast<Item*>(d->scratch + items_off);
+  // The scheduler rewrites the header (item count, T, ticket = 0) and every
+  // item the forward kernel reads, so nothing left by a previous call leaks.
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0,
+                 items, (int)cap, hdr, d->err};
+  e = launch_sched(sp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
+  FwdParams fp;
+  fp.offsets = offsets;
+  fp.B = s.B;
+  fp.H = s.H;
+  fp.Lq = s.Lq;
+  fp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+  fp.out = static_cast<__nv_bfloat16*>(out);
+  fp.lse = lse;
+  fp.items = items;
+  fp.hdr = hdr;
+  fp.err = d->err;
+  const int grid = (int)std::min<long long>(d->sms, cap);
+  e = launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return JFA_OK;
+}
+
+
+}  // extern "C"
