@@ -106,7 +106,7 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
  * self-attention and ignores q_len).  It calls no cudaMalloc, cudaFree or
  * allocating routine: its scratch lives in one 1 MiB device array inside the
  * library, which every GPU that loads the library keeps until the process
- * exits.  Limit: H * B * ceil(L / 128) <= 131040 work items, with L = max_len
+ * exits.  Limit: H * B * ceil(L / 256) <= 131040 work items, with L = max_len
  * (self-attention) or q_len (broadcast); larger problems return
  * JFA_ERR_WORKSPACE with nothing enqueued.  The first call on each device
  * looks up the device addresses it needs (no allocation); make that first

@@ -193,7 +193,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
     }
     return finish(ds, stream);
   }
-  const long long qt = s.broadcast ? cdivll(s.Lq, kBM) : cdivll(s.max_len, kBM);
+  const long long qt = s.broadcast ? cdivll(s.Lq, kFwdRows) : cdivll(s.max_len, kFwdRows);
   const long long cap = (long long)s.H * s.B * qt;
   if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");
   const size_t items_off = 256;
@@ -450,7 +450,7 @@ namespace {
 
 // Maximum scratch of the allocation-free forward: 256 B header plus 8 B per
 // work item, i.e. at most (1 MiB - 256 B) / 8 = 131040 items, where items =
-// H * B * ceil(max_len / 128) (self-attention) or H * B * ceil(q_len / 128)
+// H * B * ceil(max_len / 256) (self-attention) or H * B * ceil(q_len / 256)
 // (broadcast-Q).  Every GPU that loads the library holds this array until
 // the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
@@ -524,14 +524,14 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return fail(JFA_ERR_INVALID_ARG, "lse must be non-null, 4-byte aligned");
-  const long long qt = s.broadcast ? cdivll(s.Lq, kBM) : cdivll(s.max_len, kBM);
+  const long long qt = s.broadcast ? cdivll(s.Lq, kFwdRows) : cdivll(s.max_len, kFwdRows);
   const long long cap = (long long)s.H * s.B * qt;
   const size_t items_off = 256;
   const long long max_items = (long long)((kNoAllocScratchBytes - items_off) / sizeof(Item));
   if (cap > max_items)
     return fail(JFA_ERR_WORKSPACE,
                 "jfa_fwd_bq_noalloc: this problem needs up to %lld work items (H * B * "
-                "ceil(len / 128)) but the static scratch array (%zu bytes) holds at most %lld; "
+                "ceil(len / 256)) but the static scratch array (%zu bytes) holds at most %lld; "
                 "use jfa_fwd / jfa_fwd_bq",
                 cap, kNoAllocScratchBytes, max_items);
   NoAllocDevice* d = nullptr;

@@ -14,12 +14,13 @@ constexpr int kMaxBuckets = 1024;
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Tiles of sequence b that become work items (one item per head and tile).
-//  forward:  query tiles (self: of the sequence; broadcast: of the dense Q)
+//  forward:  256-row query tiles (two 128-row MMA tiles; self: of the
+//            sequence; broadcast: of the dense Q)
 //  backward: key/value blocks of the sequence
 __device__ __forceinline__ int n_tiles(const SchedParams& p, int L) {
   if (p.backward) return cdiv(L, kBN);
   // broadcast: every sequence, even an empty one, owns its output rows
-  return p.broadcast ? cdiv(p.Lq, kBM) : cdiv(L, kBM);
+  return p.broadcast ? cdiv(p.Lq, kFwdRows) : cdiv(L, kFwdRows);
 }
 
 // Cost bucket of sequence b: work of its longest item, in tile units.

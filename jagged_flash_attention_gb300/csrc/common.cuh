@@ -14,6 +14,7 @@ namespace jfa {
 
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;  // keys per tile
+constexpr int kFwdRows = 256;  // query rows per forward work item (two tiles)
 
 // Small header at the start of every scratch block, written by the
 // scheduler kernel and read by the kernels that follow it on the stream.

@@ -1,51 +1,62 @@
 // Jagged flash attention forward for sm_103a.
 //
 // Method: "Optimizing Jagged Flash Attention with TLX" (pytorch.org),
-// section 2.1 (role-specialised warps, hand-allocated SMEM/TMEM buffers with
-// S and P sharing one TMEM allocation while the PV accumulator keeps its
-// own, persistent CTAs) and section 2.2 (longest-first scheduling, masking
-// only the ragged tail tile); per-row math from "cuTile Kernels - FMHA
-// Implementation", "Flash Attention Algorithm" and "exp2 + flush_to_zero"
-// (online softmax in base 2 with the scale folded into one multiply).
+// section 2.1 (role-specialised warps; hand-allocated SMEM/TMEM buffers; S
+// and P sharing one TMEM allocation while the PV accumulator keeps its own;
+// the M dimension split into two groups; persistent CTAs) and section 2.2
+// (longest-first scheduling, masks only on the ragged tail tile); per-row
+// math from "cuTile Kernels - FMHA Implementation", "Flash Attention
+// Algorithm" and "exp2 + flush_to_zero" (online softmax in base 2 with the
+// scale folded into one multiply-add).
 //
-// CTA = 6 warps, one CTA per SM, looping over work items (b, h, q-tile):
-//   warps 0-3  softmax / correction / epilogue; thread r owns query row r
-//              (TMEM lane r) of the 128-row tile
-//   warp 4     TMA producer (Q once per item, K and V tiles into NS-deep
-//              rings) and the dynamic work ticket
-//   warp 5     TMEM allocation and the single-thread tcgen05 MMA issuer
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+D).  P (bf16)
-// overwrites the first 64 columns of the S buffer it was computed from and
-// is read from TMEM by the PV MMA.
+// A work item is (sequence b, head h, pair of 128-row query tiles).  Both
+// query tiles share every K/V tile the CTA loads.  CTA = 10 warps, one CTA
+// per SM:
+//   warps 0-3, 4-7  softmax / correction / epilogue of query tile 0 and 1;
+//                   thread r owns row r of its tile (TMEM lane r)
+//   warp 8          TMA producer (the two Q tiles once per item, K and V
+//                   tiles into rings) and the dynamic work ticket
+//   warp 9          TMEM allocation and the single-thread tcgen05 issuer
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them.  P_t
+// (bf16) overwrites the first 64 columns of S_t and is read from TMEM by the
+// PV MMA.  Issue order per K/V tile j: PV0(j-1), S0(j), PV1(j-1), S1(j), so
+// each softmax group has the time of two MMAs to turn S into P.  S_t(j)
+// overwrites the columns that PV_t(j-1), issued just before it, reads P from;
+// tcgen05 MMAs of one CTA execute in issue order.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kFwdThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kFwdThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kLn2 = 0.6931471805599453f;
+// Conditional rescaling: the running max used for exp2 is only raised when
+// the row max grows by more than 2^kRescaleLog2, so P <= 2^8 and most tiles
+// skip the O correction.  The result is exact either way.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NS = (D == 128) ? 2 : 4;  // K and V ring depth
-  static constexpr int kTile = kBM * D * 2;      // bytes of a 128-row bf16 tile
-  static constexpr int kSlabs = D / 64;          // 64-column (128 B) slabs per row
-  static constexpr int kQ = 0;
-  static constexpr int kK = kTile;
-  static constexpr int kV = kK + NS * kTile;
-  static constexpr int kCtl = kV + NS * kTile;  // barriers and small state
+  static constexpr int NSK = (D == 128) ? 3 : 4;  // K ring depth
+  static constexpr int NSV = (D == 128) ? 2 : 4;  // V ring depth
+  static constexpr int kTile = kBM * D * 2;       // bytes of a 128-row bf16 tile
+  static constexpr int kSlabs = D / 64;           // 64-column (128 B) slabs per row
+  static constexpr int kQ = 0;                    // two Q tiles
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = kK + NSK * kTile;
+  static constexpr int kCtl = kV + NSV * kTile;  // barriers and small state
   static constexpr int kSmem = kCtl + 512;
-  static constexpr uint32_t kColO = 256;
+  __host__ __device__ static constexpr uint32_t colS(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + D * t; }
 };
 
 struct FwdCtl {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_ready, o_free;
+  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item_slot[2];
@@ -55,38 +66,48 @@ struct FwdCtl {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-struct FwdTile {
-  int b, h, t;
+struct QTile {
+  int q_lo;   // local index of the tile's first query row
+  int nq;     // valid query rows (<= 0: tile absent)
+  int shift;  // rows the Q box was moved back to stay inside [0, T)
+  int row;    // TMA row coordinate of the Q box
+  int n_kv;   // key tiles this query tile visits
+};
+
+struct FwdItem {
+  int b, h;
   int off0, L;
-  int q_lo;     // local index of the tile's first query row
-  int nq;       // valid query rows
-  int q_shift;  // rows the Q box was moved back to stay inside [0, T)
-  int q_row;    // TMA row coordinate of the Q box
-  int n_kv;     // key tiles to visit
+  QTile t[2];
+  int N;  // key tiles loaded for the item (max over the two query tiles)
 };
 
 template <bool BCAST, bool CAUSAL>
-__device__ __forceinline__ FwdTile decode(const FwdParams& p, int idx, int T) {
-  FwdTile f;
+__device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
+  FwdItem f;
   const Item it = p.items[idx];
   f.b = it.x;
   f.h = it.y >> 16;
-  f.t = it.y & 0xffff;
+  const int pair = it.y & 0xffff;
   f.off0 = p.offsets[f.b];
   f.L = p.offsets[f.b + 1] - f.off0;
-  f.q_lo = f.t * kBM;
-  if (BCAST) {
-    f.nq = min(kBM, p.Lq - f.q_lo);
-    f.q_shift = 0;
-    f.q_row = f.q_lo;
-    f.n_kv = cdiv(f.L, kBN);
-  } else {
-    f.nq = min(kBM, f.L - f.q_lo);
-    const int start = f.off0 + f.q_lo;
-    f.q_shift = max(0, start + kBM - T);
-    f.q_row = start - f.q_shift;
-    f.n_kv = CAUSAL ? cdiv(f.q_lo + f.nq, kBN) : cdiv(f.L, kBN);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    QTile& q = f.t[t];
+    q.q_lo = (2 * pair + t) * kBM;
+    if (BCAST) {
+      q.nq = min(kBM, p.Lq - q.q_lo);
+      q.shift = 0;
+      q.row = q.q_lo;
+      q.n_kv = q.nq > 0 ? cdiv(f.L, kBN) : 0;
+    } else {
+      q.nq = min(kBM, f.L - q.q_lo);
+      const int start = f.off0 + q.q_lo;
+      q.shift = max(0, start + kBM - T);
+      q.row = start - q.shift;
+      q.n_kv = q.nq > 0 ? (CAUSAL ? cdiv(q.q_lo + q.nq, kBN) : cdiv(f.L, kBN)) : 0;
+    }
   }
+  f.N = max(f.t[0].n_kv, f.t[1].n_kv);
   return f;
 }
 
@@ -137,7 +158,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   using C = FwdCfg<D>;
   const int n_items = p.hdr->n_items;
   const int T = p.hdr->T;
-  uint32_t it = 0, kv = 0, nk_issued = 0, nv_issued = 0;
+  uint32_t itq = 0, nk = 0, nv = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
     const int slot = n & 1;
@@ -146,111 +167,146 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     c->item_slot[slot] = idx < n_items ? idx : -1;
     mbar_arrive(&c->item_full[slot]);
     if (idx >= n_items) break;
-    const FwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
-    if (f.n_kv == 0) continue;
-    if (!mbar_wait(&c->q_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
-    mbar_arrive_expect_tx(&c->q_full, C::kTile);
+    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
+    if (f.N == 0) continue;
+    if (!mbar_wait(&c->q_empty, (itq & 1) ^ 1, &c->abort, p.err)) break;
+    const int ntl = (f.t[0].n_kv > 0 ? 1 : 0) + (f.t[1].n_kv > 0 ? 1 : 0);
+    mbar_arrive_expect_tx(&c->q_full, ntl * C::kTile);
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s)
-      tma_load_3d(smem + C::kQ + s * 16384, tq, &c->q_full, s * 64, f.h, f.q_row);
-    ++it;
-    for (int j = 0; j < f.n_kv; ++j, ++kv) {
-      const int st = kv % C::NS;
-      const uint32_t ph = ((kv / C::NS) & 1) ^ 1;
-      const KvTile kt = kv_tile(f.off0, f.L, j, T);
-      if (!mbar_wait(&c->k_empty[st], ph, &c->abort, p.err)) { ok = false; break; }
-      mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
+    for (int t = 0; t < 2; ++t) {
+      if (f.t[t].n_kv == 0) continue;
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
-                    kt.row);
-      ++nk_issued;
-      if (!mbar_wait(&c->v_empty[st], ph, &c->abort, p.err)) { ok = false; break; }
-      mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
+        tma_load_3d(smem + C::kQ + t * C::kTile + s * 16384, tq, &c->q_full, s * 64, f.h,
+                    f.t[t].row);
+    }
+    ++itq;
+    // Order K0, K1, V0, K2, V1, ...: the MMA needs K(j) and V(j-1) together.
+    for (int j = 0; j <= f.N && ok; ++j) {
+      if (j < f.N) {
+        const int st = nk % C::NSK;
+        const KvTile kt = kv_tile(f.off0, f.L, j, T);
+        if (!mbar_wait(&c->k_empty[st], ((nk / C::NSK) & 1) ^ 1, &c->abort, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
 #pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
-                    kt.row);
-      ++nv_issued;
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
+                      kt.row);
+        ++nk;
+      }
+      if (j >= 1) {
+        const int st = nv % C::NSV;
+        const KvTile kt = kv_tile(f.off0, f.L, j - 1, T);
+        if (!mbar_wait(&c->v_empty[st], ((nv / C::NSV) & 1) ^ 1, &c->abort, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
+#pragma unroll
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
+                      kt.row);
+        ++nv;
+      }
     }
   }
   // Drain: make sure every copy this CTA issued has landed before exit.
-  if (it > 0) drain_wait(&c->q_full, (it - 1) & 1, p.err);
-  for (uint32_t g = nk_issued > C::NS ? nk_issued - C::NS : 0; g < nk_issued; ++g)
-    drain_wait(&c->k_full[g % C::NS], (g / C::NS) & 1, p.err);
-  for (uint32_t g = nv_issued > C::NS ? nv_issued - C::NS : 0; g < nv_issued; ++g)
-    drain_wait(&c->v_full[g % C::NS], (g / C::NS) & 1, p.err);
+  if (itq > 0) drain_wait(&c->q_full, (itq - 1) & 1, p.err);
+  for (uint32_t g = nk > C::NSK ? nk - C::NSK : 0; g < nk; ++g)
+    drain_wait(&c->k_full[g % C::NSK], (g / C::NSK) & 1, p.err);
+  for (uint32_t g = nv > C::NSV ? nv - C::NSV : 0; g < nv; ++g)
+    drain_wait(&c->v_full[g % C::NSV], (g / C::NSV) & 1, p.err);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tbase, int t, uint32_t sq, uint32_t sk) {
+  using C = FwdCfg<D>;
+  const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+    mma_ss(tmem_at(tbase, 0, C::colS(t)), smem_desc_sw128(sq + off, 16, 1024),
+           smem_desc_sw128(sk + off, 16, 1024), id_s, k > 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tbase, int t, uint32_t sv, bool accumulate) {
+  using C = FwdCfg<D>;
+  const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
+#pragma unroll
+  for (int k = 0; k < kBN / 16; ++k) {
+    mma_ts(tmem_at(tbase, 0, C::colO(t)), tmem_at(tbase, 0, C::colS(t) + k * 8),
+           smem_desc_sw128(sv + k * 2048, 16384, 1024), id_pv, accumulate || (k > 0));
+  }
 }
 
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
   const int T = p.hdr->T;
-  const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
-  const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
-  const uint32_t sq = smem_addr(smem + C::kQ);
-  uint32_t it = 0, kv = 0;
-  // PV completions observed so far through o_ready.  A parity wait is only
-  // valid while the barrier is at most one phase ahead of the waiter, so PV_x
-  // is issued only after PV_{x-1} has been observed (free in steady state:
-  // the softmax warps waited for PV_{x-1} before releasing P_x).
-  uint32_t pv_seen = 0;
-  auto wait_pv = [&](uint32_t x) -> bool {
-    if (x < pv_seen) return true;
-    if (!mbar_wait(&c->o_ready, x & 1, &c->abort, p.err)) return false;
-    pv_seen = x + 1;
-    return true;
-  };
+  const uint32_t sq0 = smem_addr(smem + C::kQ);
+  uint32_t itq = 0, nk = 0, nv = 0;
+  uint32_t np[2] = {0, 0};   // P tiles consumed per query tile
+  uint32_t ito[2] = {0, 0};  // items per query tile (for o_free)
   bool ok = true;
   bool issued = false;
   for (uint32_t n = 0; ok; ++n) {
     const int idx = next_item(c, n, false, &ok, p.err);
     if (idx < 0) break;
-    const FwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
-    if (f.n_kv == 0) continue;
-    if (!mbar_wait(&c->q_full, it & 1, &c->abort, p.err)) break;
-    for (int j = 0; j <= f.n_kv && ok; ++j) {
-      if (j < f.n_kv) {
-        const uint32_t g = kv + j;
-        const int st = g % C::NS;
-        const uint32_t buf = g & 1;
-        if (!mbar_wait(&c->k_full[st], (g / C::NS) & 1, &c->abort, p.err)) { ok = false; break; }
-        // S buffer `buf` last held P_{g-2}; its PV must have finished reading it.
-        if (g >= 2 && !wait_pv(g - 2)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sk = smem_addr(smem + C::kK + st * C::kTile);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          mma_ss(tmem_at(tbase, 0, buf * 128), smem_desc_sw128(sq + off, 16, 1024),
-                 smem_desc_sw128(sk + off, 16, 1024), id_s, k > 0);
-        }
-        mma_commit(&c->s_full[buf]);
-        mma_commit(&c->k_empty[st]);
-        if (j == f.n_kv - 1) mma_commit(&c->q_empty);
-        issued = true;
+    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
+    if (f.N == 0) continue;
+    if (!mbar_wait(&c->q_full, itq & 1, &c->abort, p.err)) break;
+    ++itq;
+    for (int j = 0; j <= f.N && ok; ++j) {
+      uint32_t sk = 0, sv = 0;
+      if (j < f.N) {
+        const int st = nk % C::NSK;
+        if (!mbar_wait(&c->k_full[st], (nk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
+        sk = smem_addr(smem + C::kK + st * C::kTile);
       }
       if (j >= 1) {
-        const uint32_t g = kv + j - 1;
-        const int st = g % C::NS;
-        const uint32_t buf = g & 1;
-        if (!mbar_wait(&c->p_full[buf], (g >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
-        if (!mbar_wait(&c->v_full[st], (g / C::NS) & 1, &c->abort, p.err)) { ok = false; break; }
-        if (j == 1 && !mbar_wait(&c->o_free, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
-        if (g >= 1 && !wait_pv(g - 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sv = smem_addr(smem + C::kV + st * C::kTile);
+        const int st = nv % C::NSV;
+        if (!mbar_wait(&c->v_full[st], (nv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
+        sv = smem_addr(smem + C::kV + st * C::kTile);
+      }
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
-          mma_ts(tmem_at(tbase, 0, C::kColO), tmem_at(tbase, 0, buf * 128 + k * 8),
-                 smem_desc_sw128(sv + k * 2048, 16384, 1024), id_pv, (j > 1) || (k > 0));
+      for (int t = 0; t < 2; ++t) {
+        const int nkv = f.t[t].n_kv;
+        if (j >= 1 && j - 1 < nkv) {  // O_t += P_t(j-1) V(j-1)
+          if (!mbar_wait(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
+          ++np[t];
+          if (j == 1 && !mbar_wait(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv<D>(tbase, t, sv, j > 1);
+          mma_commit(&c->o_ready[t]);
         }
-        mma_commit(&c->v_empty[st]);
-        mma_commit(&c->o_ready);
+        if (j < nkv) {  // S_t(j) = Q_t K(j)^T
+          issue_s<D>(tbase, t, sq0 + t * C::kTile, sk);
+          mma_commit(&c->s_full[t]);
+          issued = true;
+        }
+      }
+      if (!ok) break;
+      if (j >= 1) {
+        mma_commit(&c->v_empty[nv % C::NSV]);
+        ++nv;
+      }
+      if (j < f.N) {
+        mma_commit(&c->k_empty[nk % C::NSK]);
+        ++nk;
+        if (j == f.N - 1) mma_commit(&c->q_empty);
       }
     }
-    kv += f.n_kv;
-    ++it;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (f.t[t].n_kv > 0) ++ito[t];
   }
   if (issued) {
     mma_commit(&c->drain);
@@ -258,22 +314,47 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   }
 }
 
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  return static_cast<uint64_t>(__float_as_uint(a)) |
+         (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
+                     __uint_as_float(static_cast<uint32_t>(v >> 32)));
+}
+// (a0, a1) * (b0, b1) + (c0, c1) with the paired fp32 FMA of sm_100+.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
-  const int r = threadIdx.x;  // row of the tile == TMEM lane
-  const int warp = r >> 5;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const int t = threadIdx.x >> 7;   // query tile of this warpgroup
+  const int r = threadIdx.x & 127;  // row of the tile == TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t ts = tbase + lane_base + C::colS(t);
+  const uint32_t to = tbase + lane_base + C::colO(t);
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
-  uint32_t it = 0, kv = 0;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  uint32_t u = 0;  // S tiles of this query tile processed so far (all items)
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
     const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
-    const FwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
-    const int qi = f.q_lo - f.q_shift + r;  // local query index of this row
-    const bool row_valid = r >= f.q_shift && r < f.q_shift + f.nq;
+    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
+    const QTile q = t == 0 ? f.t[0] : f.t[1];  // no dynamic indexing (keeps f in registers)
+    if (q.nq <= 0) continue;
+    const int qi = q.q_lo - q.shift + r;  // local query index of this row
+    const bool row_valid = r >= q.shift && r < q.shift + q.nq;
     __nv_bfloat16* orow;
     float* lrow;
     if (BCAST) {
@@ -283,20 +364,17 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       orow = p.out + ((static_cast<long long>(f.off0) + qi) * p.H + f.h) * D;
       lrow = p.lse + static_cast<long long>(f.h) * T + f.off0 + qi;
     }
-    if (f.n_kv == 0) {  // empty broadcast sequence: O = 0, LSE = -inf
+    if (q.n_kv == 0) {  // empty broadcast sequence: O = 0, LSE = -inf
       if (row_valid) {
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         *lrow = -INFINITY;
       }
       continue;
     }
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; j < f.n_kv; ++j) {
-      const uint32_t g = kv + j;
-      const uint32_t buf = g & 1;
-      if (!mbar_wait_warp(&c->s_full[buf], (g >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+    float m_used = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < q.n_kv; ++j, ++u) {
+      if (!mbar_wait_warp(&c->s_full[t], u & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t ts = tbase + lane_base + buf * 128;
       uint32_t raw[4][32];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) tmem_ld32(ts + ch * 32, raw[ch]);
@@ -309,7 +387,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       const KvTile kt = kv_tile(f.off0, f.L, j, T);
       const int key0 = j * kBN - kt.shift;  // local key index of column 0
       const bool need_mask =
-          kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > f.q_lo - f.q_shift);
+          kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > q.q_lo - q.shift);
       if (need_mask) {
         // Peeled tail: only the ragged last tile (and the diagonal tile when
         // causal) pays for the per-element mask.
@@ -329,30 +407,42 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
         mx2 = fmaxf(mx2, s[cc + 2]);
         mx3 = fmaxf(mx3, s[cc + 3]);
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m_run, mx * sl2);
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      // Raise the exponent base only when the max grew by more than 2^8.
+      const bool raise = m_tile > m_used + kRescaleLog2;
+      const float m_new = raise ? m_tile : m_used;
+      const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;
+      m_used = m_new;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[4][16];
+      const uint64_t negm = f2_pack(-m_use, -m_use);
+      uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-      for (int cc = 0; cc < 128; cc += 2) {
-        const float p0 = ex2_approx(fmaf(s[cc], sl2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[cc + 1], sl2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
-        pk[cc / 32][(cc % 32) / 2] = pack_bf16x2(p0, p1);
+      for (int ch = 0; ch < 4; ++ch) {
+        // 32 columns -> 16 packed bf16 pairs, stored to TMEM right away so
+        // that only one chunk of P is live in registers.
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const int cc = ch * 32 + i;
+          const float2 x0 = f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), sl2x2, negm));
+          const float2 x1 = f2_unpack(ffma2(f2_pack(s[cc + 2], s[cc + 3]), sl2x2, negm));
+          const float p0 = ex2_approx(x0.x), p1 = ex2_approx(x0.y);
+          const float p2 = ex2_approx(x1.x), p3 = ex2_approx(x1.y);
+          acc0 = fadd2(acc0, f2_pack(p0, p1));
+          acc1 = fadd2(acc1, f2_pack(p2, p3));
+          pk[i / 2] = pack_bf16x2(p0, p1);
+          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(ts + ch * 16, pk);
       }
-      l_run = l_run * alpha + (sum0 + sum1);
-      m_run = m_new;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_st16(ts + ch * 16, pk[ch]);
+      const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+      l_run = l_run * alpha + ((a0.x + a0.y) + (a1.x + a1.y));
       if (j > 0) {
-        // Correction: rescale the running O once PV_{g-1} has landed.
-        if (!mbar_wait_warp(&c->o_ready, (g - 1) & 1, &c->abort, p.err)) { ok = false; break; }
+        // PV of the previous tile has landed before S of this one (issue
+        // order); observe it, then correct O if any row raised its max.
+        if (!mbar_wait_warp(&c->o_ready[t], (u - 1) & 1, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t to = tbase + lane_base + C::kColO;
+        if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
@@ -366,15 +456,13 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&c->p_full[buf]);
+      mbar_arrive(&c->p_full[t]);
     }
     if (!ok) break;
-    kv += f.n_kv;
     // Epilogue: O / l in bf16 and the natural-log LSE.
-    if (!mbar_wait_warp(&c->o_ready, (kv - 1) & 1, &c->abort, p.err)) break;
+    if (!mbar_wait_warp(&c->o_ready[t], (u - 1) & 1, &c->abort, p.err)) break;
     tc_fence_after();
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    const uint32_t to = tbase + lane_base + C::kColO;
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t o[32];
@@ -392,10 +480,9 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
         dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
       }
     }
-    if (row_valid) *lrow = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+    if (row_valid) *lrow = l_run > 0.f ? (m_used + lg2_approx(l_run)) * kLn2 : -INFINITY;
     tc_fence_before();
-    mbar_arrive(&c->o_free);
-    ++it;
+    mbar_arrive(&c->o_free[t]);
   }
 }
 
@@ -414,20 +501,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&c->q_full, 1);
     mbar_init(&c->q_empty, 1);
-    for (int i = 0; i < C::NS; ++i) {
+    for (int i = 0; i < C::NSK; ++i) {
       mbar_init(&c->k_full[i], 1);
       mbar_init(&c->k_empty[i], 1);
+    }
+    for (int i = 0; i < C::NSV; ++i) {
       mbar_init(&c->v_full[i], 1);
       mbar_init(&c->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->s_full[i], 1);
       mbar_init(&c->p_full[i], kBM);
+      mbar_init(&c->o_ready[i], 1);
+      mbar_init(&c->o_free[i], kBM);
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 5);  // 4 softmax warps + the MMA thread
+      mbar_init(&c->item_empty[i], 9);  // 8 softmax warps + the MMA thread
     }
-    mbar_init(&c->o_ready, 1);
-    mbar_init(&c->o_free, kBM);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();
@@ -446,7 +535,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
 
-  if (warp < 4) {
+  if (warp < 8) {
     softmax_role<D, CAUSAL, BCAST>(p, c, tbase);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, p, smem, c);
@@ -468,6 +557,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   using C = FwdCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(FwdCtl) <= 512, "control block");
+  static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
   auto kern = fwd_kernel<D, CAUSAL, BCAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
