@@ -314,8 +314,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="draw this many sequences instead of the workload's B "
+                         "(same length distribution; for profiling captures)")
     args = ap.parse_args()
-    x = W.make_inputs(W.WORKLOADS[args.workload])
+    w = W.WORKLOADS[args.workload]
+    lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
+    x = W.make_inputs(w, lengths=lengths)
     if args.impl == "reference":
         run_reference(args, x, args.workload)
     else:

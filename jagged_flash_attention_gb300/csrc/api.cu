@@ -208,7 +208,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   uint8_t* base = static_cast<uint8_t*>(scratch);
   WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
   Item* items = reinterpret_cast<Item*>(base + items_off);
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0,
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0, kFwdRows,
                  items, (int)cap, hdr, ds->err};
   e = launch_sched(sp, stream);
   if (e == cudaSuccess) {
@@ -228,6 +228,89 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(ds, stream);
+}
+
+// Self-attention backward: dK/dV pass (K/V-block outer) and dQ pass
+// (query-tile outer, dQ accumulated on chip), so no fp32 dQ accumulator is
+// needed.  Work lists, Delta and the two headers are the only scratch.
+jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const void* k,
+                       const void* v, const int32_t* offsets, const void* out, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, cudaStream_t stream) {
+  jfa_status st;
+  const long long cap_kv = (long long)s.H * s.B * cdivll(s.max_len, kBN);
+  const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kBM);
+  if (cap_kv >= (1LL << 31) || cap_q >= (1LL << 31))
+    return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  const long long delta_elems = (long long)s.H * s.Tcap;
+  size_t off = 0;
+  const size_t hkv_off = off;
+  off = align256(off + 256 + cap_kv * sizeof(Item));
+  const size_t hq_off = off;
+  off = align256(off + 256 + cap_q * sizeof(Item));
+  const size_t delta_off = off;
+  off = align256(off + delta_elems * sizeof(float));
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_rows(&tdo, dout, s.D, s.H, s.Tcap, "dout")) != JFA_OK) return st;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr_kv = reinterpret_cast<WorkHeader*>(base + hkv_off);
+  Item* items_kv = reinterpret_cast<Item*>(base + hkv_off + 256);
+  WorkHeader* hdr_q = reinterpret_cast<WorkHeader*>(base + hq_off);
+  Item* items_q = reinterpret_cast<Item*>(base + hq_off + 256);
+  float* delta = reinterpret_cast<float*>(base + delta_off);
+  SchedParams sk{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 1, kBM,
+                 items_kv, (int)cap_kv, hdr_kv, ds->err};
+  SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kBM,
+                 items_q, (int)cap_q, hdr_q, ds->err};
+  BwdParams bp;
+  memset(&bp, 0, sizeof(bp));
+  bp.offsets = offsets;
+  bp.B = s.B;
+  bp.H = s.H;
+  bp.Lq = 0;
+  bp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+  bp.scale = s.scale;
+  bp.lse = lse;
+  bp.delta = delta;
+  bp.dq = static_cast<__nv_bfloat16*>(dq);
+  bp.dk = static_cast<__nv_bfloat16*>(dk);
+  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.err = ds->err;
+  e = launch_sched(sk, stream);
+  if (e == cudaSuccess) e = launch_sched(sq, stream);
+  if (e == cudaSuccess) {
+    PrepParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.out = static_cast<const __nv_bfloat16*>(out);
+    pp.dout = static_cast<const __nv_bfloat16*>(dout);
+    pp.delta = delta;
+    pp.B = s.B;
+    pp.H = s.H;
+    pp.D = s.D;
+    pp.hdr = hdr_kv;
+    e = launch_prep(pp, ds->sms, stream);
+  }
+  if (e == cudaSuccess) {
+    bp.items = items_kv;
+    bp.hdr = hdr_kv;
+    e = launch_bwd_kv(s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_kv),
+                      stream);
+  }
+  if (e == cudaSuccess) {
+    bp.items = items_q;
+    bp.hdr = hdr_q;
+    e = launch_bwd_q(s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_q),
+                     stream);
+  }
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
   return finish(ds, stream);
 }
@@ -254,6 +337,8 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     }
     return finish(ds, stream);
   }
+  if (!s.broadcast)
+    return do_bwd_self(ds, s, q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
   const long long cap = (long long)s.H * s.B * cdivll(s.max_len, kBN);
   if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");
   const int grid = (int)std::min<long long>(ds->sms, cap);
@@ -286,7 +371,7 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
   Item* items = reinterpret_cast<Item*>(base + items_off);
   float* delta = reinterpret_cast<float*>(base + delta_off);
   float* acc = reinterpret_cast<float*>(base + acc_off);
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1,
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1, kBM,
                  items, (int)cap, hdr, ds->err};
   e = launch_sched(sp, stream);
   if (e == cudaSuccess) {
@@ -301,6 +386,7 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     pp.D = s.D;
     pp.Lq = s.Lq;
     pp.broadcast = s.broadcast;
+    pp.zero_self_acc = 0;
     pp.hdr = hdr;
     e = launch_prep(pp, ds->sms, stream);
   }
@@ -317,6 +403,7 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     bp.dq_acc = acc;
     bp.dq_shards = shards;
     bp.shard_stride = shard_elems;
+    bp.dq = static_cast<__nv_bfloat16*>(dq);
     bp.dk = static_cast<__nv_bfloat16*>(dk);
     bp.dv = static_cast<__nv_bfloat16*>(dv);
     bp.items = items;
@@ -553,7 +640,7 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   Item* items = reinterpret_cast<Item*>(d->scratch + items_off);
   // The scheduler rewrites the header (item count, T, ticket = 0) and every
   // item the forward kernel reads, so nothing left by a previous call leaks.
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0,
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0, kFwdRows,
                  items, (int)cap, hdr, d->err};
   e = launch_sched(sp, stream);
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");

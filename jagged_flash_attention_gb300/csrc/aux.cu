@@ -14,13 +14,14 @@ constexpr int kMaxBuckets = 1024;
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Tiles of sequence b that become work items (one item per head and tile).
-//  forward:  256-row query tiles (two 128-row MMA tiles; self: of the
-//            sequence; broadcast: of the dense Q)
+//  query items: tiles of `qrows` query rows (forward: 256 = two 128-row MMA
+//            tiles; self-attention dQ pass: 128); self: of the sequence,
+//            broadcast: of the dense Q
 //  backward: key/value blocks of the sequence
 __device__ __forceinline__ int n_tiles(const SchedParams& p, int L) {
   if (p.backward) return cdiv(L, kBN);
   // broadcast: every sequence, even an empty one, owns its output rows
-  return p.broadcast ? cdiv(p.Lq, kFwdRows) : cdiv(L, kFwdRows);
+  return p.broadcast ? cdiv(p.Lq, p.qrows) : cdiv(L, p.qrows);
 }
 
 // Cost bucket of sequence b: work of its longest item, in tile units.
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
     }
   }
   // zero the fp32 dQ accumulator
-  const long long n = p.broadcast ? p.dq_acc_elems_bcast : (ok ? (long long)T * p.H * p.D : 0);
+  const long long n = p.broadcast ? p.dq_acc_elems_bcast
+                                  : (ok && p.zero_self_acc ? (long long)T * p.H * p.D : 0);
   float4* z = reinterpret_cast<float4*>(p.dq_acc);
   for (long long i = gtid; i < n / 4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }

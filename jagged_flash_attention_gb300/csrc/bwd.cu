@@ -1,38 +1,43 @@
-// Jagged flash attention backward (dK/dV main loop + dQ reduction) for sm_103a.
+// Jagged flash attention backward for broadcast-Q (dK/dV main loop + dQ
+// reduction across the batch) for sm_103a.
 //
 // Method: "Optimizing Jagged Flash Attention with TLX" (pytorch.org):
 //  * "Scheduling jagged tiles across SMs": the backward loops over K/V
 //    blocks on the outside and Q tiles on the inside; work items are the
 //    valid (sequence, head, K/V block) tiles, block-innermost.
 //  * "2-CTA collaborative MMA": five GEMMs per K/V block produce dQ, dK, dV.
-//  * "Multi-stage dQ staging": dQ partials of every K/V block are summed in
-//    fp32 across CTAs (broadcast-Q: across the whole batch); here each CTA
-//    adds into one of several fp32 shards with vector red.global.add and a
-//    separate kernel sums the shards and casts to bf16.
+//  * section 2.1: a dedicated dQ-reduction role next to the load, MMA and
+//    softmax roles; "Multi-stage dQ staging" / "Early tensor-memory
+//    release": the dQ partial of every K/V block is summed in fp32 across
+//    CTAs (broadcast-Q: across the whole batch, into one of several shards)
+//    while the MMA warp already works on the next Q tile.
 //  * "Loop peeling": masks cost nothing on interior tiles; invalid query
 //    columns are removed through an LSE of +inf and invalid key rows through
 //    a per-thread predicate, so only causal diagonal tiles test elements.
 //
-// Per K/V block (128 keys) and Q tile (128 queries), with scores kept
-// transposed (keys on TMEM lanes) so that P^T and dS^T can feed the next
-// MMAs straight from tensor memory:
-//   S^T  = K Q^T            (SS, K-major / K-major)
-//   dP^T = V dO^T           (SS)
-//   P^T  = exp2(S^T * scale*log2e - LSE*log2e),  dS^T = P^T (dP^T - Delta)
+// Per K/V block (128 keys) and Q tile (128 queries), scores are kept
+// transposed (keys on TMEM lanes):
+//   S^T  = K Q^T            (SS, K-major / K-major)        -> TMEM [0,128)
+//   dP^T = V dO^T           (SS)                           -> TMEM [128,256)
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e) -> TMEM (bf16, over S^T)
+//   dS   = P (dP - Delta)                      -> SMEM (bf16, swizzled)
 //   dV  += P^T dO           (TS: A = P^T in TMEM, B = dO MN-major)
-//   dK  += dS^T Q           (TS: A = dS^T in TMEM, B = Q MN-major)
-//   dQ   = dS K             (SS: A = dS MN-major from SMEM, B = K MN-major)
-// CTA = 6 warps: warps 0-3 score/gradient math, dQ drain and dK/dV epilogue
-// (thread r owns TMEM lane r), warp 4 TMA producer, warp 5 MMA issuer.
+//   dK  += dS^T Q           (SS: A = dS^T K-major, B = Q MN-major)
+//   D=128: dQ^T = K^T dS^T  (SS, both MN-major) -> TMEM [128,256), head dims
+//          on lanes so that each warp of the reduction adds whole 128-byte
+//          lines of the fp32 accumulator
+//   D=64:  dQ = dS K        (SS, both MN-major) -> TMEM [384,448)
+// CTA = 10 warps: warps 0-3 score/gradient math and the dK/dV epilogue,
+// warps 4-7 dQ reduction, warp 8 TMA producer, warp 9 MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -50,7 +55,8 @@ struct BwdCfg {
   static constexpr int kSmem = kCtl + 512;
   static constexpr uint32_t kColS = 0, kColDP = 128;
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
-  static constexpr uint32_t kColDQ = (D == 128) ? 0 : 384;  // D=128: reuses S
+  static constexpr bool kDqT = (D == 128);                  // dQ computed transposed
+  static constexpr uint32_t kColDQ = kDqT ? kColDP : 384;  // D=128: reuses dP^T
 };
 
 struct BwdCtl {
@@ -59,8 +65,7 @@ struct BwdCtl {
   uint64_t st_full, ds_full;
   uint64_t dq_full, dq_empty;
   uint64_t dkdv_full, dkdv_empty;
-  uint64_t tmp;
-  uint64_t stat_full;  // LSE/Delta of the current Q tile staged by all 128 threads
+  uint64_t stat_full;  // LSE/Delta of the current Q tile staged by all 128 math threads
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item_slot[2];
@@ -73,8 +78,8 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 struct RowBox {
   int row, shift, n;  // TMA row coordinate, rows moved back, valid rows
 };
-// 128-row box starting at packed row `start` of a sequence of `len` rows
-// remaining; moved back so it never reads past row T.
+// 128-row box starting at packed row `start` of a sequence with `remaining`
+// rows left; moved back so it never reads past row T.
 __device__ __forceinline__ RowBox row_box(int start, int remaining, int T) {
   RowBox r;
   r.shift = max(0, start + 128 - T);
@@ -88,6 +93,7 @@ struct BwdTile {
   int off0, L;
   RowBox kt;   // keys of this block
   int t0, nt;  // first query tile and count
+  int rot;     // the Q tiles are visited starting at t0 + rot (mod nt)
 };
 
 template <bool BCAST, bool CAUSAL>
@@ -103,14 +109,24 @@ __device__ __forceinline__ BwdTile decode(const BwdParams& p, int idx, int T) {
   if (BCAST) {
     f.t0 = 0;
     f.nt = cdiv(p.Lq, kBM);
+    f.rot = (f.b + f.kb) % f.nt;
   } else {
     f.t0 = CAUSAL ? (f.kb * kBN) / kBM : 0;
     f.nt = cdiv(f.L, kBM) - f.t0;
+    // Concurrent K/V blocks of one sequence start on different Q tiles so
+    // their dQ additions land on different rows.
+    f.rot = CAUSAL ? 0 : f.kb % f.nt;
   }
   return f;
 }
 
-// Query tile t of the item: box (self) and local index of its row 0.
+__device__ __forceinline__ int q_tile_at(const BwdTile& f, int i) {
+  int t = f.rot + i;
+  if (t >= f.nt) t -= f.nt;
+  return f.t0 + t;
+}
+
+// Query tile t of the item: box and valid rows.
 template <bool BCAST>
 __device__ __forceinline__ RowBox q_box(const BwdParams& p, const BwdTile& f, int t, int T) {
   if (BCAST) {
@@ -181,7 +197,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         ok = false;
         break;
       }
-      const int t = f.t0 + i;
+      const int t = q_tile_at(f, i);
       const RowBox qb = q_box<BCAST>(p, f, t, T);
       mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile);
 #pragma unroll
@@ -208,8 +224,10 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
   using C = BwdCfg<D>;
   const int T = p.hdr->T;
   const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-  const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
-  const uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS MN-major)
+  const uint32_t id_dv = idesc_bf16_f32(128, D, false, true);     // dV (A = P^T in TMEM)
+  const uint32_t id_dk = idesc_bf16_f32(128, D, false, true);     // dK (A = dS^T K-major)
+  const uint32_t id_dq = C::kDqT ? idesc_bf16_f32(128, 128, true, true)  // dQ^T
+                                 : idesc_bf16_f32(128, D, true, true);   // dQ
   const uint32_t sk = smem_addr(smem + C::kK), sv = smem_addr(smem + C::kV);
   const uint32_t sds = smem_addr(smem + C::kDS);
   uint32_t it = 0, gq = 0;
@@ -225,18 +243,21 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
       const uint32_t sq = smem_addr(smem + C::kQ + st * C::kTile);
       const uint32_t sdo = smem_addr(smem + C::kDO + st * C::kTile);
       if (!mbar_wait(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
-      // D=128: dQ_{g-1} lives in the S columns; it must be drained first.
-      if (D == 128 && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
+      // S^T overwrites P^T of the previous tile, read by its dV MMA issued
+      // earlier (MMAs of one CTA execute in issue order).
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
         mma_ss(tmem_at(tbase, 0, C::kColS), smem_desc_sw128(sk + off, 16, 1024),
                smem_desc_sw128(sq + off, 16, 1024), id_st, k > 0);
       }
+      // D=128: dQ^T of the previous tile lives in the dP^T columns.
+      if (C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
@@ -251,27 +272,28 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 #pragma unroll
       for (int k = 0; k < kBM / 16; ++k) {
         mma_ts(tmem_at(tbase, 0, C::kColDV), tmem_at(tbase, 0, C::kColS + k * 8),
-               smem_desc_sw128(sdo + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+               smem_desc_sw128(sdo + k * 2048, 16384, 1024), id_dv, (i > 0) || (k > 0));
       }
 #pragma unroll
       for (int k = 0; k < kBM / 16; ++k) {
-        mma_ts(tmem_at(tbase, 0, C::kColDK), tmem_at(tbase, 0, C::kColDP + k * 8),
-               smem_desc_sw128(sq + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+        mma_ss(tmem_at(tbase, 0, C::kColDK), smem_desc_sw128(sds + off, 16, 1024),
+               smem_desc_sw128(sq + k * 2048, 16384, 1024), id_dk, (i > 0) || (k > 0));
       }
       mma_commit(&c->qdo_empty[st]);
-      if (D == 128) {
-        // dQ overwrites the S columns that the dV MMA reads P^T from.
-        mma_commit(&c->tmp);
-        if (!mbar_wait(&c->tmp, g & 1, &c->abort, p.err)) { ok = false; break; }
-      } else if (g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+      if (!C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < kBN / 16; ++k) {
-        mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sds + k * 2048, 16384, 1024),
-               smem_desc_sw128(sk + k * 2048, 16384, 1024), id_dq, k > 0);
+        if (C::kDqT)
+          mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sk + k * 2048, 16384, 1024),
+                 smem_desc_sw128(sds + k * 2048, 16384, 1024), id_dq, k > 0);
+        else
+          mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sds + k * 2048, 16384, 1024),
+                 smem_desc_sw128(sk + k * 2048, 16384, 1024), id_dq, k > 0);
       }
       mma_commit(&c->dq_full);
     }
@@ -289,7 +311,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t tbase) {
   using C = BwdCfg<D>;
-  const int r = threadIdx.x;  // TMEM lane: key row for S/dP/dK/dV, query row for dQ
+  const int r = threadIdx.x;  // TMEM lane = key row of the block
   const int warp = r >> 5;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
   const int T = p.hdr->T;
@@ -297,7 +319,6 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t
   float* s_lse = reinterpret_cast<float*>(smem + C::kStat);  // [2][128]
   float* s_dlt = s_lse + 2 * kBM;                            // [2][128]
   uint8_t* sds = smem + C::kDS;
-  const int shard = BCAST ? static_cast<int>(blockIdx.x % p.dq_shards) : 0;
   uint32_t it = 0, gq = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
@@ -308,7 +329,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t
     const bool key_ok = r >= f.kt.shift && r < f.kt.shift + f.kt.n;
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
-      const int t = f.t0 + i;
+      const int t = q_tile_at(f, i);
       const RowBox qb = q_box<BCAST>(p, f, t, T);
       const int q0 = t * kBM - qb.shift;  // local query index of column 0
       // Stage LSE*log2e and Delta of this Q tile's rows (thread r: row r).
@@ -357,7 +378,6 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t
           dk[cc / 2] = pack_bf16x2(d0, d1);
         }
         tmem_st16(tbase + lane_base + C::kColS + ch * 16, pk);
-        tmem_st16(tbase + lane_base + C::kColDP + ch * 16, dk);
         // dS row r (queries ch*32 .. ch*32+31) into the swizzled SMEM tile.
         uint8_t* slab = sds + (ch >> 1) * 16384 + r * 128;
 #pragma unroll
@@ -371,31 +391,6 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&c->ds_full);
-      // dQ drain: lane r is query row r of dQ = dS K.
-      if (!mbar_wait_warp(&c->dq_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
-      {
-        const int qi = q0 + r;
-        const bool q_ok = r >= qb.shift && r < qb.shift + qb.n;
-        float* dst = BCAST ? p.dq_acc + shard * p.shard_stride +
-                                 (static_cast<long long>(qi) * p.H + f.h) * D
-                           : p.dq_acc + (static_cast<long long>(f.off0 + qi) * p.H + f.h) * D;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t q[32];
-          tmem_ld32(tbase + lane_base + C::kColDQ + ch * 32, q);
-          tmem_wait_ld();
-          if (q_ok) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              atomicAdd(reinterpret_cast<float4*>(dst + ch * 32 + 4 * u),
-                        make_float4(__uint_as_float(q[4 * u]), __uint_as_float(q[4 * u + 1]),
-                                    __uint_as_float(q[4 * u + 2]), __uint_as_float(q[4 * u + 3])));
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&c->dq_empty);
     }
     if (!ok) break;
     // Item epilogue: dV and scale * dK rows of this K/V block.
@@ -431,6 +426,72 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t
   }
 }
 
+// dQ reduction role (warps 4-7): drains each Q tile's dQ partial from TMEM
+// into the fp32 accumulator while the other roles move on.
+template <int D, bool CAUSAL, bool BCAST>
+__device__ void dq_role(const BwdParams& p, BwdCtl* c, uint32_t tbase) {
+  using C = BwdCfg<D>;
+  const int r = threadIdx.x - 128;  // TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
+  const int T = p.hdr->T;
+  const int shard = BCAST ? static_cast<int>(blockIdx.x % p.dq_shards) : 0;
+  float* acc = p.dq_acc + (BCAST ? shard * p.shard_stride : 0);
+  uint32_t gq = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    const int idx = next_item(c, n, true, &ok, p.err);
+    if (idx < 0) break;
+    const BwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
+    for (int i = 0; i < f.nt; ++i, ++gq) {
+      const uint32_t g = gq;
+      const int t = q_tile_at(f, i);
+      const RowBox qb = q_box<BCAST>(p, f, t, T);
+      const int q0 = t * kBM - qb.shift;  // local query index of column / lane 0
+      // Row (query) index into the accumulator for local query qi.
+      const long long rbase = BCAST ? 0 : f.off0;
+      if (!mbar_wait_warp(&c->dq_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      if (C::kDqT) {
+        // Lane r holds head dim r of every query column: each warp adds 32
+        // consecutive floats (one 128-byte line) per query row.
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_base + C::kColDQ + ch * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const int col = ch * 32 + cc;
+            if (col >= qb.shift && col < qb.shift + qb.n) {  // warp-uniform
+              float* dst = acc + ((rbase + q0 + col) * p.H + f.h) * D + r;
+              atomicAdd(dst, __uint_as_float(v[cc]));
+            }
+          }
+        }
+      } else {
+        // Lane r holds query row r: 16-byte vector additions along the row.
+        const bool q_ok = r >= qb.shift && r < qb.shift + qb.n;
+        float* dst = acc + ((rbase + q0 + r) * p.H + f.h) * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_base + C::kColDQ + ch * 32, v);
+          tmem_wait_ld();
+          if (q_ok) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              atomicAdd(reinterpret_cast<float4*>(dst + ch * 32 + 4 * u),
+                        make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&c->dq_empty);
+    }
+  }
+}
+
 template <int D, bool CAUSAL, bool BCAST>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -451,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&c->qdo_full[i], 1);
       mbar_init(&c->qdo_empty[i], 1);
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 5);
+      mbar_init(&c->item_empty[i], 9);  // 4 math + 4 dQ warps + the MMA thread
     }
     mbar_init(&c->st_full, 1);
     mbar_init(&c->ds_full, kBM);
@@ -459,7 +520,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c->dq_empty, kBM);
     mbar_init(&c->dkdv_full, 1);
     mbar_init(&c->dkdv_empty, kBM);
-    mbar_init(&c->tmp, 1);
     mbar_init(&c->stat_full, kBM);
     mbar_init(&c->drain, 1);
     c->abort = 0;
@@ -481,6 +541,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tbase = c->tmem_base;
   if (warp < 4) {
     math_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+  } else if (warp < 8) {
+    dq_role<D, CAUSAL, BCAST>(p, c, tbase);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
@@ -510,17 +572,14 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 }  // namespace
 
+// Broadcast-Q backward (self-attention uses the two-pass kernels of
+// bwd_kv.cu and bwd_q.cu, which need no dQ accumulator).
 cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const BwdParams& p, int grid, cudaStream_t s) {
-  if (D == 128) {
-    if (bcast) return launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, grid, s);
-    if (causal) return launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, grid, s);
-    return launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, grid, s);
-  }
-  if (bcast) return launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, grid, s);
-  if (causal) return launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, grid, s);
-  return launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, grid, s);
+  if (!bcast || causal) return cudaErrorInvalidValue;
+  if (D == 128) return launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, grid, s);
+  return launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, grid, s);
 }
 
 }  // namespace jfa

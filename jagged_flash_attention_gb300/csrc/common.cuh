@@ -33,6 +33,7 @@ struct SchedParams {
   const int32_t* offsets;
   int B, H, Lq, max_len;
   int causal, broadcast, backward;
+  int qrows;  // query rows per item when backward == 0 (forward: 256, dQ pass: 128)
   Item* items;
   int capacity;
   WorkHeader* hdr;
@@ -60,6 +61,7 @@ struct BwdParams {
   float* dq_acc;       // fp32 accumulator: self [Tcap,H,D]; broadcast [shards,Lq,H,D]
   int dq_shards;       // broadcast only
   long long shard_stride;  // elements per shard
+  __nv_bfloat16* dq;  // self-attention dQ pass: written directly
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const Item* items;
@@ -72,7 +74,8 @@ struct PrepParams {
   const __nv_bfloat16* dout;
   float* delta;
   float* dq_acc;
-  long long dq_acc_elems_bcast;  // broadcast: elements to zero; self: 0 (uses T)
+  long long dq_acc_elems_bcast;  // broadcast: elements to zero
+  int zero_self_acc;             // self-attention: zero T*H*D accumulator elements
   int B, H, D, Lq, broadcast;
   const WorkHeader* hdr;
 };
@@ -93,6 +96,12 @@ cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, co
 cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const BwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                          int grid, cudaStream_t s);
+cudaError_t launch_bwd_q(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                         int grid, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams& p, int sms, cudaStream_t s);
 cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s);
 cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
