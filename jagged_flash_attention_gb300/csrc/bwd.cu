@@ -228,8 +228,16 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
   const uint32_t id_dk = idesc_bf16_f32(128, D, false, true);     // dK (A = dS^T K-major)
   const uint32_t id_dq = C::kDqT ? idesc_bf16_f32(128, 128, true, true)  // dQ^T
                                  : idesc_bf16_f32(128, D, true, true);   // dQ
-  const uint32_t sk = smem_addr(smem + C::kK), sv = smem_addr(smem + C::kV);
-  const uint32_t sds = smem_addr(smem + C::kDS);
+  // Descriptors built once; per tile and K step only adds remain.
+  const uint64_t dk_k = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dk_m = smem_desc_sw128(smem_addr(smem + C::kK), 16384, 1024);
+  const uint64_t dv_k = smem_desc_sw128(smem_addr(smem + C::kV), 16, 1024);
+  const uint64_t dq_k0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
+  const uint64_t dq_m0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16384, 1024);
+  const uint64_t ddo_k0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16, 1024);
+  const uint64_t ddo_m0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16384, 1024);
+  const uint64_t dds_k = smem_desc_sw128(smem_addr(smem + C::kDS), 16, 1024);
+  const uint64_t dds_m = smem_desc_sw128(smem_addr(smem + C::kDS), 16384, 1024);
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
@@ -240,8 +248,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
       const int st = g % C::NSQ;
-      const uint32_t sq = smem_addr(smem + C::kQ + st * C::kTile);
-      const uint32_t sdo = smem_addr(smem + C::kDO + st * C::kTile);
+      const uint32_t so = st * C::kTile;
+      const uint64_t dq_k = desc_add(dq_k0, so), dq_m = desc_add(dq_m0, so);
+      const uint64_t ddo_k = desc_add(ddo_k0, so), ddo_m = desc_add(ddo_m0, so);
       if (!mbar_wait(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
       // S^T overwrites P^T of the previous tile, read by its dV MMA issued
@@ -249,8 +258,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColS), smem_desc_sw128(sk + off, 16, 1024),
-               smem_desc_sw128(sq + off, 16, 1024), id_st, k > 0);
+        mma_ss(tbase + C::kColS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
       }
       // D=128: dQ^T of the previous tile lives in the dP^T columns.
       if (C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
@@ -261,8 +269,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColDP), smem_desc_sw128(sv + off, 16, 1024),
-               smem_desc_sw128(sdo + off, 16, 1024), id_st, k > 0);
+        mma_ss(tbase + C::kColDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
       }
       mma_commit(&c->st_full);
       issued = true;
@@ -270,15 +277,14 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
       if (i == 0 && !mbar_wait(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < kBM / 16; ++k) {
-        mma_ts(tmem_at(tbase, 0, C::kColDV), tmem_at(tbase, 0, C::kColS + k * 8),
-               smem_desc_sw128(sdo + k * 2048, 16384, 1024), id_dv, (i > 0) || (k > 0));
-      }
+      for (int k = 0; k < kBM / 16; ++k)
+        mma_ts(tbase + C::kColDV, tbase + C::kColS + k * 8, desc_add(ddo_m, k * 2048), id_dv,
+               (i > 0) || (k > 0));
 #pragma unroll
       for (int k = 0; k < kBM / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColDK), smem_desc_sw128(sds + off, 16, 1024),
-               smem_desc_sw128(sq + k * 2048, 16384, 1024), id_dk, (i > 0) || (k > 0));
+        mma_ss(tbase + C::kColDK, desc_add(dds_k, off), desc_add(dq_m, k * 2048), id_dk,
+               (i > 0) || (k > 0));
       }
       mma_commit(&c->qdo_empty[st]);
       if (!C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
@@ -289,11 +295,11 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 #pragma unroll
       for (int k = 0; k < kBN / 16; ++k) {
         if (C::kDqT)
-          mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sk + k * 2048, 16384, 1024),
-                 smem_desc_sw128(sds + k * 2048, 16384, 1024), id_dq, k > 0);
+          mma_ss(tbase + C::kColDQ, desc_add(dk_m, k * 2048), desc_add(dds_m, k * 2048), id_dq,
+                 k > 0);
         else
-          mma_ss(tmem_at(tbase, 0, C::kColDQ), smem_desc_sw128(sds + k * 2048, 16384, 1024),
-                 smem_desc_sw128(sk + k * 2048, 16384, 1024), id_dq, k > 0);
+          mma_ss(tbase + C::kColDQ, desc_add(dds_m, k * 2048), desc_add(dk_m, k * 2048), id_dq,
+                 k > 0);
       }
       mma_commit(&c->dq_full);
     }

@@ -13,13 +13,16 @@
 //   dS^T = P^T (dP^T - Delta),                bf16 over dP^T's columns
 //   dV  += P^T dO       (TS, B = dO MN-major)
 //   dK  += dS^T Q       (TS, B = Q MN-major)
-// The next S^T / dP^T overwrite P^T / dS^T right after the dV / dK MMAs that
-// read them (MMAs of one CTA execute in issue order), so the tensor pipe
-// never waits for TMEM to be released.
+// The score math is split into a P part (needs S^T) and a dS part (needs
+// dP^T), and the MMAs of consecutive query tiles are interleaved:
+//   dV(g), S(g+1), dK(g), dP(g+1), dV(g+1), ...
+// so the P part of tile g+1 runs under dK(g) + dP(g+1) and its dS part under
+// dV(g+1) + S(g+2).  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) right after
+// the dV / dK MMAs that read them (MMAs of one CTA execute in issue order).
 //
 // CTA = 10 warps: warps 0-7 score/gradient math (warp w: TMEM lanes
-// 32*(w%4).., query columns 64*(w/4)..) and the dK/dV epilogue, warp 8 TMA
-// producer, warp 9 MMA issuer.
+// 32*(w%4).. = key rows, query columns 64*(w/4)..) and the dK/dV epilogue,
+// warp 8 TMA producer, warp 9 MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -51,9 +54,9 @@ struct KvCfg {
 struct KvCtl {
   uint64_t kv_full, kv_empty;
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t st_full, ds_full;
+  uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dkdv_full, dkdv_empty;
-  uint64_t stat_full;
+  uint64_t stat_full[2];  // per query half: LSE / Delta of the next tile staged
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item_slot[2];
@@ -176,7 +179,45 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   const int T = p.hdr->T;
   const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
-  const uint32_t sk = smem_addr(smem + C::kK), sv = smem_addr(smem + C::kV);
+  // Descriptors built once; per tile and K step only adds remain.
+  const uint64_t dk_k = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dv_k = smem_desc_sw128(smem_addr(smem + C::kV), 16, 1024);
+  const uint64_t dq_k0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
+  const uint64_t ddo_k0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16, 1024);
+  const uint64_t dq_m0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16384, 1024);
+  const uint64_t ddo_m0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16384, 1024);
+  const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP;
+  const uint32_t tDV = tbase + C::kColDV, tDK = tbase + C::kColDK;
+  auto issue_s = [&](uint32_t g) {
+    const uint64_t dq_k = desc_add(dq_k0, (g % C::NSQ) * C::kTile);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+      mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
+    }
+  };
+  auto issue_dp = [&](uint32_t g) {
+    const uint64_t ddo_k = desc_add(ddo_k0, (g % C::NSQ) * C::kTile);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+      mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
+    }
+  };
+  // A operand column of query block k (16 queries): packed P^T / dS^T of
+  // queries 0-63 start at +0, of queries 64-127 at +64.
+  auto issue_dv = [&](uint32_t g, bool acc) {
+    const uint64_t ddo_m = desc_add(ddo_m0, (g % C::NSQ) * C::kTile);
+#pragma unroll
+    for (int k = 0; k < kBM / 16; ++k)
+      mma_ts(tDV, tS + k * 8 + (k >= 4 ? 32 : 0), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
+  };
+  auto issue_dk = [&](uint32_t g, bool acc) {
+    const uint64_t dq_m = desc_add(dq_m0, (g % C::NSQ) * C::kTile);
+#pragma unroll
+    for (int k = 0; k < kBM / 16; ++k)
+      mma_ts(tDK, tDP + k * 8 + (k >= 4 ? 32 : 0), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
+  };
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
@@ -184,47 +225,39 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     if (idx < 0) break;
     const KvItem f = decode<CAUSAL>(p, idx, T);
     if (!mbar_wait(&c->kv_full, it & 1, &c->abort, p.err)) break;
-    for (int i = 0; i < f.nt; ++i, ++gq) {
-      const uint32_t g = gq;
-      const int st = g % C::NSQ;
-      const uint32_t sq = smem_addr(smem + C::kQ + st * C::kTile);
-      const uint32_t sdo = smem_addr(smem + C::kDO + st * C::kTile);
-      if (!mbar_wait(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColS), smem_desc_sw128(sk + off, 16, 1024),
-               smem_desc_sw128(sq + off, 16, 1024), id_st, k > 0);
-      }
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColDP), smem_desc_sw128(sv + off, 16, 1024),
-               smem_desc_sw128(sdo + off, 16, 1024), id_st, k > 0);
-      }
-      mma_commit(&c->st_full);
-      issued = true;
-      if (!mbar_wait(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+    const uint32_t g0 = gq;
+    if (!mbar_wait(&c->qdo_full[g0 % C::NSQ], (g0 / C::NSQ) & 1, &c->abort, p.err)) break;
+    tc_fence_after();
+    issue_s(g0);
+    mma_commit(&c->s_full);
+    issue_dp(g0);
+    mma_commit(&c->dp_full);
+    issued = true;
+    for (int i = 0; i < f.nt; ++i) {
+      const uint32_t g = g0 + i;
+      if (!mbar_wait(&c->p_full, g & 1, &c->abort, p.err)) { ok = false; break; }
       if (i == 0 && !mbar_wait(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
-      // A operand column of query block k (16 queries): packed P^T / dS^T of
-      // queries 0-63 start at +0, of queries 64-127 at +64.
-#pragma unroll
-      for (int k = 0; k < kBM / 16; ++k) {
-        const uint32_t acol = k * 8 + (k >= 4 ? 32 : 0);
-        mma_ts(tmem_at(tbase, 0, C::kColDV), tmem_at(tbase, 0, C::kColS + acol),
-               smem_desc_sw128(sdo + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+      issue_dv(g, i > 0);
+      if (i + 1 < f.nt) {  // S(g+1): its P^T(g) columns were just read by dV(g)
+        if (!mbar_wait(&c->qdo_full[(g + 1) % C::NSQ], ((g + 1) / C::NSQ) & 1, &c->abort, p.err)) {
+          ok = false;
+          break;
+        }
+        issue_s(g + 1);
+        mma_commit(&c->s_full);
       }
-#pragma unroll
-      for (int k = 0; k < kBM / 16; ++k) {
-        const uint32_t acol = k * 8 + (k >= 4 ? 32 : 0);
-        mma_ts(tmem_at(tbase, 0, C::kColDK), tmem_at(tbase, 0, C::kColDP + acol),
-               smem_desc_sw128(sq + k * 2048, 16384, 1024), id_kv, (i > 0) || (k > 0));
+      if (!mbar_wait(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      issue_dk(g, i > 0);
+      mma_commit(&c->qdo_empty[g % C::NSQ]);
+      if (i + 1 < f.nt) {  // dP(g+1): its dS^T(g) columns were just read by dK(g)
+        issue_dp(g + 1);
+        mma_commit(&c->dp_full);
       }
-      mma_commit(&c->qdo_empty[st]);
     }
     if (!ok) break;
+    gq += f.nt;
     mma_commit(&c->dkdv_full);
     mma_commit(&c->kv_empty);
     ++it;
@@ -238,13 +271,24 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
 template <int D, bool CAUSAL>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
-  const int r = threadIdx.x & 127;  // TMEM lane = key row of the block
+  const int r = threadIdx.x & 127;    // TMEM lane = key row of the block
   const int half = threadIdx.x >> 7;  // query columns [64*half, 64*half + 64)
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
   float* s_lse = reinterpret_cast<float*>(smem + C::kStat);  // [2][128]
   float* s_dlt = s_lse + 2 * kBM;                            // [2][128]
+  // LSE*log2e and Delta of query column `col` of tile t (+inf / 0 outside).
+  auto stat_of = [&](const KvItem& f, int t, int col, float& lv, float& dv) {
+    const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+    lv = INFINITY;
+    dv = 0.f;
+    if (col >= qb.shift && col < qb.shift + qb.n) {
+      const long long si = static_cast<long long>(f.h) * T + f.off0 + t * kBM - qb.shift + col;
+      lv = p.lse[si] * kLog2e;
+      dv = p.delta[si];
+    }
+  };
   uint32_t it = 0, gq = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
@@ -253,41 +297,39 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     const KvItem f = decode<CAUSAL>(p, idx, T);
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
     const bool key_ok = r >= f.kt.shift && r < f.kt.shift + f.kt.n;
+    const int scol = 64 * half + r;  // staging column written by threads r < 64
+    // Stage the first tile's LSE / Delta (later tiles are prefetched).
+    if (r < 64) {
+      float lv, dv;
+      stat_of(f, f.t0, scol, lv, dv);
+      s_lse[(gq & 1) * kBM + scol] = lv;
+      s_dlt[(gq & 1) * kBM + scol] = dv;
+    }
+    mbar_arrive(&c->stat_full[half]);
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
       const int q0 = t * kBM - qb.shift;  // local query index of column 0
-      if (half == 0) {  // stage LSE*log2e and Delta of the tile's 128 queries
-        const int qi = q0 + r;
-        const bool q_ok = r >= qb.shift && r < qb.shift + qb.n;
-        float lv = INFINITY, dv = 0.f;
-        if (q_ok) {
-          const long long si = static_cast<long long>(f.h) * T + f.off0 + qi;
-          lv = p.lse[si] * kLog2e;
-          dv = p.delta[si];
-        }
-        s_lse[(g & 1) * kBM + r] = lv;
-        s_dlt[(g & 1) * kBM + r] = dv;
-      }
-      // All 256 threads arrive, so a buffer is rewritten only after every
-      // thread has finished reading it two tiles earlier.
-      mbar_arrive(&c->stat_full);
-      if (!mbar_wait_warp(&c->stat_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      // Prefetch the next tile's LSE / Delta into registers.
+      float nlv = INFINITY, ndv = 0.f;
+      if (r < 64 && i + 1 < f.nt) stat_of(f, t + 1, scol, nlv, ndv);
+      if (!mbar_wait_warp(&c->stat_full[half], g & 1, &c->abort, p.err)) { ok = false; break; }
       const float* lse_t = s_lse + (g & 1) * kBM;
       const float* dlt_t = s_dlt + (g & 1) * kBM;
-      if (!mbar_wait_warp(&c->st_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
       const int c_min = CAUSAL ? key - q0 : -1;  // causal: column c admissible iff c >= c_min
       const bool diag = CAUSAL && __any_sync(0xffffffffu, c_min > 64 * half);
+      // ---- P part: P^T = exp2(S^T * scale*log2e - LSE*log2e)
+      if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float pv[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int cbase = 64 * half + 32 * ch;
-        uint32_t sraw[32], praw[32];
+        uint32_t sraw[32];
         tmem_ld32(tbase + lane_base + C::kColS + cbase, sraw);
-        tmem_ld32(tbase + lane_base + C::kColDP + cbase, praw);
         tmem_wait_ld();
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 2) {
           const int col = cbase + cc;
@@ -298,20 +340,49 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
             p0 = col >= c_min ? p0 : 0.f;
             p1 = col + 1 >= c_min ? p1 : 0.f;
           }
-          const float d0 = p0 * (__uint_as_float(praw[cc]) - dlt_t[col]);
-          const float d1 = p1 * (__uint_as_float(praw[cc + 1]) - dlt_t[col + 1]);
+          pv[32 * ch + cc] = p0;
+          pv[32 * ch + cc + 1] = p1;
           pk[cc / 2] = pack_bf16x2(p0, p1);
-          dk[cc / 2] = pack_bf16x2(d0, d1);
         }
         // bf16 pairs of query columns cbase.. land in packed column
-        // cbase / 2 + 32 * half: each half writes only inside the fp32
-        // columns it has already read itself (no race with the other half).
-        tmem_st16(tbase + lane_base + C::kColS + cbase / 2 + 32 * half, pk);
-        tmem_st16(tbase + lane_base + C::kColDP + cbase / 2 + 32 * half, dk);
+        // 64 * half + 16 * ch: inside this half's own, already read columns.
+        tmem_st16(tbase + lane_base + C::kColS + 64 * half + 16 * ch, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&c->p_full);
+      // ---- dS part: dS^T = P^T (dP^T - Delta)
+      if (!mbar_wait_warp(&c->dp_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int cbase = 64 * half + 32 * ch;
+        uint32_t praw[32];
+        tmem_ld32(tbase + lane_base + C::kColDP + cbase, praw);
+        tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 2) {
+          const int col = cbase + cc;
+          const float d0 = pv[32 * ch + cc] * (__uint_as_float(praw[cc]) - dlt_t[col]);
+          const float d1 = pv[32 * ch + cc + 1] * (__uint_as_float(praw[cc + 1]) - dlt_t[col + 1]);
+          dk[cc / 2] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tbase + lane_base + C::kColDP + 64 * half + 16 * ch, dk);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->ds_full);
+      // Stage the prefetched LSE / Delta of the next tile; every thread of
+      // the half has passed this tile's stat wait, so buffer (g+1)&1 (last
+      // read in tile g-1) is free.
+      if (i + 1 < f.nt) {
+        if (r < 64) {
+          s_lse[((g + 1) & 1) * kBM + scol] = nlv;
+          s_dlt[((g + 1) & 1) * kBM + scol] = ndv;
+        }
+        mbar_arrive(&c->stat_full[half]);
+      }
     }
     if (!ok) break;
     // Item epilogue: dV and scale * dK rows of this K/V block (this warp's
@@ -371,11 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c->item_full[i], 1);
       mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA thread
     }
-    mbar_init(&c->st_full, 1);
+    mbar_init(&c->s_full, 1);
+    mbar_init(&c->dp_full, 1);
+    mbar_init(&c->p_full, kMath);
     mbar_init(&c->ds_full, kMath);
     mbar_init(&c->dkdv_full, 1);
     mbar_init(&c->dkdv_empty, kMath);
-    mbar_init(&c->stat_full, kMath);
+    mbar_init(&c->stat_full[0], kBM);
+    mbar_init(&c->stat_full[1], kBM);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();

@@ -180,26 +180,38 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
   const int T = p.hdr->T;
   const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
   const uint32_t id_dq = idesc_bf16_f32(128, D, false, true);    // dQ (A = dS in TMEM)
-  const uint32_t sq = smem_addr(smem + C::kQ), sdo = smem_addr(smem + C::kDO);
   uint32_t it = 0, nk = 0, nv = 0, g = 0;  // g: key tiles processed over all items
   bool ok = true, issued = false;
-  auto k_addr = [&](uint32_t kidx) { return smem_addr(smem + C::kK + (kidx % C::NSK) * C::kTile); };
-  auto v_addr = [&](uint32_t vidx) { return smem_addr(smem + C::kV + (vidx % C::NSV) * C::kTile); };
-  auto issue_s = [&](uint32_t buf, uint32_t skk) {
+  // Descriptors built once; per tile and K step only adds remain.
+  const uint64_t dq_k = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
+  const uint64_t ddo_k = smem_desc_sw128(smem_addr(smem + C::kDO), 16, 1024);
+  const uint64_t dk_k0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dk_m0 = smem_desc_sw128(smem_addr(smem + C::kK), 16384, 1024);
+  const uint64_t dv_k0 = smem_desc_sw128(smem_addr(smem + C::kV), 16, 1024);
+  auto issue_s = [&](uint32_t buf, uint32_t kidx) {
+    const uint64_t dk = desc_add(dk_k0, (kidx % C::NSK) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      mma_ss(tmem_at(tbase, 0, C::colS(buf)), smem_desc_sw128(sq + off, 16, 1024),
-             smem_desc_sw128(skk + off, 16, 1024), id_s, k > 0);
+      mma_ss(tbase + C::colS(buf), desc_add(dq_k, off), desc_add(dk, off), id_s, k > 0);
     }
   };
-  auto issue_dq = [&](uint32_t buf, uint32_t skk, bool acc) {
+  auto issue_dp = [&](uint32_t vidx) {
+    const uint64_t dv = desc_add(dv_k0, (vidx % C::NSV) * C::kTile);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+      mma_ss(tbase + C::kColDP, desc_add(ddo_k, off), desc_add(dv, off), id_s, k > 0);
+    }
+  };
+  auto issue_dq = [&](uint32_t buf, uint32_t kidx, bool acc) {
     // A = dS (bf16 in S[buf]): keys 0-63 packed at +0, keys 64-127 at +64.
+    const uint64_t dk = desc_add(dk_m0, (kidx % C::NSK) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBN / 16; ++k) {
       const uint32_t acol = k * 8 + (k >= 4 ? 32 : 0);
-      mma_ts(tmem_at(tbase, 0, C::kColDQ), tmem_at(tbase, 0, C::colS(buf) + acol),
-             smem_desc_sw128(skk + k * 2048, 16384, 1024), id_dq, acc || (k > 0));
+      mma_ts(tbase + C::kColDQ, tbase + C::colS(buf) + acol, desc_add(dk, k * 2048), id_dq,
+             acc || (k > 0));
     }
   };
   for (uint32_t n = 0; ok; ++n) {
@@ -211,7 +223,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     // S(0)
     if (!mbar_wait(&c->k_full[k0 % C::NSK], (k0 / C::NSK) & 1, &c->abort, p.err)) break;
     tc_fence_after();
-    issue_s(g0 & 1, k_addr(k0));
+    issue_s(g0 & 1, k0);
     issued = true;
     for (int j = 0; j < f.n_kv && ok; ++j) {
       const uint32_t gj = g0 + j;
@@ -220,23 +232,17 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
         if (!mbar_wait(&c->ds_full, (gj - 1) & 1, &c->abort, p.err)) { ok = false; break; }
         if (j == 1 && !mbar_wait(&c->dq_free, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
-        issue_dq((gj - 1) & 1, k_addr(k0 + j - 1), j > 1);
+        issue_dq((gj - 1) & 1, k0 + j - 1, j > 1);
         mma_commit(&c->k_empty[(k0 + j - 1) % C::NSK]);
       }
-      // dP(j) = dO V(j)^T
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tmem_at(tbase, 0, C::kColDP), smem_desc_sw128(sdo + off, 16, 1024),
-               smem_desc_sw128(v_addr(nv) + off, 16, 1024), id_s, k > 0);
-      }
+      issue_dp(nv);  // dP(j) = dO V(j)^T
       mma_commit(&c->sd_full);  // S(j) and dP(j) ready
       mma_commit(&c->v_empty[nv % C::NSV]);
       ++nv;
       if (j + 1 < f.n_kv) {  // S(j+1) into the other buffer (its dS(j-1) is consumed)
         const uint32_t kk = k0 + j + 1;
         if (!mbar_wait(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
-        issue_s((gj + 1) & 1, k_addr(kk));
+        issue_s((gj + 1) & 1, kk);
       }
     }
     if (!ok) break;
@@ -244,7 +250,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     if (!mbar_wait(&c->ds_full, gl & 1, &c->abort, p.err)) break;
     if (f.n_kv == 1 && !mbar_wait(&c->dq_free, (it & 1) ^ 1, &c->abort, p.err)) break;
     tc_fence_after();
-    issue_dq(gl & 1, k_addr(k0 + f.n_kv - 1), f.n_kv > 1);
+    issue_dq(gl & 1, k0 + f.n_kv - 1, f.n_kv > 1);
     mma_commit(&c->k_empty[(k0 + f.n_kv - 1) % C::NSK]);
     mma_commit(&c->dq_full);
     mma_commit(&c->qdo_empty);

@@ -221,26 +221,28 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     drain_wait(&c->v_full[g % C::NSV], (g / C::NSV) & 1, p.err);
 }
 
+// S_t = Q_t K^T: dq / dk are the K-major descriptors of the Q tile and the
+// K stage (start of the tile); K steps advance them inside 128-byte rows.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tbase, int t, uint32_t sq, uint32_t sk) {
+__device__ __forceinline__ void issue_s(uint32_t tbase, int t, uint64_t dq, uint64_t dk) {
   using C = FwdCfg<D>;
   const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-    mma_ss(tmem_at(tbase, 0, C::colS(t)), smem_desc_sw128(sq + off, 16, 1024),
-           smem_desc_sw128(sk + off, 16, 1024), id_s, k > 0);
+    mma_ss(tbase + C::colS(t), desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
   }
 }
 
+// O_t += P_t V: dv is the MN-major descriptor of the V stage.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tbase, int t, uint32_t sv, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tbase, int t, uint64_t dv, bool accumulate) {
   using C = FwdCfg<D>;
   const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
 #pragma unroll
   for (int k = 0; k < kBN / 16; ++k) {
-    mma_ts(tmem_at(tbase, 0, C::colO(t)), tmem_at(tbase, 0, C::colS(t) + k * 8),
-           smem_desc_sw128(sv + k * 2048, 16384, 1024), id_pv, accumulate || (k > 0));
+    mma_ts(tbase + C::colO(t), tbase + C::colS(t) + k * 8, desc_add(dv, k * 2048), id_pv,
+           accumulate || (k > 0));
   }
 }
 
@@ -248,7 +250,9 @@ template <int D, bool CAUSAL, bool BCAST>
 __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
   const int T = p.hdr->T;
-  const uint32_t sq0 = smem_addr(smem + C::kQ);
+  const uint64_t dq0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
+  const uint64_t dk0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(smem_addr(smem + C::kV), 16384, 1024);
   uint32_t itq = 0, nk = 0, nv = 0;
   uint32_t np[2] = {0, 0};   // P tiles consumed per query tile
   uint32_t ito[2] = {0, 0};  // items per query tile (for o_free)
@@ -262,16 +266,16 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
     if (!mbar_wait(&c->q_full, itq & 1, &c->abort, p.err)) break;
     ++itq;
     for (int j = 0; j <= f.N && ok; ++j) {
-      uint32_t sk = 0, sv = 0;
+      uint64_t dk = 0, dv = 0;
       if (j < f.N) {
         const int st = nk % C::NSK;
         if (!mbar_wait(&c->k_full[st], (nk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
-        sk = smem_addr(smem + C::kK + st * C::kTile);
+        dk = desc_add(dk0, st * C::kTile);
       }
       if (j >= 1) {
         const int st = nv % C::NSV;
         if (!mbar_wait(&c->v_full[st], (nv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
-        sv = smem_addr(smem + C::kV + st * C::kTile);
+        dv = desc_add(dv0, st * C::kTile);
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -284,11 +288,11 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
             break;
           }
           tc_fence_after();
-          issue_pv<D>(tbase, t, sv, j > 1);
+          issue_pv<D>(tbase, t, dv, j > 1);
           mma_commit(&c->o_ready[t]);
         }
         if (j < nkv) {  // S_t(j) = Q_t K(j)^T
-          issue_s<D>(tbase, t, sq0 + t * C::kTile, sk);
+          issue_s<D>(tbase, t, desc_add(dq0, t * C::kTile), dk);
           mma_commit(&c->s_full[t]);
           issued = true;
         }

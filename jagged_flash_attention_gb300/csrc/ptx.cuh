@@ -228,6 +228,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Advance a descriptor's start address by `bytes` (multiple of 16).  The
+// start-address field is the low 14 bits and shared memory is below 256 KB,
+// so the add never carries into the other fields.  Building each buffer's
+// descriptor once and advancing it per K step keeps the single MMA-issuing
+// thread from spending most of its time on descriptor arithmetic.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
