@@ -240,7 +240,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
                        const void* dout, void* dq, void* dk, void* dv, cudaStream_t stream) {
   jfa_status st;
   const long long cap_kv = (long long)s.H * s.B * cdivll(s.max_len, kBN);
-  const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kBM);
+  const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kFwdRows);
   if (cap_kv >= (1LL << 31) || cap_q >= (1LL << 31))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
   const long long delta_elems = (long long)s.H * s.Tcap;
@@ -267,7 +267,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   float* delta = reinterpret_cast<float*>(base + delta_off);
   SchedParams sk{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 1, kBM,
                  items_kv, (int)cap_kv, hdr_kv, ds->err};
-  SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kBM,
+  SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kFwdRows,
                  items_q, (int)cap_q, hdr_q, ds->err};
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));

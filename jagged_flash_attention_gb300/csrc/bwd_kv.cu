@@ -329,21 +329,20 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         uint32_t sraw[32];
         tmem_ld32(tbase + lane_base + C::kColS + cbase, sraw);
         tmem_wait_ld();
+        // Rows of keys outside the sequence are left unmasked: row r of dV
+        // and dK depends only on row r of P^T and dS^T, and those rows are
+        // never stored.
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          pv[32 * ch + cc] = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -lse_t[cbase + cc]));
+        if (diag) {  // causal diagonal tile: queries before this key
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc)
+            pv[32 * ch + cc] = cbase + cc >= c_min ? pv[32 * ch + cc] : 0.f;
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          const int col = cbase + cc;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -lse_t[col]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sraw[cc + 1]), sl2, -lse_t[col + 1]));
-          if (!key_ok) p0 = 0.f, p1 = 0.f;
-          if (diag) {
-            p0 = col >= c_min ? p0 : 0.f;
-            p1 = col + 1 >= c_min ? p1 : 0.f;
-          }
-          pv[32 * ch + cc] = p0;
-          pv[32 * ch + cc + 1] = p1;
-          pk[cc / 2] = pack_bf16x2(p0, p1);
-        }
+        for (int cc = 0; cc < 32; cc += 2) pk[cc / 2] = pack_bf16x2(pv[32 * ch + cc], pv[32 * ch + cc + 1]);
         // bf16 pairs of query columns cbase.. land in packed column
         // 64 * half + 16 * ch: inside this half's own, already read columns.
         tmem_st16(tbase + lane_base + C::kColS + 64 * half + 16 * ch, pk);

@@ -33,7 +33,7 @@ struct SchedParams {
   const int32_t* offsets;
   int B, H, Lq, max_len;
   int causal, broadcast, backward;
-  int qrows;  // query rows per item when backward == 0 (forward: 256, dQ pass: 128)
+  int qrows;  // query rows per item when backward == 0 (forward and dQ pass: 256)
   Item* items;
   int capacity;
   WorkHeader* hdr;

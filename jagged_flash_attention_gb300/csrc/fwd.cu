@@ -318,26 +318,6 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   }
 }
 
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  return static_cast<uint64_t>(__float_as_uint(a)) |
-         (static_cast<uint64_t>(__float_as_uint(b)) << 32);
-}
-__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
-  return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
-                     __uint_as_float(static_cast<uint32_t>(v >> 32)));
-}
-// (a0, a1) * (b0, b1) + (c0, c1) with the paired fp32 FMA of sm_100+.
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;

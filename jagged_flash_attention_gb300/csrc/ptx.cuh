@@ -298,6 +298,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Paired fp32 arithmetic of sm_100+ on two floats held in one 64-bit value.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  return static_cast<uint64_t>(__float_as_uint(a)) |
+         (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
+                     __uint_as_float(static_cast<uint32_t>(v >> 32)));
+}
+// (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Elementwise product of two bf16 pairs, rounded to nearest bf16.
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 
