@@ -11,24 +11,25 @@
 //   P    = exp2(S * scale*log2e - LSE*log2e)    (math, kept in registers as bf16)
 //   dP_j = dO V_j^T     (SS)                  -> TMEM SP (over S, once P is read)
 //   dS   = P (dP - Delta): dP - Delta in fp32, then a bf16 pair product,
-//          into SP's first 64 columns
+//          packed into SP (keys 0-63 at +0, keys 64-127 at +64)
 //   dQ  += dS K_j       (TS, B = K MN-major)  -> TMEM DQ
 // Each item is a pair of 128-row query tiles of one (sequence, head) that
-// share every K / V tile.  The two tiles ping-pong: math warpgroup g owns
-// tile g, and the MMA issuer interleaves
+// share every K / V tile, which halves the K / V bytes each SM must take in
+// per product (an SM ingests about 48 B per cycle from L2; one 128-row tile
+// at full tensor rate would need about 42).  The MMA issuer interleaves the
+// two tiles,
 //   dQ_0(j-1) S_0(j) | dQ_1(j-1) S_1(j) | dP_0(j) | dP_1(j)
-// so that one tile's score math runs under the other tile's products.  One
-// chain per tile (S -> P math -> dP -> dS math -> dQ) has several hand-offs
-// of a few hundred cycles each; with a single tile in flight the tensor pipe
-// idles for most of every chain.
+// and all eight math warps work on both tiles in that order (P_0, P_1,
+// dS_0, dS_1), so each tile's score math runs under the other tile's
+// products at the full warp count.
 //
 // TMEM (512 columns): tile g uses SP at 256g (128 fp32 columns) and DQ at
 // 256g + 128 (D columns).  SMEM: Q and dO of both tiles, a K ring and a V
 // ring (D = 128: 128 + 64 + 32 KB).
 //
-// CTA = 10 warps: warpgroup g = warps 4g..4g+3 (thread = query row of tile
-// g, all 128 key columns) does tile g's math and its dQ epilogue, warp 8 is
-// the TMA producer, warp 9 the MMA issuer.
+// CTA = 10 warps: warps 0-7 score math (warp w: TMEM lanes 32*(w%4).. =
+// query rows of both tiles, key columns 64*(w/4)..) and the dQ epilogues,
+// warp 8 TMA producer, warp 9 MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -36,7 +37,7 @@ namespace jfa {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kGroup = 128;  // threads of one math warpgroup
+constexpr int kMath = 256;  // score-math threads
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -232,12 +233,12 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     }
   };
   auto issue_dq = [&](int g, uint32_t kidx, bool acc) {
-    // A = dS, bf16 pairs of key columns packed in SP's columns [0, 64).
+    // A = dS: bf16 pairs of keys 0-63 packed at SP + 0, of keys 64-127 at SP + 64.
     const uint64_t dk = desc_add(dk_m0, (kidx % C::NSK) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBN / 16; ++k)
-      mma_ts(tbase + 256 * g + 128, tbase + 256 * g + 8 * k, desc_add(dk, k * 2048), id_dq,
-             acc || (k > 0));
+      mma_ts(tbase + 256 * g + 128, tbase + 256 * g + 8 * k + (k >= 4 ? 32 : 0),
+             desc_add(dk, k * 2048), id_dq, acc || (k > 0));
   };
   uint32_t it = 0, nk = 0, nv = 0;
   uint32_t gt[2] = {0, 0};  // tiles processed per query tile slot, over all items
@@ -312,119 +313,149 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
 
 template <int D, bool CAUSAL>
 __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
-  const int g = threadIdx.x >> 7;     // query tile of the item this warpgroup owns
-  const int r = threadIdx.x & 127;    // query row of the tile == TMEM lane
+  const int r = threadIdx.x & 127;    // query row of each tile == TMEM lane
+  const int half = threadIdx.x >> 7;  // key columns [64*half, 64*half + 64)
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
-  const uint32_t tsp = tbase + lane_base + 256 * g;
-  const uint32_t tdq = tsp + 128;
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
-  uint32_t u = 0, ic = 0;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  uint32_t gt[2] = {0, 0};  // tiles processed per query tile slot
+  uint32_t gi[2] = {0, 0};  // items in which the slot was present
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
     const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
     const QItem f = decode<CAUSAL>(p, idx, T);
-    const QTile q = g == 0 ? f.t[0] : f.t[1];
-    if (q.n == 0) continue;
-    const int qi = q.q_lo - q.shift + r;  // local query index of this row
-    const bool row_valid = r >= q.shift && r < q.shift + q.nq;
-    float lse2 = INFINITY, dlt = 0.f;  // rows outside the sequence: P = 0
-    if (row_valid) {
-      const long long si = static_cast<long long>(f.h) * T + f.off0 + qi;
-      lse2 = p.lse[si] * kLog2e;
-      dlt = p.delta[si];
-    }
-    const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse2, -lse2);
-    const uint64_t ndlt2 = f2_pack(-dlt, -dlt);
-    for (int j = 0; j < q.n; ++j, ++u) {
-      const KvTile kt = kv_tile(f.off0, f.L, j, T);
-      const int key0 = j * kBN - kt.shift;  // local key index of column 0
-      const bool need_mask =
-          kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > q.q_lo - q.shift);
-      // Admissible key columns of this row: [c_lo, c_lo + span]; an empty
-      // range moves c_lo past every column.
-      const int c_last = CAUSAL ? min(kt.shift + kt.nk - 1, qi - key0) : kt.shift + kt.nk - 1;
-      const int c_lo = c_last >= kt.shift ? kt.shift : kBN;
-      const uint32_t span = c_last >= kt.shift ? static_cast<uint32_t>(c_last - kt.shift) : 0u;
-      // ---- P = exp2(S * scale*log2e - LSE*log2e), kept as bf16 pairs
-      if (!mbar_wait_warp(&c->s_full[g], u & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[64];
+    // Per query tile g of the item: this row's local query index, validity,
+    // LSE*log2e and Delta.
+    int qi[2];
+    bool row_valid[2];
+    uint64_t nlse2[2], ndlt2[2];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+    for (int g = 0; g < 2; ++g) {
+      const QTile& q = f.t[g];
+      qi[g] = q.q_lo - q.shift + r;
+      row_valid[g] = q.n > 0 && r >= q.shift && r < q.shift + q.nq;
+      float lse2 = INFINITY, dlt = 0.f;  // rows outside the sequence: P = 0
+      if (row_valid[g]) {
+        const long long si = static_cast<long long>(f.h) * T + f.off0 + qi[g];
+        lse2 = p.lse[si] * kLog2e;
+        dlt = p.delta[si];
+      }
+      nlse2[g] = f2_pack(-lse2, -lse2);
+      ndlt2[g] = f2_pack(-dlt, -dlt);
+    }
+    // P of tile g at key tile j: this thread's 64 columns -> 32 bf16 pairs.
+    auto p_part = [&](int g, int j, uint32_t (&pk)[32]) {
+      const uint32_t u = gt[g] + j;
+      if (!mbar_wait_warp(&c->s_full[g], u & 1, &c->abort, p.err)) return false;
+      tc_fence_after();
+      const uint32_t ts = tbase + lane_base + 256 * g + 64 * half;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t sraw[32];
-        tmem_ld32(tsp + 32 * ch, sraw);
+        tmem_ld32(ts + 32 * ch, sraw);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 x = f2_unpack(ffma2(
-              f2_pack(__uint_as_float(sraw[2 * i]), __uint_as_float(sraw[2 * i + 1])), sl2x2, nlse2));
+              f2_pack(__uint_as_float(sraw[2 * i]), __uint_as_float(sraw[2 * i + 1])), sl2x2,
+              nlse2[g]));
           pk[16 * ch + i] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
         }
-        if (need_mask) {  // ragged or diagonal tile: zero the inadmissible columns
+      }
+      const QTile& q = f.t[g];
+      const KvTile kt = kv_tile(f.off0, f.L, j, T);
+      const int key0 = j * kBN - kt.shift;  // local key index of column 0
+      if (kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > q.q_lo - q.shift)) {
+        // Ragged or diagonal tile: zero the inadmissible columns.  The
+        // admissible ones are [lo, lo + span] (relative to this thread's
+        // first column); an empty range moves lo past every column.
+        const int last = CAUSAL ? min(kt.shift + kt.nk - 1, qi[g] - key0) : kt.shift + kt.nk - 1;
+        const int lo = (last >= kt.shift ? kt.shift : kBN) - 64 * half;
+        const uint32_t span = last >= kt.shift ? static_cast<uint32_t>(last - kt.shift) : 0u;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = 32 * ch + 2 * i;
-            const uint32_t keep =
-                (static_cast<uint32_t>(col - c_lo) <= span ? 0x0000ffffu : 0u) |
-                (static_cast<uint32_t>(col + 1 - c_lo) <= span ? 0xffff0000u : 0u);
-            pk[16 * ch + i] &= keep;
-          }
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t keep = (static_cast<uint32_t>(2 * i - lo) <= span ? 0x0000ffffu : 0u) |
+                                (static_cast<uint32_t>(2 * i + 1 - lo) <= span ? 0xffff0000u : 0u);
+          pk[i] &= keep;
         }
       }
       tc_fence_before();
       mbar_arrive(&c->p_done[g]);  // S read: dP may overwrite SP
-      // ---- dS = P (dP - Delta), bf16 pairs into SP's columns [0, 64)
-      if (!mbar_wait_warp(&c->dp_full[g], u & 1, &c->abort, p.err)) { ok = false; break; }
+      return true;
+    };
+    // dS = P (dP - Delta) of tile g at key tile j, bf16 pairs into SP's
+    // columns 64*half + [0, 32): inside this thread's own, already read
+    // columns.
+    auto ds_part = [&](int g, int j, const uint32_t (&pk)[32]) {
+      const uint32_t u = gt[g] + j;
+      if (!mbar_wait_warp(&c->dp_full[g], u & 1, &c->abort, p.err)) return false;
       tc_fence_after();
+      const uint32_t ts = tbase + lane_base + 256 * g + 64 * half;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t praw[32];
-        tmem_ld32(tsp + 32 * ch, praw);
+        tmem_ld32(ts + 32 * ch, praw);
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           // (dP - Delta) in fp32, rounded to bf16, times the bf16 P.
-          const float2 t = f2_unpack(fadd2(
-              f2_pack(__uint_as_float(praw[2 * i]), __uint_as_float(praw[2 * i + 1])), ndlt2));
-          w[i] = bmul2(pk[16 * ch + i], pack_bf16x2(t.x, t.y));
+          const float2 d = f2_unpack(fadd2(
+              f2_pack(__uint_as_float(praw[2 * i]), __uint_as_float(praw[2 * i + 1])), ndlt2[g]));
+          w[i] = bmul2(pk[16 * ch + i], pack_bf16x2(d.x, d.y));
         }
-        // Packed columns [16ch, 16ch + 16) lie in dP columns this thread has
-        // already read (chunks 0 .. ch).
-        tmem_st16(tsp + 16 * ch, w);
+        tmem_st16(ts + 16 * ch, w);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->ds_full[g]);
+      return true;
+    };
+    // Per key tile j: P of both tiles, then dS of both tiles (in the order
+    // the MMA issuer produces S_0, S_1, dP_0, dP_1).
+    const int n0 = f.t[0].n, n1 = f.t[1].n;
+    for (int j = 0; j < f.N && ok; ++j) {
+      uint32_t p0[32], p1[32];
+      if (j < n0 && !p_part(0, j, p0)) { ok = false; break; }
+      if (j < n1 && !p_part(1, j, p1)) { ok = false; break; }
+      if (j < n0 && !ds_part(0, j, p0)) { ok = false; break; }
+      if (j < n1 && !ds_part(1, j, p1)) { ok = false; break; }
     }
     if (!ok) break;
-    // Epilogue: dQ = scale * acc in bf16.
-    if (!mbar_wait_warp(&c->dq_full[g], ic & 1, &c->abort, p.err)) break;
-    tc_fence_after();
-    __nv_bfloat16* dst = p.dq + ((static_cast<long long>(f.off0) + qi) * p.H + f.h) * D;
+    // Epilogues: dQ = scale * acc in bf16 (this thread's half of the head dim).
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(tdq + 32 * ch, v);
-      tmem_wait_ld();
-      uint32_t w[16];
+    for (int g = 0; g < 2; ++g) {
+      if (f.t[g].n == 0) continue;
+      if (!mbar_wait_warp(&c->dq_full[g], gi[g] & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      __nv_bfloat16* dst = p.dq + ((static_cast<long long>(f.off0) + qi[g]) * p.H + f.h) * D;
 #pragma unroll
-      for (int i2 = 0; i2 < 16; ++i2)
-        w[i2] = pack_bf16x2(__uint_as_float(v[2 * i2]) * p.scale,
-                            __uint_as_float(v[2 * i2 + 1]) * p.scale);
-      if (row_valid) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
-        d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+      for (int ch = 0; ch < D / 64; ++ch) {
+        const int dbase = (D / 2) * half + 32 * ch;
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_base + 256 * g + 128 + dbase, v);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2)
+          w[i2] = pack_bf16x2(__uint_as_float(v[2 * i2]) * p.scale,
+                              __uint_as_float(v[2 * i2 + 1]) * p.scale);
+        if (row_valid[g]) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + dbase);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
       }
+      tc_fence_before();
+      mbar_arrive(&c->dq_free[g]);
+      ++gi[g];
     }
-    tc_fence_before();
-    mbar_arrive(&c->dq_free[g]);
-    ++ic;
+    gt[0] += n0;
+    gt[1] += n1;
   }
 }
 
@@ -454,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&c->s_full[g], 1);
-      mbar_init(&c->p_done[g], kGroup);
+      mbar_init(&c->p_done[g], kMath);
       mbar_init(&c->dp_full[g], 1);
-      mbar_init(&c->ds_full[g], kGroup);
+      mbar_init(&c->ds_full[g], kMath);
       mbar_init(&c->dq_full[g], 1);
-      mbar_init(&c->dq_free[g], kGroup);
+      mbar_init(&c->dq_free[g], kMath);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->item_full[i], 1);
