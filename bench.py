@@ -46,6 +46,21 @@ def _flops(x):
     return f, 2.5 * f, p
 
 
+# Algorithmic tensor-core FLOPs of one launch of each product kernel, per
+# head and query-key pair (2 * D per product): forward S and PV; dK/dV pass
+# S^T, dP^T, dV, dK; dQ pass S, dP, dQ; broadcast-Q backward all five.
+KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4.0, "bwd_kv": 8.0, "bwd_q": 6.0, "bwd_fused": 10.0}
+KERNEL_DESC = {
+    "fwd": "forward (S = QK^T, O += PV)",
+    "bwd_kv": "backward dK/dV pass (S^T, dP^T, dV += P^T dO, dK += dS^T Q)",
+    "bwd_q": "backward dQ pass (S, dP, dQ += dS K)",
+    "bwd_fused": "broadcast-Q backward (five products)",
+}
+# DRAM bytes per launch from one ncu capture of the kernel as it is now, on
+# this workload (profiles/ names the capture); None once the kernel changed.
+KERNEL_TRAFFIC = {}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
 
@@ -61,7 +76,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -207,6 +222,7 @@ def run_ours(args, x, wname):
         fwd()
         bwd()
     jfa.jfa_sync_and_check()
+    jfa.profile_read()  # discard anything recorded before the timed region
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -214,6 +230,8 @@ def run_ours(args, x, wname):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    launches0 = jfa.launch_count()
+    jfa.profile_enable(True)
     with ClockSampler(local) as clk:
         t_start.record(stream)
         for i in range(args.steps):
@@ -224,6 +242,9 @@ def run_ours(args, x, wname):
             ev[i][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+    jfa.profile_enable(False)
+    launches = jfa.launch_count() - launches0
+    kprof = jfa.profile_read()
     if ws > 1:
         torch.distributed.barrier()
     jfa.jfa_sync_and_check()
@@ -278,6 +299,21 @@ def run_ours(args, x, wname):
                          f"({t:.1f} s)"}
     bwd_tf = bwd_f / (bwd_ms * 1e-3) / 1e12
     fwd_tf = fwd_f / (fwd_ms * 1e-3) / 1e12
+    # Per-kernel device time over the timed region (events on the launching
+    # stream, recorded by the library); roofline of the dominant kernel.
+    kernels = {k: {"ms_per_launch": t / n, "launches": n, "share": 0.0}
+               for k, (t, n) in kprof.items() if n > 0}
+    tot = sum(t for t, n in kprof.values())
+    for k, (t, n) in kprof.items():
+        if n > 0:
+            kernels[k]["share"] = t / tot
+    dom = max((k for k in kernels if k in KERNEL_FLOPS_PER_PAIR_D),
+              key=lambda k: kprof[k][0])
+    dom_flops = KERNEL_FLOPS_PER_PAIR_D[dom] * H * D * pairs
+    dom_tf = dom_flops / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e12
+    for k, v in kernels.items():
+        if k in KERNEL_FLOPS_PER_PAIR_D:
+            v["tflops"] = KERNEL_FLOPS_PER_PAIR_D[k] * H * D * pairs / (v["ms_per_launch"] * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -289,14 +325,17 @@ def run_ours(args, x, wname):
         "frac_of_peak": value / peak,
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak},
-        "roofline": {"bound": "tensor", "kernel": "backward pass (scheduler + Delta pre-pass + "
-                                                  "dK/dV/dQ kernel + dQ finalize)",
-                     "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
-                     "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": None},
+        "roofline": {"bound": "tensor", "kernel": KERNEL_DESC[dom],
+                     "algorithmic_tflop_per_launch": dom_flops / 1e12,
+                     "ms_per_launch": kernels[dom]["ms_per_launch"],
+                     "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "traffic": KERNEL_TRAFFIC.get(dom)},
+        "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

@@ -76,10 +76,13 @@ jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* o
                    float* lse, cudaStream_t stream);
 
 /* Backward pass, self-attention: given out, lse from jfa_fwd and dout,
- * writes dq, dk, dv (gradients of sum(out * dout)).  Five products per K/V
- * block, as in "Optimizing Jagged Flash Attention with TLX", section
- * "2-CTA collaborative MMA", with the Delta = rowsum(dout * out) pre-pass
- * and an fp32 dq accumulator ("Multi-stage dQ staging"). */
+ * writes dq, dk, dv (gradients of sum(out * dout)).  The products of
+ * "Optimizing Jagged Flash Attention with TLX", section "2-CTA
+ * collaborative MMA", after the Delta = rowsum(dout * out) pre-pass, in two
+ * passes: a K/V-block-outer pass for dk and dv and a query-tile-outer pass
+ * for dq, so that dq accumulates on chip and needs no global fp32
+ * accumulator (the page's "Multi-stage dQ staging" is not needed).  Five
+ * kernels: two schedulers, the pre-pass and the two passes. */
 jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
                    int H, int D, int max_len, int broadcast_q, int causal, float scale,
                    const void* out, const float* lse, const void* dout, void* dq, void* dk,
@@ -130,6 +133,43 @@ const char* jfa_last_error(void);
 
 /* Library version string. */
 const char* jfa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Launch accounting.  A library facility with no counterpart in the pages:
+ * it lets a caller count the kernels this library enqueues and time each
+ * kind on the stream it runs on.
+ * ------------------------------------------------------------------------ */
+
+/* Kernel kinds reported by jfa_profile_read (array index). */
+typedef enum {
+  JFA_KERNEL_SCHED = 0,     /* work-list scheduler */
+  JFA_KERNEL_FWD = 1,       /* forward */
+  JFA_KERNEL_PREP = 2,      /* Delta = rowsum(dO * O) pre-pass */
+  JFA_KERNEL_BWD_KV = 3,    /* self-attention backward, dK / dV pass */
+  JFA_KERNEL_BWD_Q = 4,     /* self-attention backward, dQ pass */
+  JFA_KERNEL_BWD_FUSED = 5, /* broadcast-Q backward (dK, dV, dQ partials) */
+  JFA_KERNEL_FINALIZE = 6,  /* broadcast-Q dQ shard sum and bf16 cast */
+  JFA_KERNEL_FILL = 7,      /* outputs of an all-empty broadcast batch */
+  JFA_KERNEL_KINDS = 8
+} jfa_kernel_kind;
+
+/* Kernels enqueued by this library since the process started (all threads,
+ * devices and streams; a failed launch is not counted).  Never fails. */
+long long jfa_launch_count(void);
+
+/* on != 0: every later launch is bracketed by a CUDA event pair recorded on
+ * its own stream, until profiling is switched off.  Process-wide.  Do not
+ * enable while a stream of this library is being captured into a graph.
+ * Always returns JFA_OK. */
+jfa_status jfa_profile_enable(int on);
+
+/* Waits for every event pair recorded so far, writes per kernel kind the
+ * summed device time in milliseconds (ms[kind]) and the number of launches
+ * (launches[kind]) for kinds < n, and releases the records.  ms and
+ * launches are HOST arrays of n elements owned by the caller (n >= 0; both
+ * may be null when n == 0).  JFA_ERR_CUDA if an event could not be read
+ * (the remaining records are still released). */
+jfa_status jfa_profile_read(double* ms, long long* launches, int n);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,12 @@ def lib() -> ctypes.CDLL:
         L.jfa_sync_and_check.argtypes = [_P]
         L.jfa_sync_and_check.restype = _I
         L.jfa_last_error.restype = ctypes.c_char_p
+        L.jfa_launch_count.restype = ctypes.c_longlong
+        L.jfa_launch_count.argtypes = []
+        L.jfa_profile_enable.argtypes = [_I]
+        L.jfa_profile_enable.restype = _I
+        L.jfa_profile_read.argtypes = [_P, _P, _I]
+        L.jfa_profile_read.restype = _I
         L.jfa_version.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -119,6 +125,27 @@ def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, c
 
 def jfa_sync_and_check(stream=None):
     _check(lib().jfa_sync_and_check(_stream(stream)))
+
+
+KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_fused", "finalize", "fill")
+
+
+def launch_count() -> int:
+    """Kernels this library has enqueued in this process."""
+    return int(lib().jfa_launch_count())
+
+
+def profile_enable(on: bool):
+    _check(lib().jfa_profile_enable(1 if on else 0))
+
+
+def profile_read():
+    """{kind: (total device ms, launches)} since the last read (synchronises)."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    _check(lib().jfa_profile_read(ctypes.addressof(ms), ctypes.addressof(cnt), n))
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
 
 
 def _shapes(q, k, offsets, broadcast_q):

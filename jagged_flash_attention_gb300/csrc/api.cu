@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/jfa.h: argument validation,
 // stream-ordered scratch memory, TMA tensor-map encoding and the launch
 // sequence of the forward and backward passes.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -8,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -24,6 +26,37 @@ namespace {
 using namespace jfa;
 
 thread_local std::string t_last_error;
+
+// Kernel launch accounting: a process-wide count of enqueued kernels and,
+// while profiling is on, a CUDA event pair around every launch, recorded on
+// the launch's own stream (read back by jfa_profile_read).
+std::atomic<long long> g_launch_count{0};
+std::atomic<int> g_profile_on{0};
+struct ProfRecord {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_prof;
+
+template <class F>
+cudaError_t run_kernel(jfa_kernel_kind kind, cudaStream_t stream, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  const bool prof = g_profile_on.load(std::memory_order_relaxed) != 0 &&
+                    cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess;
+  if (prof) cudaEventRecord(a, stream);
+  const cudaError_t e = launch();
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  if (prof) {
+    cudaEventRecord(b, stream);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({static_cast<int>(kind), a, b});
+  } else {
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+  }
+  return e;
+}
 
 jfa_status fail(jfa_status st, const char* fmt, ...) {
   char buf[512];
@@ -187,8 +220,10 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   cudaError_t e;
   if (s.max_len == 0) {  // every sequence is empty
     if (s.broadcast) {
-      e = launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H, s.D,
-                            stream);
+      e = run_kernel(JFA_KERNEL_FILL, stream, [&] {
+        return launch_fill_empty(
+            static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H, s.D, stream);
+      });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
     return finish(ds, stream);
@@ -210,7 +245,9 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   Item* items = reinterpret_cast<Item*>(base + items_off);
   SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0, kFwdRows,
                  items, (int)cap, hdr, ds->err};
-  e = launch_sched(sp, stream);
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
+    return launch_sched(sp, stream);
+  });
   if (e == cudaSuccess) {
     FwdParams fp;
     fp.offsets = offsets;
@@ -224,7 +261,9 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
     fp.hdr = hdr;
     fp.err = ds->err;
     const int grid = (int)std::min<long long>(ds->sms, cap);
-    e = launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+    e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
+      return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+    });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -283,8 +322,12 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
   bp.err = ds->err;
-  e = launch_sched(sk, stream);
-  if (e == cudaSuccess) e = launch_sched(sq, stream);
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
+    return launch_sched(sk, stream);
+  });
+  if (e == cudaSuccess) e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
+    return launch_sched(sq, stream);
+  });
   if (e == cudaSuccess) {
     PrepParams pp;
     memset(&pp, 0, sizeof(pp));
@@ -295,19 +338,25 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     pp.H = s.H;
     pp.D = s.D;
     pp.hdr = hdr_kv;
-    e = launch_prep(pp, ds->sms, stream);
+    e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
+      return launch_prep(pp, ds->sms, stream);
+    });
   }
   if (e == cudaSuccess) {
     bp.items = items_kv;
     bp.hdr = hdr_kv;
-    e = launch_bwd_kv(s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_kv),
-                      stream);
+    e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
+      return launch_bwd_kv(
+          s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_kv), stream);
+    });
   }
   if (e == cudaSuccess) {
     bp.items = items_q;
     bp.hdr = hdr_q;
-    e = launch_bwd_q(s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_q),
-                     stream);
+    e = run_kernel(JFA_KERNEL_BWD_Q, stream, [&] {
+      return launch_bwd_q(
+          s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_q), stream);
+    });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -331,8 +380,10 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
   cudaError_t e;
   if (s.max_len == 0) {
     if (s.broadcast) {  // no keys anywhere: dq = 0
-      e = launch_fill_empty(static_cast<__nv_bfloat16*>(dq), nullptr, (long long)s.Lq * s.H, s.D,
-                            stream);
+      e = run_kernel(JFA_KERNEL_FILL, stream, [&] {
+        return launch_fill_empty(
+            static_cast<__nv_bfloat16*>(dq), nullptr, (long long)s.Lq * s.H, s.D, stream);
+      });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
     return finish(ds, stream);
@@ -373,7 +424,9 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
   float* acc = reinterpret_cast<float*>(base + acc_off);
   SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1, kBM,
                  items, (int)cap, hdr, ds->err};
-  e = launch_sched(sp, stream);
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
+    return launch_sched(sp, stream);
+  });
   if (e == cudaSuccess) {
     PrepParams pp;
     pp.out = static_cast<const __nv_bfloat16*>(out);
@@ -388,7 +441,9 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     pp.broadcast = s.broadcast;
     pp.zero_self_acc = 0;
     pp.hdr = hdr;
-    e = launch_prep(pp, ds->sms, stream);
+    e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
+      return launch_prep(pp, ds->sms, stream);
+    });
   }
   if (e == cudaSuccess) {
     BwdParams bp;
@@ -409,7 +464,9 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     bp.items = items;
     bp.hdr = hdr;
     bp.err = ds->err;
-    e = launch_bwd(s.D, s.causal, s.broadcast, tq, tk, tv, tdo, bp, grid, stream);
+    e = run_kernel(JFA_KERNEL_BWD_FUSED, stream, [&] {
+      return launch_bwd(s.D, s.causal, s.broadcast, tq, tk, tv, tdo, bp, grid, stream);
+    });
   }
   if (e == cudaSuccess) {
     FinParams fp;
@@ -423,7 +480,9 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
     fp.shards = shards;
     fp.shard_stride = shard_elems;
     fp.hdr = hdr;
-    e = launch_finalize(fp, ds->sms, stream);
+    e = run_kernel(JFA_KERNEL_FINALIZE, stream, [&] {
+      return launch_finalize(fp, ds->sms, stream);
+    });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -488,6 +547,42 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
   t_last_error.clear();
   return do_bwd(make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale), q, k, v, offsets,
                 out, lse, dout, dq, dk, dv, stream);
+}
+
+long long jfa_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
+
+jfa_status jfa_profile_enable(int on) {
+  g_profile_on.store(on ? 1 : 0, std::memory_order_relaxed);
+  return JFA_OK;
+}
+
+jfa_status jfa_profile_read(double* ms, long long* launches, int n) {
+  if (n < 0 || (n > 0 && (ms == nullptr || launches == nullptr)))
+    return fail(JFA_ERR_INVALID_ARG, "profile_read: n must be >= 0 and the arrays non-null");
+  for (int i = 0; i < n; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  jfa_status st = JFA_OK;
+  for (const ProfRecord& r : recs) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e != cudaSuccess) {
+      if (st == JFA_OK) st = cuda_fail(e, "profile event");
+    } else if (r.kind < n) {
+      ms[r.kind] += t;
+      launches[r.kind] += 1;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  return st;
 }
 
 jfa_status jfa_sync_and_check(cudaStream_t stream) {
@@ -626,8 +721,10 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   cudaError_t e;
   if (s.max_len == 0) {
     if (s.broadcast) {
-      e = launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H,
-                            s.D, stream);
+      e = run_kernel(JFA_KERNEL_FILL, stream, [&] {
+        return launch_fill_empty(
+            static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H, s.D, stream);
+      });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
     return JFA_OK;
@@ -642,7 +739,9 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   // item the forward kernel reads, so nothing left by a previous call leaks.
   SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0, kFwdRows,
                  items, (int)cap, hdr, d->err};
-  e = launch_sched(sp, stream);
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
+    return launch_sched(sp, stream);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
   FwdParams fp;
   fp.offsets = offsets;
@@ -656,7 +755,9 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   fp.hdr = hdr;
   fp.err = d->err;
   const int grid = (int)std::min<long long>(d->sms, cap);
-  e = launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+  e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
+    return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return JFA_OK;
 }

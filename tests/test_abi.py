@@ -91,3 +91,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(jfa, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         jfa.lib()
+
+
+def test_profile_read_arguments(L):
+    L.jfa_profile_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    assert L.jfa_profile_read(None, None, 0) == 0
+    assert L.jfa_profile_read(None, None, 3) == 1
+    assert b"profile_read" in L.jfa_last_error()
+    assert L.jfa_profile_read(None, None, -1) == 1
+
+
+def test_launch_count_without_launches():
+    import jagged_flash_attention_gb300 as jfa
+    n0 = jfa.launch_count()
+    assert n0 >= 0
+    jfa.profile_enable(True)
+    jfa.profile_enable(False)
+    prof = jfa.profile_read()
+    assert set(prof) == set(jfa.KERNEL_KINDS)
+    assert jfa.launch_count() == n0

@@ -1,0 +1,36 @@
+"""The library's launch accounting on the GPU: one self-attention forward
+plus backward enqueues exactly the kernels the design names (a scheduler and
+the forward; two schedulers, the Delta pre-pass, the dK/dV pass and the dQ
+pass), and the event timer sees each of them on the launching stream."""
+import pytest
+import torch
+
+from tests.gpu_common import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_self_attention_launches_and_kernel_times():
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs("tiny_self")
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    out, lse = jfa.forward(q, k, v, off, x["max_len"])
+    torch.cuda.synchronize()
+    jfa.profile_read()
+    n0 = jfa.launch_count()
+    jfa.profile_enable(True)
+    try:
+        out, lse = jfa.forward(q, k, v, off, x["max_len"])
+        jfa.backward(q, k, v, off, x["max_len"], out, lse, do)
+        torch.cuda.synchronize()
+    finally:
+        jfa.profile_enable(False)
+    assert jfa.launch_count() - n0 == 7
+    prof = jfa.profile_read()
+    counts = {k: n for k, (t, n) in prof.items() if n}
+    assert counts == {"sched": 3, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_q": 1}
+    for k in counts:
+        assert prof[k][0] > 0.0, k
+    jfa.jfa_sync_and_check()
