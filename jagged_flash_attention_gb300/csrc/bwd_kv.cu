@@ -177,6 +177,8 @@ template <int D, bool CAUSAL>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   const int T = p.hdr->T;
+  // Run by the whole warp; the elected lane issues products and commits.
+  const uint32_t leader = elect_one();
   const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
   // Descriptors built once; per tile and K step only adds remain.
@@ -188,81 +190,102 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   const uint64_t ddo_m0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16384, 1024);
   const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP;
   const uint32_t tDV = tbase + C::kColDV, tDK = tbase + C::kColDK;
-  auto issue_s = [&](uint32_t g) {
+  // Each issue function runs `mid` before its group's last product: the
+  // wait for the next group then overlaps tensor work still queued (issue
+  // blocks while the pipe is full; a wait right after a group would leave it
+  // idle for the wait's own latency).
+  auto issue_s = [&](uint32_t g, auto&& mid) {
     const uint64_t dq_k = desc_add(dq_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
+      if (k == D / 16 - 1 && !mid()) return false;
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
+      if (leader) mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
     }
+    return true;
   };
-  auto issue_dp = [&](uint32_t g) {
+  auto issue_dp = [&](uint32_t g, auto&& mid) {
     const uint64_t ddo_k = desc_add(ddo_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
+      if (k == D / 16 - 1 && !mid()) return false;
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
+      if (leader) mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
     }
+    return true;
   };
   // A operand column of query block k (16 queries): packed P^T / dS^T of
   // queries 0-63 start at +0, of queries 64-127 at +64.
-  auto issue_dv = [&](uint32_t g, bool acc) {
+  auto issue_dv = [&](uint32_t g, bool acc, auto&& mid) {
     const uint64_t ddo_m = desc_add(ddo_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
-    for (int k = 0; k < kBM / 16; ++k)
-      mma_ts(tDV, tS + k * 8 + (k >= 4 ? 32 : 0), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
+    for (int k = 0; k < kBM / 16; ++k) {
+      if (k == kBM / 16 - 1 && !mid()) return false;
+      if (leader) mma_ts(tDV, tS + k * 8 + (k >= 4 ? 32 : 0), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
+    }
+    return true;
   };
   auto issue_dk = [&](uint32_t g, bool acc) {
     const uint64_t dq_m = desc_add(dq_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBM / 16; ++k)
-      mma_ts(tDK, tDP + k * 8 + (k >= 4 ? 32 : 0), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
+      if (leader) mma_ts(tDK, tDP + k * 8 + (k >= 4 ? 32 : 0), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
   };
+  auto none = [] { return true; };
+  auto wait_qdo = [&](uint32_t g) {
+    return mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
+  };
+  auto wait_p = [&](uint32_t g) { return mbar_wait_warp(&c->p_full, g & 1, &c->abort, p.err); };
+  auto wait_ds = [&](uint32_t g) { return mbar_wait_warp(&c->ds_full, g & 1, &c->abort, p.err); };
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, false, &ok, p.err);
+    const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
     const KvItem f = decode<CAUSAL>(p, idx, T);
-    if (!mbar_wait(&c->kv_full, it & 1, &c->abort, p.err)) break;
+    if (!mbar_wait_warp(&c->kv_full, it & 1, &c->abort, p.err)) break;
     const uint32_t g0 = gq;
-    if (!mbar_wait(&c->qdo_full[g0 % C::NSQ], (g0 / C::NSQ) & 1, &c->abort, p.err)) break;
+    if (!wait_qdo(g0)) break;
     tc_fence_after();
-    issue_s(g0);
-    mma_commit(&c->s_full);
-    issue_dp(g0);
-    mma_commit(&c->dp_full);
     issued = true;
+    if (!issue_s(g0, none)) break;
+    if (leader) mma_commit(&c->s_full);
+    // Inside dP(g0): P^T(g0) ready, and the previous item's epilogue has read
+    // the dV / dK accumulators.
+    if (!issue_dp(g0, [&] {
+          return wait_p(g0) && mbar_wait_warp(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err);
+        }))
+      break;
+    if (leader) mma_commit(&c->dp_full);
+    // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = g0 + i;
-      if (!mbar_wait(&c->p_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      if (i == 0 && !mbar_wait(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+      const bool more = i + 1 < f.nt;
       tc_fence_after();
-      issue_dv(g, i > 0);
-      if (i + 1 < f.nt) {  // S(g+1): its P^T(g) columns were just read by dV(g)
-        if (!mbar_wait(&c->qdo_full[(g + 1) % C::NSQ], ((g + 1) / C::NSQ) & 1, &c->abort, p.err)) {
-          ok = false;
-          break;
-        }
-        issue_s(g + 1);
-        mma_commit(&c->s_full);
+      if (!issue_dv(g, i > 0, [&] { return !more || wait_qdo(g + 1); })) { ok = false; break; }
+      if (more) {  // S(g+1): its P^T(g) columns were just read by dV(g)
+        tc_fence_after();
+        if (!issue_s(g + 1, [&] { return wait_ds(g); })) { ok = false; break; }
+        if (leader) mma_commit(&c->s_full);
+      } else if (!wait_ds(g)) {
+        ok = false;
+        break;
       }
-      if (!mbar_wait(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
       issue_dk(g, i > 0);
-      mma_commit(&c->qdo_empty[g % C::NSQ]);
-      if (i + 1 < f.nt) {  // dP(g+1): its dS^T(g) columns were just read by dK(g)
-        issue_dp(g + 1);
-        mma_commit(&c->dp_full);
+      if (leader) mma_commit(&c->qdo_empty[g % C::NSQ]);
+      if (more) {  // dP(g+1): its dS^T(g) columns were just read by dK(g)
+        if (!issue_dp(g + 1, [&] { return wait_p(g + 1); })) { ok = false; break; }
+        if (leader) mma_commit(&c->dp_full);
       }
     }
     if (!ok) break;
     gq += f.nt;
-    mma_commit(&c->dkdv_full);
-    mma_commit(&c->kv_empty);
+    if (leader) mma_commit(&c->dkdv_full);
+    if (leader) mma_commit(&c->kv_empty);
     ++it;
   }
-  if (issued) {
+  if (issued && leader) {
     mma_commit(&c->drain);
     drain_wait(&c->drain, 0, p.err);
   }
@@ -439,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c->qdo_full[i], 1);
       mbar_init(&c->qdo_empty[i], 1);
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA thread
+      mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA warp
     }
     mbar_init(&c->s_full, 1);
     mbar_init(&c->dp_full, 1);
@@ -472,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
-    if (lane == 0) mma_role<D, CAUSAL>(p, smem, c, tbase);
+    mma_role<D, CAUSAL>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();

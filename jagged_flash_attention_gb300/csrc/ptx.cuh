@@ -271,6 +271,22 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// 1 in exactly one lane of the calling warp, 0 in the others.  Every lane of
+// the warp must execute it.  An MMA role run by the whole warp, with products
+// and commits issued by the elected lane, keeps its descriptor arithmetic
+// warp-uniform; a role run by one lane inside a divergent branch needs
+// several issue slots per product, which busy warps sharing its
+// sub-partition then delay.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t is_leader;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(is_leader));
+  return is_leader;
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
