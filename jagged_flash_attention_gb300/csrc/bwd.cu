@@ -222,6 +222,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t tbase) {
   using C = BwdCfg<D>;
+  // Run by the whole warp; the elected lane issues products and commits.
+  const uint32_t leader = elect_one();
   const int T = p.hdr->T;
   const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   const uint32_t id_dv = idesc_bf16_f32(128, D, false, true);     // dV (A = P^T in TMEM)
@@ -241,27 +243,27 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, false, &ok, p.err);
+    const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
     const BwdTile f = decode<BCAST, CAUSAL>(p, idx, T);
-    if (!mbar_wait(&c->kv_full, it & 1, &c->abort, p.err)) break;
+    if (!mbar_wait_warp(&c->kv_full, it & 1, &c->abort, p.err)) break;
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
       const int st = g % C::NSQ;
       const uint32_t so = st * C::kTile;
       const uint64_t dq_k = desc_add(dq_k0, so), dq_m = desc_add(dq_m0, so);
       const uint64_t ddo_k = desc_add(ddo_k0, so), ddo_m = desc_add(ddo_m0, so);
-      if (!mbar_wait(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
+      if (!mbar_wait_warp(&c->qdo_full[st], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
       // S^T overwrites P^T of the previous tile, read by its dV MMA issued
       // earlier (MMAs of one CTA execute in issue order).
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tbase + C::kColS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
+        if (leader) mma_ss(tbase + C::kColS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
       }
       // D=128: dQ^T of the previous tile lives in the dP^T columns.
-      if (C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+      if (C::kDqT && g > 0 && !mbar_wait_warp(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
@@ -269,31 +271,32 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tbase + C::kColDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
+        if (leader) mma_ss(tbase + C::kColDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
       }
-      mma_commit(&c->st_full);
+      if (leader) mma_commit(&c->st_full);
       issued = true;
-      if (!mbar_wait(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      if (i == 0 && !mbar_wait(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+      if (!mbar_wait_warp(&c->ds_full, g & 1, &c->abort, p.err)) { ok = false; break; }
+      if (i == 0 && !mbar_wait_warp(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < kBM / 16; ++k)
-        mma_ts(tbase + C::kColDV, tbase + C::kColS + k * 8, desc_add(ddo_m, k * 2048), id_dv,
+        if (leader) mma_ts(tbase + C::kColDV, tbase + C::kColS + k * 8, desc_add(ddo_m, k * 2048), id_dv,
                (i > 0) || (k > 0));
 #pragma unroll
       for (int k = 0; k < kBM / 16; ++k) {
         const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-        mma_ss(tbase + C::kColDK, desc_add(dds_k, off), desc_add(dq_m, k * 2048), id_dk,
+        if (leader) mma_ss(tbase + C::kColDK, desc_add(dds_k, off), desc_add(dq_m, k * 2048), id_dk,
                (i > 0) || (k > 0));
       }
-      mma_commit(&c->qdo_empty[st]);
-      if (!C::kDqT && g > 0 && !mbar_wait(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
+      if (leader) mma_commit(&c->qdo_empty[st]);
+      if (!C::kDqT && g > 0 && !mbar_wait_warp(&c->dq_empty, (g - 1) & 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < kBN / 16; ++k) {
+        if (!leader) continue;
         if (C::kDqT)
           mma_ss(tbase + C::kColDQ, desc_add(dk_m, k * 2048), desc_add(dds_m, k * 2048), id_dq,
                  k > 0);
@@ -301,14 +304,14 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BwdCtl* c, uint32_t 
           mma_ss(tbase + C::kColDQ, desc_add(dds_m, k * 2048), desc_add(dk_m, k * 2048), id_dq,
                  k > 0);
       }
-      mma_commit(&c->dq_full);
+      if (leader) mma_commit(&c->dq_full);
     }
     if (!ok) break;
-    mma_commit(&c->dkdv_full);
-    mma_commit(&c->kv_empty);
+    if (leader) mma_commit(&c->dkdv_full);
+    if (leader) mma_commit(&c->kv_empty);
     ++it;
   }
-  if (issued) {
+  if (issued && leader) {
     mma_commit(&c->drain);
     drain_wait(&c->drain, 0, p.err);
   }
@@ -552,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
-    if (lane == 0) mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+    mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();

@@ -206,6 +206,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 template <int D, bool CAUSAL>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tbase) {
   using C = QCfg<D>;
+  // Run by the whole warp; the elected lane issues products and commits.
+  const uint32_t leader = elect_one();
   const int T = p.hdr->T;
   const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
   const uint32_t id_dq = idesc_bf16_f32(128, D, false, true);    // dQ (A = dS in TMEM)
@@ -220,7 +222,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      mma_ss(tbase + 256 * g, desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
+      if (leader) mma_ss(tbase + 256 * g, desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
     }
   };
   auto issue_dp = [&](int g, uint32_t vidx) {
@@ -229,7 +231,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      mma_ss(tbase + 256 * g, desc_add(ddo, off), desc_add(dv, off), id_s, k > 0);
+      if (leader) mma_ss(tbase + 256 * g, desc_add(ddo, off), desc_add(dv, off), id_s, k > 0);
     }
   };
   auto issue_dq = [&](int g, uint32_t kidx, bool acc) {
@@ -237,7 +239,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     const uint64_t dk = desc_add(dk_m0, (kidx % C::NSK) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBN / 16; ++k)
-      mma_ts(tbase + 256 * g + 128, tbase + 256 * g + 8 * k + (k >= 4 ? 32 : 0),
+      if (leader) mma_ts(tbase + 256 * g + 128, tbase + 256 * g + 8 * k + (k >= 4 ? 32 : 0),
              desc_add(dk, k * 2048), id_dq, acc || (k > 0));
   };
   uint32_t it = 0, nk = 0, nv = 0;
@@ -245,10 +247,10 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
   uint32_t gi[2] = {0, 0};  // items in which the slot was present
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, false, &ok, p.err);
+    const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
     const QItem f = decode<CAUSAL>(p, idx, T);
-    if (!mbar_wait(&c->qdo_full, it & 1, &c->abort, p.err)) break;
+    if (!mbar_wait_warp(&c->qdo_full, it & 1, &c->abort, p.err)) break;
     const int N = f.N;
     const int nt[2] = {f.t[0].n, f.t[1].n};
     const uint32_t k0 = nk, v0 = nv;
@@ -259,41 +261,41 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
       for (int g = 0; g < 2; ++g) {
         if (j >= 1 && j - 1 < nt[g]) {
           const uint32_t u = gt[g] + j - 1;
-          if (!mbar_wait(&c->ds_full[g], u & 1, &c->abort, p.err)) { ok = false; break; }
-          if (j == 1 && !mbar_wait(&c->dq_free[g], (gi[g] & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+          if (!mbar_wait_warp(&c->ds_full[g], u & 1, &c->abort, p.err)) { ok = false; break; }
+          if (j == 1 && !mbar_wait_warp(&c->dq_free[g], (gi[g] & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
           tc_fence_after();
           issue_dq(g, k0 + j - 1, j > 1);
-          if (j == nt[g]) mma_commit(&c->dq_full[g]);
+          if (j == nt[g]) if (leader) mma_commit(&c->dq_full[g]);
         }
         if (j < nt[g]) {
           if (!k_ready) {
             const uint32_t kk = k0 + j;
-            if (!mbar_wait(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
+            if (!mbar_wait_warp(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
             k_ready = true;
           }
           tc_fence_after();
           issue_s(g, k0 + j);
-          mma_commit(&c->s_full[g]);
+          if (leader) mma_commit(&c->s_full[g]);
           issued = true;
         }
       }
       if (!ok) break;
-      if (j >= 1) mma_commit(&c->k_empty[(k0 + j - 1) % C::NSK]);  // K(j-1) fully read
+      if (j >= 1) if (leader) mma_commit(&c->k_empty[(k0 + j - 1) % C::NSK]);  // K(j-1) fully read
       if (j < N) {
         const uint32_t vv = v0 + j;
-        if (!mbar_wait(&c->v_full[vv % C::NSV], (vv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&c->v_full[vv % C::NSV], (vv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           if (j < nt[g]) {
-            if (!mbar_wait(&c->p_done[g], (gt[g] + j) & 1, &c->abort, p.err)) { ok = false; break; }
+            if (!mbar_wait_warp(&c->p_done[g], (gt[g] + j) & 1, &c->abort, p.err)) { ok = false; break; }
             tc_fence_after();
             issue_dp(g, vv);
-            mma_commit(&c->dp_full[g]);
+            if (leader) mma_commit(&c->dp_full[g]);
           }
         }
         if (!ok) break;
-        mma_commit(&c->v_empty[vv % C::NSV]);
-        if (j == N - 1) mma_commit(&c->qdo_empty);  // Q and dO are read by S and dP only
+        if (leader) mma_commit(&c->v_empty[vv % C::NSV]);
+        if (j == N - 1) if (leader) mma_commit(&c->qdo_empty);  // Q and dO are read by S and dP only
       }
     }
     if (!ok) break;
@@ -305,7 +307,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     nv += N;
     ++it;
   }
-  if (issued) {
+  if (issued && leader) {
     mma_commit(&c->drain);
     drain_wait(&c->drain, 0, p.err);
   }
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA thread
+      mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA warp
     }
     mbar_init(&c->drain, 1);
     c->abort = 0;
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
-    if (lane == 0) mma_role<D, CAUSAL>(p, smem, c, tbase);
+    mma_role<D, CAUSAL>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();

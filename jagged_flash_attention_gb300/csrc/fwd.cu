@@ -224,31 +224,36 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 // S_t = Q_t K^T: dq / dk are the K-major descriptors of the Q tile and the
 // K stage (start of the tile); K steps advance them inside 128-byte rows.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tbase, int t, uint64_t dq, uint64_t dk) {
+__device__ __forceinline__ void issue_s(uint32_t leader, uint32_t tbase, int t, uint64_t dq,
+                                        uint64_t dk) {
   using C = FwdCfg<D>;
   const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-    mma_ss(tbase + C::colS(t), desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
+    if (leader) mma_ss(tbase + C::colS(t), desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
   }
 }
 
 // O_t += P_t V: dv is the MN-major descriptor of the V stage.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tbase, int t, uint64_t dv, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t tbase, int t, uint64_t dv,
+                                         bool accumulate) {
   using C = FwdCfg<D>;
   const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
 #pragma unroll
   for (int k = 0; k < kBN / 16; ++k) {
-    mma_ts(tbase + C::colO(t), tbase + C::colS(t) + k * 8, desc_add(dv, k * 2048), id_pv,
-           accumulate || (k > 0));
+    if (leader)
+      mma_ts(tbase + C::colO(t), tbase + C::colS(t) + k * 8, desc_add(dv, k * 2048), id_pv,
+             accumulate || (k > 0));
   }
 }
 
 template <int D, bool CAUSAL, bool BCAST>
 __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
+  // Run by the whole warp; the elected lane issues products and commits.
+  const uint32_t leader = elect_one();
   const int T = p.hdr->T;
   const uint64_t dq0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
   const uint64_t dk0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
@@ -259,60 +264,60 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   bool ok = true;
   bool issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, false, &ok, p.err);
+    const int idx = next_item(c, n, true, &ok, p.err);
     if (idx < 0) break;
     const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
     if (f.N == 0) continue;
-    if (!mbar_wait(&c->q_full, itq & 1, &c->abort, p.err)) break;
+    if (!mbar_wait_warp(&c->q_full, itq & 1, &c->abort, p.err)) break;
     ++itq;
     for (int j = 0; j <= f.N && ok; ++j) {
       uint64_t dk = 0, dv = 0;
       if (j < f.N) {
         const int st = nk % C::NSK;
-        if (!mbar_wait(&c->k_full[st], (nk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&c->k_full[st], (nk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
         dk = desc_add(dk0, st * C::kTile);
       }
       if (j >= 1) {
         const int st = nv % C::NSV;
-        if (!mbar_wait(&c->v_full[st], (nv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&c->v_full[st], (nv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
         dv = desc_add(dv0, st * C::kTile);
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int nkv = f.t[t].n_kv;
         if (j >= 1 && j - 1 < nkv) {  // O_t += P_t(j-1) V(j-1)
-          if (!mbar_wait(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
+          if (!mbar_wait_warp(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
           ++np[t];
-          if (j == 1 && !mbar_wait(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
+          if (j == 1 && !mbar_wait_warp(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv<D>(tbase, t, dv, j > 1);
-          mma_commit(&c->o_ready[t]);
+          issue_pv<D>(leader, tbase, t, dv, j > 1);
+          if (leader) mma_commit(&c->o_ready[t]);
         }
         if (j < nkv) {  // S_t(j) = Q_t K(j)^T
-          issue_s<D>(tbase, t, desc_add(dq0, t * C::kTile), dk);
-          mma_commit(&c->s_full[t]);
+          issue_s<D>(leader, tbase, t, desc_add(dq0, t * C::kTile), dk);
+          if (leader) mma_commit(&c->s_full[t]);
           issued = true;
         }
       }
       if (!ok) break;
       if (j >= 1) {
-        mma_commit(&c->v_empty[nv % C::NSV]);
+        if (leader) mma_commit(&c->v_empty[nv % C::NSV]);
         ++nv;
       }
       if (j < f.N) {
-        mma_commit(&c->k_empty[nk % C::NSK]);
+        if (leader) mma_commit(&c->k_empty[nk % C::NSK]);
         ++nk;
-        if (j == f.N - 1) mma_commit(&c->q_empty);
+        if (j == f.N - 1) if (leader) mma_commit(&c->q_empty);
       }
     }
 #pragma unroll
     for (int t = 0; t < 2; ++t)
       if (f.t[t].n_kv > 0) ++ito[t];
   }
-  if (issued) {
+  if (issued && leader) {
     mma_commit(&c->drain);
     drain_wait(&c->drain, 0, p.err);
   }
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, p, smem, c);
   } else {
-    if (lane == 0) mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+    mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();
