@@ -78,11 +78,12 @@ jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* o
 /* Backward pass, self-attention: given out, lse from jfa_fwd and dout,
  * writes dq, dk, dv (gradients of sum(out * dout)).  The products of
  * "Optimizing Jagged Flash Attention with TLX", section "2-CTA
- * collaborative MMA", after the Delta = rowsum(dout * out) pre-pass, in two
- * passes: a K/V-block-outer pass for dk and dv and a query-tile-outer pass
- * for dq, so that dq accumulates on chip and needs no global fp32
- * accumulator (the page's "Multi-stage dQ staging" is not needed).  Five
- * kernels: two schedulers, the pre-pass and the two passes. */
+ * collaborative MMA", after a pre-pass (the two work lists and the row
+ * statistics LSE*log2(e) and Delta = rowsum(dout * out)), in two passes: a
+ * K/V-block-outer pass for dk and dv and a query-tile-outer pass for dq, so
+ * that dq accumulates on chip and needs no global fp32 accumulator (the
+ * page's "Multi-stage dQ staging" is not needed).  Three kernels: the
+ * pre-pass and the two passes. */
 jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
                    int H, int D, int max_len, int broadcast_q, int causal, float scale,
                    const void* out, const float* lse, const void* dout, void* dq, void* dk,
@@ -142,9 +143,9 @@ const char* jfa_version(void);
 
 /* Kernel kinds reported by jfa_profile_read (array index). */
 typedef enum {
-  JFA_KERNEL_SCHED = 0,     /* work-list scheduler */
+  JFA_KERNEL_SCHED = 0,     /* forward work-list scheduler */
   JFA_KERNEL_FWD = 1,       /* forward */
-  JFA_KERNEL_PREP = 2,      /* Delta = rowsum(dO * O) pre-pass */
+  JFA_KERNEL_PREP = 2,      /* backward pre-pass: work lists, LSE*log2e, Delta */
   JFA_KERNEL_BWD_KV = 3,    /* self-attention backward, dK / dV pass */
   JFA_KERNEL_BWD_Q = 4,     /* self-attention backward, dQ pass */
   JFA_KERNEL_BWD_FUSED = 5, /* broadcast-Q backward (dK, dV, dQ partials) */

@@ -282,14 +282,16 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kFwdRows);
   if (cap_kv >= (1LL << 31) || cap_q >= (1LL << 31))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
-  const long long delta_elems = (long long)s.H * s.Tcap;
+  const long long stat_elems = (long long)s.H * s.Tcap;
   size_t off = 0;
   const size_t hkv_off = off;
   off = align256(off + 256 + cap_kv * sizeof(Item));
   const size_t hq_off = off;
   off = align256(off + 256 + cap_q * sizeof(Item));
-  const size_t delta_off = off;
-  off = align256(off + delta_elems * sizeof(float));
+  const size_t stat_off = off;
+  off = align256(off + (kStatPad + stat_elems) * sizeof(float2));
+  const size_t stat_odd_off = off;
+  off = align256(off + (kStatPad + stat_elems) * sizeof(float2));
   CUtensorMap tq, tk, tv, tdo;
   if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
   if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
@@ -303,7 +305,8 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   Item* items_kv = reinterpret_cast<Item*>(base + hkv_off + 256);
   WorkHeader* hdr_q = reinterpret_cast<WorkHeader*>(base + hq_off);
   Item* items_q = reinterpret_cast<Item*>(base + hq_off + 256);
-  float* delta = reinterpret_cast<float*>(base + delta_off);
+  float2* stat = reinterpret_cast<float2*>(base + stat_off) + kStatPad;
+  float2* stat_odd = reinterpret_cast<float2*>(base + stat_odd_off) + kStatPad;
   SchedParams sk{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 1, kBM,
                  items_kv, (int)cap_kv, hdr_kv, ds->err};
   SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kFwdRows,
@@ -317,29 +320,31 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   bp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
   bp.scale = s.scale;
   bp.lse = lse;
-  bp.delta = delta;
+  bp.stat = stat;
+  bp.stat_odd = stat_odd;
   bp.dq = static_cast<__nv_bfloat16*>(dq);
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
   bp.err = ds->err;
-  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
-    return launch_sched(sk, stream);
-  });
-  if (e == cudaSuccess) e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
-    return launch_sched(sq, stream);
-  });
-  if (e == cudaSuccess) {
+  {
+    // One launch: both work lists and the row statistics.
     PrepParams pp;
     memset(&pp, 0, sizeof(pp));
     pp.out = static_cast<const __nv_bfloat16*>(out);
     pp.dout = static_cast<const __nv_bfloat16*>(dout);
-    pp.delta = delta;
+    pp.offsets = offsets;
+    pp.lse = lse;
+    pp.stat = stat;
+    pp.stat_odd = stat_odd;
+    pp.Tcap = s.Tcap;
     pp.B = s.B;
     pp.H = s.H;
     pp.D = s.D;
-    pp.hdr = hdr_kv;
+    pp.n_sched = 2;
+    pp.sched[0] = sk;
+    pp.sched[1] = sq;
     e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
-      return launch_prep(pp, ds->sms, stream);
+      return launch_bwd_prep(pp, ds->sms, stream);
     });
   }
   if (e == cudaSuccess) {
@@ -424,29 +429,30 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
   float* acc = reinterpret_cast<float*>(base + acc_off);
   SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1, kBM,
                  items, (int)cap, hdr, ds->err};
-  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
-    return launch_sched(sp, stream);
-  });
-  if (e == cudaSuccess) {
+  {
+    // One launch: the work list, Delta and the zeroed dQ accumulator.
     PrepParams pp;
+    memset(&pp, 0, sizeof(pp));
     pp.out = static_cast<const __nv_bfloat16*>(out);
     pp.dout = static_cast<const __nv_bfloat16*>(dout);
+    pp.offsets = offsets;
     pp.delta = delta;
     pp.dq_acc = acc;
-    pp.dq_acc_elems_bcast = s.broadcast ? acc_elems : 0;
+    pp.dq_acc_elems_bcast = acc_elems;
     pp.B = s.B;
     pp.H = s.H;
     pp.D = s.D;
     pp.Lq = s.Lq;
-    pp.broadcast = s.broadcast;
-    pp.zero_self_acc = 0;
-    pp.hdr = hdr;
+    pp.broadcast = 1;
+    pp.n_sched = 1;
+    pp.sched[0] = sp;
     e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
-      return launch_prep(pp, ds->sms, stream);
+      return launch_bwd_prep(pp, ds->sms, stream);
     });
   }
   if (e == cudaSuccess) {
     BwdParams bp;
+    memset(&bp, 0, sizeof(bp));
     bp.offsets = offsets;
     bp.B = s.B;
     bp.H = s.H;

@@ -1,6 +1,7 @@
-// Device work-list scheduler, backward pre-pass (Delta = rowsum(dO * O) and
-// zeroing of the fp32 dQ accumulator), dQ finalisation, and a fill kernel
-// for the all-empty broadcast case.
+// Device work-list scheduler, backward pre-pass (work lists, the row
+// statistics LSE*log2e and Delta = rowsum(dO * O), zeroing of the broadcast
+// fp32 dQ accumulator), dQ finalisation, and a fill kernel for the
+// all-empty broadcast case.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -60,7 +61,8 @@ __device__ void scan_desc(const int* hist, int* base, int* warp_tot) {
   base[k] = warp_tot[tid >> 5] + x - v;
 }
 
-__global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) {
+// Builds one work list with the whole block (kSchedThreads threads).
+__device__ void sched_body(const SchedParams& p) {
   __shared__ int hist[kMaxBuckets];
   __shared__ int base[kMaxBuckets];
   __shared__ int cursor[kMaxBuckets];
@@ -103,20 +105,25 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) {
     }
     return;
   }
-  for (int b = tid; b < p.B; b += blockDim.x) {
+  // One warp per sequence: lane 0 reserves the sequence's slots in its
+  // bucket, the lanes write the items.  Heads outer, tiles inner, so that
+  // consecutive items share K/V (or Q) in L2; forward causal: longest query
+  // tile first.
+  const int lane = tid & 31, nwarps = blockDim.x >> 5;
+  const bool reverse = !p.backward && p.causal;
+  for (int b = tid >> 5; b < p.B; b += nwarps) {
     const int L = p.offsets[b + 1] - p.offsets[b];
     const int nt = n_tiles(p, L);
     if (nt == 0) continue;
-    const int key = bucket_of(p, L);
-    int pos = base[key] + atomicAdd(&cursor[key], p.H * nt);
-    // Heads outer, tiles inner, so that consecutive items share K/V (or Q)
-    // in L2.  Forward causal: longest query tile first.
-    const bool reverse = !p.backward && p.causal;
-    for (int h = 0; h < p.H; ++h)
-      for (int t = 0; t < nt; ++t) {
-        const int tt = reverse ? nt - 1 - t : t;
-        p.items[pos++] = make_int2(b, (h << 16) | tt);
-      }
+    const int n = p.H * nt;
+    int pos = 0;
+    if (lane == 0) pos = base[bucket_of(p, L)] + atomicAdd(&cursor[bucket_of(p, L)], n);
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    for (int j = lane; j < n; j += 32) {
+      const int h = j / nt, t = j - h * nt;
+      const int tt = reverse ? nt - 1 - t : t;
+      p.items[pos + j] = make_int2(b, (h << 16) | tt);
+    }
   }
   if (tid == 0) {
     p.hdr->n_items = total;
@@ -126,59 +133,108 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) {
   }
 }
 
-// Delta[row] = sum_d dO[row, d] * O[row, d] in fp32; 16 threads per row of
-// D=128 (8 for D=64), each reading 16 bytes of both tensors.
-__global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
-  const int T = p.hdr->T;
-  const bool ok = p.hdr->valid != 0;
-  const int tpr = p.D / 8;  // threads per row
-  const long long rows = p.broadcast ? (long long)p.B * p.Lq * p.H : (long long)T * p.H;
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  if (ok) {
-    // Warp-uniform loop: each warp owns 32/tpr consecutive rows per step.
-    const int lane = threadIdx.x & 31;
-    const int rows_per_warp = 32 / tpr;
-    const long long wid = gtid >> 5, nwarps = nthreads >> 5;
-    for (long long r0 = wid * rows_per_warp; r0 < rows; r0 += nwarps * rows_per_warp) {
-      const long long row = r0 + lane / tpr;
-      const int part = lane % tpr;
-      const bool valid = row < rows;
-      float acc = 0.f;
-      if (valid) {
-        const uint4 o = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
-        const uint4 g = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+__global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) { sched_body(p); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Row statistics of the backward pass with blocks [0, nblk) of the caller's
+// grid: Delta[row] = sum_d dO[row, d] * O[row, d] in fp32 (the rowsum the
+// gradient of the softmax subtracts), and for self-attention LSE*log2e next
+// to it.  tpr = D/8 threads per row, each reading 16 bytes of both tensors;
+// kUnroll rows per thread in flight.
+constexpr int kUnroll = 2;
+
+__device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
+  long long rows;
+  int T = 0;
+  if (p.broadcast) {
+    rows = static_cast<long long>(p.B) * p.Lq * p.H;
+  } else {
+    // T is validated by the scheduler blocks; here it only has to keep the
+    // reads inside the caller's Tcap rows.
+    T = p.offsets[p.B];
+    if (T < 0 || T > p.Tcap) return;
+    rows = static_cast<long long>(T) * p.H;
+  }
+  if (!p.broadcast && blk == 0) {
+    // The front padding that boxes starting before row 0 read: zeros (a
+    // finite Delta for the columns those boxes mask), except stat_odd[-1],
+    // which is stat[0] and written below.
+    for (int i = threadIdx.x; i < kStatPad; i += blockDim.x) {
+      p.stat[i - kStatPad] = make_float2(0.f, 0.f);
+      if (i < kStatPad - 1) p.stat_odd[i - kStatPad] = make_float2(0.f, 0.f);
+    }
+  }
+  const int tpr = p.D / 8;
+  const int rpw = 32 / tpr;  // rows per warp and unroll step
+  const int lane = threadIdx.x & 31;
+  const int part = lane % tpr;
+  const long long wid = (blk * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (nblk * blockDim.x) >> 5;
+  const long long step = static_cast<long long>(rpw) * kUnroll;
+  for (long long r0 = wid * step; r0 < rows; r0 += nw * step) {
+    uint4 o[kUnroll], g[kUnroll];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 a = __bfloat1622float2(o2[i]);
-          const float2 c = __bfloat1622float2(g2[i]);
-          acc = fmaf(a.x, c.x, acc);
-          acc = fmaf(a.y, c.y, acc);
-        }
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long row = r0 + u * rpw + lane / tpr;
+      if (row < rows) {
+        o[u] = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
+        g[u] = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
+      } else {
+        o[u] = make_uint4(0, 0, 0, 0);
+        g[u] = o[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o[u]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(o2[i]);
+        const float2 c = __bfloat1622float2(g2[i]);
+        acc = fmaf(a.x, c.x, acc);
+        acc = fmaf(a.y, c.y, acc);
       }
       for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (valid && part == 0) {
-        long long di;
+      const long long row = r0 + u * rpw + lane / tpr;
+      if (row < rows && part == 0) {
         if (p.broadcast) {
           const long long h = row % p.H;
           const long long bi = row / p.H;  // b * Lq + i
           const long long b = bi / p.Lq, i = bi % p.Lq;
-          di = (b * p.H + h) * p.Lq + i;
+          p.delta[(b * p.H + h) * p.Lq + i] = acc;
         } else {
           const long long h = row % p.H, t = row / p.H;
-          di = h * T + t;
+          const long long si = h * T + t;
+          const float2 v = make_float2(p.lse[si] * kLog2e, acc);
+          p.stat[si] = v;
+          p.stat_odd[si - 1] = v;
         }
-        p.delta[di] = acc;
       }
     }
   }
-  // zero the fp32 dQ accumulator
-  const long long n = p.broadcast ? p.dq_acc_elems_bcast
-                                  : (ok && p.zero_self_acc ? (long long)T * p.H * p.D : 0);
-  float4* z = reinterpret_cast<float4*>(p.dq_acc);
-  for (long long i = gtid; i < n / 4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Backward pre-pass: work lists (blocks [0, n_sched)), row statistics and,
+// for broadcast-Q, zeroing of the fp32 dQ accumulator (the other blocks).
+__global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
+  if (blockIdx.x < p.n_sched) {
+    if (blockIdx.x == 0)
+      sched_body(p.sched[0]);
+    else
+      sched_body(p.sched[1]);
+    return;
+  }
+  const long long blk = blockIdx.x - p.n_sched, nblk = gridDim.x - p.n_sched;
+  stats_body(p, blk, nblk);
+  if (p.broadcast) {
+    const long long gtid = blk * blockDim.x + threadIdx.x;
+    float4* z = reinterpret_cast<float4*>(p.dq_acc);
+    for (long long i = gtid; i < p.dq_acc_elems_bcast / 4; i += nblk * blockDim.x)
+      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // dq = bf16(scale * sum over shards of the fp32 accumulator)
@@ -220,8 +276,8 @@ cudaError_t launch_sched(const SchedParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const PrepParams& p, int sms, cudaStream_t s) {
-  prep_kernel<<<sms * 8, 256, 0, s>>>(p);
+cudaError_t launch_bwd_prep(const PrepParams& p, int sms, cudaStream_t s) {
+  bwd_prep_kernel<<<p.n_sched + sms * 2, kSchedThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -33,7 +33,6 @@ constexpr int kThreads = 320;
 constexpr int kMath = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct KvCfg {
@@ -44,8 +43,10 @@ struct KvCfg {
   static constexpr int kV = kTile;
   static constexpr int kQ = 2 * kTile;
   static constexpr int kDO = kQ + NSQ * kTile;
-  static constexpr int kStat = kDO + NSQ * kTile;  // LSE*log2e and Delta, 2 buffers
-  static constexpr int kCtl = kStat + 2 * 2 * kBM * 4;
+  // {LSE*log2e, Delta} of the 128 query rows of each Q / dO stage
+  static constexpr int kStatBytes = kBM * 8;
+  static constexpr int kStat = kDO + NSQ * kTile;
+  static constexpr int kCtl = kStat + NSQ * kStatBytes;
   static constexpr int kSmem = kCtl + 512;
   static constexpr uint32_t kColS = 0, kColDP = 128;
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
@@ -56,7 +57,6 @@ struct KvCtl {
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dkdv_full, dkdv_empty;
-  uint64_t stat_full[2];  // per query half: LSE / Delta of the next tile staged
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item_slot[2];
@@ -157,7 +157,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
-      mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile);
+      // Row statistics of the box: from stat if its first entry is 16-byte
+      // aligned there, else from the copy shifted by one entry.
+      const long long sidx = static_cast<long long>(f.h) * T + qb.row;
+      const float2* ssrc = (sidx & 1) ? p.stat_odd + (sidx - 1) : p.stat + sidx;
+      mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile + C::kStatBytes);
+      bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->qdo_full[st]);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
         tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->qdo_full[st], s * 64, f.h,
@@ -299,19 +304,6 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
-  float* s_lse = reinterpret_cast<float*>(smem + C::kStat);  // [2][128]
-  float* s_dlt = s_lse + 2 * kBM;                            // [2][128]
-  // LSE*log2e and Delta of query column `col` of tile t (+inf / 0 outside).
-  auto stat_of = [&](const KvItem& f, int t, int col, float& lv, float& dv) {
-    const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
-    lv = INFINITY;
-    dv = 0.f;
-    if (col >= qb.shift && col < qb.shift + qb.n) {
-      const long long si = static_cast<long long>(f.h) * T + f.off0 + t * kBM - qb.shift + col;
-      lv = p.lse[si] * kLog2e;
-      dv = p.delta[si];
-    }
-  };
   uint32_t it = 0, gq = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
@@ -320,28 +312,24 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     const KvItem f = decode<CAUSAL>(p, idx, T);
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
     const bool key_ok = r >= f.kt.shift && r < f.kt.shift + f.kt.n;
-    const int scol = 64 * half + r;  // staging column written by threads r < 64
-    // Stage the first tile's LSE / Delta (later tiles are prefetched).
-    if (r < 64) {
-      float lv, dv;
-      stat_of(f, f.t0, scol, lv, dv);
-      s_lse[(gq & 1) * kBM + scol] = lv;
-      s_dlt[(gq & 1) * kBM + scol] = dv;
-    }
-    mbar_arrive(&c->stat_full[half]);
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
       const int q0 = t * kBM - qb.shift;  // local query index of column 0
-      // Prefetch the next tile's LSE / Delta into registers.
-      float nlv = INFINITY, ndv = 0.f;
-      if (r < 64 && i + 1 < f.nt) stat_of(f, t + 1, scol, nlv, ndv);
-      if (!mbar_wait_warp(&c->stat_full[half], g & 1, &c->abort, p.err)) { ok = false; break; }
-      const float* lse_t = s_lse + (g & 1) * kBM;
-      const float* dlt_t = s_dlt + (g & 1) * kBM;
-      const int c_min = CAUSAL ? key - q0 : -1;  // causal: column c admissible iff c >= c_min
-      const bool diag = CAUSAL && __any_sync(0xffffffffu, c_min > 64 * half);
+      // The statistics arrived with Q / dO of the stage (already complete
+      // once S^T is; waited on here for their visibility).
+      if (!mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
+      // Column c: {LSE*log2e, Delta, and the same of column c+1} at stat4[c/2].
+      const float4* stat4 = reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
+      // Admissible query columns [lo, hi): the box's rows of the sequence
+      // and, causal, the queries at or after this key.
+      int lo = qb.shift;
+      const int hi = qb.shift + qb.n;
+      if (CAUSAL) lo = max(lo, key - q0);
+      const bool ragged = qb.shift > 0 || qb.n < kBM;
+      const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > 64 * half));
+      const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
       // ---- P part: P^T = exp2(S^T * scale*log2e - LSE*log2e)
       if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
@@ -356,12 +344,16 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         // and dK depends only on row r of P^T and dS^T, and those rows are
         // never stored.
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc)
-          pv[32 * ch + cc] = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -lse_t[cbase + cc]));
-        if (diag) {  // causal diagonal tile: queries before this key
+        for (int cc = 0; cc < 32; cc += 2) {
+          const float4 st2 = stat4[(cbase + cc) / 2];
+          pv[32 * ch + cc] = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -st2.x));
+          pv[32 * ch + cc + 1] = ex2_approx(fmaf(__uint_as_float(sraw[cc + 1]), sl2, -st2.z));
+        }
+        if (mask) {  // ragged or causal diagonal tile: zero inadmissible columns
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc)
-            pv[32 * ch + cc] = cbase + cc >= c_min ? pv[32 * ch + cc] : 0.f;
+            pv[32 * ch + cc] =
+                static_cast<uint32_t>(cbase + cc - lo) < span ? pv[32 * ch + cc] : 0.f;
         }
         uint32_t pk[16];
 #pragma unroll
@@ -385,9 +377,9 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         uint32_t dk[16];
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 2) {
-          const int col = cbase + cc;
-          const float d0 = pv[32 * ch + cc] * (__uint_as_float(praw[cc]) - dlt_t[col]);
-          const float d1 = pv[32 * ch + cc + 1] * (__uint_as_float(praw[cc + 1]) - dlt_t[col + 1]);
+          const float4 st2 = stat4[(cbase + cc) / 2];
+          const float d0 = pv[32 * ch + cc] * (__uint_as_float(praw[cc]) - st2.y);
+          const float d1 = pv[32 * ch + cc + 1] * (__uint_as_float(praw[cc + 1]) - st2.w);
           dk[cc / 2] = pack_bf16x2(d0, d1);
         }
         tmem_st16(tbase + lane_base + C::kColDP + 64 * half + 16 * ch, dk);
@@ -395,16 +387,6 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->ds_full);
-      // Stage the prefetched LSE / Delta of the next tile; every thread of
-      // the half has passed this tile's stat wait, so buffer (g+1)&1 (last
-      // read in tile g-1) is free.
-      if (i + 1 < f.nt) {
-        if (r < 64) {
-          s_lse[((g + 1) & 1) * kBM + scol] = nlv;
-          s_dlt[((g + 1) & 1) * kBM + scol] = ndv;
-        }
-        mbar_arrive(&c->stat_full[half]);
-      }
     }
     if (!ok) break;
     // Item epilogue: dV and scale * dK rows of this K/V block (this warp's
@@ -470,8 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c->ds_full, kMath);
     mbar_init(&c->dkdv_full, 1);
     mbar_init(&c->dkdv_empty, kMath);
-    mbar_init(&c->stat_full[0], kBM);
-    mbar_init(&c->stat_full[1], kBM);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();

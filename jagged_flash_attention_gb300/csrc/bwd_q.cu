@@ -40,7 +40,6 @@ constexpr int kThreads = 320;
 constexpr int kMath = 256;  // score-math threads
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct QCfg {
@@ -341,8 +340,9 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
       float lse2 = INFINITY, dlt = 0.f;  // rows outside the sequence: P = 0
       if (row_valid[g]) {
         const long long si = static_cast<long long>(f.h) * T + f.off0 + qi[g];
-        lse2 = p.lse[si] * kLog2e;
-        dlt = p.delta[si];
+        const float2 st = p.stat[si];  // {LSE*log2e, Delta}
+        lse2 = st.x;
+        dlt = st.y;
       }
       nlse2[g] = f2_pack(-lse2, -lse2);
       ndlt2[g] = f2_pack(-dlt, -dlt);

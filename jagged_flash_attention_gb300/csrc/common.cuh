@@ -15,6 +15,7 @@ namespace jfa {
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;  // keys per tile
 constexpr int kFwdRows = 256;  // query rows per forward work item (two tiles)
+constexpr int kStatPad = 128;  // entries before the backward row-statistics arrays
 
 // Small header at the start of every scratch block, written by the
 // scheduler kernel and read by the kernels that follow it on the stream.
@@ -57,7 +58,14 @@ struct BwdParams {
   float scale_log2;
   float scale;
   const float* lse;    // caller's LSE (natural log)
-  const float* delta;  // rowsum(dO * O), same layout as lse
+  const float* delta;  // broadcast: rowsum(dO * O), same layout as lse
+  // Self-attention: {LSE*log2e, Delta} of query row (h, t) at stat[h*T + t]
+  // and, one entry earlier, at stat_odd[h*T + t - 1] (so that a 128-row box
+  // always has a 16-byte aligned source in one of the two).  Both arrays are
+  // preceded by kStatPad entries: a box of a batch shorter than one tile
+  // starts up to 127 rows before row 0.
+  const float2* stat;
+  const float2* stat_odd;
   float* dq_acc;       // fp32 accumulator: self [Tcap,H,D]; broadcast [shards,Lq,H,D]
   int dq_shards;       // broadcast only
   long long shard_stride;  // elements per shard
@@ -69,15 +77,24 @@ struct BwdParams {
   int* err;
 };
 
+// Backward pre-pass: blocks [0, n_sched) build work lists, the others the
+// row statistics.
 struct PrepParams {
   const __nv_bfloat16* out;
   const __nv_bfloat16* dout;
+  const int32_t* offsets;
+  // self-attention: stat / stat_odd as in BwdParams, from the caller's LSE
+  const float* lse;
+  float2* stat;
+  float2* stat_odd;
+  long long Tcap;  // B * max_len: rows of q, k, v, out, dout the caller provides
+  // broadcast-Q: Delta [B, H, Lq] and the fp32 dQ accumulator to zero
   float* delta;
   float* dq_acc;
-  long long dq_acc_elems_bcast;  // broadcast: elements to zero
-  int zero_self_acc;             // self-attention: zero T*H*D accumulator elements
+  long long dq_acc_elems_bcast;
   int B, H, D, Lq, broadcast;
-  const WorkHeader* hdr;
+  int n_sched;  // 1 or 2
+  SchedParams sched[2];
 };
 
 struct FinParams {
@@ -102,7 +119,7 @@ cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUten
 cudaError_t launch_bwd_q(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                          int grid, cudaStream_t s);
-cudaError_t launch_prep(const PrepParams& p, int sms, cudaStream_t s);
+cudaError_t launch_bwd_prep(const PrepParams& p, int sms, cudaStream_t s);
 cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s);
 cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
                               cudaStream_t s);

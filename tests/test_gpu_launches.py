@@ -1,7 +1,8 @@
 """The library's launch accounting on the GPU: one self-attention forward
 plus backward enqueues exactly the kernels the design names (a scheduler and
-the forward; two schedulers, the Delta pre-pass, the dK/dV pass and the dQ
-pass), and the event timer sees each of them on the launching stream."""
+the forward; the pre-pass that builds both backward work lists and the row
+statistics, the dK/dV pass and the dQ pass), and the event timer sees each
+of them on the launching stream."""
 import pytest
 import torch
 
@@ -27,10 +28,10 @@ def test_self_attention_launches_and_kernel_times():
         torch.cuda.synchronize()
     finally:
         jfa.profile_enable(False)
-    assert jfa.launch_count() - n0 == 7
+    assert jfa.launch_count() - n0 == 5
     prof = jfa.profile_read()
     counts = {k: n for k, (t, n) in prof.items() if n}
-    assert counts == {"sched": 3, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_q": 1}
+    assert counts == {"sched": 1, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_q": 1}
     for k in counts:
         assert prof[k][0] > 0.0, k
     jfa.jfa_sync_and_check()
