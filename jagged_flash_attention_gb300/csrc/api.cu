@@ -282,16 +282,14 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kFwdRows);
   if (cap_kv >= (1LL << 31) || cap_q >= (1LL << 31))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
-  const long long stat_elems = (long long)s.H * s.Tcap;
+  const long long stat_stride = stat_copy_floats((long long)s.H * s.Tcap);
   size_t off = 0;
   const size_t hkv_off = off;
   off = align256(off + 256 + cap_kv * sizeof(Item));
   const size_t hq_off = off;
   off = align256(off + 256 + cap_q * sizeof(Item));
   const size_t stat_off = off;
-  off = align256(off + (kStatPad + stat_elems) * sizeof(float2));
-  const size_t stat_odd_off = off;
-  off = align256(off + (kStatPad + stat_elems) * sizeof(float2));
+  off = align256(off + kStatCopies * stat_stride * sizeof(float));
   CUtensorMap tq, tk, tv, tdo;
   if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
   if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
@@ -305,8 +303,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   Item* items_kv = reinterpret_cast<Item*>(base + hkv_off + 256);
   WorkHeader* hdr_q = reinterpret_cast<WorkHeader*>(base + hq_off);
   Item* items_q = reinterpret_cast<Item*>(base + hq_off + 256);
-  float2* stat = reinterpret_cast<float2*>(base + stat_off) + kStatPad;
-  float2* stat_odd = reinterpret_cast<float2*>(base + stat_odd_off) + kStatPad;
+  float* stat = reinterpret_cast<float*>(base + stat_off);
   SchedParams sk{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 1, kBM,
                  items_kv, (int)cap_kv, hdr_kv, ds->err};
   SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kFwdRows,
@@ -321,7 +318,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   bp.scale = s.scale;
   bp.lse = lse;
   bp.stat = stat;
-  bp.stat_odd = stat_odd;
+  bp.stat_stride = stat_stride;
   bp.dq = static_cast<__nv_bfloat16*>(dq);
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
@@ -335,7 +332,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     pp.offsets = offsets;
     pp.lse = lse;
     pp.stat = stat;
-    pp.stat_odd = stat_odd;
+    pp.stat_stride = stat_stride;
     pp.Tcap = s.Tcap;
     pp.B = s.B;
     pp.H = s.H;

@@ -157,12 +157,16 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
     rows = static_cast<long long>(T) * p.H;
   }
   if (!p.broadcast && blk == 0) {
-    // The front padding that boxes starting before row 0 read: zeros (a
-    // finite Delta for the columns those boxes mask), except stat_odd[-1],
-    // which is stat[0] and written below.
-    for (int i = threadIdx.x; i < kStatPad; i += blockDim.x) {
-      p.stat[i - kStatPad] = make_float2(0.f, 0.f);
-      if (i < kStatPad - 1) p.stat_odd[i - kStatPad] = make_float2(0.f, 0.f);
+    // Positions of rows before 0, read by boxes that start early: zeros (a
+    // finite Delta for the columns those boxes mask).
+    for (int i = threadIdx.x; i < kStatCopies * kStatPad; i += blockDim.x) {
+      const int k = i / kStatPad;
+      const long long u = i % kStatPad;
+      if (u < stat_pos(0, k)) {
+        float* f = p.stat + k * p.stat_stride + stat_float(u);
+        f[0] = 0.f;
+        f[4] = 0.f;
+      }
     }
   }
   const int tpr = p.D / 8;
@@ -208,9 +212,13 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
         } else {
           const long long h = row % p.H, t = row / p.H;
           const long long si = h * T + t;
-          const float2 v = make_float2(p.lse[si] * kLog2e, acc);
-          p.stat[si] = v;
-          p.stat_odd[si - 1] = v;
+          const float nl = -p.lse[si] * kLog2e;
+#pragma unroll
+          for (int k = 0; k < kStatCopies; ++k) {
+            float* f = p.stat + k * p.stat_stride + stat_float(stat_pos(si, k));
+            f[0] = nl;
+            f[4] = -acc;
+          }
         }
       }
     }

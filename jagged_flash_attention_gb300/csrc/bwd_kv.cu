@@ -20,30 +20,35 @@
 // dV(g+1) + S(g+2).  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) right after
 // the dV / dK MMAs that read them (MMAs of one CTA execute in issue order).
 //
-// CTA = 10 warps: warps 0-7 score/gradient math (warp w: TMEM lanes
-// 32*(w%4).. = key rows, query columns 64*(w/4)..) and the dK/dV epilogue,
-// warp 8 TMA producer, warp 9 MMA issuer.
+// CTA = 18 warps: warps 0-15 score/gradient math (warp w: TMEM lanes
+// 32*(w%4).. = key rows, query columns 32*(w/4)..; four math warps per SM
+// sub-partition, so that each part's TMEM load -> math -> TMEM store chain
+// is hidden by the others) and the dK/dV epilogue, warp 16 TMA producer,
+// warp 17 MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kMath = 256;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMathWarps = 16;
+constexpr int kMath = 32 * kMathWarps;
+constexpr int kProducerWarp = kMathWarps;
+constexpr int kMmaWarp = kMathWarps + 1;
+constexpr int kThreads = 32 * (kMathWarps + 2);
 
 template <int D>
 struct KvCfg {
   static constexpr int NSQ = 2;              // Q / dO ring depth
   static constexpr int kTile = kBM * D * 2;  // bytes of a 128-row bf16 tile
   static constexpr int kSlabs = D / 64;
+  // Two K buffers (the next item's K is loaded while this item runs), one V
+  // buffer (released once the item's last dP^T has read it).
   static constexpr int kK = 0;
-  static constexpr int kV = kTile;
-  static constexpr int kQ = 2 * kTile;
+  static constexpr int kV = 2 * kTile;
+  static constexpr int kQ = 3 * kTile;
   static constexpr int kDO = kQ + NSQ * kTile;
-  // {LSE*log2e, Delta} of the 128 query rows of each Q / dO stage
+  // {-LSE*log2e, -Delta} of the 128 query rows of each Q / dO stage
   static constexpr int kStatBytes = kBM * 8;
   static constexpr int kStat = kDO + NSQ * kTile;
   static constexpr int kCtl = kStat + NSQ * kStatBytes;
@@ -51,20 +56,6 @@ struct KvCfg {
   static constexpr uint32_t kColS = 0, kColDP = 128;
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 };
-
-struct KvCtl {
-  uint64_t kv_full, kv_empty;
-  uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full;
-  uint64_t dkdv_full, dkdv_empty;
-  uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
-  int item_slot[2];
-  uint32_t tmem_base;
-  int abort;
-};
-
-__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 struct RowBox {
   int row, shift, n;  // TMA row coordinate, rows moved back, valid rows
@@ -83,6 +74,27 @@ struct KvItem {
   RowBox kt;   // keys of this block
   int t0, nt;  // first query tile and count
 };
+
+struct KvCtl {
+  uint64_t k_full[2], k_empty[2], v_full, v_empty;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dkdv_full, dkdv_empty;
+  uint64_t epi;  // math-warp sync of the staged epilogue stores
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  KvItem item[2];  // decoded by the producer; b < 0: no more items
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// TMEM column of the bf16 pairs of queries 16k..16k+15 in a packed P^T /
+// dS^T: query quarter q = k/2 (columns 32q..32q+31 of the fp32 tile) keeps
+// its 16 packed columns at 32q.
+__device__ __forceinline__ uint32_t pack_col(int k) { return 32 * (k >> 1) + 8 * (k & 1); }
+
 
 template <bool CAUSAL>
 __device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
@@ -109,18 +121,19 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
-__device__ __forceinline__ int next_item(KvCtl* c, uint32_t n, bool warp, bool* ok, int* err) {
+// Next work item of the CTA as the producer decoded it (called by whole
+// warps: the math warps and the MMA warp).  False when the list is done or a
+// wait gave up (then *ok is false too).
+__device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool* ok, int* err) {
   const int slot = n & 1;
-  const bool got = warp ? mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)
-                        : mbar_wait(&c->item_full[slot], (n >> 1) & 1, &c->abort, err);
-  if (!got) {
+  if (!mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)) {
     *ok = false;
-    return -1;
+    return false;
   }
-  const int idx = c->item_slot[slot];
-  if (warp) __syncwarp();
-  if (!warp || (threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
-  return idx;
+  *f = c->item[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  return f->b >= 0;
 }
 
 template <int D, bool CAUSAL>
@@ -130,24 +143,30 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   using C = KvCfg<D>;
   const int n_items = p.hdr->n_items;
   const int T = p.hdr->T;
-  uint32_t it = 0, gq = 0;
+  uint32_t it = 0, gq = 0, nk = 0, nv = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
     const int slot = n & 1;
     if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
     const int idx = atomicAdd(&p.hdr->ticket, 1);
-    c->item_slot[slot] = idx < n_items ? idx : -1;
+    KvItem f;
+    if (idx < n_items)
+      f = decode<CAUSAL>(p, idx, T);
+    else
+      f.b = -1;
+    c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
     if (idx >= n_items) break;
-    const KvItem f = decode<CAUSAL>(p, idx, T);
-    if (!mbar_wait(&c->kv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
-    mbar_arrive_expect_tx(&c->kv_full, 2 * C::kTile);
+    // Order of the item's loads: K, the first Q / dO, V (V waits for the
+    // previous item's last dP^T), then the other Q / dO tiles.
+    const int ks = it & 1;
+    if (!mbar_wait(&c->k_empty[ks], ((it >> 1) & 1) ^ 1, &c->abort, p.err)) break;
+    mbar_arrive_expect_tx(&c->k_full[ks], C::kTile);
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) {
-      tma_load_3d(smem + C::kK + s * 16384, tk, &c->kv_full, s * 64, f.h, f.kt.row);
-      tma_load_3d(smem + C::kV + s * 16384, tv, &c->kv_full, s * 64, f.h, f.kt.row);
-    }
-    ++it;
+    for (int s = 0; s < C::kSlabs; ++s)
+      tma_load_3d(smem + C::kK + ks * C::kTile + s * 16384, tk, &c->k_full[ks], s * 64, f.h,
+                  f.kt.row);
+    ++nk;
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = gq;
       const int st = g % C::NSQ;
@@ -157,10 +176,11 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
-      // Row statistics of the box: from stat if its first entry is 16-byte
-      // aligned there, else from the copy shifted by one entry.
+      // Row statistics of the box: 32 whole groups of the copy in which
+      // its first row starts a group.
       const long long sidx = static_cast<long long>(f.h) * T + qb.row;
-      const float2* ssrc = (sidx & 1) ? p.stat_odd + (sidx - 1) : p.stat + sidx;
+      const int sk = static_cast<int>((sidx + kStatPad) & 3);
+      const float* ssrc = p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
       mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile + C::kStatBytes);
       bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->qdo_full[st]);
 #pragma unroll
@@ -171,9 +191,23 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
                     qb.row);
       }
       ++gq;
+      if (i == 0) {
+        if (!mbar_wait(&c->v_empty, (it & 1) ^ 1, &c->abort, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c->v_full, C::kTile);
+#pragma unroll
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kV + s * 16384, tv, &c->v_full, s * 64, f.h, f.kt.row);
+        ++nv;
+      }
     }
+    ++it;
   }
-  if (it > 0) drain_wait(&c->kv_full, (it - 1) & 1, p.err);
+  for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
+    drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
+  if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
   for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
     drain_wait(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
 }
@@ -181,13 +215,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 template <int D, bool CAUSAL>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
-  const int T = p.hdr->T;
   // Run by the whole warp; the elected lane issues products and commits.
   const uint32_t leader = elect_one();
   const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
   // Descriptors built once; per tile and K step only adds remain.
-  const uint64_t dk_k = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dk_k0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
   const uint64_t dv_k = smem_desc_sw128(smem_addr(smem + C::kV), 16, 1024);
   const uint64_t dq_k0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
   const uint64_t ddo_k0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16, 1024);
@@ -195,48 +228,36 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   const uint64_t ddo_m0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16384, 1024);
   const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP;
   const uint32_t tDV = tbase + C::kColDV, tDK = tbase + C::kColDK;
-  // Each issue function runs `mid` before its group's last product: the
-  // wait for the next group then overlaps tensor work still queued (issue
-  // blocks while the pipe is full; a wait right after a group would leave it
-  // idle for the wait's own latency).
-  auto issue_s = [&](uint32_t g, auto&& mid) {
+  auto issue_s = [&](uint32_t g, uint64_t dk_k) {
     const uint64_t dq_k = desc_add(dq_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      if (k == D / 16 - 1 && !mid()) return false;
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
       if (leader) mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
     }
-    return true;
   };
-  auto issue_dp = [&](uint32_t g, auto&& mid) {
+  auto issue_dp = [&](uint32_t g) {
     const uint64_t ddo_k = desc_add(ddo_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      if (k == D / 16 - 1 && !mid()) return false;
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
       if (leader) mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
     }
-    return true;
   };
-  // A operand column of query block k (16 queries): packed P^T / dS^T of
-  // queries 0-63 start at +0, of queries 64-127 at +64.
-  auto issue_dv = [&](uint32_t g, bool acc, auto&& mid) {
+  // A operand column of query block k (16 queries): the packed P^T / dS^T
+  // of query quarter k/2 starts at its own first column, 32 * (k/2).
+  auto issue_dv = [&](uint32_t g, bool acc) {
     const uint64_t ddo_m = desc_add(ddo_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
-    for (int k = 0; k < kBM / 16; ++k) {
-      if (k == kBM / 16 - 1 && !mid()) return false;
-      if (leader) mma_ts(tDV, tS + k * 8 + (k >= 4 ? 32 : 0), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
-    }
-    return true;
+    for (int k = 0; k < kBM / 16; ++k)
+      if (leader) mma_ts(tDV, tS + pack_col(k), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
   };
   auto issue_dk = [&](uint32_t g, bool acc) {
     const uint64_t dq_m = desc_add(dq_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBM / 16; ++k)
-      if (leader) mma_ts(tDK, tDP + k * 8 + (k >= 4 ? 32 : 0), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
+      if (leader) mma_ts(tDK, tDP + pack_col(k), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
   };
-  auto none = [] { return true; };
   auto wait_qdo = [&](uint32_t g) {
     return mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
   };
@@ -245,49 +266,58 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const KvItem f = decode<CAUSAL>(p, idx, T);
-    if (!mbar_wait_warp(&c->kv_full, it & 1, &c->abort, p.err)) break;
+    KvItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
+    const int ks = it & 1;
+    if (!mbar_wait_warp(&c->k_full[ks], (it >> 1) & 1, &c->abort, p.err)) break;
+    const uint64_t dk_k = desc_add(dk_k0, ks * C::kTile);
     const uint32_t g0 = gq;
     if (!wait_qdo(g0)) break;
     tc_fence_after();
     issued = true;
-    if (!issue_s(g0, none)) break;
+    issue_s(g0, dk_k);
     if (leader) mma_commit(&c->s_full);
-    // Inside dP(g0): P^T(g0) ready, and the previous item's epilogue has read
-    // the dV / dK accumulators.
-    if (!issue_dp(g0, [&] {
-          return wait_p(g0) && mbar_wait_warp(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err);
-        }))
-      break;
+    // V is released after the item's last dP^T; K after the item epilogue,
+    // which stages its stores in the K buffer.
+    if (!mbar_wait_warp(&c->v_full, it & 1, &c->abort, p.err)) break;
+    tc_fence_after();
+    issue_dp(g0);
     if (leader) mma_commit(&c->dp_full);
-    // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).
+    if (f.nt == 1 && leader) mma_commit(&c->v_empty);
+    // dV(g0) and dK(g0) restart the accumulators the previous item's
+    // epilogue reads.
+    if (!mbar_wait_warp(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
+    // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).  Every product is
+    // issued and committed whole; the issuer waits only before a product
+    // that reads what the math produced (P^T before dV, dS^T before dK), so
+    // that S(g+1) and dP(g+1), which the math waits for, never queue behind
+    // a wait.  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) after dV(g) /
+    // dK(g), which were issued before them.
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = g0 + i;
       const bool more = i + 1 < f.nt;
+      if (!wait_p(g)) { ok = false; break; }
       tc_fence_after();
-      if (!issue_dv(g, i > 0, [&] { return !more || wait_qdo(g + 1); })) { ok = false; break; }
-      if (more) {  // S(g+1): its P^T(g) columns were just read by dV(g)
+      issue_dv(g, i > 0);
+      if (more) {
+        if (!wait_qdo(g + 1)) { ok = false; break; }
         tc_fence_after();
-        if (!issue_s(g + 1, [&] { return wait_ds(g); })) { ok = false; break; }
+        issue_s(g + 1, dk_k);
         if (leader) mma_commit(&c->s_full);
-      } else if (!wait_ds(g)) {
-        ok = false;
-        break;
       }
+      if (!wait_ds(g)) { ok = false; break; }
       tc_fence_after();
       issue_dk(g, i > 0);
       if (leader) mma_commit(&c->qdo_empty[g % C::NSQ]);
-      if (more) {  // dP(g+1): its dS^T(g) columns were just read by dK(g)
-        if (!issue_dp(g + 1, [&] { return wait_p(g + 1); })) { ok = false; break; }
+      if (more) {
+        issue_dp(g + 1);
         if (leader) mma_commit(&c->dp_full);
+        if (i + 2 == f.nt && leader) mma_commit(&c->v_empty);
       }
     }
     if (!ok) break;
     gq += f.nt;
     if (leader) mma_commit(&c->dkdv_full);
-    if (leader) mma_commit(&c->kv_empty);
     ++it;
   }
   if (issued && leader) {
@@ -300,18 +330,18 @@ template <int D, bool CAUSAL>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   const int r = threadIdx.x & 127;    // TMEM lane = key row of the block
-  const int half = threadIdx.x >> 7;  // query columns [64*half, 64*half + 64)
+  const int qd = threadIdx.x >> 7;    // query columns [32*qd, 32*qd + 32)
+  const int cbase = 32 * qd;
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
-  uint32_t it = 0, gq = 0;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  uint32_t it = 0, gq = 0, ep = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const KvItem f = decode<CAUSAL>(p, idx, T);
+    KvItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
-    const bool key_ok = r >= f.kt.shift && r < f.kt.shift + f.kt.n;
     for (int i = 0; i < f.nt; ++i, ++gq) {
       const uint32_t g = gq;
       const int t = f.t0 + i;
@@ -320,23 +350,24 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
       // The statistics arrived with Q / dO of the stage (already complete
       // once S^T is; waited on here for their visibility).
       if (!mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
-      // Column c: {LSE*log2e, Delta, and the same of column c+1} at stat4[c/2].
-      const float4* stat4 = reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
+      // Statistics of columns 4j..4j+3: -LSE*log2e at st4[2j], -Delta at
+      // st4[2j + 1].
+      const float4* st4 =
+          reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
       // Admissible query columns [lo, hi): the box's rows of the sequence
       // and, causal, the queries at or after this key.
       int lo = qb.shift;
       const int hi = qb.shift + qb.n;
       if (CAUSAL) lo = max(lo, key - q0);
       const bool ragged = qb.shift > 0 || qb.n < kBM;
-      const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > 64 * half));
+      const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > cbase));
       const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
-      // ---- P part: P^T = exp2(S^T * scale*log2e - LSE*log2e)
+      // ---- P part: P^T = exp2(S^T * scale*log2e - LSE*log2e), kept as bf16
+      // pairs of this thread's 64 columns.
       if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
-      float pv[64];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int cbase = 64 * half + 32 * ch;
+      uint32_t pk[16];
+      {
         uint32_t sraw[32];
         tmem_ld32(tbase + lane_base + C::kColS + cbase, sraw);
         tmem_wait_ld();
@@ -344,82 +375,132 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         // and dK depends only on row r of P^T and dS^T, and those rows are
         // never stored.
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          const float4 st2 = stat4[(cbase + cc) / 2];
-          pv[32 * ch + cc] = ex2_approx(fmaf(__uint_as_float(sraw[cc]), sl2, -st2.x));
-          pv[32 * ch + cc + 1] = ex2_approx(fmaf(__uint_as_float(sraw[cc + 1]), sl2, -st2.z));
+        for (int j = 0; j < 8; ++j) {
+          const float4 nl = st4[2 * (cbase / 4 + j)];
+          const float2 x01 = f2_unpack(ffma2(
+              f2_pack(__uint_as_float(sraw[4 * j]), __uint_as_float(sraw[4 * j + 1])), sl2x2,
+              f2_pack(nl.x, nl.y)));
+          const float2 x23 = f2_unpack(ffma2(
+              f2_pack(__uint_as_float(sraw[4 * j + 2]), __uint_as_float(sraw[4 * j + 3])), sl2x2,
+              f2_pack(nl.z, nl.w)));
+          pk[2 * j] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
+          pk[2 * j + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
         }
         if (mask) {  // ragged or causal diagonal tile: zero inadmissible columns
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc)
-            pv[32 * ch + cc] =
-                static_cast<uint32_t>(cbase + cc - lo) < span ? pv[32 * ch + cc] : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            const int col = cbase + 2 * i;
+            pk[i] &= (static_cast<uint32_t>(col - lo) < span ? 0x0000ffffu : 0u) |
+                     (static_cast<uint32_t>(col + 1 - lo) < span ? 0xffff0000u : 0u);
+          }
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) pk[cc / 2] = pack_bf16x2(pv[32 * ch + cc], pv[32 * ch + cc + 1]);
-        // bf16 pairs of query columns cbase.. land in packed column
-        // 64 * half + 16 * ch: inside this half's own, already read columns.
-        tmem_st16(tbase + lane_base + C::kColS + 64 * half + 16 * ch, pk);
+        // bf16 pairs of this quarter's columns land in its own first 16
+        // columns, already read above.
+        tmem_st16(tbase + lane_base + C::kColS + cbase, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->p_full);
-      // ---- dS part: dS^T = P^T (dP^T - Delta)
+      // ---- dS part: dS^T = P^T (dP^T - Delta): the difference in fp32,
+      // rounded to bf16, times the bf16 P.
       if (!mbar_wait_warp(&c->dp_full, g & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int cbase = 64 * half + 32 * ch;
+      {
         uint32_t praw[32];
         tmem_ld32(tbase + lane_base + C::kColDP + cbase, praw);
         tmem_wait_ld();
-        uint32_t dk[16];
+        uint32_t w[16];
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          const float4 st2 = stat4[(cbase + cc) / 2];
-          const float d0 = pv[32 * ch + cc] * (__uint_as_float(praw[cc]) - st2.y);
-          const float d1 = pv[32 * ch + cc + 1] * (__uint_as_float(praw[cc + 1]) - st2.w);
-          dk[cc / 2] = pack_bf16x2(d0, d1);
+        for (int j = 0; j < 8; ++j) {
+          const float4 nd = st4[2 * (cbase / 4 + j) + 1];
+          const float2 d01 = f2_unpack(fadd2(
+              f2_pack(__uint_as_float(praw[4 * j]), __uint_as_float(praw[4 * j + 1])),
+              f2_pack(nd.x, nd.y)));
+          const float2 d23 = f2_unpack(fadd2(
+              f2_pack(__uint_as_float(praw[4 * j + 2]), __uint_as_float(praw[4 * j + 3])),
+              f2_pack(nd.z, nd.w)));
+          w[2 * j] = bmul2(pk[2 * j], pack_bf16x2(d01.x, d01.y));
+          w[2 * j + 1] = bmul2(pk[2 * j + 1], pack_bf16x2(d23.x, d23.y));
         }
-        tmem_st16(tbase + lane_base + C::kColDP + 64 * half + 16 * ch, dk);
+        tmem_st16(tbase + lane_base + C::kColDP + cbase, w);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->ds_full);
     }
     if (!ok) break;
-    // Item epilogue: dV and scale * dK rows of this K/V block (this warp's
-    // half of the head dimension).
+    // Item epilogue: dV and scale * dK rows of this K/V block.  The
+    // accumulators leave TMEM first and are released at once, so that the
+    // next item's dV / dK products do not wait for the stores.  D = 128:
+    // quarter qd holds head-dim columns 32*qd.. of both; D = 64: quarters
+    // 0-1 hold dV, 2-3 dK, 32 columns each.
     if (!mbar_wait_warp(&c->dkdv_full, it & 1, &c->abort, p.err)) break;
     tc_fence_after();
-    const long long row = (static_cast<long long>(f.off0) + key) * p.H + f.h;
+    constexpr int kParts = D == 128 ? 2 : 1;
+    const int dbase = D == 128 ? 32 * qd : 32 * (qd & 1);
+    uint32_t acc[kParts][32];
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-      const float mul = which == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row * D;
+    for (int w = 0; w < kParts; ++w) {
+      const int which = D == 128 ? w : (qd >> 1);
+      tmem_ld32(tbase + lane_base + (which == 0 ? C::kColDV : C::kColDK) + dbase, acc[w]);
+    }
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&c->dkdv_empty);
+    // Each tensor goes through this item's K buffer (every product of the
+    // item has completed), so that warps store whole rows: one thread's
+    // registers hold 64 bytes of one key row, 2 KB away from the next
+    // row's, and stored directly every warp store would touch 32 lines.
+    // Staging layout: row r at 2*D bytes per row, 16-byte chunk c at
+    // c ^ (r mod D/8) (conflict-free both ways).
+    uint8_t* stg = smem + C::kK + (it & 1) * C::kTile;
+    constexpr int kCpr = D / 8;           // 16-byte chunks per row
+    constexpr int kRpi = 32 / kCpr;       // rows per warp store
+    const int wi = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    auto epi_sync = [&]() {
+      mbar_arrive(&c->epi);
+      const bool r_ = mbar_wait_warp(&c->epi, ep & 1, &c->abort, p.err);
+      ++ep;
+      return r_;
+    };
+    bool eok = true;
 #pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) {
-        const int dbase = (D / 2) * half + 32 * ch;
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_base + col + dbase, v);
-        tmem_wait_ld();
-        uint32_t w[16];
+    for (int w = 0; w < 2; ++w) {
+      if (w == 1 && !(eok = epi_sync())) break;  // the dV rows are read
+      if (D == 128 || (qd >> 1) == w) {
+        const float mul = w == 0 ? 1.f : p.scale;
+        const uint32_t* a = acc[D == 128 ? w : 0];
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2)
-          w[i2] = pack_bf16x2(__uint_as_float(v[2 * i2]) * mul, __uint_as_float(v[2 * i2 + 1]) * mul);
-        if (key_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + dbase);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t o[4];
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2)
+            o[i2] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * i2]) * mul,
+                                __uint_as_float(a[8 * q4 + 2 * i2 + 1]) * mul);
+          const int ch = dbase / 8 + q4;
+          *reinterpret_cast<uint4*>(stg + r * (2 * D) + ((ch ^ (r & (kCpr - 1))) * 16)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (!(eok = epi_sync())) break;  // the tensor is staged
+      __nv_bfloat16* dst = w == 0 ? p.dv : p.dk;
+#pragma unroll
+      for (int j = 0; j < 128 / (16 * kRpi); ++j) {
+        const int row = wi * (128 / 16) + j * kRpi + ln / kCpr;
+        const int ch = ln % kCpr;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + row * (2 * D) +
+                                                        ((ch ^ (row & (kCpr - 1))) * 16));
+        if (row >= f.kt.shift && row < f.kt.shift + f.kt.n) {
+          const long long tok = f.off0 + f.kb * kBN - f.kt.shift + row;
+          *reinterpret_cast<uint4*>(dst + (tok * p.H + f.h) * D + ch * 8) = v;
         }
       }
     }
-    tc_fence_before();
-    mbar_arrive(&c->dkdv_empty);
+    if (!eok) break;
+    // The K buffer goes back to the producer (a TMA load may follow the
+    // generic-proxy accesses above).
+    fence_proxy_async_smem();
+    mbar_arrive(&c->k_empty[it & 1]);
     ++it;
   }
 }
@@ -438,13 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (threadIdx.x == 0) {
-    mbar_init(&c->kv_full, 1);
-    mbar_init(&c->kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->k_full[i], 1);
+      mbar_init(&c->k_empty[i], kMath);  // released by the math warps' epilogue
+    }
+    mbar_init(&c->v_full, 1);
+    mbar_init(&c->v_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->qdo_full[i], 1);
       mbar_init(&c->qdo_empty[i], 1);
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 9);  // 8 math warps + the MMA warp
+      mbar_init(&c->item_empty[i], kMathWarps + 1);  // math warps + the MMA warp
     }
     mbar_init(&c->s_full, 1);
     mbar_init(&c->dp_full, 1);
@@ -452,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c->ds_full, kMath);
     mbar_init(&c->dkdv_full, 1);
     mbar_init(&c->dkdv_empty, kMath);
+    mbar_init(&c->epi, kMath);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();
@@ -470,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
-  if (warp < 8) {
+  if (warp < kMathWarps) {
     math_role<D, CAUSAL>(p, smem, c, tbase);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);

@@ -337,15 +337,15 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
       const QTile& q = f.t[g];
       qi[g] = q.q_lo - q.shift + r;
       row_valid[g] = q.n > 0 && r >= q.shift && r < q.shift + q.nq;
-      float lse2 = INFINITY, dlt = 0.f;  // rows outside the sequence: P = 0
+      float nl = -INFINITY, nd = 0.f;  // rows outside the sequence: P = 0
       if (row_valid[g]) {
         const long long si = static_cast<long long>(f.h) * T + f.off0 + qi[g];
-        const float2 st = p.stat[si];  // {LSE*log2e, Delta}
-        lse2 = st.x;
-        dlt = st.y;
+        const float* st = p.stat + stat_float(stat_pos(si, 0));
+        nl = st[0];  // -LSE*log2e
+        nd = st[4];  // -Delta
       }
-      nlse2[g] = f2_pack(-lse2, -lse2);
-      ndlt2[g] = f2_pack(-dlt, -dlt);
+      nlse2[g] = f2_pack(nl, nl);
+      ndlt2[g] = f2_pack(nd, nd);
     }
     // P of tile g at key tile j: this thread's 64 columns -> 32 bf16 pairs.
     auto p_part = [&](int g, int j, uint32_t (&pk)[32]) {

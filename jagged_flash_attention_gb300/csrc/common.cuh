@@ -15,7 +15,28 @@ namespace jfa {
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;  // keys per tile
 constexpr int kFwdRows = 256;  // query rows per forward work item (two tiles)
-constexpr int kStatPad = 128;  // entries before the backward row-statistics arrays
+
+// Row statistics of the self-attention backward, {-LSE*log2e, -Delta} per
+// query row (h, t) at row index si = h*T + t, in a blocked layout: every
+// aligned group of 4 positions stores the 4 rows' -LSE*log2e (16 bytes),
+// then their -Delta (16 bytes).  kStatCopies copies differ in where their
+// groups start: copy k holds row si at position si + kStatPad - k, so a
+// 128-row box starting at row s0 is 32 whole groups (1 KB, 32-byte aligned)
+// of copy (s0 + kStatPad) % 4.  Positions of rows before 0 (a box of a
+// batch shorter than one tile starts up to 127 rows early) hold zeros.
+constexpr int kStatPad = 128;
+constexpr int kStatCopies = 4;
+__host__ __device__ __forceinline__ long long stat_pos(long long si, int k) {
+  return si + kStatPad - k;
+}
+// float index of -LSE*log2e at position u (-Delta is 4 floats further)
+__host__ __device__ __forceinline__ long long stat_float(long long u) {
+  return (u >> 2) * 8 + (u & 3);
+}
+// floats per copy for rows [0, rows)
+__host__ __device__ __forceinline__ long long stat_copy_floats(long long rows) {
+  return ((2 * (rows + kStatPad + 4) + 63) / 64) * 64;
+}
 
 // Small header at the start of every scratch block, written by the
 // scheduler kernel and read by the kernels that follow it on the stream.
@@ -59,13 +80,10 @@ struct BwdParams {
   float scale;
   const float* lse;    // caller's LSE (natural log)
   const float* delta;  // broadcast: rowsum(dO * O), same layout as lse
-  // Self-attention: {LSE*log2e, Delta} of query row (h, t) at stat[h*T + t]
-  // and, one entry earlier, at stat_odd[h*T + t - 1] (so that a 128-row box
-  // always has a 16-byte aligned source in one of the two).  Both arrays are
-  // preceded by kStatPad entries: a box of a batch shorter than one tile
-  // starts up to 127 rows before row 0.
-  const float2* stat;
-  const float2* stat_odd;
+  // Self-attention row statistics: kStatCopies copies of stat_stride floats
+  // (layout at kStatPad above).
+  const float* stat;
+  long long stat_stride;
   float* dq_acc;       // fp32 accumulator: self [Tcap,H,D]; broadcast [shards,Lq,H,D]
   int dq_shards;       // broadcast only
   long long shard_stride;  // elements per shard
@@ -83,10 +101,10 @@ struct PrepParams {
   const __nv_bfloat16* out;
   const __nv_bfloat16* dout;
   const int32_t* offsets;
-  // self-attention: stat / stat_odd as in BwdParams, from the caller's LSE
+  // self-attention: the row statistics as in BwdParams, from the caller's LSE
   const float* lse;
-  float2* stat;
-  float2* stat_odd;
+  float* stat;
+  long long stat_stride;
   long long Tcap;  // B * max_len: rows of q, k, v, out, dout the caller provides
   // broadcast-Q: Delta [B, H, Lq] and the fp32 dQ accumulator to zero
   float* delta;
