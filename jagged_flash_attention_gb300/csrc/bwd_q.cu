@@ -54,17 +54,6 @@ struct QCfg {
   static constexpr int kSmem = kCtl + 512;
 };
 
-struct QCtl {
-  uint64_t qdo_full, qdo_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_done[2], dp_full[2], ds_full[2];  // per query tile
-  uint64_t dq_full[2], dq_free[2];
-  uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
-  int item_slot[2];
-  uint32_t tmem_base;
-  int abort;
-};
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -80,6 +69,18 @@ struct QItem {
   int b, h, off0, L;
   int N;  // key tiles of the item = max over its two query tiles
   QTile t[2];
+};
+
+struct QCtl {
+  uint64_t qdo_full, qdo_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_done[2], dp_full[2], ds_full[2];  // per query tile
+  uint64_t dq_full[2], dq_free[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  QItem item[2];  // decoded by the producer; b < 0: no more items
+  uint32_t tmem_base;
+  int abort;
 };
 
 template <bool CAUSAL>
@@ -127,18 +128,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
-__device__ __forceinline__ int next_item(QCtl* c, uint32_t n, bool warp, bool* ok, int* err) {
+// Next work item of the CTA as the producer decoded it (called by whole
+// warps).  False when the list is done or a wait gave up (then *ok is false).
+__device__ __forceinline__ bool next_item(QCtl* c, uint32_t n, QItem* f, bool* ok, int* err) {
   const int slot = n & 1;
-  const bool got = warp ? mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)
-                        : mbar_wait(&c->item_full[slot], (n >> 1) & 1, &c->abort, err);
-  if (!got) {
+  if (!mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)) {
     *ok = false;
-    return -1;
+    return false;
   }
-  const int idx = c->item_slot[slot];
-  if (warp) __syncwarp();
-  if (!warp || (threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
-  return idx;
+  *f = c->item[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  return f->b >= 0;
 }
 
 template <int D, bool CAUSAL>
@@ -154,10 +155,14 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     const int slot = n & 1;
     if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
     const int idx = atomicAdd(&p.hdr->ticket, 1);
-    c->item_slot[slot] = idx < n_items ? idx : -1;
+    QItem f;
+    if (idx < n_items)
+      f = decode<CAUSAL>(p, idx, T);
+    else
+      f.b = -1;
+    c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
     if (idx >= n_items) break;
-    const QItem f = decode<CAUSAL>(p, idx, T);
     if (!mbar_wait(&c->qdo_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
     const int ntiles = f.t[1].n > 0 ? 2 : 1;
     mbar_arrive_expect_tx(&c->qdo_full, ntiles * 2 * C::kTile);
@@ -207,7 +212,6 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
   using C = QCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
   const uint32_t leader = elect_one();
-  const int T = p.hdr->T;
   const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
   const uint32_t id_dq = idesc_bf16_f32(128, D, false, true);    // dQ (A = dS in TMEM)
   // Descriptors built once; per tile and K step only adds remain.
@@ -246,9 +250,8 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
   uint32_t gi[2] = {0, 0};  // items in which the slot was present
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const QItem f = decode<CAUSAL>(p, idx, T);
+    QItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
     if (!mbar_wait_warp(&c->qdo_full, it & 1, &c->abort, p.err)) break;
     const int N = f.N;
     const int nt[2] = {f.t[0].n, f.t[1].n};
@@ -324,9 +327,8 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
   uint32_t gi[2] = {0, 0};  // items in which the slot was present
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const QItem f = decode<CAUSAL>(p, idx, T);
+    QItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
     // Per query tile g of the item: this row's local query index, validity,
     // LSE*log2e and Delta.
     int qi[2];
@@ -444,13 +446,7 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
         for (int i2 = 0; i2 < 16; ++i2)
           w[i2] = pack_bf16x2(__uint_as_float(v[2 * i2]) * p.scale,
                               __uint_as_float(v[2 * i2 + 1]) * p.scale);
-        if (row_valid[g]) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + dbase);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
-        }
+        if (row_valid[g]) st_global_64B(dst + dbase, w);
       }
       tc_fence_before();
       mbar_arrive(&c->dq_free[g]);

@@ -53,16 +53,6 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + D * t; }
 };
 
-struct FwdCtl {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
-  uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
-  int item_slot[2];
-  uint32_t tmem_base;
-  int abort;
-};
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -79,6 +69,17 @@ struct FwdItem {
   int off0, L;
   QTile t[2];
   int N;  // key tiles loaded for the item (max over the two query tiles)
+};
+
+struct FwdCtl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  FwdItem item[2];  // decoded by the producer; b < 0: no more items
+  uint32_t tmem_base;
+  int abort;
 };
 
 template <bool BCAST, bool CAUSAL>
@@ -136,20 +137,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
-// Item queue consumer: returns the item index or -1 at the end.  `warp`:
-// called by a whole warp (lane 0 arrives) rather than by a single thread.
-__device__ __forceinline__ int next_item(FwdCtl* c, uint32_t n, bool warp, bool* ok, int* err) {
+// Next work item of the CTA as the producer decoded it (called by whole
+// warps).  False when the list is done or a wait gave up (then *ok is false).
+__device__ __forceinline__ bool next_item(FwdCtl* c, uint32_t n, FwdItem* f, bool* ok, int* err) {
   const int slot = n & 1;
-  const bool got = warp ? mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)
-                        : mbar_wait(&c->item_full[slot], (n >> 1) & 1, &c->abort, err);
-  if (!got) {
+  if (!mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)) {
     *ok = false;
-    return -1;
+    return false;
   }
-  const int idx = c->item_slot[slot];
-  if (warp) __syncwarp();
-  if (!warp || (threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
-  return idx;
+  *f = c->item[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  return f->b >= 0;
 }
 
 template <int D, bool CAUSAL, bool BCAST>
@@ -164,10 +163,14 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     const int slot = n & 1;
     if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
     const int idx = atomicAdd(&p.hdr->ticket, 1);
-    c->item_slot[slot] = idx < n_items ? idx : -1;
+    FwdItem f;
+    if (idx < n_items)
+      f = decode<BCAST, CAUSAL>(p, idx, T);
+    else
+      f.b = -1;
+    c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
     if (idx >= n_items) break;
-    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
     if (f.N == 0) continue;
     if (!mbar_wait(&c->q_empty, (itq & 1) ^ 1, &c->abort, p.err)) break;
     const int ntl = (f.t[0].n_kv > 0 ? 1 : 0) + (f.t[1].n_kv > 0 ? 1 : 0);
@@ -254,7 +257,6 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   using C = FwdCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
   const uint32_t leader = elect_one();
-  const int T = p.hdr->T;
   const uint64_t dq0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
   const uint64_t dk0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
   const uint64_t dv0 = smem_desc_sw128(smem_addr(smem + C::kV), 16384, 1024);
@@ -264,9 +266,8 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   bool ok = true;
   bool issued = false;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
+    FwdItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
     if (f.N == 0) continue;
     if (!mbar_wait_warp(&c->q_full, itq & 1, &c->abort, p.err)) break;
     ++itq;
@@ -337,9 +338,8 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   uint32_t u = 0;  // S tiles of this query tile processed so far (all items)
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
-    const int idx = next_item(c, n, true, &ok, p.err);
-    if (idx < 0) break;
-    const FwdItem f = decode<BCAST, CAUSAL>(p, idx, T);
+    FwdItem f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
     const QTile q = t == 0 ? f.t[0] : f.t[1];  // no dynamic indexing (keeps f in registers)
     if (q.nq <= 0) continue;
     const int qi = q.q_lo - q.shift + r;  // local query index of this row
@@ -461,13 +461,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (row_valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-        dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-      }
+      if (row_valid) st_global_64B(orow + ch * 32, w);
     }
     if (row_valid) *lrow = l_run > 0.f ? (m_used + lg2_approx(l_run)) * kLn2 : -INFINITY;
     tc_fence_before();

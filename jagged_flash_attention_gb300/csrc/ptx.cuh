@@ -145,6 +145,28 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// 32-byte global store (one whole sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Stores 16 packed words (64 bytes) at p: two whole-sector stores when p is
+// 32-byte aligned, else four 16-byte stores.
+__device__ __forceinline__ void st_global_64B(void* p, const uint32_t* w) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+    st_global_v8(p, w);
+    st_global_v8(static_cast<uint8_t*>(p) + 32, w + 8);
+  } else {
+    uint4* d = static_cast<uint4*>(p);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    d[2] = make_uint4(w[8], w[9], w[10], w[11]);
+    d[3] = make_uint4(w[12], w[13], w[14], w[15]);
+  }
+}
+
 // ----------------------------------------------------------- tensor memory
 
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
