@@ -10,7 +10,7 @@ namespace jfa {
 namespace {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kMaxBuckets = 1024;
+constexpr int kMaxBuckets = kSchedThreads;  // one bucket per thread in the scan
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -48,7 +48,7 @@ __device__ void scan_desc(const int* hist, int* base, int* warp_tot) {
   if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
   __syncthreads();
   if (tid < 32) {
-    int w = warp_tot[tid];
+    int w = tid < static_cast<int>(blockDim.x >> 5) ? warp_tot[tid] : 0;
     int z = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -142,7 +142,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // gradient of the softmax subtracts), and for self-attention LSE*log2e next
 // to it.  tpr = D/8 threads per row, each reading 16 bytes of both tensors;
 // kUnroll rows per thread in flight.
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 2;      // broadcast-Q rows in flight per thread
+constexpr int kUnrollSelf = 2;  // self-attention steps in flight per warp
 
 __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   long long rows;
@@ -174,6 +175,67 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   const int lane = threadIdx.x & 31;
   const int part = lane % tpr;
   const long long wid = (blk * blockDim.x + threadIdx.x) >> 5;
+  if (!p.broadcast) {
+    // Self-attention: a warp takes 32 consecutive tokens t0.. of one head h
+    // (rpw rows per step, tpr threads per row, 16 bytes of O and dO each);
+    // the row sums are gathered so that lane l ends with token t0 + l, and
+    // the statistics are written for consecutive rows.
+    const long long nwarps = (nblk * blockDim.x) >> 5;
+    const long long tblocks = (T + 31) / 32;
+    for (long long wb = wid; wb < tblocks * p.H; wb += nwarps) {
+      const int h = static_cast<int>(wb % p.H);
+      const long long t0 = (wb / p.H) * 32;
+      float mine = 0.f;
+      for (int s0 = 0; s0 < 32; s0 += rpw * kUnrollSelf) {
+        uint4 o[kUnrollSelf], g[kUnrollSelf];
+#pragma unroll
+        for (int u = 0; u < kUnrollSelf; ++u) {
+          const long long t = t0 + s0 + u * rpw + lane / tpr;
+          if (t < T) {
+            const long long row = t * p.H + h;
+            o[u] = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
+            g[u] = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
+          } else {
+            o[u] = make_uint4(0, 0, 0, 0);
+            g[u] = o[u];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnrollSelf; ++u) {
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o[u]);
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 a = __bfloat1622float2(o2[i]);
+            const float2 c = __bfloat1622float2(g2[i]);
+            acc = fmaf(a.x, c.x, acc);
+            acc = fmaf(a.y, c.y, acc);
+          }
+          for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          // row s0 + u*rpw + j sits in lanes [j*tpr, (j+1)*tpr); lane l keeps row l
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j >= rpw) break;
+            const float v = __shfl_sync(0xffffffffu, acc, j * tpr);
+            if (lane == s0 + u * rpw + j) mine = v;
+          }
+        }
+      }
+      const long long t = t0 + lane;
+      if (t < T) {
+        const long long si = static_cast<long long>(h) * T + t;
+        const float nl = -p.lse[si] * kLog2e;
+#pragma unroll
+        for (int k = 0; k < kStatCopies; ++k) {
+          float* f = p.stat + k * p.stat_stride + stat_float(stat_pos(si, k));
+          f[0] = nl;
+          f[4] = -mine;
+        }
+      }
+    }
+    return;
+  }
   const long long nw = (nblk * blockDim.x) >> 5;
   const long long step = static_cast<long long>(rpw) * kUnroll;
   for (long long r0 = wid * step; r0 < rows; r0 += nw * step) {
