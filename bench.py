@@ -56,9 +56,14 @@ KERNEL_DESC = {
     "bwd_q": "backward dQ pass (S, dP, dQ += dS K)",
     "bwd_fused": "broadcast-Q backward (five products)",
 }
-# DRAM bytes per launch from one ncu capture of the kernel as it is now, on
-# this workload (profiles/ names the capture); None once the kernel changed.
-KERNEL_TRAFFIC = {}
+# DRAM bytes (read + write) per launch from one ncu capture of the kernels
+# as they are now, on the jagged self-attention workload (B=64, H=8, D=128;
+# profiles/dram_jagged_self.md has the command and the split); to be reset
+# to {} whenever one of these kernels changes.
+KERNEL_TRAFFIC = {
+    "jagged_self": {"fwd": 449422080 + 119499776, "bwd_kv": 605448448 + 253744128,
+                    "bwd_q": 604941312 + 124831232},
+}
 
 
 class ClockSampler:
@@ -314,6 +319,10 @@ def run_ours(args, x, wname):
     for k, v in kernels.items():
         if k in KERNEL_FLOPS_PER_PAIR_D:
             v["tflops"] = KERNEL_FLOPS_PER_PAIR_D[k] * H * D * pairs / (v["ms_per_launch"] * 1e-3) / 1e12
+        tr = KERNEL_TRAFFIC.get(wname, {}).get(k)
+        if tr is not None:
+            v["dram_bytes"] = tr
+            v["dram_gbs"] = tr / (v["ms_per_launch"] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -330,7 +339,8 @@ def run_ours(args, x, wname):
                      "ms_per_launch": kernels[dom]["ms_per_launch"],
                      "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
                      "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "traffic": KERNEL_TRAFFIC.get(dom)},
+                     "traffic": KERNEL_TRAFFIC.get(wname, {}).get(dom),
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
