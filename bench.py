@@ -61,8 +61,7 @@ KERNEL_DESC = {
 # profiles/dram_jagged_self.md has the command and the split); to be reset
 # to {} whenever one of these kernels changes.
 KERNEL_TRAFFIC = {
-    "jagged_self": {"fwd": 449422080 + 119499776, "bwd_kv": 605448448 + 253744128,
-                    "bwd_q": 604941312 + 124831232},
+    "jagged_self": {"fwd": 449422080 + 119499776},
 }
 
 

@@ -145,18 +145,40 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   const int T = p.hdr->T;
   uint32_t it = 0, gq = 0, nk = 0, nv = 0;
   bool ok = true;
-  for (uint32_t n = 0; ok; ++n) {
-    const int slot = n & 1;
-    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
+  // One-item lookahead: the next item is taken and decoded while this one's
+  // loads go out, and its K, V and first Q / dO boxes are prefetched into
+  // L2, so that at the item boundary they come from L2 rather than HBM.
+  auto fetch = [&](KvItem& f) {
     const int idx = atomicAdd(&p.hdr->ticket, 1);
-    KvItem f;
     if (idx < n_items)
       f = decode<CAUSAL>(p, idx, T);
     else
       f.b = -1;
+  };
+  auto prefetch = [&](const KvItem& f) {
+    const RowBox qb = row_box(f.off0 + f.t0 * kBM, f.L - f.t0 * kBM, T);
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) {
+      if (f.kt.row >= 0) {
+        tma_prefetch_l2_3d(tk, s * 64, f.h, f.kt.row);
+        tma_prefetch_l2_3d(tv, s * 64, f.h, f.kt.row);
+      }
+      if (qb.row >= 0) {
+        tma_prefetch_l2_3d(tq, s * 64, f.h, qb.row);
+        tma_prefetch_l2_3d(tdo, s * 64, f.h, qb.row);
+      }
+    }
+  };
+  KvItem f;
+  fetch(f);
+  for (uint32_t n = 0; ok; ++n) {
+    const int slot = n & 1;
+    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
     c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
-    if (idx >= n_items) break;
+    if (f.b < 0) break;
+    KvItem nx;
+    nx.b = -1;
     // Order of the item's loads: K, the first Q / dO, V (V waits for the
     // previous item's last dP^T), then the other Q / dO tiles.
     const int ks = it & 1;
@@ -192,6 +214,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       ++gq;
       if (i == 0) {
+        fetch(nx);
+        if (nx.b >= 0) prefetch(nx);
         if (!mbar_wait(&c->v_empty, (it & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -204,6 +228,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
     }
     ++it;
+    f = nx;
   }
   for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
     drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);

@@ -151,18 +151,40 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   const int T = p.hdr->T;
   uint32_t it = 0, nk = 0, nv = 0;
   bool ok = true;
-  for (uint32_t n = 0; ok; ++n) {
-    const int slot = n & 1;
-    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
+  // One-item lookahead: the next item is taken and decoded while this one's
+  // loads go out, and its Q / dO boxes and first K / V boxes are prefetched
+  // into L2, so that at the item boundary they come from L2 rather than HBM.
+  auto fetch = [&](QItem& f) {
     const int idx = atomicAdd(&p.hdr->ticket, 1);
-    QItem f;
     if (idx < n_items)
       f = decode<CAUSAL>(p, idx, T);
     else
       f.b = -1;
+  };
+  auto prefetch = [&](const QItem& f) {
+    const KvTile kt = kv_tile(f.off0, f.L, 0, T);
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (f.t[g].n > 0 && f.t[g].row >= 0) {
+          tma_prefetch_l2_3d(tq, s * 64, f.h, f.t[g].row);
+          tma_prefetch_l2_3d(tdo, s * 64, f.h, f.t[g].row);
+        }
+      if (kt.row >= 0) {
+        tma_prefetch_l2_3d(tk, s * 64, f.h, kt.row);
+        tma_prefetch_l2_3d(tv, s * 64, f.h, kt.row);
+      }
+    }
+  };
+  QItem f, nx;
+  fetch(f);
+  for (uint32_t n = 0; ok; ++n, f = nx) {
+    const int slot = n & 1;
+    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
     c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
-    if (idx >= n_items) break;
+    if (f.b < 0) break;
     if (!mbar_wait(&c->qdo_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
     const int ntiles = f.t[1].n > 0 ? 2 : 1;
     mbar_arrive_expect_tx(&c->qdo_full, ntiles * 2 * C::kTile);
@@ -197,6 +219,10 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
           tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
                       kt.row);
         ++nv;
+      }
+      if (j == 0) {  // after the item's first K / V loads
+        fetch(nx);
+        if (nx.b >= 0) prefetch(nx);
       }
     }
   }

@@ -125,6 +125,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Prefetch of one tensor-map box into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Plain bulk copy global -> shared (no tensor map): both addresses 16-byte
 // aligned, `bytes` a multiple of 16; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
