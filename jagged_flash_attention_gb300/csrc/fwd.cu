@@ -388,15 +388,19 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
           s[cc] = keep ? s[cc] : -INFINITY;
         }
       }
+      // Row max with three-input max: two new columns per instruction, four
+      // independent chains.
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int cc = 4; cc < 128; cc += 4) {
-        mx0 = fmaxf(mx0, s[cc]);
-        mx1 = fmaxf(mx1, s[cc + 1]);
-        mx2 = fmaxf(mx2, s[cc + 2]);
-        mx3 = fmaxf(mx3, s[cc + 3]);
+      for (int cc = 4; cc < 124; cc += 8) {
+        mx0 = fmax3(mx0, s[cc], s[cc + 1]);
+        mx1 = fmax3(mx1, s[cc + 2], s[cc + 3]);
+        mx2 = fmax3(mx2, s[cc + 4], s[cc + 5]);
+        mx3 = fmax3(mx3, s[cc + 6], s[cc + 7]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      mx0 = fmax3(mx0, s[124], s[125]);
+      mx1 = fmax3(mx1, s[126], s[127]);
+      const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
       // Raise the exponent base only when the max grew by more than 2^8.
       const bool raise = m_tile > m_used + kRescaleLog2;
       const float m_new = raise ? m_tile : m_used;
