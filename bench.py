@@ -61,7 +61,8 @@ KERNEL_DESC = {
 # profiles/dram_jagged_self.md has the command and the split); to be reset
 # to {} whenever one of these kernels changes.
 KERNEL_TRAFFIC = {
-    "jagged_self": {"fwd": 449422080 + 119499776},
+    "jagged_self": {"fwd": 449446656 + 119704320, "bwd_kv": 607665152 + 254846976,
+                    "bwd_q": 623944448 + 125608448},
 }
 
 
