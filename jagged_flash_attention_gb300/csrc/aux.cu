@@ -67,6 +67,7 @@ __device__ void sched_body(const SchedParams& p) {
   __shared__ int base[kMaxBuckets];
   __shared__ int cursor[kMaxBuckets];
   __shared__ int warp_tot[32];
+  __shared__ int s_pos[kSchedThreads], s_nt[kSchedThreads];
   __shared__ int s_bad;
   const int tid = threadIdx.x;
   for (int i = tid; i < kMaxBuckets; i += blockDim.x) hist[i] = 0, cursor[i] = 0;
@@ -105,25 +106,54 @@ __device__ void sched_body(const SchedParams& p) {
     }
     return;
   }
-  // One warp per sequence: lane 0 reserves the sequence's slots in its
-  // bucket, the lanes write the items.  Heads outer, tiles inner, so that
-  // consecutive items share K/V (or Q) in L2; forward causal: longest query
-  // tile first.
+  // Chunks of blockDim sequences.  Each thread reserves the slots of one
+  // sequence; threads of a warp whose sequences fall in the same cost bucket
+  // do it with one shared atomic (many short sequences share a few buckets).
+  // Then each warp writes the items of its share of the chunk's sequences,
+  // lanes over items.  Heads outer, tiles inner, so that consecutive items
+  // share K/V (or Q) in L2; forward causal: longest query tile first.
   const int lane = tid & 31, nwarps = blockDim.x >> 5;
   const bool reverse = !p.backward && p.causal;
-  for (int b = tid >> 5; b < p.B; b += nwarps) {
-    const int L = p.offsets[b + 1] - p.offsets[b];
-    const int nt = n_tiles(p, L);
-    if (nt == 0) continue;
-    const int n = p.H * nt;
-    int pos = 0;
-    if (lane == 0) pos = base[bucket_of(p, L)] + atomicAdd(&cursor[bucket_of(p, L)], n);
-    pos = __shfl_sync(0xffffffffu, pos, 0);
-    for (int j = lane; j < n; j += 32) {
-      const int h = j / nt, t = j - h * nt;
-      const int tt = reverse ? nt - 1 - t : t;
-      p.items[pos + j] = make_int2(b, (h << 16) | tt);
+  for (int c0 = 0; c0 < p.B; c0 += blockDim.x) {
+    const int b = c0 + tid;
+    int nt = 0, n = 0, key = 0;
+    if (b < p.B) {
+      const int L = p.offsets[b + 1] - p.offsets[b];
+      nt = n_tiles(p, L);
+      n = p.H * nt;
+      key = bucket_of(p, L);
     }
+    const unsigned active = __ballot_sync(0xffffffffu, n > 0);
+    int pos = 0;
+    if (n > 0) {
+      const unsigned peers = __match_any_sync(active, key);
+      const int leader = __ffs(peers) - 1;
+      int pre = 0, tot = 0;
+      for (unsigned m = peers; m; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const int nj = __shfl_sync(peers, n, j);
+        tot += nj;
+        if (j < lane) pre += nj;
+      }
+      int first = 0;
+      if (lane == leader) first = atomicAdd(&cursor[key], tot);
+      first = __shfl_sync(peers, first, leader);
+      pos = base[key] + first + pre;
+    }
+    s_pos[tid] = pos;
+    s_nt[tid] = nt;
+    __syncthreads();
+    for (int w = tid >> 5; w < kSchedThreads && c0 + w < p.B; w += nwarps) {
+      const int ntl = s_nt[w];
+      if (ntl == 0) continue;
+      const int nl = p.H * ntl, pl = s_pos[w];
+      for (int j = lane; j < nl; j += 32) {
+        const int h = j / ntl, t = j - h * ntl;
+        const int tt = reverse ? ntl - 1 - t : t;
+        p.items[pl + j] = make_int2(c0 + w, (h << 16) | tt);
+      }
+    }
+    __syncthreads();
   }
   if (tid == 0) {
     p.hdr->n_items = total;
