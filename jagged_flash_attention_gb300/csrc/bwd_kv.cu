@@ -9,8 +9,8 @@
 // global dQ accumulator:
 //   S^T  = K Q^T        (SS)                 -> TMEM [0,128)
 //   dP^T = V dO^T       (SS)                 -> TMEM [128,256)
-//   P^T  = exp2(S^T * scale*log2e - LSE*log2e), bf16 over S^T's columns
-//   dS^T = P^T (dP^T - Delta),                bf16 over dP^T's columns
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e), bf16 pairs over S^T's columns
+//   dS^T = bf16(P^T) * bf16(dP^T - Delta),     bf16 pairs over dP^T's columns
 //   dV  += P^T dO       (TS, B = dO MN-major)
 //   dK  += dS^T Q       (TS, B = Q MN-major)
 // The score math is split into a P part (needs S^T) and a dS part (needs
@@ -23,8 +23,10 @@
 // CTA = 18 warps: warps 0-15 score/gradient math (warp w: TMEM lanes
 // 32*(w%4).. = key rows, query columns 32*(w/4)..; four math warps per SM
 // sub-partition, so that each part's TMEM load -> math -> TMEM store chain
-// is hidden by the others) and the dK/dV epilogue, warp 16 TMA producer,
-// warp 17 MMA issuer.
+// is hidden by the others) and the dK/dV epilogue, warp 16 TMA producer
+// (decodes items one ahead, publishes them in shared memory, prefetches the
+// next item's first boxes into L2; each Q/dO stage carries its tile's row
+// statistics), warp 17 MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
