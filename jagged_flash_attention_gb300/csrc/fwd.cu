@@ -16,7 +16,8 @@
 //                   thread r owns row r of its tile (TMEM lane r)
 //   warp 8          TMA producer (the two Q tiles once per item, K and V
 //                   tiles into rings) and the dynamic work ticket
-//   warp 9          TMEM allocation and the single-thread tcgen05 issuer
+//   warp 9          TMEM allocation and the tcgen05 issuer (the whole warp
+//                   waits; an elect.sync lane issues)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them.  P_t
 // (bf16) overwrites the first 64 columns of S_t and is read from TMEM by the
 // PV MMA.  Issue order per K/V tile j: PV0(j-1), S0(j), PV1(j-1), S1(j), so
