@@ -206,23 +206,20 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   const int part = lane % tpr;
   const long long wid = (blk * blockDim.x + threadIdx.x) >> 5;
   if (!p.broadcast) {
-    // Self-attention: a warp takes 32 consecutive tokens t0.. of one head h
-    // (rpw rows per step, tpr threads per row, 16 bytes of O and dO each);
-    // the row sums are gathered so that lane l ends with token t0 + l, and
-    // the statistics are written for consecutive rows.
+    // Self-attention: a warp takes 32 consecutive rows r0.. of O and dO in
+    // memory order (row = t*H + h), one contiguous block (rpw rows per step,
+    // tpr threads per row, 16 bytes of O and dO each); the row sums are
+    // gathered so that lane l ends with row r0 + l, and the statistics of
+    // lanes with the same head land on consecutive tokens.
     const long long nwarps = (nblk * blockDim.x) >> 5;
-    const long long tblocks = (T + 31) / 32;
-    for (long long wb = wid; wb < tblocks * p.H; wb += nwarps) {
-      const int h = static_cast<int>(wb % p.H);
-      const long long t0 = (wb / p.H) * 32;
+    for (long long r0 = wid * 32; r0 < rows; r0 += nwarps * 32) {
       float mine = 0.f;
       for (int s0 = 0; s0 < 32; s0 += rpw * kUnrollSelf) {
         uint4 o[kUnrollSelf], g[kUnrollSelf];
 #pragma unroll
         for (int u = 0; u < kUnrollSelf; ++u) {
-          const long long t = t0 + s0 + u * rpw + lane / tpr;
-          if (t < T) {
-            const long long row = t * p.H + h;
+          const long long row = r0 + s0 + u * rpw + lane / tpr;
+          if (row < rows) {
             o[u] = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
             g[u] = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
           } else {
@@ -252,9 +249,10 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
           }
         }
       }
-      const long long t = t0 + lane;
-      if (t < T) {
-        const long long si = static_cast<long long>(h) * T + t;
+      const long long row = r0 + lane;
+      if (row < rows) {
+        const long long t = row / p.H, h = row % p.H;
+        const long long si = h * T + t;
         const float nl = -p.lse[si] * kLog2e;
 #pragma unroll
         for (int k = 0; k < kStatCopies; ++k) {
