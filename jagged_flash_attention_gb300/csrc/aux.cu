@@ -173,7 +173,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // to it.  tpr = D/8 threads per row, each reading 16 bytes of both tensors;
 // kUnroll rows per thread in flight.
 constexpr int kUnroll = 2;      // broadcast-Q rows in flight per thread
-constexpr int kUnrollSelf = 2;  // self-attention steps in flight per warp
+constexpr int kUnrollSelf = 1;  // self-attention steps in flight per warp (32-byte loads)
 
 __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   long long rows;
@@ -207,45 +207,56 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   const long long wid = (blk * blockDim.x + threadIdx.x) >> 5;
   if (!p.broadcast) {
     // Self-attention: a warp takes 32 consecutive rows r0.. of O and dO in
-    // memory order (row = t*H + h), one contiguous block (rpw rows per step,
-    // tpr threads per row, 16 bytes of O and dO each); the row sums are
-    // gathered so that lane l ends with row r0 + l, and the statistics of
-    // lanes with the same head land on consecutive tokens.
+    // memory order (row = t*H + h), one contiguous block (D/16 threads per
+    // row, 32 bytes of O and dO each, 32/(D/16) rows per step); the row sums
+    // are gathered so that lane l ends with row r0 + l, and the statistics
+    // of lanes with the same head land on consecutive tokens.
+    const int tpr32 = p.D / 16, rpw32 = 32 / tpr32, part32 = lane % tpr32;
+    const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | reinterpret_cast<uintptr_t>(p.dout)) & 31) == 0;
     const long long nwarps = (nblk * blockDim.x) >> 5;
     for (long long r0 = wid * 32; r0 < rows; r0 += nwarps * 32) {
       float mine = 0.f;
-      for (int s0 = 0; s0 < 32; s0 += rpw * kUnrollSelf) {
-        uint4 o[kUnrollSelf], g[kUnrollSelf];
+      for (int s0 = 0; s0 < 32; s0 += rpw32 * kUnrollSelf) {
+        uint32_t o[kUnrollSelf][8], g[kUnrollSelf][8];
 #pragma unroll
         for (int u = 0; u < kUnrollSelf; ++u) {
-          const long long row = r0 + s0 + u * rpw + lane / tpr;
+          const long long row = r0 + s0 + u * rpw32 + lane / tpr32;
           if (row < rows) {
-            o[u] = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
-            g[u] = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
+            const __nv_bfloat16* po = p.out + row * p.D + part32 * 16;
+            const __nv_bfloat16* pg = p.dout + row * p.D + part32 * 16;
+            if (v8) {
+              ld_global_v8(po, o[u]);
+              ld_global_v8(pg, g[u]);
+            } else {  // the caller's buffers are only 16-byte aligned
+              const uint4 o0 = reinterpret_cast<const uint4*>(po)[0], o1 = reinterpret_cast<const uint4*>(po)[1];
+              const uint4 g0 = reinterpret_cast<const uint4*>(pg)[0], g1 = reinterpret_cast<const uint4*>(pg)[1];
+              o[u][0] = o0.x, o[u][1] = o0.y, o[u][2] = o0.z, o[u][3] = o0.w;
+              o[u][4] = o1.x, o[u][5] = o1.y, o[u][6] = o1.z, o[u][7] = o1.w;
+              g[u][0] = g0.x, g[u][1] = g0.y, g[u][2] = g0.z, g[u][3] = g0.w;
+              g[u][4] = g1.x, g[u][5] = g1.y, g[u][6] = g1.z, g[u][7] = g1.w;
+            }
           } else {
-            o[u] = make_uint4(0, 0, 0, 0);
-            g[u] = o[u];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[u][i] = g[u][i] = 0u;
           }
         }
 #pragma unroll
         for (int u = 0; u < kUnrollSelf; ++u) {
-          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o[u]);
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
           float acc = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 a = __bfloat1622float2(o2[i]);
-            const float2 c = __bfloat1622float2(g2[i]);
+          for (int i = 0; i < 8; ++i) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o[u][i]));
+            const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g[u][i]));
             acc = fmaf(a.x, c.x, acc);
             acc = fmaf(a.y, c.y, acc);
           }
-          for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          // row s0 + u*rpw + j sits in lanes [j*tpr, (j+1)*tpr); lane l keeps row l
+          for (int off = tpr32 / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          // row s0 + u*rpw32 + j sits in lanes [j*tpr32, (j+1)*tpr32); lane l keeps row l
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j >= rpw) break;
-            const float v = __shfl_sync(0xffffffffu, acc, j * tpr);
-            if (lane == s0 + u * rpw + j) mine = v;
+          for (int j = 0; j < 8; ++j) {
+            if (j >= rpw32) break;
+            const float v = __shfl_sync(0xffffffffu, acc, j * tpr32);
+            if (lane == s0 + u * rpw32 + j) mine = v;
           }
         }
       }

@@ -181,3 +181,36 @@ def test_zero_max_len_broadcast():
     jfa.jfa_sync_and_check()
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
     del k
+
+
+@pytest.mark.parametrize("name", ["jagged_self", "tiny_self"])
+def test_buffers_aligned_to_16_bytes_only(name):
+    """Every tensor starts 16 bytes into a larger allocation (16-byte but not
+    32-byte aligned), so the kernels' 32-byte load and store paths must take
+    their 16-byte fallbacks; results match the oracle as for aligned buffers."""
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs(name, EDGE, H=2)
+    dev = torch.device("cuda")
+
+    def shifted(shape, dtype=torch.bfloat16, src=None):
+        n = int(np.prod(shape))
+        buf = torch.zeros(n + 8, dtype=dtype, device=dev)
+        view = buf[8:].view(*shape)
+        assert view.data_ptr() % 32 == 16
+        if src is not None:
+            view.copy_(src.to(dev))
+        return view
+
+    q, k, v, do = (shifted(tuple(x[n].shape), src=x[n]) for n in ("q", "k", "v", "dout"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    T, H, D = q.shape
+    out = shifted((T, H, D))
+    lse = torch.empty(H, T, dtype=torch.float32, device=dev)
+    jfa.forward(q, k, v, off, x["max_len"], scale=x["scale"], out=out, lse=lse)
+    dq, dk, dv = (shifted((T, H, D)) for _ in range(3))
+    jfa.backward(q, k, v, off, x["max_len"], out, lse, do, scale=x["scale"], dq=dq, dk=dk,
+                 dv=dv)
+    jfa.jfa_sync_and_check()
+    g = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    g = {n: t.detach().float().cpu().numpy().astype(np.float64) for n, t in g.items()}
+    compare(g, run_oracle(x))
