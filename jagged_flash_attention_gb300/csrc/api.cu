@@ -295,6 +295,9 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
   if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
   if ((st = map_rows(&tdo, dout, s.D, s.H, s.Tcap, "dout")) != JFA_OK) return st;
+  CUtensorMap tdk, tdv;
+  if ((st = map_rows(&tdk, dk, s.D, s.H, s.Tcap, "dk")) != JFA_OK) return st;
+  if ((st = map_rows(&tdv, dv, s.D, s.H, s.Tcap, "dv")) != JFA_OK) return st;
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -348,8 +351,8 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     bp.items = items_kv;
     bp.hdr = hdr_kv;
     e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
-      return launch_bwd_kv(
-          s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_kv), stream);
+      return launch_bwd_kv(s.D, s.causal, tq, tk, tv, tdo, tdk, tdv, bp,
+                           (int)std::min<long long>(ds->sms, cap_kv), stream);
     });
   }
   if (e == cudaSuccess) {

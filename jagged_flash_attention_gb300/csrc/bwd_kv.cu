@@ -37,7 +37,8 @@ constexpr int kMathWarps = 16;
 constexpr int kMath = 32 * kMathWarps;
 constexpr int kProducerWarp = kMathWarps;
 constexpr int kMmaWarp = kMathWarps + 1;
-constexpr int kThreads = 32 * (kMathWarps + 2);
+constexpr int kStoreWarp = kMathWarps + 2;
+constexpr int kThreads = 32 * (kMathWarps + 3);
 
 template <int D>
 struct KvCfg {
@@ -77,12 +78,23 @@ struct KvItem {
   int t0, nt;  // first query tile and count
 };
 
+// One staged output tensor for the store warp: which = 0: dV, 1: dK, -1:
+// no more; buf: byte offset of the staging buffer in shared memory.
+struct StoreJob {
+  int which, buf, h, row, kbuf;
+};
+
 struct KvCtl {
   uint64_t k_full[2], k_empty[2], v_full, v_empty;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
-  uint64_t dkdv_full, dkdv_empty;
+  uint64_t dkdv_full, dv_empty, dk_empty;
   uint64_t epi;  // math-warp sync of the staged epilogue stores
+  // Staged tensor -> store warp, one barrier per job slot (a slot's next
+  // phase can complete only after the store warp has taken its job); dV's
+  // rows read by the store.
+  uint64_t stg_full[2], stg_empty;
+  StoreJob job[2];               // what the store warp stores, by submission
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   KvItem item[2];  // decoded by the producer; b < 0: no more items
@@ -126,7 +138,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 // Next work item of the CTA as the producer decoded it (called by whole
 // warps: the math warps and the MMA warp).  False when the list is done or a
 // wait gave up (then *ok is false too).
-__device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool* ok, int* err) {
+__device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool* ok, int* err,
+                                          bool release = true) {
   const int slot = n & 1;
   if (!mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)) {
     *ok = false;
@@ -134,7 +147,7 @@ __device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool*
   }
   *f = c->item[slot];
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  if (release && (threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
   return f->b >= 0;
 }
 
@@ -311,9 +324,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     issue_dp(g0);
     if (leader) mma_commit(&c->dp_full);
     if (f.nt == 1 && leader) mma_commit(&c->v_empty);
-    // dV(g0) and dK(g0) restart the accumulators the previous item's
-    // epilogue reads.
-    if (!mbar_wait_warp(&c->dkdv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
+    // dV(g0) restarts the accumulator the previous item's epilogue reads
+    // (dK(g0) waits below for the dK one).
+    if (!mbar_wait_warp(&c->dv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
     // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).  Every product is
     // issued and committed whole; the issuer waits only before a product
     // that reads what the math produced (P^T before dV, dS^T before dK), so
@@ -333,6 +346,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
         if (leader) mma_commit(&c->s_full);
       }
       if (!wait_ds(g)) { ok = false; break; }
+      if (i == 0 && !mbar_wait_warp(&c->dk_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
       issue_dk(g, i > 0);
       if (leader) mma_commit(&c->qdo_empty[g % C::NSQ]);
@@ -363,179 +377,282 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
-  uint32_t it = 0, gq = 0, ep = 0;
-  bool ok = true;
-  for (uint32_t n = 0; ok; ++n) {
-    KvItem f;
-    if (!next_item(c, n, &f, &ok, p.err)) break;
+  // Statistics of columns 4j..4j+3 of tile g: -LSE*log2e at st4[2j], -Delta
+  // at st4[2j + 1]; they arrive with Q / dO of the tile's stage.
+  auto stats = [&](uint32_t g) {
+    return reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
+  };
+  // ---- P part of tile i (ring index g) of item f: P^T = exp2(S^T *
+  // scale*log2e - LSE*log2e), kept as bf16 pairs of this thread's 32 columns.
+  auto p_part = [&](const KvItem& f, int i, uint32_t g, uint32_t (&pk)[16]) {
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
-    for (int i = 0; i < f.nt; ++i, ++gq) {
-      const uint32_t g = gq;
-      const int t = f.t0 + i;
-      const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
-      const int q0 = t * kBM - qb.shift;  // local query index of column 0
-      // The statistics arrived with Q / dO of the stage (already complete
-      // once S^T is; waited on here for their visibility).
-      if (!mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) { ok = false; break; }
-      // Statistics of columns 4j..4j+3: -LSE*log2e at st4[2j], -Delta at
-      // st4[2j + 1].
-      const float4* st4 =
-          reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
-      // Admissible query columns [lo, hi): the box's rows of the sequence
-      // and, causal, the queries at or after this key.
-      int lo = qb.shift;
-      const int hi = qb.shift + qb.n;
-      if (CAUSAL) lo = max(lo, key - q0);
-      const bool ragged = qb.shift > 0 || qb.n < kBM;
-      const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > cbase));
-      const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
-      // ---- P part: P^T = exp2(S^T * scale*log2e - LSE*log2e), kept as bf16
-      // pairs of this thread's 64 columns.
-      if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[16];
-      {
-        uint32_t sraw[32];
-        tmem_ld32(tbase + lane_base + C::kColS + cbase, sraw);
-        tmem_wait_ld();
-        // Rows of keys outside the sequence are left unmasked: row r of dV
-        // and dK depends only on row r of P^T and dS^T, and those rows are
-        // never stored.
+    const int t = f.t0 + i;
+    const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+    const int q0 = t * kBM - qb.shift;  // local query index of column 0
+    // (already complete once S^T is; waited on here for the statistics'
+    // visibility)
+    if (!mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
+    const float4* st4 = stats(g);
+    // Admissible query columns [lo, hi): the box's rows of the sequence
+    // and, causal, the queries at or after this key.
+    int lo = qb.shift;
+    const int hi = qb.shift + qb.n;
+    if (CAUSAL) lo = max(lo, key - q0);
+    const bool ragged = qb.shift > 0 || qb.n < kBM;
+    const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > cbase));
+    const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+    if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) return false;
+    tc_fence_after();
+    {
+      uint32_t sraw[32];
+      tmem_ld32(tbase + lane_base + C::kColS + cbase, sraw);
+      tmem_wait_ld();
+      // Rows of keys outside the sequence are left unmasked: row r of dV
+      // and dK depends only on row r of P^T and dS^T, and those rows are
+      // never stored.
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 nl = st4[2 * (cbase / 4 + j)];
-          const float2 x01 = f2_unpack(ffma2(
-              f2_pack(__uint_as_float(sraw[4 * j]), __uint_as_float(sraw[4 * j + 1])), sl2x2,
-              f2_pack(nl.x, nl.y)));
-          const float2 x23 = f2_unpack(ffma2(
-              f2_pack(__uint_as_float(sraw[4 * j + 2]), __uint_as_float(sraw[4 * j + 3])), sl2x2,
-              f2_pack(nl.z, nl.w)));
-          pk[2 * j] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
-          pk[2 * j + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
-        }
-        if (mask) {  // ragged or causal diagonal tile: zero inadmissible columns
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = cbase + 2 * i;
-            pk[i] &= (static_cast<uint32_t>(col - lo) < span ? 0x0000ffffu : 0u) |
-                     (static_cast<uint32_t>(col + 1 - lo) < span ? 0xffff0000u : 0u);
-          }
-        }
-        // bf16 pairs of this quarter's columns land in its own first 16
-        // columns, already read above.
-        tmem_st16(tbase + lane_base + C::kColS + cbase, pk);
+      for (int j = 0; j < 8; ++j) {
+        const float4 nl = st4[2 * (cbase / 4 + j)];
+        const float2 x01 = f2_unpack(ffma2(
+            f2_pack(__uint_as_float(sraw[4 * j]), __uint_as_float(sraw[4 * j + 1])), sl2x2,
+            f2_pack(nl.x, nl.y)));
+        const float2 x23 = f2_unpack(ffma2(
+            f2_pack(__uint_as_float(sraw[4 * j + 2]), __uint_as_float(sraw[4 * j + 3])), sl2x2,
+            f2_pack(nl.z, nl.w)));
+        pk[2 * j] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
+        pk[2 * j + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&c->p_full);
-      // ---- dS part: dS^T = P^T (dP^T - Delta): the difference in fp32,
-      // rounded to bf16, times the bf16 P.
-      if (!mbar_wait_warp(&c->dp_full, g & 1, &c->abort, p.err)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t praw[32];
-        tmem_ld32(tbase + lane_base + C::kColDP + cbase, praw);
-        tmem_wait_ld();
-        uint32_t w[16];
+      if (mask) {  // ragged or causal diagonal tile: zero inadmissible columns
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 nd = st4[2 * (cbase / 4 + j) + 1];
-          const float2 d01 = f2_unpack(fadd2(
-              f2_pack(__uint_as_float(praw[4 * j]), __uint_as_float(praw[4 * j + 1])),
-              f2_pack(nd.x, nd.y)));
-          const float2 d23 = f2_unpack(fadd2(
-              f2_pack(__uint_as_float(praw[4 * j + 2]), __uint_as_float(praw[4 * j + 3])),
-              f2_pack(nd.z, nd.w)));
-          w[2 * j] = bmul2(pk[2 * j], pack_bf16x2(d01.x, d01.y));
-          w[2 * j + 1] = bmul2(pk[2 * j + 1], pack_bf16x2(d23.x, d23.y));
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const int col = cbase + 2 * i2;
+          pk[i2] &= (static_cast<uint32_t>(col - lo) < span ? 0x0000ffffu : 0u) |
+                    (static_cast<uint32_t>(col + 1 - lo) < span ? 0xffff0000u : 0u);
         }
-        tmem_st16(tbase + lane_base + C::kColDP + cbase, w);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&c->ds_full);
+      // bf16 pairs of this quarter's columns land in its own first 16
+      // columns, already read above.
+      tmem_st16(tbase + lane_base + C::kColS + cbase, pk);
     }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&c->p_full);
+    return true;
+  };
+  // ---- dS part of tile g: dS^T = P^T (dP^T - Delta): the difference in
+  // fp32, rounded to bf16, times the bf16 P.
+  auto ds_part = [&](uint32_t g, const uint32_t (&pk)[16]) {
+    const float4* st4 = stats(g);
+    if (!mbar_wait_warp(&c->dp_full, g & 1, &c->abort, p.err)) return false;
+    tc_fence_after();
+    {
+      uint32_t praw[32];
+      tmem_ld32(tbase + lane_base + C::kColDP + cbase, praw);
+      tmem_wait_ld();
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 nd = st4[2 * (cbase / 4 + j) + 1];
+        const float2 d01 = f2_unpack(fadd2(
+            f2_pack(__uint_as_float(praw[4 * j]), __uint_as_float(praw[4 * j + 1])),
+            f2_pack(nd.x, nd.y)));
+        const float2 d23 = f2_unpack(fadd2(
+            f2_pack(__uint_as_float(praw[4 * j + 2]), __uint_as_float(praw[4 * j + 3])),
+            f2_pack(nd.z, nd.w)));
+        w[2 * j] = bmul2(pk[2 * j], pack_bf16x2(d01.x, d01.y));
+        w[2 * j + 1] = bmul2(pk[2 * j + 1], pack_bf16x2(d23.x, d23.y));
+      }
+      tmem_st16(tbase + lane_base + C::kColDP + cbase, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&c->ds_full);
+    return true;
+  };
+  uint32_t it = 0, gq = 0, ep = 0;
+  // Sync of the 512 math threads (bounded mbarrier phases).
+  auto epi_sync = [&]() {
+    mbar_arrive(&c->epi);
+    const bool r_ = mbar_wait_warp(&c->epi, ep & 1, &c->abort, p.err);
+    ++ep;
+    return r_;
+  };
+  // This thread's 32 head-dim columns of dV or dK: D = 128: quarter qd holds
+  // columns 32*qd.. of both; D = 64: quarters 0-1 hold dV, 2-3 dK.
+  const int dbase = D == 128 ? 32 * qd : 32 * (qd & 1);
+  const bool has_dv = D == 128 || qd < 2, has_dk = D == 128 || qd >= 2;
+  // One tensor of the item epilogue (which = 0: dV, 1: scale * dK): the
+  // accumulator leaves TMEM and is released at once (the next item's first
+  // product into it then waits only for this load), then goes through the
+  // item's K buffer.  A full key block (all 128 rows in the sequence) is
+  // staged in the 128-byte-swizzled layout of the output tensor map (slab s
+  // of 64 columns at s*16 KB, row r at r*128 bytes, 16-byte chunk c at
+  // c ^ (r mod 8)) and handed to the store warp, which stores it by TMA:
+  // the math warps wait neither for the stores nor for the store warp,
+  // except, before staging dK, for dV's store to have read the buffer.  The
+  // rows of a ragged block are stored by the math warps, whole rows per
+  // warp store (one thread holds 64 bytes of one key row, 2 KB from the next
+  // row's; stored directly, every warp store would touch 32 lines), from the
+  // layout row r at 2*D bytes, 16-byte chunk c at c ^ (r mod D/8)
+  // (conflict-free both ways).
+  // Tensors handed to the store warp: full blocks hand over dV, dK, dV, ...,
+  // so dK is always the odd one and its dV the (ns >> 1)-th dV.
+  uint32_t ns = 0;
+  auto epi_tensor = [&](const KvItem& f, uint32_t itf, int which, bool full) {
+    uint8_t* stg = smem + C::kK + (itf & 1) * C::kTile;
+    const bool mine = which == 0 ? has_dv : has_dk;
+    uint32_t w16[16];
+    if (mine) {
+      uint32_t a[32];
+      tmem_ld32(tbase + lane_base + (which == 0 ? C::kColDV : C::kColDK) + dbase, a);
+      tmem_wait_ld();
+      const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll
+      for (int i2 = 0; i2 < 16; ++i2)
+        w16[i2] = pack_bf16x2(__uint_as_float(a[2 * i2]) * mul, __uint_as_float(a[2 * i2 + 1]) * mul);
+    }
+    tc_fence_before();
+    mbar_arrive(which == 0 ? &c->dv_empty : &c->dk_empty);
+    constexpr int kCpr = D / 8;       // 16-byte chunks per row
+    constexpr int kRpi = 32 / kCpr;   // rows per warp store
+    if (which == 1) {  // dV's rows have left the buffer
+      if (full) {
+        if (!mbar_wait_warp(&c->stg_empty, (ns >> 1) & 1, &c->abort, p.err)) return false;
+      } else if (!epi_sync()) {
+        return false;
+      }
+    }
+    if (mine) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 v4 = make_uint4(w16[4 * q4], w16[4 * q4 + 1], w16[4 * q4 + 2], w16[4 * q4 + 3]);
+        if (full) {
+          const int ch = (dbase % 64) / 8 + q4;
+          *reinterpret_cast<uint4*>(stg + (dbase / 64) * 16384 + r * 128 + ((ch ^ (r & 7)) * 16)) = v4;
+        } else {
+          const int ch = dbase / 8 + q4;
+          *reinterpret_cast<uint4*>(stg + r * (2 * D) + ((ch ^ (r & (kCpr - 1))) * 16)) = v4;
+        }
+      }
+    }
+    if (full) {
+      if (threadIdx.x == 0) {
+        StoreJob& j = c->job[ns & 1];
+        j.which = which;
+        j.buf = C::kK + (itf & 1) * C::kTile;
+        j.h = f.h;
+        j.row = f.kt.row;
+        j.kbuf = itf & 1;
+      }
+      fence_proxy_async_smem();  // the staged rows, for the TMA store
+      mbar_arrive(&c->stg_full[ns & 1]);
+      ++ns;
+      return true;
+    }
+    if (!epi_sync()) return false;  // the tensor is staged
+    __nv_bfloat16* dst = which == 0 ? p.dv : p.dk;
+    const int wi = threadIdx.x >> 5, ln = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 128 / (16 * kRpi); ++j) {
+      const int row = wi * (128 / 16) + j * kRpi + ln / kCpr;
+      const int ch = ln % kCpr;
+      const uint4 v = *reinterpret_cast<const uint4*>(stg + row * (2 * D) +
+                                                      ((ch ^ (row & (kCpr - 1))) * 16));
+      if (row >= f.kt.shift && row < f.kt.shift + f.kt.n) {
+        const long long tok = f.off0 + f.kb * kBN - f.kt.shift + row;
+        *reinterpret_cast<uint4*>(dst + (tok * p.H + f.h) * D + ch * 8) = v;
+      }
+    }
+    return true;
+  };
+  // dK of item itf, then its K buffer back to the producer (a TMA load may
+  // follow the generic-proxy accesses above): every math thread arrives, and
+  // once more the store warp after its store has read a full block, or
+  // thread 0 for a ragged one.
+  auto epi_dk = [&](const KvItem& f, uint32_t itf) {
+    const bool full = f.kt.shift == 0 && f.kt.n == kBN;
+    if (!epi_tensor(f, itf, 1, full)) return false;
+    fence_proxy_async_smem();
+    mbar_arrive(&c->k_empty[itf & 1]);
+    if (!full && threadIdx.x == 0) mbar_arrive(&c->k_empty[itf & 1]);
+    return true;
+  };
+  bool ok = true;
+  uint32_t n = 0;
+  KvItem f;
+  uint32_t pk[16];
+  // The math warps keep an item's slot of the item ring until its dK has
+  // left TMEM.  The previous item's dK epilogue follows this item's first dS
+  // part, so that the issuer's dK(g0) waits for one TMEM load rather than
+  // for the whole epilogue; the previous item is read back from its slot.
+  const bool any = next_item(c, n++, &f, &ok, p.err, false) && p_part(f, 0, gq, pk);
+  // fin: a last pass that only runs the last item's dK epilogue (from the
+  // same place in the loop as every other item's).
+  bool fin = false;
+  while (any) {
+    bool fine = true;
+    for (int i = 0; i < f.nt; ++i) {
+      const uint32_t g = gq + i;
+      if (!fin) {
+        if (i > 0 && !p_part(f, i, g, pk)) { fine = false; break; }
+        if (!ds_part(g, pk)) { fine = false; break; }
+      }
+      if (i == 0 && it > 0) {
+        const uint32_t slot = (n - 2) & 1;
+        if (!epi_dk(c->item[slot], it - 1)) { fine = false; break; }
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+      }
+      if (fin) break;
+    }
+    if (!fine || fin) break;
+    // The next item's first P part comes before this item's epilogue: its
+    // S^T is issued right after this item's last dK.
+    KvItem fn;
+    const bool have_n = next_item(c, n++, &fn, &ok, p.err, false);
     if (!ok) break;
-    // Item epilogue: dV and scale * dK rows of this K/V block.  The
-    // accumulators leave TMEM first and are released at once, so that the
-    // next item's dV / dK products do not wait for the stores.  D = 128:
-    // quarter qd holds head-dim columns 32*qd.. of both; D = 64: quarters
-    // 0-1 hold dV, 2-3 dK, 32 columns each.
+    if (have_n && !p_part(fn, 0, gq + f.nt, pk)) break;
     if (!mbar_wait_warp(&c->dkdv_full, it & 1, &c->abort, p.err)) break;
     tc_fence_after();
-    constexpr int kParts = D == 128 ? 2 : 1;
-    const int dbase = D == 128 ? 32 * qd : 32 * (qd & 1);
-    uint32_t acc[kParts][32];
-#pragma unroll
-    for (int w = 0; w < kParts; ++w) {
-      const int which = D == 128 ? w : (qd >> 1);
-      tmem_ld32(tbase + lane_base + (which == 0 ? C::kColDV : C::kColDK) + dbase, acc[w]);
-    }
-    tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(&c->dkdv_empty);
-    // Each tensor goes through this item's K buffer (every product of the
-    // item has completed), so that warps store whole rows: one thread's
-    // registers hold 64 bytes of one key row, 2 KB away from the next
-    // row's, and stored directly every warp store would touch 32 lines.
-    // Staging layout: row r at 2*D bytes per row, 16-byte chunk c at
-    // c ^ (r mod D/8) (conflict-free both ways).
-    uint8_t* stg = smem + C::kK + (it & 1) * C::kTile;
-    constexpr int kCpr = D / 8;           // 16-byte chunks per row
-    constexpr int kRpi = 32 / kCpr;       // rows per warp store
-    const int wi = threadIdx.x >> 5, ln = threadIdx.x & 31;
-    auto epi_sync = [&]() {
-      mbar_arrive(&c->epi);
-      const bool r_ = mbar_wait_warp(&c->epi, ep & 1, &c->abort, p.err);
-      ++ep;
-      return r_;
-    };
-    bool eok = true;
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      if (w == 1 && !(eok = epi_sync())) break;  // the dV rows are read
-      if (D == 128 || (qd >> 1) == w) {
-        const float mul = w == 0 ? 1.f : p.scale;
-        const uint32_t* a = acc[D == 128 ? w : 0];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t o[4];
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2)
-            o[i2] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * i2]) * mul,
-                                __uint_as_float(a[8 * q4 + 2 * i2 + 1]) * mul);
-          const int ch = dbase / 8 + q4;
-          *reinterpret_cast<uint4*>(stg + r * (2 * D) + ((ch ^ (r & (kCpr - 1))) * 16)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      if (!(eok = epi_sync())) break;  // the tensor is staged
-      __nv_bfloat16* dst = w == 0 ? p.dv : p.dk;
-#pragma unroll
-      for (int j = 0; j < 128 / (16 * kRpi); ++j) {
-        const int row = wi * (128 / 16) + j * kRpi + ln / kCpr;
-        const int ch = ln % kCpr;
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + row * (2 * D) +
-                                                        ((ch ^ (row & (kCpr - 1))) * 16));
-        if (row >= f.kt.shift && row < f.kt.shift + f.kt.n) {
-          const long long tok = f.off0 + f.kb * kBN - f.kt.shift + row;
-          *reinterpret_cast<uint4*>(dst + (tok * p.H + f.h) * D + ch * 8) = v;
-        }
-      }
-    }
-    if (!eok) break;
-    // The K buffer goes back to the producer (a TMA load may follow the
-    // generic-proxy accesses above).
-    fence_proxy_async_smem();
-    mbar_arrive(&c->k_empty[it & 1]);
+    if (!epi_tensor(f, it, 0, f.kt.shift == 0 && f.kt.n == kBN)) break;
+    gq += f.nt;
     ++it;
+    if (have_n)
+      f = fn;
+    else
+      fin = true;
   }
+  // No more tensors for the store warp.
+  if (threadIdx.x == 0) c->job[ns & 1].which = -1;
+  mbar_arrive(&c->stg_full[ns & 1]);
+}
+
+// Store warp (one thread): TMA stores of the staged full blocks, in order.
+// After dV's store has read the buffer, the math warps may stage dK there;
+// after dK's, the K buffer goes back to the producer.
+template <int D>
+__device__ void store_role(const CUtensorMap* tdk, const CUtensorMap* tdv, uint8_t* smem,
+                           KvCtl* c, int* err) {
+  for (uint32_t e = 0;; ++e) {
+    if (!mbar_wait(&c->stg_full[e & 1], (e >> 1) & 1, &c->abort, err)) break;
+    const StoreJob j = c->job[e & 1];
+    if (j.which < 0) break;
+#pragma unroll
+    for (int s = 0; s < D / 64; ++s)
+      tma_store_3d(j.which == 0 ? tdv : tdk, smem + j.buf + s * 16384, s * 64, j.h, j.row);
+    bulk_commit();
+    bulk_wait_read0();
+    mbar_arrive(j.which == 0 ? &c->stg_empty : &c->k_empty[j.kbuf]);
+  }
+  // The stores are complete before the CTA's shared memory goes away.
+  bulk_wait0();
 }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                   const BwdParams p) {
   using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -548,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->k_full[i], 1);
-      mbar_init(&c->k_empty[i], kMath);  // released by the math warps' epilogue
+      // released by the math warps' epilogue and the store warp (a ragged
+      // block: math thread 0 twice)
+      mbar_init(&c->k_empty[i], kMath + 1);
     }
     mbar_init(&c->v_full, 1);
     mbar_init(&c->v_empty, 1);
@@ -563,8 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c->p_full, kMath);
     mbar_init(&c->ds_full, kMath);
     mbar_init(&c->dkdv_full, 1);
-    mbar_init(&c->dkdv_empty, kMath);
+    mbar_init(&c->dv_empty, kMath);
+    mbar_init(&c->dk_empty, kMath);
     mbar_init(&c->epi, kMath);
+    mbar_init(&c->stg_full[0], kMath);
+    mbar_init(&c->stg_full[1], kMath);
+    mbar_init(&c->stg_empty, 1);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();
@@ -574,6 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdk);
+    tma_prefetch_desc(&tdv);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&c->tmem_base, 512);
@@ -585,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = c->tmem_base;
   if (warp < kMathWarps) {
     math_role<D, CAUSAL>(p, smem, c, tbase);
+  } else if (warp == kStoreWarp) {
+    if (lane == 0) store_role<D>(&tdk, &tdv, smem, c, p.err);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
@@ -601,28 +728,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t s) {
+                     const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                     const BwdParams& p, int grid, cudaStream_t s) {
   using C = KvCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(KvCtl) <= 512, "control block");
   auto kern = bwd_kv_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                          int grid, cudaStream_t s) {
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                          const CUtensorMap& tdv, const BwdParams& p, int grid, cudaStream_t s) {
   if (D == 128) {
-    if (causal) return launch_t<128, true>(tq, tk, tv, tdo, p, grid, s);
-    return launch_t<128, false>(tq, tk, tv, tdo, p, grid, s);
+    if (causal) return launch_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+    return launch_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
   }
-  if (causal) return launch_t<64, true>(tq, tk, tv, tdo, p, grid, s);
-  return launch_t<64, false>(tq, tk, tv, tdo, p, grid, s);
+  if (causal) return launch_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  return launch_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
 }
 
 }  // namespace jfa

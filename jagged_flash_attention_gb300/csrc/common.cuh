@@ -131,9 +131,10 @@ cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, co
 cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const BwdParams& p, int grid, cudaStream_t s);
+// tdk / tdv: the dK / dV outputs as maps like the inputs' (TMA stores).
 cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                          int grid, cudaStream_t s);
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                          const CUtensorMap& tdv, const BwdParams& p, int grid, cudaStream_t s);
 cudaError_t launch_bwd_q(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                          int grid, cudaStream_t s);

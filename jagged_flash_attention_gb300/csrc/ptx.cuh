@@ -132,6 +132,22 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0,
                : "memory");
 }
 
+// TMA store of one tensor-map box from shared memory, in the thread's bulk
+// async-group (source 128-byte aligned in the map's swizzle layout).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(m),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until the thread's committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Until the thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Plain bulk copy global -> shared (no tensor map): both addresses 16-byte
 // aligned, `bytes` a multiple of 16; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
