@@ -86,7 +86,9 @@ struct StoreJob {
 
 struct KvCtl {
   uint64_t k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t qdo_full[2], qdo_empty[2];
+  // Query-tile ring: Q (with the rows' statistics) and dO of a stage have
+  // their own barriers: Q is read by S^T and dK, dO by dP^T and dV.
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dkdv_full, dv_empty, dk_empty;
   uint64_t epi;  // math-warp sync of the staged epilogue stores
@@ -207,7 +209,9 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = gq;
       const int st = g % C::NSQ;
-      if (!mbar_wait(&c->qdo_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+      // Q first: the issuer's S^T(g) waits for it a product before dP^T(g)
+      // waits for dO.
+      if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
@@ -218,15 +222,21 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       const long long sidx = static_cast<long long>(f.h) * T + qb.row;
       const int sk = static_cast<int>((sidx + kStatPad) & 3);
       const float* ssrc = p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
-      mbar_arrive_expect_tx(&c->qdo_full[st], 2 * C::kTile + C::kStatBytes);
-      bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->qdo_full[st]);
+      mbar_arrive_expect_tx(&c->q_full[st], C::kTile + C::kStatBytes);
+      bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->q_full[st]);
 #pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s) {
-        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->qdo_full[st], s * 64, f.h,
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st], s * 64, f.h,
                     qb.row);
-        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->qdo_full[st], s * 64, f.h,
-                    qb.row);
+      if (!mbar_wait(&c->do_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+        ok = false;
+        break;
       }
+      mbar_arrive_expect_tx(&c->do_full[st], C::kTile);
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st], s * 64, f.h,
+                    qb.row);
       ++gq;
       if (i == 0) {
         fetch(nx);
@@ -248,8 +258,10 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
     drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
   if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
-  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
-    drain_wait(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
+  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g) {
+    drain_wait(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
+    drain_wait(&c->do_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
+  }
 }
 
 template <int D, bool CAUSAL>
@@ -298,8 +310,11 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     for (int k = 0; k < kBM / 16; ++k)
       if (leader) mma_ts(tDK, tDP + pack_col(k), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
   };
-  auto wait_qdo = [&](uint32_t g) {
-    return mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
+  auto wait_q = [&](uint32_t g) {
+    return mbar_wait_warp(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
+  };
+  auto wait_do = [&](uint32_t g) {
+    return mbar_wait_warp(&c->do_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
   };
   auto wait_p = [&](uint32_t g) { return mbar_wait_warp(&c->p_full, g & 1, &c->abort, p.err); };
   auto wait_ds = [&](uint32_t g) { return mbar_wait_warp(&c->ds_full, g & 1, &c->abort, p.err); };
@@ -312,7 +327,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     if (!mbar_wait_warp(&c->k_full[ks], (it >> 1) & 1, &c->abort, p.err)) break;
     const uint64_t dk_k = desc_add(dk_k0, ks * C::kTile);
     const uint32_t g0 = gq;
-    if (!wait_qdo(g0)) break;
+    if (!wait_q(g0)) break;
     tc_fence_after();
     issued = true;
     issue_s(g0, dk_k);
@@ -320,6 +335,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     // V is released after the item's last dP^T; K after the item epilogue,
     // which stages its stores in the K buffer.
     if (!mbar_wait_warp(&c->v_full, it & 1, &c->abort, p.err)) break;
+    if (!wait_do(g0)) break;
     tc_fence_after();
     issue_dp(g0);
     if (leader) mma_commit(&c->dp_full);
@@ -339,8 +355,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
       if (!wait_p(g)) { ok = false; break; }
       tc_fence_after();
       issue_dv(g, i > 0);
+      if (leader) mma_commit(&c->do_empty[g % C::NSQ]);
       if (more) {
-        if (!wait_qdo(g + 1)) { ok = false; break; }
+        if (!wait_q(g + 1)) { ok = false; break; }
         tc_fence_after();
         issue_s(g + 1, dk_k);
         if (leader) mma_commit(&c->s_full);
@@ -349,8 +366,10 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
       if (i == 0 && !mbar_wait_warp(&c->dk_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
       issue_dk(g, i > 0);
-      if (leader) mma_commit(&c->qdo_empty[g % C::NSQ]);
+      if (leader) mma_commit(&c->q_empty[g % C::NSQ]);
       if (more) {
+        if (!wait_do(g + 1)) { ok = false; break; }
+        tc_fence_after();
         issue_dp(g + 1);
         if (leader) mma_commit(&c->dp_full);
         if (i + 2 == f.nt && leader) mma_commit(&c->v_empty);
@@ -391,7 +410,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     const int q0 = t * kBM - qb.shift;  // local query index of column 0
     // (already complete once S^T is; waited on here for the statistics'
     // visibility)
-    if (!mbar_wait_warp(&c->qdo_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
+    if (!mbar_wait_warp(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
     const float4* st4 = stats(g);
     // Admissible query columns [lo, hi): the box's rows of the sequence
     // and, causal, the queries at or after this key.
@@ -672,8 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c->v_full, 1);
     mbar_init(&c->v_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&c->qdo_full[i], 1);
-      mbar_init(&c->qdo_empty[i], 1);
+      mbar_init(&c->q_full[i], 1);
+      mbar_init(&c->q_empty[i], 1);
+      mbar_init(&c->do_full[i], 1);
+      mbar_init(&c->do_empty[i], 1);
       mbar_init(&c->item_full[i], 1);
       mbar_init(&c->item_empty[i], kMathWarps + 1);  // math warps + the MMA warp
     }
