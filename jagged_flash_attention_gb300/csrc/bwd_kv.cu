@@ -209,14 +209,24 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = gq;
       const int st = g % C::NSQ;
-      // Q first: the issuer's S^T(g) waits for it a product before dP^T(g)
-      // waits for dO.
-      if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+      // dO first: its stage frees after dV, a product before Q's (after dK),
+      // so that its bytes are in by the time Q's load starts, and Q, which
+      // S^T(g) waits for, has the L2 path to itself.
+      if (!mbar_wait(&c->do_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+      mbar_arrive_expect_tx(&c->do_full[st], C::kTile);
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st], s * 64, f.h,
+                    qb.row);
+      if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
       // Row statistics of the box: 32 whole groups of the copy in which
       // its first row starts a group.
       const long long sidx = static_cast<long long>(f.h) * T + qb.row;
@@ -227,15 +237,6 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s)
         tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st], s * 64, f.h,
-                    qb.row);
-      if (!mbar_wait(&c->do_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(&c->do_full[st], C::kTile);
-#pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st], s * 64, f.h,
                     qb.row);
       ++gq;
       if (i == 0) {
