@@ -381,16 +381,21 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
       if (!mbar_wait_warp(&c->s_full[g], u & 1, &c->abort, p.err)) return false;
       tc_fence_after();
       const uint32_t ts = tbase + lane_base + 256 * g + 64 * half;
+      // All 64 columns leave TMEM first, so that dP may overwrite SP while
+      // the exponentials are computed.
+      uint32_t sraw[2][32];
+      tmem_ld32(ts, sraw[0]);
+      tmem_ld32(ts + 32, sraw[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&c->p_done[g]);  // S read: dP may overwrite SP
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sraw[32];
-        tmem_ld32(ts + 32 * ch, sraw);
-        tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 x = f2_unpack(ffma2(
-              f2_pack(__uint_as_float(sraw[2 * i]), __uint_as_float(sraw[2 * i + 1])), sl2x2,
-              nlse2[g]));
+          const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(sraw[ch][2 * i]),
+                                                   __uint_as_float(sraw[ch][2 * i + 1])),
+                                           sl2x2, nlse2[g]));
           pk[16 * ch + i] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
         }
       }
@@ -411,8 +416,6 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
           pk[i] &= keep;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&c->p_done[g]);  // S read: dP may overwrite SP
       return true;
     };
     // dS = P (dP - Delta) of tile g at key tile j, bf16 pairs into SP's
