@@ -61,8 +61,8 @@ KERNEL_DESC = {
 # profiles/dram_jagged_self.md has the command and the split); to be reset
 # to {} whenever one of these kernels changes.
 KERNEL_TRAFFIC = {
-    "jagged_self": {"fwd": 449446656 + 119704320, "bwd_kv": 607665152 + 254846976,
-                    "bwd_q": 623944448 + 125608448},
+    "jagged_self": {"fwd": 449218560 + 119739648, "bwd_kv": 606578688 + 253614848,
+                    "bwd_q": 627068928 + 126120704},
 }
 
 

@@ -20,13 +20,18 @@
 // dV(g+1) + S(g+2).  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) right after
 // the dV / dK MMAs that read them (MMAs of one CTA execute in issue order).
 //
-// CTA = 18 warps: warps 0-15 score/gradient math (warp w: TMEM lanes
+// CTA = 19 warps: warps 0-15 score/gradient math (warp w: TMEM lanes
 // 32*(w%4).. = key rows, query columns 32*(w/4)..; four math warps per SM
 // sub-partition, so that each part's TMEM load -> math -> TMEM store chain
 // is hidden by the others) and the dK/dV epilogue, warp 16 TMA producer
 // (decodes items one ahead, publishes them in shared memory, prefetches the
-// next item's first boxes into L2; each Q/dO stage carries its tile's row
-// statistics), warp 17 MMA issuer.
+// next item's first boxes into L2; each Q stage carries its tile's row
+// statistics, and Q and dO of a stage have their own barriers), warp 17 MMA
+// issuer, warp 18 the store warp (TMA stores of full dK/dV blocks).
+// At an item boundary the math warps compute the next item's first P part,
+// then the item's dV epilogue, the next item's first dS part, and only then
+// the item's dK epilogue, so that the first products of the next item wait
+// for one TMEM load each rather than for the epilogue.
 #include "common.cuh"
 #include "ptx.cuh"
 
