@@ -92,8 +92,10 @@ struct StoreJob {
 struct KvCtl {
   uint64_t k_full[2], k_empty[2], v_full, v_empty;
   // Query-tile ring: Q (with the rows' statistics) and dO of a stage have
-  // their own barriers: Q is read by S^T and dK, dO by dP^T and dV.
-  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  // their own barriers: Q is read by S^T and dK, dO by dP^T and dV.  The
+  // full barriers are per 64-column slab ([stage][slab]; the statistics
+  // ride with slab 0), so that a product's first K steps need only slab 0.
+  uint64_t q_full[2][2], q_empty[2], do_full[2][2], do_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dkdv_full, dv_empty, dk_empty;
   uint64_t epi;  // math-warp sync of the staged epilogue stores
@@ -223,11 +225,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       const int t = f.t0 + i;
       const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
-      mbar_arrive_expect_tx(&c->do_full[st], C::kTile);
 #pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st], s * 64, f.h,
-                    qb.row);
+      for (int s = 0; s < C::kSlabs; ++s) {
+        mbar_arrive_expect_tx(&c->do_full[st][s], 16384);
+        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
+                    f.h, qb.row);
+      }
       if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
@@ -237,12 +240,14 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       const long long sidx = static_cast<long long>(f.h) * T + qb.row;
       const int sk = static_cast<int>((sidx + kStatPad) & 3);
       const float* ssrc = p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
-      mbar_arrive_expect_tx(&c->q_full[st], C::kTile + C::kStatBytes);
-      bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->q_full[st]);
 #pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st], s * 64, f.h,
+      for (int s = 0; s < C::kSlabs; ++s) {
+        mbar_arrive_expect_tx(&c->q_full[st][s], 16384 + (s == 0 ? C::kStatBytes : 0));
+        if (s == 0)
+          bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->q_full[st][0]);
+        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st][s], s * 64, f.h,
                     qb.row);
+      }
       ++gq;
       if (i == 0) {
         fetch(nx);
@@ -265,8 +270,11 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
   if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
   for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g) {
-    drain_wait(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
-    drain_wait(&c->do_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) {
+      drain_wait(&c->q_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+      drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+    }
   }
 }
 
@@ -286,21 +294,38 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   const uint64_t ddo_m0 = smem_desc_sw128(smem_addr(smem + C::kDO), 16384, 1024);
   const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP;
   const uint32_t tDV = tbase + C::kColDV, tDK = tbase + C::kColDK;
+  // Slab s of the query tile of ring index g (Q or dO), before its first K step.
+  auto wait_slab = [&](uint64_t (*full)[2], uint32_t g, int s) {
+    return mbar_wait_warp(&full[g % C::NSQ][s], (g / C::NSQ) & 1, &c->abort, p.err);
+  };
+  // S^T(g) and dP^T(g): K steps 4k.. read 64-column slab k of Q / dO; the
+  // issuer waits for slab 0 before the product (wait_q / wait_do) and for
+  // slab 1 between its K steps 3 and 4.
   auto issue_s = [&](uint32_t g, uint64_t dk_k) {
     const uint64_t dq_k = desc_add(dq_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
+      if (k > 0 && k % 4 == 0) {
+        if (!wait_slab(c->q_full, g, k / 4)) return false;
+        tc_fence_after();
+      }
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
       if (leader) mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
     }
+    return true;
   };
   auto issue_dp = [&](uint32_t g) {
     const uint64_t ddo_k = desc_add(ddo_k0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
+      if (k > 0 && k % 4 == 0) {
+        if (!wait_slab(c->do_full, g, k / 4)) return false;
+        tc_fence_after();
+      }
       const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
       if (leader) mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
     }
+    return true;
   };
   // A operand column of query block k (16 queries): the packed P^T / dS^T
   // of query quarter k/2 starts at its own first column, 32 * (k/2).
@@ -316,12 +341,8 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     for (int k = 0; k < kBM / 16; ++k)
       if (leader) mma_ts(tDK, tDP + pack_col(k), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
   };
-  auto wait_q = [&](uint32_t g) {
-    return mbar_wait_warp(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
-  };
-  auto wait_do = [&](uint32_t g) {
-    return mbar_wait_warp(&c->do_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err);
-  };
+  auto wait_q = [&](uint32_t g) { return wait_slab(c->q_full, g, 0); };
+  auto wait_do = [&](uint32_t g) { return wait_slab(c->do_full, g, 0); };
   auto wait_p = [&](uint32_t g) { return mbar_wait_warp(&c->p_full, g & 1, &c->abort, p.err); };
   auto wait_ds = [&](uint32_t g) { return mbar_wait_warp(&c->ds_full, g & 1, &c->abort, p.err); };
   uint32_t it = 0, gq = 0;
@@ -336,24 +357,24 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     if (!wait_q(g0)) break;
     tc_fence_after();
     issued = true;
-    issue_s(g0, dk_k);
+    if (!issue_s(g0, dk_k)) break;
     if (leader) mma_commit(&c->s_full);
     // V is released after the item's last dP^T; K after the item epilogue,
     // which stages its stores in the K buffer.
     if (!mbar_wait_warp(&c->v_full, it & 1, &c->abort, p.err)) break;
     if (!wait_do(g0)) break;
     tc_fence_after();
-    issue_dp(g0);
+    if (!issue_dp(g0)) break;
     if (leader) mma_commit(&c->dp_full);
     if (f.nt == 1 && leader) mma_commit(&c->v_empty);
     // dV(g0) restarts the accumulator the previous item's epilogue reads
     // (dK(g0) waits below for the dK one).
     if (!mbar_wait_warp(&c->dv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
     // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).  Every product is
-    // issued and committed whole; the issuer waits only before a product
-    // that reads what the math produced (P^T before dV, dS^T before dK), so
-    // that S(g+1) and dP(g+1), which the math waits for, never queue behind
-    // a wait.  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) after dV(g) /
+    // committed whole, and the issuer waits only before a product that reads
+    // what the math produced (P^T before dV, dS^T before dK) or for the query
+    // tile's slabs that S(g+1) and dP(g+1) read (slab 1 between their K
+    // steps 3 and 4, so that the first half runs while it lands).  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) after dV(g) /
     // dK(g), which were issued before them.
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = g0 + i;
@@ -365,7 +386,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
       if (more) {
         if (!wait_q(g + 1)) { ok = false; break; }
         tc_fence_after();
-        issue_s(g + 1, dk_k);
+        if (!issue_s(g + 1, dk_k)) { ok = false; break; }
         if (leader) mma_commit(&c->s_full);
       }
       if (!wait_ds(g)) { ok = false; break; }
@@ -376,7 +397,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
       if (more) {
         if (!wait_do(g + 1)) { ok = false; break; }
         tc_fence_after();
-        issue_dp(g + 1);
+        if (!issue_dp(g + 1)) { ok = false; break; }
         if (leader) mma_commit(&c->dp_full);
         if (i + 2 == f.nt && leader) mma_commit(&c->v_empty);
       }
@@ -416,7 +437,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     const int q0 = t * kBM - qb.shift;  // local query index of column 0
     // (already complete once S^T is; waited on here for the statistics'
     // visibility)
-    if (!mbar_wait_warp(&c->q_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
+    if (!mbar_wait_warp(&c->q_full[g % C::NSQ][0], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
     const float4* st4 = stats(g);
     // Admissible query columns [lo, hi): the box's rows of the sequence
     // and, causal, the queries at or after this key.
@@ -697,9 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c->v_full, 1);
     mbar_init(&c->v_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&c->q_full[i], 1);
+      mbar_init(&c->q_full[i][0], 1);
+      mbar_init(&c->q_full[i][1], 1);
       mbar_init(&c->q_empty[i], 1);
-      mbar_init(&c->do_full[i], 1);
+      mbar_init(&c->do_full[i][0], 1);
+      mbar_init(&c->do_full[i][1], 1);
       mbar_init(&c->do_empty[i], 1);
       mbar_init(&c->item_full[i], 1);
       mbar_init(&c->item_empty[i], kMathWarps + 1);  // math warps + the MMA warp
