@@ -74,7 +74,9 @@ struct FwdItem {
 
 struct FwdCtl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  // K stages have one full barrier per 64-column slab ([stage][slab]): S's
+  // first K steps need only slab 0.
+  uint64_t k_full[4][2], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
@@ -194,11 +196,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
 #pragma unroll
-        for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
+        for (int s = 0; s < C::kSlabs; ++s) {
+          mbar_arrive_expect_tx(&c->k_full[st][s], 16384);
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st][s], s * 64, f.h,
                       kt.row);
+        }
         ++nk;
       }
       if (j >= 1) {
@@ -220,20 +223,21 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   // Drain: make sure every copy this CTA issued has landed before exit.
   if (itq > 0) drain_wait(&c->q_full, (itq - 1) & 1, p.err);
   for (uint32_t g = nk > C::NSK ? nk - C::NSK : 0; g < nk; ++g)
-    drain_wait(&c->k_full[g % C::NSK], (g / C::NSK) & 1, p.err);
+    for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->k_full[g % C::NSK][s], (g / C::NSK) & 1, p.err);
   for (uint32_t g = nv > C::NSV ? nv - C::NSV : 0; g < nv; ++g)
     drain_wait(&c->v_full[g % C::NSV], (g / C::NSV) & 1, p.err);
 }
 
-// S_t = Q_t K^T: dq / dk are the K-major descriptors of the Q tile and the
-// K stage (start of the tile); K steps advance them inside 128-byte rows.
+// S_t = Q_t K^T, K steps [k0, k1): dq / dk are the K-major descriptors of
+// the Q tile and the K stage (start of the tile); K steps advance them inside
+// 128-byte rows, step k in 64-column slab k/4.
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t leader, uint32_t tbase, int t, uint64_t dq,
-                                        uint64_t dk) {
+                                        uint64_t dk, int k0, int k1) {
   using C = FwdCfg<D>;
   const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
 #pragma unroll
-  for (int k = 0; k < D / 16; ++k) {
+  for (int k = k0; k < k1; ++k) {
     const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
     if (leader) mma_ss(tbase + C::colS(t), desc_add(dq, off), desc_add(dk, off), id_s, k > 0);
   }
@@ -274,11 +278,10 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
     ++itq;
     for (int j = 0; j <= f.N && ok; ++j) {
       uint64_t dk = 0, dv = 0;
-      if (j < f.N) {
-        const int st = nk % C::NSK;
-        if (!mbar_wait_warp(&c->k_full[st], (nk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
-        dk = desc_add(dk0, st * C::kTile);
-      }
+      const int kst = nk % C::NSK;
+      const uint32_t kph = (nk / C::NSK) & 1;
+      int k_have = 0;  // slabs of K(j) waited for; K is read only by S, after PV_0(j-1)
+      if (j < f.N) dk = desc_add(dk0, kst * C::kTile);
       if (j >= 1) {
         const int st = nv % C::NSV;
         if (!mbar_wait_warp(&c->v_full[st], (nv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
@@ -298,8 +301,18 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
           issue_pv<D>(leader, tbase, t, dv, j > 1);
           if (leader) mma_commit(&c->o_ready[t]);
         }
-        if (j < nkv) {  // S_t(j) = Q_t K(j)^T
-          issue_s<D>(leader, tbase, t, desc_add(dq0, t * C::kTile), dk);
+        if (j < nkv) {  // S_t(j) = Q_t K(j)^T, slab 1 of K waited for between its halves
+          const uint64_t dq = desc_add(dq0, t * C::kTile);
+#pragma unroll
+          for (int sl = 0; sl < C::kSlabs; ++sl) {
+            if (k_have <= sl) {
+              if (!mbar_wait_warp(&c->k_full[kst][sl], kph, &c->abort, p.err)) { ok = false; break; }
+              tc_fence_after();
+              k_have = sl + 1;
+            }
+            issue_s<D>(leader, tbase, t, dq, dk, 4 * sl, 4 * sl + 4);
+          }
+          if (!ok) break;
           if (leader) mma_commit(&c->s_full[t]);
           issued = true;
         }
@@ -490,7 +503,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(&c->q_full, 1);
     mbar_init(&c->q_empty, 1);
     for (int i = 0; i < C::NSK; ++i) {
-      mbar_init(&c->k_full[i], 1);
+      mbar_init(&c->k_full[i][0], 1);
+      mbar_init(&c->k_full[i][1], 1);
       mbar_init(&c->k_empty[i], 1);
     }
     for (int i = 0; i < C::NSV; ++i) {
