@@ -61,8 +61,8 @@ KERNEL_DESC = {
 # profiles/dram_jagged_self.md has the command and the split); to be reset
 # to {} whenever one of these kernels changes.
 KERNEL_TRAFFIC = {
-    "jagged_self": {"fwd": 449218560 + 119739648, "bwd_kv": 606578688 + 253614848,
-                    "bwd_q": 627068928 + 126120704},
+    "jagged_self": {"fwd": 449209856 + 120235520, "bwd_kv": 606568448 + 253562112,
+                    "bwd_q": 627318528 + 126046720},
 }
 
 
