@@ -424,7 +424,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   // Statistics of columns 4j..4j+3 of tile g: -LSE*log2e at st4[2j], -Delta
-  // at st4[2j + 1]; they arrive with Q / dO of the tile's stage.
+  // at st4[2j + 1]; they arrive with slab 0 of the tile's Q stage.
   auto stats = [&](uint32_t g) {
     return reinterpret_cast<const float4*>(smem + C::kStat + (g % C::NSQ) * C::kStatBytes);
   };
@@ -516,7 +516,8 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     return true;
   };
   uint32_t it = 0, gq = 0, ep = 0;
-  // Sync of the 512 math threads (bounded mbarrier phases).
+  // Sync of the 512 math threads (bounded mbarrier phases), around the
+  // staging of a ragged block's epilogue.
   auto epi_sync = [&]() {
     mbar_arrive(&c->epi);
     const bool r_ = mbar_wait_warp(&c->epi, ep & 1, &c->abort, p.err);
