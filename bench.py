@@ -126,6 +126,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value, ws, device="cpu"):
+    """The job's figure for a per-rank time: its maximum over all ranks (one
+    all-reduce, which every rank calls; it also orders the ranks like a
+    barrier).  One rank: the value itself."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws, step_flops, ms_per_step):
+    """Whole-job TFLOPS: each of the ws ranks runs one replica of the step,
+    and the step takes ms_per_step (the slowest rank's time)."""
+    return ws * step_flops / (ms_per_step * 1e-3) / 1e12
+
+
 def _oracle_sample(x, budget_s, max_seqs=None):
     """Time the fp64 oracle (fwd + bwd) on the workload's sequences, in order,
     until `budget_s` seconds of CPU work; returns (flops, seconds, n_seqs)."""
@@ -253,15 +272,11 @@ def run_ours(args, x, wname):
     if ws > 1:
         torch.distributed.barrier()
     jfa.jfa_sync_and_check()
-    total_ms = t_start.elapsed_time(t_end)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws, dev)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms_per_step = total_ms / args.steps
-    value = ws * step_f / (ms_per_step * 1e-3) / 1e12
+    value = job_value(ws, step_f, ms_per_step)
 
     # End to end through the public API: every step copies its inputs from
     # pinned host memory to the device, makes the two calls and copies every
@@ -319,8 +334,8 @@ def run_ours(args, x, wname):
     e1.record(s_out)
     torch.cuda.synchronize()
     jfa.jfa_sync_and_check()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_val = ws * step_f / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    e2e_val = job_value(ws, step_f, e2e_ms)
 
     if rank != 0:
         if ws > 1:
