@@ -374,8 +374,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     // committed whole, and the issuer waits only before a product that reads
     // what the math produced (P^T before dV, dS^T before dK) or for the query
     // tile's slabs that S(g+1) and dP(g+1) read (slab 1 between their K
-    // steps 3 and 4, so that the first half runs while it lands).  S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) after dV(g) /
-    // dK(g), which were issued before them.
+    // steps 3 and 4, so that the first half runs while it lands).
+    // S(g+1) / dP(g+1) overwrite P^T(g) / dS^T(g) after dV(g) / dK(g),
+    // which were issued before them.
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = g0 + i;
       const bool more = i + 1 < f.nt;
