@@ -42,7 +42,10 @@ a hand-derived two-key example in tests/golden), row-stochasticity, LSE by a
 direct sum, padded-dense equality against torch's float64 SDPA on CPU (a
 library special case), float64 autograd of that library route, central finite
 differences of the gradients, broadcast = stacked per-sequence attention, and
-permutation invariants.
+permutation invariants.  The query-row chunking (ROW_CHUNK) is pinned in
+tests/test_oracle_chunks.py: blocks of 3 and 7 rows against the same torch
+float64 routes, with planted slips (causal offset lost, dK / dV overwritten
+instead of summed, block rows taken from the wrong place) caught.
 """
 from __future__ import annotations
 
