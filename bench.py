@@ -1,19 +1,24 @@
 """Benchmark of the jagged flash attention hot path (forward + backward).
 
-One step = jfa_fwd + jfa_bwd over one batch of the jagged self-attention
-workload (B=64 sequences, lengths uniform in [16, 2048], H=8, D=128, bf16,
-non-causal).  value = useful TFLOPS on true lengths: (4 + 10) * H * D * pairs
-per step.  Prints ONE JSON line (rank 0).
+One step = jfa_fwd + jfa_bwd over one batch of a workload.  The headline
+workload is the jagged self-attention batch (B=64 sequences, lengths uniform
+in [16, 2048], H=8, D=128, bf16, non-causal); value = useful TFLOPS on true
+lengths: (4 + 10) * H * D * pairs per step.  The same JSON line carries, under
+`workloads`, the other four workloads (tiny self-attention, broadcast-Q,
+causal self-attention, skewed broadcast-Q), each device-timed with its
+per-kernel roofline fractions.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--only]
 
---impl reference times the fp64 CPU oracle on the host cores (bounded
-sample of the same workload); there is no GPU reference implementation.
+--only times the named workload alone (no `workloads` object).
+--impl reference times the fp64 CPU oracle on the host cores (bounded sample
+of the same workload); there is no GPU reference implementation.
 """
 import argparse
+import datetime
+import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -29,6 +34,7 @@ import jfa_workloads as W  # noqa: E402
 
 METRIC = "JFA fwd and bwd useful TFLOPS (bf16) and % of GB300 tensor peak"
 DEFAULT_WORKLOAD = "jagged_self"
+L2_BYTES = 129 * 2 ** 20
 
 
 def _peaks():
@@ -46,36 +52,109 @@ def _flops(x):
     return f, 2.5 * f, p
 
 
-# Algorithmic tensor-core FLOPs of one launch of each product kernel, per
-# head and query-key pair (2 * D per product): forward S and PV; dK/dV pass
-# S^T, dP^T, dV, dK; dQ pass S, dP, dQ; broadcast-Q backward all five.
-KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4.0, "bwd_kv": 8.0, "bwd_q": 6.0, "bwd_fused": 10.0}
 KERNEL_DESC = {
+    "sched": "forward work-list scheduler",
     "fwd": "forward (S = QK^T, O += PV)",
+    "prep": "backward pre-pass (work lists, LSE*log2e, Delta = rowsum(dO*O))",
     "bwd_kv": "backward dK/dV pass (S^T, dP^T, dV += P^T dO, dK += dS^T Q)",
-    "bwd_q": "backward dQ pass (S, dP, dQ += dS K)",
-    "bwd_fused": "broadcast-Q backward (five products)",
+    "bwd_q": "self-attention backward dQ pass (S, dP, dQ += dS K)",
+    "bwd_qb": "broadcast-Q backward dQ pass (S, dP, dQ += dS K over key-tile chunks)",
+    "finalize": "broadcast-Q dQ: sum of the chunk partials, bf16",
 }
-# DRAM bytes (read + write) per launch from one ncu capture of the kernels
-# as they are now, on the jagged self-attention workload (B=64, H=8, D=128;
-# profiles/dram_jagged_self.md has the command and the split); to be reset
-# to {} whenever one of these kernels changes.
-KERNEL_TRAFFIC = {
-    "jagged_self": {"fwd": 449209856 + 120235520, "bwd_kv": 606568448 + 253562112,
-                    "bwd_q": 627318528 + 126046720},
+
+
+def kernel_model(x):
+    """Algorithmic work of one launch of each kernel kind on workload x:
+    {kind: (tensor FLOPs, DRAM bytes)}.  FLOPs count true (query, key) pairs
+    (2 * D per pair and product); bytes count each tensor the kernel must
+    read or write once: Q rows are T (self) or q_len (broadcast), O / dO rows
+    T or B * q_len, K / V rows T; bf16 tensors, fp32 LSE and statistics
+    (8 bytes per row and head; self-attention keeps four copies)."""
+    H, D, T, B, Lq = x["H"], x["D"], x["T"], x["B"], x["q_len"]
+    bq = x["broadcast_q"]
+    pairs = W.pairs(x["lengths"], x["causal"], Lq, bq)
+    row = H * D * 2
+    qrows, orows = (Lq, B * Lq) if bq else (T, T)
+    stat = 8 * H * orows
+    m = {
+        "sched": (0.0, 4.0 * (B + 1)),
+        "fwd": (4.0 * H * D * pairs, (qrows + 2 * T + orows) * row + 4 * H * orows),
+        "prep": (0.0, 2 * orows * row + 4 * H * orows + (stat if bq else 4 * stat)),
+        "bwd_kv": (8.0 * H * D * pairs, (4 * T + qrows + orows) * row + stat),
+    }
+    if bq:
+        m["bwd_qb"] = (6.0 * H * D * pairs, (2 * T + qrows + orows) * row + stat + 4 * Lq * H * D)
+        m["finalize"] = (0.0, 6 * Lq * H * D)
+    else:
+        m["bwd_q"] = (6.0 * H * D * pairs, (4 * T) * row + stat + T * row)
+    return m
+
+
+def step_model(x):
+    """(FLOPs, bytes) of the forward and of the backward step: the method's
+    useful FLOPs (fwd 4, bwd 10 * H * D * pairs) and the bytes each tensor
+    needs once: fwd Q, K, V, O, LSE; bwd Q, K, V, O (for Delta), dO (twice),
+    LSE, Delta, and dQ, dK, dV written."""
+    H, D, T, B, Lq = x["H"], x["D"], x["T"], x["B"], x["q_len"]
+    fwd_f, bwd_f, _ = _flops(x)
+    row = H * D * 2
+    qrows, orows = (Lq, B * Lq) if x["broadcast_q"] else (T, T)
+    fwd_b = (qrows + 2 * T + orows) * row + 4 * H * orows
+    bwd_b = (2 * qrows + 4 * T + 3 * orows) * row + 8 * H * orows
+    return (fwd_f, fwd_b), (bwd_f, bwd_b)
+
+
+def _roof(flops, nbytes, seconds, peak_tf, hbm_gbs):
+    """Roofline fraction max(flops / peak, bytes / bandwidth) / time, and the
+    bound that sets it."""
+    tf, tb = flops / (peak_tf * 1e12), nbytes / (hbm_gbs * 1e9)
+    return (max(tf, tb) / seconds if seconds > 0 else 0.0), ("tensor" if tf >= tb else "hbm")
+
+
+# DRAM bytes (read + write) per launch measured by ncu, with the sha256 of
+# the sources the kernel was built from; bench.py reports a record only while
+# those sources are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = {
+    "fwd": ["fwd.cu"], "bwd_kv": ["bwd_kv.cu"], "bwd_q": ["bwd_q.cu"], "bwd_qb": ["bwd_qb.cu"],
+    "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"],
 }
+
+
+def source_hash(kind):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "jagged_flash_attention_gb300", "csrc")
+    for f in KERNEL_SOURCES.get(kind, []) + ["common.cuh", "ptx.cuh"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_record(kind, wname):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            recs = json.load(f)["records"]
+    except Exception:
+        return None
+    for r in recs:
+        if r["kernel"] == kind and r["workload"] == wname:
+            return r["bytes_per_launch"] if r["sha256"] == source_hash(kind) else None
+    return None
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """nvidia-smi clock / throttle-reason samples, with host timestamps, for
+    the whole measurement session; summaries over any time window."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.samples = []
 
     def __enter__(self):
         try:
@@ -88,35 +167,39 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
             except Exception:
                 self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
-
-    def summary(self):
-        sms, maxs, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+        for l in out.splitlines():
+            f = [v.strip() for v in l.split(",")]
+            if len(f) < 10:
                 continue
             try:
-                sms.append(float(f[1]))
-                maxs.append(float(f[2]))
+                sm, mx = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sms:
+            try:
+                t = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = None  # unknown time: counted in every window
+            reasons = {n for n, v in zip(self.NAMES, f[6:10]) if v.lower() == "active"}
+            self.samples.append((t, sm, mx, reasons))
+
+    def summary(self, windows=None):
+        """Samples inside any of the (t0, t1) host-time windows (all samples
+        if windows is None)."""
+        sel = [s for s in self.samples
+               if windows is None or s[0] is None or any(t0 <= s[0] <= t1 for t0, t1 in windows)]
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        reasons = set().union(*(s[3] for s in sel))
+        return {"sm_mhz": statistics.median(s[1] for s in sel),
+                "sm_max_mhz": max(s[2] for s in sel), "reasons": sorted(reasons),
+                "samples": len(sel)}
 
 
 def _dist():
@@ -176,6 +259,23 @@ def _oracle_sample(x, budget_s, max_seqs=None):
     return tot_f, tot_t, n
 
 
+def _l2_note(x):
+    big = x["k"].numel() * 2
+    if big > L2_BYTES:
+        return f"inputs larger than L2 (k, v {big / 1e6:.0f} MB each); no flush"
+    return "inputs fit in L2: a 256 MB buffer is written between timed steps (flush)"
+
+
+def _config(x, wname, ws=1):
+    """The workload description both arms print (same keys)."""
+    return {"workload": wname, "B": int(x["B"]), "H": x["H"], "D": x["D"], "T": x["T"],
+            "causal": x["causal"], "broadcast_q": x["broadcast_q"], "q_len": x["q_len"],
+            "max_len": x["max_len"], "lengths": W.WORKLOADS[wname].lengths_desc,
+            "seed": W.WORKLOADS[wname].seed,
+            "pairs": W.pairs(x["lengths"], x["causal"], x["q_len"], x["broadcast_q"]),
+            "l2": _l2_note(x), "parallelism": "replicas" if ws > 1 else "single GPU"}
+
+
 def run_reference(args, x, wname):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -197,7 +297,7 @@ def run_reference(args, x, wname):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(per_step) / len(per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wname, **_cfg(x, wname)},
+        "config": _config(x, wname, args.gpus),
         "cpu_baseline": {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                          "sample": f"first {nseq} sequences (all heads) per step, fwd+bwd"},
         "e2e": {"value": tf, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -205,10 +305,110 @@ def run_reference(args, x, wname):
     print(json.dumps(line), flush=True)
 
 
-def _cfg(x, wname):
-    return {"B": int(x["B"]), "H": x["H"], "D": x["D"], "T": x["T"], "causal": x["causal"],
-            "broadcast_q": x["broadcast_q"], "q_len": x["q_len"], "max_len": x["max_len"],
-            "lengths": W.WORKLOADS[wname].lengths_desc, "seed": W.WORKLOADS[wname].seed}
+def _kernels_entry(x, kprof, peak, hbm, wname):
+    """Per kernel kind: mean device time per launch, launches, share, and its
+    roofline fraction on the algorithmic work of kernel_model."""
+    model = kernel_model(x)
+    tot = sum(t for t, n in kprof.values())
+    out = {}
+    for k, (t, n) in kprof.items():
+        if n == 0:
+            continue
+        ms = t / n
+        f, b = model.get(k, (0.0, 0.0))
+        frac, bound = _roof(f, b, ms * 1e-3, peak, hbm)
+        e = {"ms_per_launch": ms, "launches": n, "share": t / tot if tot else 0.0,
+             "tflops": f / (ms * 1e-3) / 1e12, "gbs": b / (ms * 1e-3) / 1e9,
+             "bound": bound, "roofline_frac": frac}
+        tr = traffic_record(k, wname)
+        if tr is not None:
+            e["dram_bytes"] = tr
+        out[k] = e
+    return out
+
+
+def _time_steps(jfa, torch, x, steps, warmup, stream, dev, min_seconds=0.15):
+    """Device-timed fwd / bwd steps of workload x through the public API;
+    returns (fwd ms per step, bwd ms per step, kernel profile, launches,
+    host time window of the timed steps)."""
+    B, H, D = x["B"], x["H"], x["D"]
+    bq, causal, scale, max_len = x["broadcast_q"], x["causal"], x["scale"], x["max_len"]
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    out, lse = jfa.forward(q, k, v, off, max_len, causal=causal, broadcast_q=bq, scale=scale)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    flush = None
+    if x["k"].numel() * 2 <= L2_BYTES:
+        flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        jfa.forward(q, k, v, off, max_len, causal=causal, broadcast_q=bq, scale=scale, out=out,
+                    lse=lse)
+
+    def bwd():
+        jfa.backward(q, k, v, off, max_len, out, lse, do, causal=causal, broadcast_q=bq,
+                     scale=scale, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    jfa.jfa_sync_and_check()
+    # enough steps for a timed region of about min_seconds (clock samples)
+    torch.cuda.synchronize()
+    t_probe = time.time()
+    fwd()
+    bwd()
+    torch.cuda.synchronize()
+    per_step = max(time.time() - t_probe, 1e-6)
+    steps = int(min(max(steps, round(min_seconds / per_step)), 500))
+    jfa.profile_read()  # discard anything recorded before the timed region
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    n0 = jfa.launch_count()
+    t0 = time.time()
+    jfa.profile_enable(True)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()  # torch's kernel, outside this step's events
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    jfa.profile_enable(False)
+    t1 = time.time()
+    launches = jfa.launch_count() - n0
+    kprof = jfa.profile_read()
+    jfa.jfa_sync_and_check()
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    return fwd_ms, bwd_ms, kprof, launches, (t0, t1), steps
+
+
+def _workload_entry(x, wname, fwd_ms, bwd_ms, kprof, peak, hbm, clk, window, steps):
+    fwd_f, bwd_f, pairs = _flops(x)
+    (ff, fb), (bf, bb) = step_model(x)
+    fwd_frac, fwd_bound = _roof(ff, fb, fwd_ms * 1e-3, peak, hbm)
+    bwd_frac, bwd_bound = _roof(bf, bb, bwd_ms * 1e-3, peak, hbm)
+    kernels = _kernels_entry(x, kprof, peak, hbm, wname)
+    work = [k for k in kernels if k not in ("sched", "finalize")]
+    dom = max(work, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
+    return {
+        "config": {k: v for k, v in _config(x, wname).items() if k not in ("parallelism",)},
+        "steps": steps,
+        "value": (fwd_f + bwd_f) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, "unit": "TFLOPS",
+        "fwd": {"ms": fwd_ms, "tflops": fwd_f / (fwd_ms * 1e-3) / 1e12,
+                "frac_of_peak": fwd_f / (fwd_ms * 1e-3) / 1e12 / peak,
+                "roofline_frac": fwd_frac, "bound": fwd_bound, "algorithmic_bytes": fb},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
+                "frac_of_peak": bwd_f / (bwd_ms * 1e-3) / 1e12 / peak,
+                "roofline_frac": bwd_frac, "bound": bwd_bound, "algorithmic_bytes": bb},
+        "kernels": kernels,
+        "dominant": {"kernel": dom, "desc": KERNEL_DESC.get(dom, dom),
+                     "bound": kernels[dom]["bound"], "frac": kernels[dom]["roofline_frac"]},
+        "clocks": clk.summary([window]),
+    }
 
 
 def run_ours(args, x, wname):
@@ -225,7 +425,7 @@ def run_ours(args, x, wname):
     peak, peak_sus, hbm, peak_src = _peaks()
     fwd_f, bwd_f, pairs = _flops(x)
     step_f = fwd_f + bwd_f
-    B, H, D, Lq = x["B"], x["H"], x["D"], x["q_len"]
+    B, H, D = x["B"], x["H"], x["D"]
     bq, causal, scale, max_len = x["broadcast_q"], x["causal"], x["scale"], x["max_len"]
 
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
@@ -251,21 +451,25 @@ def run_ours(args, x, wname):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(local)
+    clk.__enter__()
+    windows = []
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = jfa.launch_count()
     jfa.profile_enable(True)
-    with ClockSampler(local) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            fwd()
-            ev[i][1].record(stream)
-            bwd()
-            ev[i][2].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    h0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    windows.append((h0, time.time()))
     jfa.profile_enable(False)
     launches = jfa.launch_count() - launches0
     kprof = jfa.profile_read()
@@ -336,6 +540,30 @@ def run_ours(args, x, wname):
     jfa.jfa_sync_and_check()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
     e2e_val = job_value(ws, step_f, e2e_ms)
+    del sets, hq, hk, hv, hdo, ho, hl, hdq, hdk, hdv
+
+    # The other workloads (rank 0 of a single-GPU run, unless --only): each
+    # device-timed over a few steps through the same public API.
+    workloads = {}
+    if ws == 1 and not args.only:
+        workloads[wname] = (x, fwd_ms, bwd_ms, kprof, windows[0], args.steps)
+        for other in W.ORDER:
+            if other == wname:
+                continue
+            xo = W.make_inputs(W.WORKLOADS[other])
+            steps = max(3, min(args.steps, args.workload_steps))
+            f_ms, b_ms, kp, _, win, steps = _time_steps(jfa, torch, xo, steps,
+                                                        max(3, args.warmup), stream, dev)
+            windows.append(win)
+            workloads[other] = (xo, f_ms, b_ms, kp, win, steps)
+            del xo
+            torch.cuda.empty_cache()
+    clk.__exit__(None, None, None)
+    for other, entry in list(workloads.items()):
+        if isinstance(entry, tuple):
+            xo, f_ms, b_ms, kp, win, steps = entry
+            workloads[other] = _workload_entry(xo, other, f_ms, b_ms, kp, peak, hbm, clk, win,
+                                               steps)
 
     if rank != 0:
         if ws > 1:
@@ -349,33 +577,17 @@ def run_ours(args, x, wname):
                          f"({t:.1f} s)"}
     bwd_tf = bwd_f / (bwd_ms * 1e-3) / 1e12
     fwd_tf = fwd_f / (fwd_ms * 1e-3) / 1e12
-    # Per-kernel device time over the timed region (events on the launching
-    # stream, recorded by the library); roofline of the dominant kernel.
-    kernels = {k: {"ms_per_launch": t / n, "launches": n, "share": 0.0}
-               for k, (t, n) in kprof.items() if n > 0}
-    tot = sum(t for t, n in kprof.values())
-    for k, (t, n) in kprof.items():
-        if n > 0:
-            kernels[k]["share"] = t / tot
-    dom = max((k for k in kernels if k in KERNEL_FLOPS_PER_PAIR_D),
+    kernels = _kernels_entry(x, kprof, peak, hbm, wname)
+    model = kernel_model(x)
+    dom = max((k for k in kernels if model.get(k, (0, 0))[0] > 0),
               key=lambda k: kprof[k][0])
-    dom_flops = KERNEL_FLOPS_PER_PAIR_D[dom] * H * D * pairs
+    dom_flops = model[dom][0]
     dom_tf = dom_flops / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e12
-    for k, v in kernels.items():
-        if k in KERNEL_FLOPS_PER_PAIR_D:
-            v["tflops"] = KERNEL_FLOPS_PER_PAIR_D[k] * H * D * pairs / (v["ms_per_launch"] * 1e-3) / 1e12
-        tr = KERNEL_TRAFFIC.get(wname, {}).get(k)
-        if tr is not None:
-            v["dram_bytes"] = tr
-            v["dram_gbs"] = tr / (v["ms_per_launch"] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wname, **_cfg(x, wname), "pairs": pairs,
-                   "l2": "inputs larger than L2 (q,k,v,dout,out each "
-                         f"{x['q'].numel() * 2 / 1e6:.0f} MB); no flush",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "config": _config(x, wname, ws),
         "frac_of_peak": value / peak,
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak},
@@ -384,7 +596,7 @@ def run_ours(args, x, wname):
                      "ms_per_launch": kernels[dom]["ms_per_launch"],
                      "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
                      "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "traffic": KERNEL_TRAFFIC.get(wname, {}).get(dom),
+                     "traffic": traffic_record(dom, wname),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "kernels": kernels,
         "cpu_baseline": cpu,
@@ -394,8 +606,11 @@ def run_ours(args, x, wname):
                             "copies, compute and result copies pipelined on three streams "
                             "with two device buffer sets"},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(windows),
+        "clocks_headline": clk.summary(windows[:1]),
     }
+    if workloads:
+        line["workloads"] = workloads
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -408,6 +623,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.ORDER)
+    ap.add_argument("--only", action="store_true",
+                    help="time the named workload alone (no `workloads` object)")
+    ap.add_argument("--workload-steps", type=int, default=10,
+                    help="timed steps of each other workload (at least 3)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -45,7 +45,8 @@
  *   offsets, a bounded wait that ran out) are reported by
  *   jfa_sync_and_check().  With the environment variable JFA_VALIDATE=1
  *   every call synchronises and checks before returning.
- * - Thread safety: calls on different streams may run concurrently.
+ * - Thread safety: calls on different streams may run concurrently, except
+ *   jfa_fwd_bq_noalloc, whose calls all share one scratch array (see there).
  */
 #ifndef JFA_H_
 #define JFA_H_
@@ -117,7 +118,9 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
  * call before capturing a stream into a CUDA graph.  All calls share the one
  * array, so calls whose GPU work overlaps (different streams, or different
  * host threads) race and give wrong results: serialise them.  Device-side
- * errors set the same device error word that jfa_sync_and_check reads. */
+ * errors set the same device error word that jfa_sync_and_check reads; with
+ * JFA_VALIDATE=1 this call, like the others, synchronises and checks that
+ * word before returning (still without allocating). */
 jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const int32_t* offsets,
                               int B, int H, int D, int max_len, int q_len, int broadcast_q,
                               int causal, float scale, void* out, float* lse,
@@ -136,6 +139,29 @@ const char* jfa_last_error(void);
 const char* jfa_version(void);
 
 /* ------------------------------------------------------------------------
+ * Work-list inspection.  A library facility with no counterpart in the
+ * pages (whose tile scheduling, "Optimizing Jagged Flash Attention with
+ * TLX", section 2.2 "Scheduling jagged tiles across SMs", sorts work
+ * longest-first on the host): it builds one of the device work lists
+ * exactly as the named pass does and copies it out, so that a caller can
+ * check it.  list: 0 forward (items (b, h, pair of 128-row query tiles),
+ * longest sequences first), 1 dK/dV pass ((b, h, 128-key block), most query
+ * tiles first), 2 self-attention dQ pass ((b, h, pair), longest first), 3
+ * broadcast-Q dQ pass (equal chunks of the key-tile stream).  offsets as for
+ * jfa_fwd (device int32[B+1]); q_len as for jfa_fwd_bq.  items: DEVICE
+ * int32 buffer of 4 * capacity ints, 16-byte aligned, written with 4 ints
+ * per item in list order: lists 0-2 {b, h, tile, 0}; list 3 {h | pair << 16,
+ * b, j, n}: n key tiles from tile j of sequence b on, through the following
+ * non-empty sequences.  count: DEVICE int32[2]: {number of items (-1 if the
+ * device found the offsets invalid), chunks per (head, pair) for list 3 else
+ * 0}.  JFA_ERR_INVALID_ARG if capacity is below the list's size bound (the
+ * message names it).  Asynchronous on `stream`; scratch as for jfa_fwd.
+ * ------------------------------------------------------------------------ */
+jfa_status jfa_worklist(const int32_t* offsets, int B, int H, int max_len, int q_len,
+                        int broadcast_q, int causal, int list, int32_t* items, int capacity,
+                        int32_t* count, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Launch accounting.  A library facility with no counterpart in the pages:
  * it lets a caller count the kernels this library enqueues and time each
  * kind on the stream it runs on.
@@ -146,10 +172,10 @@ typedef enum {
   JFA_KERNEL_SCHED = 0,     /* forward work-list scheduler */
   JFA_KERNEL_FWD = 1,       /* forward */
   JFA_KERNEL_PREP = 2,      /* backward pre-pass: work lists, LSE*log2e, Delta */
-  JFA_KERNEL_BWD_KV = 3,    /* self-attention backward, dK / dV pass */
+  JFA_KERNEL_BWD_KV = 3,    /* backward dK / dV pass (self-attention and broadcast-Q) */
   JFA_KERNEL_BWD_Q = 4,     /* self-attention backward, dQ pass */
-  JFA_KERNEL_BWD_FUSED = 5, /* broadcast-Q backward (dK, dV, dQ partials) */
-  JFA_KERNEL_FINALIZE = 6,  /* broadcast-Q dQ shard sum and bf16 cast */
+  JFA_KERNEL_BWD_Q_BCAST = 5, /* broadcast-Q backward, dQ pass (per-chunk partials) */
+  JFA_KERNEL_FINALIZE = 6,  /* broadcast-Q dQ: sum of the partials, bf16 cast */
   JFA_KERNEL_FILL = 7,      /* outputs of an all-empty broadcast batch */
   JFA_KERNEL_KINDS = 8
 } jfa_kernel_kind;

@@ -14,7 +14,8 @@ import os
 from .build import LIB_PATH
 
 __all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq",
-           "jfa_sync_and_check", "forward", "backward", "STATUS"]
+           "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
+           "STATUS"]
 
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_CUDA",
           4: "JFA_ERR_TIMEOUT", 5: "JFA_ERR_WORKSPACE"}
@@ -123,11 +124,25 @@ def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, c
               int(broadcast_q), int(causal), float(scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def jfa_worklist(offsets, B, H, max_len, q_len, broadcast_q, causal, which, items, capacity,
+                 count, stream=None):
+    """Builds work list `which` (0 forward, 1 dK/dV pass, 2 self-attention dQ
+    pass, 3 broadcast dQ-pass chunks) into the device int32 buffer `items`
+    (4 ints per entry, `capacity` entries) and `count` (device int32[2])."""
+    L = lib()
+    fn = L.jfa_worklist
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(offsets), B, H, max_len, q_len, int(broadcast_q), int(causal), which,
+              _ptr(items), capacity, _ptr(count), _stream(stream)))
+
+
 def jfa_sync_and_check(stream=None):
     _check(lib().jfa_sync_and_check(_stream(stream)))
 
 
-KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_fused", "finalize", "fill")
+KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill")
 
 
 def launch_count() -> int:

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/jfa.h: argument validation,
 // stream-ordered scratch memory, TMA tensor-map encoding and the launch
 // sequence of the forward and backward passes.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -202,10 +203,13 @@ jfa_status cuda_fail(cudaError_t e, const char* what) {
   return fail(JFA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-jfa_status finish(DeviceState* ds, cudaStream_t stream) {
+jfa_status sync_and_read_error_word(cudaStream_t stream);
+
+// With JFA_VALIDATE=1 every entry point synchronises its stream and reports
+// device-side errors before returning.
+jfa_status finish(cudaStream_t stream) {
   if (!validate_mode()) return JFA_OK;
-  (void)ds;
-  return jfa_sync_and_check(stream);
+  return sync_and_read_error_word(stream);
 }
 
 jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
@@ -226,7 +230,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
       });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
-    return finish(ds, stream);
+    return finish(stream);
   }
   const long long qt = s.broadcast ? cdivll(s.Lq, kFwdRows) : cdivll(s.max_len, kFwdRows);
   const long long cap = (long long)s.H * s.B * qt;
@@ -268,7 +272,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
-  return finish(ds, stream);
+  return finish(stream);
 }
 
 // Self-attention backward: dK/dV pass (K/V-block outer) and dQ pass
@@ -351,7 +355,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     bp.items = items_kv;
     bp.hdr = hdr_kv;
     e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
-      return launch_bwd_kv(s.D, s.causal, tq, tk, tv, tdo, tdk, tdv, bp,
+      return launch_bwd_kv(s.D, s.causal, false, tq, tk, tv, tdo, tdk, tdv, bp,
                            (int)std::min<long long>(ds->sms, cap_kv), stream);
     });
   }
@@ -366,7 +370,127 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
-  return finish(ds, stream);
+  return finish(stream);
+}
+
+// Broadcast-Q backward, two passes like self-attention: a dK/dV pass whose
+// query tiles are the dense Q's (items: sequence, head, key block), and a dQ
+// pass over equal chunks of the key-tile stream of all sequences (items:
+// chunk, head, query-tile pair) that keeps dQ in tensor memory and writes
+// one fp32 partial per item; a finalize kernel sums the partials in chunk
+// order.  Scratch: the two work lists, key-tile prefix per sequence, the row
+// statistics (padded to whole query tiles) and the partials.
+jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const void* k,
+                        const void* v, const int32_t* offsets, const void* out, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, cudaStream_t stream) {
+  jfa_status st;
+  const long long cap_kv = (long long)s.H * s.B * cdivll(s.max_len, kBN);
+  const long long pairs = cdivll(s.Lq, kQbRows);
+  // chunks per (head, pair): about two items per SM in all
+  const long long chunk_cap = std::max<long long>(1, cdivll(2LL * ds->sms, s.H * pairs));
+  const long long cap_qb = chunk_cap * s.H * pairs;
+  const long long lq_pad = cdivll(s.Lq, kBM) * kBM;
+  if (cap_kv >= (1LL << 31) || (long long)s.B * s.H * lq_pad >= (1LL << 40))
+    return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  size_t off = 0;
+  const size_t hkv_off = off;
+  off = align256(off + 256 + cap_kv * sizeof(Item));
+  const size_t hqb_off = off;
+  off = align256(off + 256 + cap_qb * sizeof(QbItem));
+  const size_t ktoff_off = off;
+  off = align256(off + (s.B + 1) * sizeof(int));
+  const size_t stat_off = off;
+  off = align256(off + 2 * (size_t)s.B * s.H * lq_pad * sizeof(float));
+  const size_t part_off = off;
+  off = align256(off + (size_t)cap_qb * 2 * kBM * s.D * sizeof(float));
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_bq(&tdo, dout, s.D, s.H, s.Lq, s.B, "dout")) != JFA_OK) return st;
+  if ((st = map_rows(&tdk, dk, s.D, s.H, s.Tcap, "dk")) != JFA_OK) return st;
+  if ((st = map_rows(&tdv, dv, s.D, s.H, s.Tcap, "dv")) != JFA_OK) return st;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr_kv = reinterpret_cast<WorkHeader*>(base + hkv_off);
+  Item* items_kv = reinterpret_cast<Item*>(base + hkv_off + 256);
+  WorkHeader* hdr_qb = reinterpret_cast<WorkHeader*>(base + hqb_off);
+  QbItem* items_qb = reinterpret_cast<QbItem*>(base + hqb_off + 256);
+  int* kt_off = reinterpret_cast<int*>(base + ktoff_off);
+  float* stat = reinterpret_cast<float*>(base + stat_off);
+  float* part = reinterpret_cast<float*>(base + part_off);
+  {
+    PrepParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.out = static_cast<const __nv_bfloat16*>(out);
+    pp.dout = static_cast<const __nv_bfloat16*>(dout);
+    pp.offsets = offsets;
+    pp.lse = lse;
+    pp.stat = stat;
+    pp.B = s.B;
+    pp.H = s.H;
+    pp.D = s.D;
+    pp.Lq = s.Lq;
+    pp.broadcast = 1;
+    pp.n_sched = 2;
+    pp.sched[0] = SchedParams{offsets, s.B, s.H, s.Lq, s.max_len, 0, 1, 1, kBM,
+                              items_kv, (int)cap_kv, hdr_kv, ds->err};
+    pp.qb = QbSchedParams{offsets, s.B, s.H, s.Lq, s.max_len, (int)chunk_cap, kt_off,
+                          items_qb, (int)cap_qb, hdr_qb, ds->err};
+    e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
+      return launch_bwd_prep(pp, ds->sms, stream);
+    });
+  }
+  BwdParams bp;
+  memset(&bp, 0, sizeof(bp));
+  bp.offsets = offsets;
+  bp.B = s.B;
+  bp.H = s.H;
+  bp.Lq = s.Lq;
+  bp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+  bp.scale = s.scale;
+  bp.lse = lse;
+  bp.stat = stat;
+  bp.dq_part = part;
+  bp.dk = static_cast<__nv_bfloat16*>(dk);
+  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.err = ds->err;
+  if (e == cudaSuccess) {
+    bp.items = items_kv;
+    bp.hdr = hdr_kv;
+    e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
+      return launch_bwd_kv(s.D, false, true, tq, tk, tv, tdo, tdk, tdv, bp,
+                           (int)std::min<long long>(ds->sms, cap_kv), stream);
+    });
+  }
+  if (e == cudaSuccess) {
+    bp.items = nullptr;
+    bp.qb_items = items_qb;
+    bp.hdr = hdr_qb;
+    e = run_kernel(JFA_KERNEL_BWD_Q_BCAST, stream, [&] {
+      return launch_bwd_qb(s.D, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_qb),
+                           stream);
+    });
+  }
+  if (e == cudaSuccess) {
+    FinParams fp;
+    fp.part = part;
+    fp.dq = static_cast<__nv_bfloat16*>(dq);
+    fp.scale = s.scale;
+    fp.H = s.H;
+    fp.D = s.D;
+    fp.Lq = s.Lq;
+    fp.hdr = hdr_qb;
+    e = run_kernel(JFA_KERNEL_FINALIZE, stream, [&] {
+      return launch_finalize(fp, ds->sms, stream);
+    });
+  }
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(stream);
 }
 
 jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
@@ -391,109 +515,11 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
       });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
-    return finish(ds, stream);
+    return finish(stream);
   }
   if (!s.broadcast)
     return do_bwd_self(ds, s, q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
-  const long long cap = (long long)s.H * s.B * cdivll(s.max_len, kBN);
-  if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");
-  const int grid = (int)std::min<long long>(ds->sms, cap);
-  const int shards = s.broadcast ? std::min(16, grid) : 1;
-  const long long shard_elems = (long long)s.Lq * s.H * s.D;
-  const long long delta_elems = s.broadcast ? (long long)s.B * s.H * s.Lq : (long long)s.H * s.Tcap;
-  const long long acc_elems =
-      s.broadcast ? shards * shard_elems : s.Tcap * (long long)s.H * s.D;
-  size_t off = 256;
-  const size_t items_off = off;
-  off = align256(off + cap * sizeof(Item));
-  const size_t delta_off = off;
-  off = align256(off + delta_elems * sizeof(float));
-  const size_t acc_off = off;
-  off = align256(off + acc_elems * sizeof(float));
-  CUtensorMap tq, tk, tv, tdo;
-  if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
-  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
-  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
-  if (s.broadcast)
-    st = map_bq(&tdo, dout, s.D, s.H, s.Lq, s.B, "dout");
-  else
-    st = map_rows(&tdo, dout, s.D, s.H, s.Tcap, "dout");
-  if (st != JFA_OK) return st;
-  void* scratch = nullptr;
-  e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
-  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
-  uint8_t* base = static_cast<uint8_t*>(scratch);
-  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
-  Item* items = reinterpret_cast<Item*>(base + items_off);
-  float* delta = reinterpret_cast<float*>(base + delta_off);
-  float* acc = reinterpret_cast<float*>(base + acc_off);
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 1, kBM,
-                 items, (int)cap, hdr, ds->err};
-  {
-    // One launch: the work list, Delta and the zeroed dQ accumulator.
-    PrepParams pp;
-    memset(&pp, 0, sizeof(pp));
-    pp.out = static_cast<const __nv_bfloat16*>(out);
-    pp.dout = static_cast<const __nv_bfloat16*>(dout);
-    pp.offsets = offsets;
-    pp.delta = delta;
-    pp.dq_acc = acc;
-    pp.dq_acc_elems_bcast = acc_elems;
-    pp.B = s.B;
-    pp.H = s.H;
-    pp.D = s.D;
-    pp.Lq = s.Lq;
-    pp.broadcast = 1;
-    pp.n_sched = 1;
-    pp.sched[0] = sp;
-    e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
-      return launch_bwd_prep(pp, ds->sms, stream);
-    });
-  }
-  if (e == cudaSuccess) {
-    BwdParams bp;
-    memset(&bp, 0, sizeof(bp));
-    bp.offsets = offsets;
-    bp.B = s.B;
-    bp.H = s.H;
-    bp.Lq = s.Lq;
-    bp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
-    bp.scale = s.scale;
-    bp.lse = lse;
-    bp.delta = delta;
-    bp.dq_acc = acc;
-    bp.dq_shards = shards;
-    bp.shard_stride = shard_elems;
-    bp.dq = static_cast<__nv_bfloat16*>(dq);
-    bp.dk = static_cast<__nv_bfloat16*>(dk);
-    bp.dv = static_cast<__nv_bfloat16*>(dv);
-    bp.items = items;
-    bp.hdr = hdr;
-    bp.err = ds->err;
-    e = run_kernel(JFA_KERNEL_BWD_FUSED, stream, [&] {
-      return launch_bwd(s.D, s.causal, s.broadcast, tq, tk, tv, tdo, bp, grid, stream);
-    });
-  }
-  if (e == cudaSuccess) {
-    FinParams fp;
-    fp.dq_acc = acc;
-    fp.dq = static_cast<__nv_bfloat16*>(dq);
-    fp.scale = s.scale;
-    fp.H = s.H;
-    fp.D = s.D;
-    fp.Lq = s.Lq;
-    fp.broadcast = s.broadcast;
-    fp.shards = shards;
-    fp.shard_stride = shard_elems;
-    fp.hdr = hdr;
-    e = run_kernel(JFA_KERNEL_FINALIZE, stream, [&] {
-      return launch_finalize(fp, ds->sms, stream);
-    });
-  }
-  cudaError_t e2 = cudaFreeAsync(scratch, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
-  return finish(ds, stream);
+  return do_bwd_bcast(ds, s, q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
 }
 
 Shape make_shape(int B, int H, int D, int max_len, int q_len, int broadcast_q, int causal,
@@ -555,6 +581,70 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
                 out, lse, dout, dq, dk, dv, stream);
 }
 
+jfa_status jfa_worklist(const int32_t* offsets, int B, int H, int max_len, int q_len,
+                        int broadcast_q, int causal, int list, int32_t* items, int capacity,
+                        int32_t* count, cudaStream_t stream) {
+  t_last_error.clear();
+  if (B < 1 || H < 1 || H > 65535 || max_len < 0 || capacity < 0)
+    return fail(JFA_ERR_INVALID_ARG, "worklist: B, H >= 1, max_len, capacity >= 0");
+  if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 3u) || !count ||
+      (reinterpret_cast<uintptr_t>(count) & 3u) || (capacity > 0 && !aligned16(items)))
+    return fail(JFA_ERR_INVALID_ARG, "worklist: offsets, count 4-byte and items 16-byte aligned");
+  if (list < 0 || list > 3) return fail(JFA_ERR_INVALID_ARG, "worklist: list must be 0..3");
+  if (broadcast_q && (causal || q_len < 1))
+    return fail(JFA_ERR_INVALID_ARG, "worklist: broadcast needs q_len >= 1 and no causal mask");
+  if ((list == 2 && broadcast_q) || (list == 3 && !broadcast_q))
+    return fail(JFA_ERR_INVALID_ARG, "worklist: list 2 is self-attention only, 3 broadcast only");
+  if ((long long)B * max_len >= (1LL << 31) || cdivll(max_len, kBN) > 65535)
+    return fail(JFA_ERR_INVALID_ARG, "worklist: sequence lengths too large");
+  DeviceState* ds = nullptr;
+  jfa_status st = device_state(&ds);
+  if (st != JFA_OK) return st;
+  const int Lq = broadcast_q ? q_len : 0;
+  long long cap = 0, chunk_cap = 0;
+  const long long pairs = cdivll(Lq, kQbRows);
+  if (list == 0)
+    cap = (long long)H * B * (broadcast_q ? cdivll(Lq, kFwdRows) : cdivll(max_len, kFwdRows));
+  else if (list == 1)
+    cap = (long long)H * B * cdivll(max_len, kBN);
+  else if (list == 2)
+    cap = (long long)H * B * cdivll(max_len, kFwdRows);
+  else {
+    chunk_cap = std::max<long long>(1, cdivll(2LL * ds->sms, H * pairs));
+    cap = chunk_cap * H * pairs;
+  }
+  if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "worklist: list too large");
+  if (cap > capacity)
+    return fail(JFA_ERR_INVALID_ARG, "worklist: items must hold %lld entries (4 ints each)", cap);
+  const size_t item_bytes = list == 3 ? sizeof(QbItem) : sizeof(Item);
+  const size_t ktoff = align256(256 + cap * item_bytes);
+  const size_t bytes = align256(ktoff + (B + 1) * sizeof(int));
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
+  void* list_items = base + 256;
+  const int c = causal ? 1 : 0, bq = broadcast_q ? 1 : 0;
+  if (list == 3) {
+    QbSchedParams qp{offsets, B, H, Lq, max_len, (int)chunk_cap, reinterpret_cast<int*>(base + ktoff),
+                     static_cast<QbItem*>(list_items), (int)cap, hdr, ds->err};
+    e = run_kernel(JFA_KERNEL_PREP, stream, [&] { return launch_qb_sched(qp, stream); });
+  } else {
+    const int backward = list == 1 ? 1 : 0;
+    SchedParams sp{offsets, B, H, Lq, max_len, c, bq, backward, backward ? kBM : kFwdRows,
+                   static_cast<Item*>(list_items), (int)cap, hdr, ds->err};
+    e = run_kernel(list == 0 ? JFA_KERNEL_SCHED : JFA_KERNEL_PREP, stream,
+                   [&] { return launch_sched(sp, stream); });
+  }
+  if (e == cudaSuccess)
+    e = launch_export_list(hdr, list_items, list == 3 ? 1 : 0, items, capacity, count, stream);
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "worklist launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(stream);
+}
+
 long long jfa_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 jfa_status jfa_profile_enable(int on) {
@@ -592,9 +682,22 @@ jfa_status jfa_profile_read(double* ms, long long* launches, int n) {
 }
 
 jfa_status jfa_sync_and_check(cudaStream_t stream) {
-  DeviceState* ds = nullptr;
-  jfa_status st = device_state(&ds);
-  if (st != JFA_OK) return st;
+  // Touches neither the scratch pool nor any other per-device state, so that
+  // callers of the allocation-free entry point can use it too.
+  return sync_and_read_error_word(stream);
+}
+
+const char* jfa_last_error(void) { return t_last_error.c_str(); }
+
+const char* jfa_version(void) { return "jfa-gb300 0.2 (sm_103a)"; }
+
+}  // extern "C"
+
+namespace {
+
+// Synchronise `stream`, then read and clear the current device's error
+// word.  Allocates nothing (a synchronous copy into a host int).
+jfa_status sync_and_read_error_word(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
   int word = 0;
@@ -615,11 +718,7 @@ jfa_status jfa_sync_and_check(cudaStream_t stream) {
   return JFA_OK;
 }
 
-const char* jfa_last_error(void) { return t_last_error.c_str(); }
-
-const char* jfa_version(void) { return "jfa-gb300 0.1 (sm_103a)"; }
-
-}  // extern "C"
+}  // namespace
 
 // ---------------------------------------------------------------------------
 // Allocation-free forward entry point.
@@ -733,7 +832,7 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
       });
       if (e != cudaSuccess) return cuda_fail(e, "fill launch");
     }
-    return JFA_OK;
+    return finish(stream);
   }
   CUtensorMap tq, tk, tv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
@@ -765,7 +864,7 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
     return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
   });
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-  return JFA_OK;
+  return finish(stream);
 }
 
 

@@ -1,7 +1,8 @@
-// Device work-list scheduler, backward pre-pass (work lists, the row
-// statistics LSE*log2e and Delta = rowsum(dO * O), zeroing of the broadcast
-// fp32 dQ accumulator), dQ finalisation, and a fill kernel for the
-// all-empty broadcast case.
+// Device work-list schedulers, backward pre-pass (work lists and the row
+// statistics LSE*log2e and Delta = rowsum(dO * O)), the broadcast dQ
+// finalisation, and a fill kernel for the all-empty broadcast case.
+#include <algorithm>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -62,25 +63,56 @@ __device__ void scan_desc(const int* hist, int* base, int* warp_tot) {
 }
 
 // Builds one work list with the whole block (kSchedThreads threads).
+// Thread tid handles sequences tid, tid + blockDim, ...; the lengths of the
+// first kPer of them stay in registers between the two passes, loaded
+// together so that their latencies overlap.
+constexpr int kPer = 8;
 __device__ void sched_body(const SchedParams& p) {
   __shared__ int hist[kMaxBuckets];
   __shared__ int base[kMaxBuckets];
   __shared__ int cursor[kMaxBuckets];
   __shared__ int warp_tot[32];
-  __shared__ int s_pos[kSchedThreads], s_nt[kSchedThreads];
-  __shared__ int s_bad;
-  const int tid = threadIdx.x;
+  __shared__ int s_bad, s_nbig;
+  __shared__ int4 s_big[kSchedThreads];  // sequences with many items: {b, pos, tiles, items}
+  const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < kMaxBuckets; i += blockDim.x) hist[i] = 0, cursor[i] = 0;
   if (tid == 0) s_bad = (p.offsets[0] != 0);
+  int Lr[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int b = i * blockDim.x + tid;
+    Lr[i] = b < p.B ? p.offsets[b + 1] - p.offsets[b] : 0;
+  }
+  auto length = [&](int i, int b) {  // sequence b = i * blockDim + tid
+    int L = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (k == i) L = Lr[k];
+    return i < kPer ? L : p.offsets[b + 1] - p.offsets[b];
+  };
   __syncthreads();
-  for (int b = tid; b < p.B; b += blockDim.x) {
-    const int L = p.offsets[b + 1] - p.offsets[b];
-    if (L < 0 || L > p.max_len) {
-      s_bad = 1;
-      continue;
+  // Lanes of a warp whose sequences share a cost bucket add to it with one
+  // shared atomic (thousands of short sequences fall into a few buckets, and
+  // same-address atomics serialise).
+  for (int i = 0; i * static_cast<int>(blockDim.x) < p.B; ++i) {
+    const int b = i * blockDim.x + tid;
+    int n = 0, key = -1;
+    if (b < p.B) {
+      const int L = length(i, b);
+      if (L < 0 || L > p.max_len) {
+        s_bad = 1;
+      } else {
+        n = p.H * n_tiles(p, L);
+        if (n > 0) key = bucket_of(p, L);
+      }
     }
-    const int nt = n_tiles(p, L);
-    if (nt > 0) atomicAdd(&hist[bucket_of(p, L)], p.H * nt);
+    const unsigned active = __ballot_sync(0xffffffffu, key >= 0);
+    if (key >= 0) {
+      const unsigned peers = __match_any_sync(active, key);
+      int tot = 0;
+      for (unsigned m = peers; m; m &= m - 1) tot += __shfl_sync(peers, n, __ffs(m) - 1);
+      if (lane == __ffs(peers) - 1) atomicAdd(&hist[key], tot);
+    }
   }
   __syncthreads();
   if (s_bad) {
@@ -106,19 +138,21 @@ __device__ void sched_body(const SchedParams& p) {
     }
     return;
   }
-  // Chunks of blockDim sequences.  Each thread reserves the slots of one
-  // sequence; threads of a warp whose sequences fall in the same cost bucket
-  // do it with one shared atomic (many short sequences share a few buckets).
-  // Then each warp writes the items of its share of the chunk's sequences,
-  // lanes over items.  Heads outer, tiles inner, so that consecutive items
-  // share K/V (or Q) in L2; forward causal: longest query tile first.
-  const int lane = tid & 31, nwarps = blockDim.x >> 5;
+  // Each thread reserves the slots of its sequence; threads of a warp whose
+  // sequences fall in the same cost bucket do it with one shared atomic.  A
+  // thread writes the items of its own sequence if they are few; sequences
+  // with many items go to a shared list that all warps then write, lanes
+  // over items.  Heads outer, tiles inner, so that consecutive items share
+  // K/V (or Q) in L2; forward causal: longest query tile first.
   const bool reverse = !p.backward && p.causal;
-  for (int c0 = 0; c0 < p.B; c0 += blockDim.x) {
-    const int b = c0 + tid;
+  constexpr int kOwnItems = 32;  // at most this many: written by the thread itself
+  for (int i = 0; i * static_cast<int>(blockDim.x) < p.B; ++i) {
+    if (tid == 0) s_nbig = 0;
+    __syncthreads();
+    const int b = i * blockDim.x + tid;
     int nt = 0, n = 0, key = 0;
     if (b < p.B) {
-      const int L = p.offsets[b + 1] - p.offsets[b];
+      const int L = length(i, b);
       nt = n_tiles(p, L);
       n = p.H * nt;
       key = bucket_of(p, L);
@@ -140,17 +174,20 @@ __device__ void sched_body(const SchedParams& p) {
       first = __shfl_sync(peers, first, leader);
       pos = base[key] + first + pre;
     }
-    s_pos[tid] = pos;
-    s_nt[tid] = nt;
+    if (n > 0 && n <= kOwnItems) {
+      int j = pos;
+      for (int h = 0; h < p.H; ++h)
+        for (int t = 0; t < nt; ++t, ++j)
+          p.items[j] = make_int2(b, (h << 16) | (reverse ? nt - 1 - t : t));
+    } else if (n > kOwnItems) {
+      s_big[atomicAdd(&s_nbig, 1)] = make_int4(b, pos, nt, n);
+    }
     __syncthreads();
-    for (int w = tid >> 5; w < kSchedThreads && c0 + w < p.B; w += nwarps) {
-      const int ntl = s_nt[w];
-      if (ntl == 0) continue;
-      const int nl = p.H * ntl, pl = s_pos[w];
-      for (int j = lane; j < nl; j += 32) {
-        const int h = j / ntl, t = j - h * ntl;
-        const int tt = reverse ? ntl - 1 - t : t;
-        p.items[pl + j] = make_int2(c0 + w, (h << 16) | tt);
+    for (int k = tid >> 5; k < s_nbig; k += blockDim.x >> 5) {
+      const int4 g = s_big[k];
+      for (int j = lane; j < g.w; j += 32) {
+        const int h = j / g.z, t = j - h * g.z;
+        p.items[g.y + j] = make_int2(g.x, (h << 16) | (reverse ? g.z - 1 - t : t));
       }
     }
     __syncthreads();
@@ -165,19 +202,150 @@ __device__ void sched_body(const SchedParams& p) {
 
 __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) { sched_body(p); }
 
+// A built work list copied out as 4 ints per item, with its item count
+// (and, for the broadcast dQ-pass list, its chunk count): list inspection
+// for tests.  Forward and backward lists: {b, h, tile, 0}; broadcast dQ
+// pass: {h | pair << 16, b, j, n}.  count[0] = -1 if the list is invalid.
+__global__ void export_list_kernel(const WorkHeader* hdr, const void* items, int qb, int32_t* out,
+                                   int capacity, int32_t* count) {
+  const int n = hdr->valid ? hdr->n_items : 0;
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gtid == 0) {
+    count[0] = hdr->valid ? n : -1;
+    count[1] = qb ? hdr->n_chunks : 0;
+  }
+  for (int i = gtid; i < n && i < capacity; i += gridDim.x * blockDim.x) {
+    int4 v;
+    if (qb) {
+      const QbItem it = static_cast<const QbItem*>(items)[i];
+      v = make_int4(it.hp, it.b, it.j, it.n);
+    } else {
+      const Item it = static_cast<const Item*>(items)[i];
+      v = make_int4(it.x, it.y >> 16, it.y & 0xffff, 0);
+    }
+    reinterpret_cast<int4*>(out)[i] = v;
+  }
+}
+
+// Inclusive prefix sum over the block (blockDim a multiple of 32, at most
+// 1024); warp_tot: 32 ints of shared memory.
+__device__ int block_incl_scan(int v, int* warp_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int r = x + (w > 0 ? warp_tot[w - 1] : 0);
+  __syncthreads();
+  return r;
+}
+
+// Work list of the broadcast-Q dQ pass with the whole block: the key tiles
+// of all sequences, in order, form one stream per (head, query-tile pair);
+// it is cut into nc equal chunks, and item (c, h, pair) at list index
+// (c * H + h) * pairs + pair starts at the sequence and tile where chunk c
+// starts.  kt_off[b] = key tiles of the sequences before b.
+__device__ void qb_sched_body(const QbSchedParams& p) {
+  __shared__ int warp_tot[32];
+  __shared__ int s_bad, s_carry;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_bad = (p.offsets[0] != 0);
+    s_carry = 0;
+  }
+  __syncthreads();
+  for (int b0 = 0; b0 < p.B; b0 += blockDim.x) {
+    const int b = b0 + tid;
+    int nt = 0;
+    if (b < p.B) {
+      const int L = p.offsets[b + 1] - p.offsets[b];
+      if (L < 0 || L > p.max_len)
+        s_bad = 1;
+      else
+        nt = cdiv(L, kBN);
+    }
+    const int incl = block_incl_scan(nt, warp_tot);
+    if (b < p.B) p.kt_off[b] = s_carry + incl - nt;
+    __syncthreads();
+    if (tid == blockDim.x - 1) s_carry += incl;
+    __syncthreads();
+  }
+  const int total = s_carry;
+  if (tid == 0) p.kt_off[p.B] = total;
+  __syncthreads();  // kt_off visible to the whole block
+  const int pairs = cdiv(p.Lq, kQbRows);
+  const int nc = s_bad ? 0 : min(p.chunk_cap, (total + 3) / 4);
+  const long long n_items = static_cast<long long>(nc) * p.H * pairs;
+  if (s_bad || n_items > p.capacity) {
+    if (tid == 0) {
+      p.hdr->n_items = 0;
+      p.hdr->n_chunks = 0;
+      p.hdr->T = 0;
+      p.hdr->ticket = 0;
+      p.hdr->valid = 0;
+      atomicOr(p.err, s_bad ? kErrBadOffsets : kErrCapacity);
+    }
+    return;
+  }
+  for (int idx = tid; idx < n_items; idx += blockDim.x) {
+    const int c = idx / (p.H * pairs);
+    const int rem = idx - c * (p.H * pairs);
+    const int h = rem / pairs, pair = rem - h * pairs;
+    const int s0 = static_cast<int>(static_cast<long long>(c) * total / nc);
+    const int s1 = static_cast<int>(static_cast<long long>(c + 1) * total / nc);
+    // the last sequence b with kt_off[b] <= s0 (it is non-empty)
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.kt_off[mid] <= s0)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    QbItem it;
+    it.hp = h | (pair << 16);
+    it.b = lo;
+    it.j = s0 - p.kt_off[lo];
+    it.n = s1 - s0;
+    p.items[idx] = it;
+  }
+  if (tid == 0) {
+    p.hdr->n_items = static_cast<int>(n_items);
+    p.hdr->n_chunks = nc;
+    p.hdr->T = p.offsets[p.B];
+    p.hdr->ticket = 0;
+    p.hdr->valid = 1;
+  }
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Row statistics of the backward pass with blocks [0, nblk) of the caller's
 // grid: Delta[row] = sum_d dO[row, d] * O[row, d] in fp32 (the rowsum the
-// gradient of the softmax subtracts), and for self-attention LSE*log2e next
-// to it.  tpr = D/8 threads per row, each reading 16 bytes of both tensors;
-// kUnroll rows per thread in flight.
-constexpr int kUnroll = 2;      // broadcast-Q rows in flight per thread
-constexpr int kUnrollSelf = 1;  // self-attention steps in flight per warp (32-byte loads)
-
+// gradient of the softmax subtracts) and LSE*log2e, stored as {-LSE*log2e,
+// -Delta}.  Self-attention rows (t, h) go to every copy at position h*T + t;
+// broadcast rows (b, i, h) to position (b*H + h)*lq_pad + i.  A warp takes 32
+// consecutive rows r0.. of O and dO in memory order (one contiguous block;
+// D/16 threads per row, 32 bytes of O and dO each, 32/(D/16) rows per step);
+// the row sums are gathered so that lane l ends with row r0 + l.
 __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
   long long rows;
   int T = 0;
+  const long long lq_pad = static_cast<long long>(cdiv(p.Lq, kBM)) * kBM;
   if (p.broadcast) {
     rows = static_cast<long long>(p.B) * p.Lq * p.H;
   } else {
@@ -200,138 +368,94 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
       }
     }
   }
-  const int tpr = p.D / 8;
-  const int rpw = 32 / tpr;  // rows per warp and unroll step
   const int lane = threadIdx.x & 31;
-  const int part = lane % tpr;
   const long long wid = (blk * blockDim.x + threadIdx.x) >> 5;
-  if (!p.broadcast) {
-    // Self-attention: a warp takes 32 consecutive rows r0.. of O and dO in
-    // memory order (row = t*H + h), one contiguous block (D/16 threads per
-    // row, 32 bytes of O and dO each, 32/(D/16) rows per step); the row sums
-    // are gathered so that lane l ends with row r0 + l, and the statistics
-    // of lanes with the same head land on consecutive tokens.
-    const int tpr32 = p.D / 16, rpw32 = 32 / tpr32, part32 = lane % tpr32;
-    const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | reinterpret_cast<uintptr_t>(p.dout)) & 31) == 0;
-    const long long nwarps = (nblk * blockDim.x) >> 5;
-    for (long long r0 = wid * 32; r0 < rows; r0 += nwarps * 32) {
-      float mine = 0.f;
-      for (int s0 = 0; s0 < 32; s0 += rpw32 * kUnrollSelf) {
-        uint32_t o[kUnrollSelf][8], g[kUnrollSelf][8];
-#pragma unroll
-        for (int u = 0; u < kUnrollSelf; ++u) {
-          const long long row = r0 + s0 + u * rpw32 + lane / tpr32;
-          if (row < rows) {
-            const __nv_bfloat16* po = p.out + row * p.D + part32 * 16;
-            const __nv_bfloat16* pg = p.dout + row * p.D + part32 * 16;
-            if (v8) {
-              ld_global_v8(po, o[u]);
-              ld_global_v8(pg, g[u]);
-            } else {  // the caller's buffers are only 16-byte aligned
-              const uint4 o0 = reinterpret_cast<const uint4*>(po)[0], o1 = reinterpret_cast<const uint4*>(po)[1];
-              const uint4 g0 = reinterpret_cast<const uint4*>(pg)[0], g1 = reinterpret_cast<const uint4*>(pg)[1];
-              o[u][0] = o0.x, o[u][1] = o0.y, o[u][2] = o0.z, o[u][3] = o0.w;
-              o[u][4] = o1.x, o[u][5] = o1.y, o[u][6] = o1.z, o[u][7] = o1.w;
-              g[u][0] = g0.x, g[u][1] = g0.y, g[u][2] = g0.z, g[u][3] = g0.w;
-              g[u][4] = g1.x, g[u][5] = g1.y, g[u][6] = g1.z, g[u][7] = g1.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[u][i] = g[u][i] = 0u;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnrollSelf; ++u) {
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o[u][i]));
-            const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g[u][i]));
-            acc = fmaf(a.x, c.x, acc);
-            acc = fmaf(a.y, c.y, acc);
-          }
-          for (int off = tpr32 / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          // row s0 + u*rpw32 + j sits in lanes [j*tpr32, (j+1)*tpr32); lane l keeps row l
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (j >= rpw32) break;
-            const float v = __shfl_sync(0xffffffffu, acc, j * tpr32);
-            if (lane == s0 + u * rpw32 + j) mine = v;
-          }
-        }
-      }
-      const long long row = r0 + lane;
-      if (row < rows) {
-        const long long t = row / p.H, h = row % p.H;
-        const long long si = h * T + t;
-        const float nl = -p.lse[si] * kLog2e;
-#pragma unroll
-        for (int k = 0; k < kStatCopies; ++k) {
-          float* f = p.stat + k * p.stat_stride + stat_float(stat_pos(si, k));
-          f[0] = nl;
-          f[4] = -mine;
-        }
-      }
-    }
-    return;
-  }
-  const long long nw = (nblk * blockDim.x) >> 5;
-  const long long step = static_cast<long long>(rpw) * kUnroll;
-  for (long long r0 = wid * step; r0 < rows; r0 += nw * step) {
-    uint4 o[kUnroll], g[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long row = r0 + u * rpw + lane / tpr;
-      if (row < rows) {
-        o[u] = *reinterpret_cast<const uint4*>(p.out + row * p.D + part * 8);
-        g[u] = *reinterpret_cast<const uint4*>(p.dout + row * p.D + part * 8);
+  const int tpr32 = p.D / 16, rpw32 = 32 / tpr32;
+  const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | reinterpret_cast<uintptr_t>(p.dout)) & 31) == 0;
+  const long long nwarps = (nblk * blockDim.x) >> 5;
+  for (long long r0 = wid * 32; r0 < rows; r0 += nwarps * 32) {
+    // This lane's row: its LSE is loaded first, independently of O and dO.
+    const long long row = r0 + lane;
+    long long pos = 0;  // statistics position (self: before the copy offset)
+    float nl = 0.f;
+    if (row < rows) {
+      const long long h = row % p.H, t = row / p.H;
+      if (p.broadcast) {
+        const long long b = t / p.Lq, i = t - b * p.Lq;
+        pos = (b * p.H + h) * lq_pad + i;
+        nl = -p.lse[(b * p.H + h) * p.Lq + i] * kLog2e;
       } else {
-        o[u] = make_uint4(0, 0, 0, 0);
-        g[u] = o[u];
+        pos = h * T + t;
+        nl = -p.lse[pos] * kLog2e;
       }
     }
+    float mine = 0.f;
+    for (int s0 = 0; s0 < 32; s0 += rpw32) {
+      uint32_t o[8], g[8];
+      const long long rr = r0 + s0 + lane / tpr32;
+      const int part32 = lane % tpr32;
+      if (rr < rows) {
+        const __nv_bfloat16* po = p.out + rr * p.D + part32 * 16;
+        const __nv_bfloat16* pg = p.dout + rr * p.D + part32 * 16;
+        if (v8) {
+          ld_global_v8(po, o);
+          ld_global_v8(pg, g);
+        } else {  // the caller's buffers are only 16-byte aligned
+          const uint4 o0 = reinterpret_cast<const uint4*>(po)[0], o1 = reinterpret_cast<const uint4*>(po)[1];
+          const uint4 g0 = reinterpret_cast<const uint4*>(pg)[0], g1 = reinterpret_cast<const uint4*>(pg)[1];
+          o[0] = o0.x, o[1] = o0.y, o[2] = o0.z, o[3] = o0.w;
+          o[4] = o1.x, o[5] = o1.y, o[6] = o1.z, o[7] = o1.w;
+          g[0] = g0.x, g[1] = g0.y, g[2] = g0.z, g[3] = g0.w;
+          g[4] = g1.x, g[5] = g1.y, g[6] = g1.z, g[7] = g1.w;
+        }
+      } else {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o[u]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+        for (int i = 0; i < 8; ++i) o[i] = g[i] = 0u;
+      }
       float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 a = __bfloat1622float2(o2[i]);
-        const float2 c = __bfloat1622float2(g2[i]);
+      for (int i = 0; i < 8; ++i) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o[i]));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g[i]));
         acc = fmaf(a.x, c.x, acc);
         acc = fmaf(a.y, c.y, acc);
       }
-      for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      const long long row = r0 + u * rpw + lane / tpr;
-      if (row < rows && part == 0) {
-        if (p.broadcast) {
-          const long long h = row % p.H;
-          const long long bi = row / p.H;  // b * Lq + i
-          const long long b = bi / p.Lq, i = bi % p.Lq;
-          p.delta[(b * p.H + h) * p.Lq + i] = acc;
-        } else {
-          const long long h = row % p.H, t = row / p.H;
-          const long long si = h * T + t;
-          const float nl = -p.lse[si] * kLog2e;
+      for (int off = tpr32 / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      // row s0 + j sits in lanes [j*tpr32, (j+1)*tpr32); lane l keeps row l
 #pragma unroll
-          for (int k = 0; k < kStatCopies; ++k) {
-            float* f = p.stat + k * p.stat_stride + stat_float(stat_pos(si, k));
-            f[0] = nl;
-            f[4] = -acc;
-          }
+      for (int j = 0; j < 8; ++j) {
+        if (j >= rpw32) break;
+        const float v = __shfl_sync(0xffffffffu, acc, j * tpr32);
+        if (lane == s0 + j) mine = v;
+      }
+    }
+    if (row < rows) {
+      if (p.broadcast) {
+        float* f = p.stat + stat_float(pos);
+        f[0] = nl;
+        f[4] = -mine;
+      } else {
+#pragma unroll
+        for (int k = 0; k < kStatCopies; ++k) {
+          float* f = p.stat + k * p.stat_stride + stat_float(stat_pos(pos, k));
+          f[0] = nl;
+          f[4] = -mine;
         }
       }
     }
   }
 }
 
-// Backward pre-pass: work lists (blocks [0, n_sched)), row statistics and,
-// for broadcast-Q, zeroing of the fp32 dQ accumulator (the other blocks).
+// Backward pre-pass: work lists (blocks [0, n_sched)), then the row
+// statistics (the other blocks).  Broadcast-Q: block 1 builds the dQ-pass
+// list, and the padding rows of the statistics (rows q_len.. of each
+// sequence's last query tile) get {-inf, 0}, so that P = 0 there.
 __global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   if (blockIdx.x < p.n_sched) {
     if (blockIdx.x == 0)
       sched_body(p.sched[0]);
+    else if (p.broadcast)
+      qb_sched_body(p.qb);
     else
       sched_body(p.sched[1]);
     return;
@@ -339,31 +463,66 @@ __global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_co
   const long long blk = blockIdx.x - p.n_sched, nblk = gridDim.x - p.n_sched;
   stats_body(p, blk, nblk);
   if (p.broadcast) {
-    const long long gtid = blk * blockDim.x + threadIdx.x;
-    float4* z = reinterpret_cast<float4*>(p.dq_acc);
-    for (long long i = gtid; i < p.dq_acc_elems_bcast / 4; i += nblk * blockDim.x)
-      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int lq_pad = cdiv(p.Lq, kBM) * kBM, npad = lq_pad - p.Lq;
+    const long long n = static_cast<long long>(p.B) * p.H * npad;
+    for (long long i = blk * blockDim.x + threadIdx.x; i < n; i += nblk * blockDim.x) {
+      const long long bh = i / npad, k = i - bh * npad;
+      float* f = p.stat + stat_float(bh * lq_pad + p.Lq + k);
+      f[0] = -INFINITY;
+      f[4] = 0.f;
+    }
   }
 }
 
-// dq = bf16(scale * sum over shards of the fp32 accumulator)
-__global__ void __launch_bounds__(256) finalize_kernel(FinParams p) {
-  const long long n = p.broadcast ? (long long)p.Lq * p.H * p.D
-                                  : (p.hdr->valid ? (long long)p.hdr->T * p.H * p.D : 0);
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  for (long long i = gtid; i < n / 4; i += nthreads) {
-    float4 a = reinterpret_cast<const float4*>(p.dq_acc)[i];
-    for (int s = 1; s < p.shards; ++s) {
-      const float4 c = reinterpret_cast<const float4*>(p.dq_acc + s * p.shard_stride)[i];
-      a.x += c.x, a.y += c.y, a.z += c.z, a.w += c.w;
+__global__ void __launch_bounds__(kSchedThreads) qb_sched_kernel(QbSchedParams p) { qb_sched_body(p); }
+
+// Broadcast dQ: dq[l, h, :] = bf16(scale * sum over the chunks c of the
+// partial of item (c, h, pair = l / 256)).  A block takes 32 four-column
+// groups (l, h, d4) and splits the chunks among kFinGroups thread groups;
+// group g sums chunks g, g + kFinGroups, ..., and the group sums are added in
+// group order, so the result does not depend on timing.
+constexpr int kFinGroups = 8;
+constexpr int kFinThreads = 32 * kFinGroups;
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinParams p) {
+  __shared__ float4 part_sum[kFinGroups][32];
+  if (!p.hdr->valid) return;
+  const int nc = p.hdr->n_chunks;
+  const int pairs = cdiv(p.Lq, kQbRows);
+  const int d4n = p.D / 4;
+  const long long n = static_cast<long long>(p.Lq) * p.H * d4n;
+  const int e = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * 32; i0 < n;
+       i0 += static_cast<long long>(gridDim.x) * 32) {
+    const long long i = i0 + e;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < n) {
+      const int d4 = static_cast<int>(i % d4n);
+      const long long lh = i / d4n;
+      const int h = static_cast<int>(lh % p.H), l = static_cast<int>(lh / p.H);
+      const int pair = l / kQbRows, g = (l % kQbRows) / kBM, r = l % kBM;
+      const long long stride = static_cast<long long>(kFinGroups) * p.H * pairs * 2 * kBM * p.D;
+      const float* src = p.part + ((((static_cast<long long>(grp) * p.H + h) * pairs + pair) * 2 + g) * kBM + r) * p.D + 4 * d4;
+#pragma unroll 4
+      for (int c = grp; c < nc; c += kFinGroups, src += stride) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        a.x += v.x, a.y += v.y, a.z += v.z, a.w += v.w;
+      }
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * p.scale, a.y * p.scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * p.scale, a.w * p.scale);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&lo);
-    v.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(p.dq)[i] = v;
+    part_sum[grp][e] = a;
+    __syncthreads();
+    if (grp == 0 && i < n) {
+      for (int q = 1; q < kFinGroups; ++q) {
+        const float4 v = part_sum[q][e];
+        a.x += v.x, a.y += v.y, a.z += v.z, a.w += v.w;
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * p.scale, a.y * p.scale);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * p.scale, a.w * p.scale);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t*>(&lo);
+      v.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(p.dq)[i] = v;
+    }
+    __syncthreads();
   }
 }
 
@@ -385,13 +544,26 @@ cudaError_t launch_sched(const SchedParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_qb_sched(const QbSchedParams& p, cudaStream_t s) {
+  qb_sched_kernel<<<1, kSchedThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_list(const WorkHeader* hdr, const void* items, int qb, int32_t* out,
+                               int capacity, int32_t* count, cudaStream_t s) {
+  export_list_kernel<<<64, 256, 0, s>>>(hdr, items, qb, out, capacity, count);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_prep(const PrepParams& p, int sms, cudaStream_t s) {
   bwd_prep_kernel<<<p.n_sched + sms * 2, kSchedThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s) {
-  finalize_kernel<<<sms * 8, 256, 0, s>>>(p);
+  const long long groups = (static_cast<long long>(p.Lq) * p.H * (p.D / 4) + 31) / 32;
+  const int grid = static_cast<int>(std::min<long long>(groups, 8LL * sms));
+  finalize_kernel<<<grid > 0 ? grid : 1, kFinThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,5 @@
-// Self-attention backward, pass 1 of 2: dK and dV for sm_103a.
+// Backward, pass 1 of 2: dK and dV for sm_103a (self-attention and
+// broadcast-Q).
 //
 // "Optimizing Jagged Flash Attention with TLX" (pytorch.org), "Scheduling
 // jagged tiles across SMs": the dK/dV pass loops over K/V blocks on the
@@ -28,6 +29,11 @@
 // next item's first boxes into L2; each Q stage carries its tile's row
 // statistics, and Q and dO of a stage have their own barriers), warp 17 MMA
 // issuer, warp 18 the store warp (TMA stores of full dK/dV blocks).
+// Broadcast-Q ("Optimizing Jagged Flash Attention with TLX", section 1):
+// the query tiles of every item are the tiles of the one dense Q, dO is the
+// sequence's own [q_len, D] block of the [B, q_len, H, D] tensor (a 4-D
+// tensor map zero-fills rows past q_len), and the row statistics come from
+// a per-sequence layout padded to whole tiles (padding rows give P = 0).
 // At an item boundary the math warps compute the next item's first P part,
 // then the item's dV epilogue, the next item's first dS part, and only then
 // the item's dK epilogue, so that the first products of the next item wait
@@ -119,7 +125,7 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ uint32_t pack_col(int k) { return 32 * (k >> 1) + 8 * (k & 1); }
 
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool BCAST>
 __device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
   KvItem f;
   const Item it = p.items[idx];
@@ -129,9 +135,43 @@ __device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
   f.off0 = p.offsets[f.b];
   f.L = p.offsets[f.b + 1] - f.off0;
   f.kt = row_box(f.off0 + f.kb * kBN, f.L - f.kb * kBN, T);
-  f.t0 = CAUSAL ? (f.kb * kBN) / kBM : 0;
-  f.nt = cdiv(f.L, kBM) - f.t0;
+  if (BCAST) {
+    f.t0 = 0;
+    f.nt = cdiv(p.Lq, kBM);
+  } else {
+    f.t0 = CAUSAL ? (f.kb * kBN) / kBM : 0;
+    f.nt = cdiv(f.L, kBM) - f.t0;
+  }
   return f;
+}
+
+// Query tile t of item f: self-attention, rows of the sequence (moved back so
+// the box never reads past row T); broadcast, rows of the dense Q.
+template <bool BCAST>
+__device__ __forceinline__ RowBox q_box(const BwdParams& p, const KvItem& f, int t, int T) {
+  if (BCAST) {
+    RowBox r;
+    r.row = t * kBM;
+    r.shift = 0;
+    r.n = min(kBM, p.Lq - t * kBM);
+    return r;
+  }
+  return row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+}
+
+// Statistics of the 128 rows of query tile t (1 KB, 32-byte aligned): self,
+// the copy in which the box's first row starts a group; broadcast, the
+// sequence's rows in the layout padded to whole tiles.
+template <bool BCAST>
+__device__ __forceinline__ const float* stat_src(const BwdParams& p, const KvItem& f,
+                                                 const RowBox& qb, int t, int T) {
+  if (BCAST) {
+    const long long lq_pad = static_cast<long long>(cdiv(p.Lq, kBM)) * kBM;
+    return p.stat + stat_float((static_cast<long long>(f.b) * p.H + f.h) * lq_pad + t * kBM);
+  }
+  const long long sidx = static_cast<long long>(f.h) * T + qb.row;
+  const int sk = static_cast<int>((sidx + kStatPad) & 3);
+  return p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
@@ -160,7 +200,7 @@ __device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool*
   return f->b >= 0;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BCAST>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tdo, const BwdParams& p, uint8_t* smem,
                               KvCtl* c) {
@@ -175,19 +215,21 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   auto fetch = [&](KvItem& f) {
     const int idx = atomicAdd(&p.hdr->ticket, 1);
     if (idx < n_items)
-      f = decode<CAUSAL>(p, idx, T);
+      f = decode<CAUSAL, BCAST>(p, idx, T);
     else
       f.b = -1;
   };
   auto prefetch = [&](const KvItem& f) {
-    const RowBox qb = row_box(f.off0 + f.t0 * kBM, f.L - f.t0 * kBM, T);
+    const RowBox qb = q_box<BCAST>(p, f, f.t0, T);
 #pragma unroll
     for (int s = 0; s < C::kSlabs; ++s) {
       if (f.kt.row >= 0) {
         tma_prefetch_l2_3d(tk, s * 64, f.h, f.kt.row);
         tma_prefetch_l2_3d(tv, s * 64, f.h, f.kt.row);
       }
-      if (qb.row >= 0) {
+      if (BCAST) {  // the dense Q stays in L2; the sequence's dO
+        tma_prefetch_l2_4d(tdo, s * 64, f.h, 0, f.b);
+      } else if (qb.row >= 0) {
         tma_prefetch_l2_3d(tq, s * 64, f.h, qb.row);
         tma_prefetch_l2_3d(tdo, s * 64, f.h, qb.row);
       }
@@ -224,22 +266,23 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         break;
       }
       const int t = f.t0 + i;
-      const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+      const RowBox qb = q_box<BCAST>(p, f, t, T);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
         mbar_arrive_expect_tx(&c->do_full[st][s], 16384);
-        tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
-                    f.h, qb.row);
+        if (BCAST)
+          tma_load_4d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
+                      f.h, qb.row, f.b);
+        else
+          tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
+                      f.h, qb.row);
       }
       if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
-      // Row statistics of the box: 32 whole groups of the copy in which
-      // its first row starts a group.
-      const long long sidx = static_cast<long long>(f.h) * T + qb.row;
-      const int sk = static_cast<int>((sidx + kStatPad) & 3);
-      const float* ssrc = p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
+      // Row statistics of the box: 32 whole groups (1 KB).
+      const float* ssrc = stat_src<BCAST>(p, f, qb, t, T);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
         mbar_arrive_expect_tx(&c->q_full[st][s], 16384 + (s == 0 ? C::kStatBytes : 0));
@@ -414,7 +457,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BCAST>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   const int r = threadIdx.x & 127;    // TMEM lane = key row of the block
@@ -434,7 +477,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
   auto p_part = [&](const KvItem& f, int i, uint32_t g, uint32_t (&pk)[16]) {
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
     const int t = f.t0 + i;
-    const RowBox qb = row_box(f.off0 + t * kBM, f.L - t * kBM, T);
+    const RowBox qb = q_box<BCAST>(p, f, t, T);
     const int q0 = t * kBM - qb.shift;  // local query index of column 0
     // (already complete once S^T is; waited on here for the statistics'
     // visibility)
@@ -696,7 +739,7 @@ __device__ void store_role(const CUtensorMap* tdk, const CUtensorMap* tdv, uint8
   bulk_wait0();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BCAST>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -761,11 +804,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
   if (warp < kMathWarps) {
-    math_role<D, CAUSAL>(p, smem, c, tbase);
+    math_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
   } else if (warp == kStoreWarp) {
     if (lane == 0) store_role<D>(&tdk, &tdv, smem, c, p.err);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);
+    if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
     mma_role<D, CAUSAL>(p, smem, c, tbase);
   }
@@ -778,14 +821,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BCAST>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                      const BwdParams& p, int grid, cudaStream_t s) {
   using C = KvCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(KvCtl) <= 512, "control block");
-  auto kern = bwd_kv_kernel<D, CAUSAL>;
+  static_assert(!(CAUSAL && BCAST), "causal masking is self-attention only");
+  auto kern = bwd_kv_kernel<D, CAUSAL, BCAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
@@ -794,15 +838,19 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
-                          const CUtensorMap& tdv, const BwdParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
+                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                          int grid, cudaStream_t s) {
+  if (bcast && causal) return cudaErrorInvalidValue;
   if (D == 128) {
-    if (causal) return launch_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-    return launch_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+    if (bcast) return launch_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+    if (causal) return launch_t<128, true, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+    return launch_t<128, false, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
   }
-  if (causal) return launch_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-  return launch_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  if (bcast) return launch_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  if (causal) return launch_t<64, true, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  return launch_t<64, false, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
 }
 
 }  // namespace jfa

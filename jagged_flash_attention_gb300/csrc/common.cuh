@@ -41,15 +41,28 @@ __host__ __device__ __forceinline__ long long stat_copy_floats(long long rows) {
 // Small header at the start of every scratch block, written by the
 // scheduler kernel and read by the kernels that follow it on the stream.
 struct WorkHeader {
-  int n_items;  // number of work items in the list
-  int T;        // offsets[B], total packed tokens
-  int ticket;   // dynamic work counter of the persistent kernels
-  int valid;    // 1 if offsets passed the device checks
-  int pad[4];
+  int n_items;   // number of work items in the list
+  int T;         // offsets[B], total packed tokens
+  int ticket;    // dynamic work counter of the persistent kernels
+  int valid;     // 1 if offsets passed the device checks
+  int n_chunks;  // broadcast dQ pass: key-tile chunks per (head, query-tile pair)
+  int pad[3];
 };
 
 // A work item: x = sequence b, y = (head << 16) | tile.
 using Item = int2;
+
+// Work item of the broadcast-Q dQ pass: head h and query-tile pair `pair`
+// (hp = h | pair << 16), and a run of n key tiles of the concatenated
+// key-tile stream of all sequences, starting at tile j of sequence b (b is
+// non-empty; later tiles continue through the next non-empty sequences).
+// The item's fp32 dQ partial goes to partial slot = its list index.
+struct QbItem {
+  int hp, b, j, n;
+};
+
+// Query rows per broadcast dQ-pass item (two 128-row tiles).
+constexpr int kQbRows = 256;
 
 struct SchedParams {
   const int32_t* offsets;
@@ -79,18 +92,32 @@ struct BwdParams {
   float scale_log2;
   float scale;
   const float* lse;    // caller's LSE (natural log)
-  const float* delta;  // broadcast: rowsum(dO * O), same layout as lse
-  // Self-attention row statistics: kStatCopies copies of stat_stride floats
-  // (layout at kStatPad above).
+  // Row statistics {-LSE*log2e, -Delta} in the blocked layout of stat_float:
+  // self-attention, kStatCopies copies of stat_stride floats (layout at
+  // kStatPad above); broadcast, one copy over [B, H, Lq rounded up to 128]
+  // with padding rows {-inf, 0}.
   const float* stat;
   long long stat_stride;
-  float* dq_acc;       // fp32 accumulator: self [Tcap,H,D]; broadcast [shards,Lq,H,D]
-  int dq_shards;       // broadcast only
-  long long shard_stride;  // elements per shard
+  float* dq_part;      // broadcast dQ pass: fp32 partial of each item
   __nv_bfloat16* dq;  // self-attention dQ pass: written directly
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const Item* items;
+  const QbItem* qb_items;  // broadcast dQ pass
+  WorkHeader* hdr;
+  int* err;
+};
+
+// Work list of the broadcast-Q dQ pass (built by one block of the pre-pass):
+// the key-tile stream of every (head, pair) cut into n equal chunks, n =
+// min(chunk_cap, ceil(tiles / 4)), where tiles = sum_b ceil(L_b / 128).
+struct QbSchedParams {
+  const int32_t* offsets;
+  int B, H, Lq, max_len;
+  int chunk_cap;  // chunks per (head, pair) at most
+  int* kt_off;    // scratch int[B + 1]: key tiles before sequence b
+  QbItem* items;
+  int capacity;   // chunk_cap * H * pairs
   WorkHeader* hdr;
   int* err;
 };
@@ -106,39 +133,45 @@ struct PrepParams {
   float* stat;
   long long stat_stride;
   long long Tcap;  // B * max_len: rows of q, k, v, out, dout the caller provides
-  // broadcast-Q: Delta [B, H, Lq] and the fp32 dQ accumulator to zero
-  float* delta;
-  float* dq_acc;
-  long long dq_acc_elems_bcast;
   int B, H, D, Lq, broadcast;
-  int n_sched;  // 1 or 2
+  // Work lists: n_sched = 2; block 0 builds sched[0]; block 1 builds
+  // sched[1] (self-attention) or the broadcast dQ-pass list qb.
+  int n_sched;
   SchedParams sched[2];
+  QbSchedParams qb;
 };
 
+// Broadcast dQ: dq[l, h, :] = bf16(scale * sum over the chunks of the
+// partials of (h, pair = l / 256)), chunks summed in a fixed order.
 struct FinParams {
-  const float* dq_acc;
+  const float* part;  // [n_items][2][128][D] fp32, list order of QbSchedParams
   __nv_bfloat16* dq;
   float scale;
-  int H, D, Lq, broadcast, shards;
-  long long shard_stride;
-  const WorkHeader* hdr;
+  int H, D, Lq;
+  const WorkHeader* hdr;  // header of the dQ-pass list (n_chunks, valid)
 };
 
 // Host-side launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
-cudaError_t launch_bwd(int D, bool causal, bool bcast, const CUtensorMap& tq,
-                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdParams& p, int grid, cudaStream_t s);
 // tdk / tdv: the dK / dV outputs as maps like the inputs' (TMA stores).
-cudaError_t launch_bwd_kv(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
-                          const CUtensorMap& tdv, const BwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
+                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                          int grid, cudaStream_t s);
+// Broadcast-Q dQ pass (tdo: the 4-D [B, Lq, H, D] map).
+cudaError_t launch_bwd_qb(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                          int grid, cudaStream_t s);
 cudaError_t launch_bwd_q(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                          int grid, cudaStream_t s);
 cudaError_t launch_bwd_prep(const PrepParams& p, int sms, cudaStream_t s);
+cudaError_t launch_qb_sched(const QbSchedParams& p, cudaStream_t s);
+// Copies a work list out (4 ints per item) with its counts (list inspection).
+cudaError_t launch_export_list(const WorkHeader* hdr, const void* items, int qb, int32_t* out,
+                               int capacity, int32_t* count, cudaStream_t s);
 cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s);
 cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
                               cudaStream_t s);

@@ -110,3 +110,20 @@ def test_launch_count_without_launches():
     prof = jfa.profile_read()
     assert set(prof) == set(jfa.KERNEL_KINDS)
     assert jfa.launch_count() == n0
+
+
+def test_worklist_argument_errors(L):
+    """jfa_worklist rejects bad arguments on the host, before touching a GPU."""
+    fn = L.jfa_worklist
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    assert fn(16, 4, 2, 100, 0, 0, 0, 4, 16, 100, 16, 0) == 1
+    assert b"list must be" in L.jfa_last_error()
+    assert fn(16, 4, 2, 100, 64, 1, 0, 2, 16, 100, 16, 0) == 1
+    assert b"self-attention only" in L.jfa_last_error()
+    assert fn(16, 4, 2, 100, 0, 0, 0, 3, 16, 100, 16, 0) == 1
+    assert fn(16, 4, 2, 100, 64, 1, 1, 1, 16, 100, 16, 0) == 1
+    assert fn(16, 4, 2, 100, 0, 0, 0, 0, 8, 100, 16, 0) == 1  # items not 16-byte aligned
+    assert b"16-byte" in L.jfa_last_error()

@@ -35,3 +35,29 @@ def test_self_attention_launches_and_kernel_times():
     for k in counts:
         assert prof[k][0] > 0.0, k
     jfa.jfa_sync_and_check()
+
+
+def test_broadcast_launches():
+    """Broadcast-Q forward + backward: the scheduler and the forward, then the
+    pre-pass (both backward work lists and the padded row statistics), the
+    dK/dV pass, the chunked dQ pass and the finalize that sums its partials."""
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs("broadcast_q", [0, 130, 5, 600], H=2, q_len=200)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    out, lse = jfa.forward(q, k, v, off, x["max_len"], broadcast_q=True)
+    torch.cuda.synchronize()
+    jfa.profile_read()
+    n0 = jfa.launch_count()
+    jfa.profile_enable(True)
+    try:
+        out, lse = jfa.forward(q, k, v, off, x["max_len"], broadcast_q=True)
+        jfa.backward(q, k, v, off, x["max_len"], out, lse, do, broadcast_q=True)
+        torch.cuda.synchronize()
+    finally:
+        jfa.profile_enable(False)
+    assert jfa.launch_count() - n0 == 6
+    counts = {k: n for k, (t, n) in jfa.profile_read().items() if n}
+    assert counts == {"sched": 1, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_qb": 1, "finalize": 1}
+    jfa.jfa_sync_and_check()
