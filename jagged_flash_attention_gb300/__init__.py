@@ -142,7 +142,8 @@ def jfa_sync_and_check(stream=None):
     _check(lib().jfa_sync_and_check(_stream(stream)))
 
 
-KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill")
+KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill",
+                "bwd_bs")
 
 
 def launch_count() -> int:

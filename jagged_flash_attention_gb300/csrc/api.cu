@@ -392,9 +392,11 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   const long long lq_pad = cdivll(s.Lq, kBM) * kBM;
   if (cap_kv >= (1LL << 31) || (long long)s.B * s.H * lq_pad >= (1LL << 40))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  // A short dense Q (one tile, D = 64): dK, dV and dQ in one pass over K / V.
+  const bool one_pass = bwd_bs_supported(s.D, s.Lq);
   size_t off = 0;
   const size_t hkv_off = off;
-  off = align256(off + 256 + cap_kv * sizeof(Item));
+  off = align256(off + 256 + (one_pass ? 0 : cap_kv) * sizeof(Item));
   const size_t hqb_off = off;
   off = align256(off + 256 + cap_qb * sizeof(QbItem));
   const size_t ktoff_off = off;
@@ -434,7 +436,8 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
     pp.D = s.D;
     pp.Lq = s.Lq;
     pp.broadcast = 1;
-    pp.n_sched = 2;
+    pp.n_sched = one_pass ? 1 : 2;
+    pp.qb_only = one_pass ? 1 : 0;
     pp.sched[0] = SchedParams{offsets, s.B, s.H, s.Lq, s.max_len, 0, 1, 1, kBM,
                               items_kv, (int)cap_kv, hdr_kv, ds->err};
     pp.qb = QbSchedParams{offsets, s.B, s.H, s.Lq, s.max_len, (int)chunk_cap, kt_off,
@@ -457,7 +460,14 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
   bp.err = ds->err;
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess && one_pass) {
+    bp.qb_items = items_qb;
+    bp.hdr = hdr_qb;
+    e = run_kernel(JFA_KERNEL_BWD_BCAST_ONEPASS, stream, [&] {
+      return launch_bwd_bs(tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_qb), stream);
+    });
+  }
+  if (e == cudaSuccess && !one_pass) {
     bp.items = items_kv;
     bp.hdr = hdr_kv;
     e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
@@ -465,7 +475,7 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
                            (int)std::min<long long>(ds->sms, cap_kv), stream);
     });
   }
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess && !one_pass) {
     bp.items = nullptr;
     bp.qb_items = items_qb;
     bp.hdr = hdr_qb;

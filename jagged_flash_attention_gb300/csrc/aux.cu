@@ -452,7 +452,9 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
 // sequence's last query tile) get {-inf, 0}, so that P = 0 there.
 __global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   if (blockIdx.x < p.n_sched) {
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 && p.qb_only)
+      qb_sched_body(p.qb);
+    else if (blockIdx.x == 0)
       sched_body(p.sched[0]);
     else if (p.broadcast)
       qb_sched_body(p.qb);

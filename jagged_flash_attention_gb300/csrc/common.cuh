@@ -139,6 +139,7 @@ struct PrepParams {
   int n_sched;
   SchedParams sched[2];
   QbSchedParams qb;
+  int qb_only;  // broadcast one-pass backward: block 0 builds the dQ-pass list alone
 };
 
 // Broadcast dQ: dq[l, h, :] = bf16(scale * sum over the chunks of the
@@ -160,6 +161,11 @@ cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
                           int grid, cudaStream_t s);
+// Broadcast-Q backward in one pass for a short dense Q (bwd_bs.cu): dK, dV
+// and the dQ partials of the items of the dQ-pass list.
+bool bwd_bs_supported(int D, int Lq);
+cudaError_t launch_bwd_bs(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t s);
 // Broadcast-Q dQ pass (tdo: the 4-D [B, Lq, H, D] map).
 cudaError_t launch_bwd_qb(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,

@@ -61,3 +61,26 @@ def test_broadcast_launches():
     counts = {k: n for k, (t, n) in jfa.profile_read().items() if n}
     assert counts == {"sched": 1, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_qb": 1, "finalize": 1}
     jfa.jfa_sync_and_check()
+
+
+def test_broadcast_short_q_one_pass_launches():
+    """Broadcast-Q with D = 64 and q_len <= 128: the backward is the pre-pass
+    (dQ-pass list and statistics only), one pass for dK, dV and the dQ
+    partials, and the finalize."""
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs("skewed_broadcast_q", [0, 130, 5, 600], H=2)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    out, lse = jfa.forward(q, k, v, off, x["max_len"], broadcast_q=True)
+    torch.cuda.synchronize()
+    jfa.profile_read()
+    jfa.profile_enable(True)
+    try:
+        jfa.backward(q, k, v, off, x["max_len"], out, lse, do, broadcast_q=True)
+        torch.cuda.synchronize()
+    finally:
+        jfa.profile_enable(False)
+    counts = {k: n for k, (t, n) in jfa.profile_read().items() if n}
+    assert counts == {"prep": 1, "bwd_bs": 1, "finalize": 1}
+    jfa.jfa_sync_and_check()

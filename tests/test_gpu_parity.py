@@ -27,6 +27,13 @@ SMALL = {
     "bcast_d64": dict(name="skewed_broadcast_q", lengths=[0, 7, 129, 1, 500], H=2),
     "bcast_three_q_tiles": dict(name="broadcast_q", lengths=[40, 256, 1], H=2, q_len=300),
     "bcast_all_empty_but_one": dict(name="broadcast_q", lengths=[0, 0, 3, 0], H=1, q_len=17),
+    # D = 64: q_len <= 128 takes the one-pass backward, longer q_len two passes
+    "bcast_d64_q128_one_pass": dict(name="skewed_broadcast_q", lengths=[130, 0, 1, 257, 128],
+                                    H=3, q_len=128),
+    "bcast_d64_q1_one_pass": dict(name="skewed_broadcast_q", lengths=[5, 300, 0, 2], H=2,
+                                  q_len=1),
+    "bcast_d64_q200_two_pass": dict(name="skewed_broadcast_q", lengths=[3, 0, 300, 129, 1], H=2,
+                                    q_len=200),
     "jagged_self_B6": dict(name="jagged_self", lengths=W.sample_lengths(
         W.WORKLOADS["jagged_self"], B=6)),
     "broadcast_q_B16": dict(name="broadcast_q", lengths=W.sample_lengths(
