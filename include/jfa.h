@@ -178,7 +178,8 @@ typedef enum {
   JFA_KERNEL_FINALIZE = 6,  /* broadcast-Q dQ: sum of the partials, bf16 cast */
   JFA_KERNEL_FILL = 7,      /* outputs of an all-empty broadcast batch */
   JFA_KERNEL_BWD_BCAST_ONEPASS = 8, /* broadcast-Q backward, one pass (D = 64, q_len <= 128) */
-  JFA_KERNEL_KINDS = 9
+  JFA_KERNEL_FWD_COMBINE = 9, /* broadcast-Q forward (q_len <= 128): merge of split sequences */
+  JFA_KERNEL_KINDS = 10
 } jfa_kernel_kind;
 
 /* Kernels enqueued by this library since the process started (all threads,

@@ -143,7 +143,7 @@ def jfa_sync_and_check(stream=None):
 
 
 KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill",
-                "bwd_bs")
+                "bwd_bs", "fwd_combine")
 
 
 def launch_count() -> int:

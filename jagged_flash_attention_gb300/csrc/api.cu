@@ -212,6 +212,66 @@ jfa_status finish(cudaStream_t stream) {
   return sync_and_read_error_word(stream);
 }
 
+// Broadcast-Q forward with a short dense Q (one 128-row tile): the key
+// tiles of all sequences cut into equal chunks per head (the dQ-pass chunk
+// list), a streamed forward over the chunks, and the merge of the sequences
+// that a chunk boundary splits.
+jfa_status do_fwd_bs(DeviceState* ds, const Shape& s, const void* q, const void* k, const void* v,
+                     const int32_t* offsets, void* out, float* lse, cudaStream_t stream) {
+  jfa_status st;
+  const long long chunk_cap = std::max<long long>(1, cdivll(2LL * ds->sms, s.H));
+  const long long cap = chunk_cap * s.H;
+  size_t off = 256;
+  const size_t items_off = off;
+  off = align256(off + cap * sizeof(QbItem));
+  const size_t ktoff_off = off;
+  off = align256(off + (s.B + 1) * sizeof(int));
+  const size_t parto_off = off;
+  off = align256(off + (size_t)cap * 2 * kBM * s.D * sizeof(float));
+  const size_t partl_off = off;
+  off = align256(off + (size_t)cap * 2 * kBM * sizeof(float));
+  CUtensorMap tq, tk, tv;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
+  QbItem* items = reinterpret_cast<QbItem*>(base + items_off);
+  int* kt_off = reinterpret_cast<int*>(base + ktoff_off);
+  QbSchedParams qp{offsets, s.B, s.H, s.Lq, s.max_len, (int)chunk_cap, kt_off, items, (int)cap,
+                   hdr, ds->err};
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] { return launch_qb_sched(qp, stream); });
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fp.offsets = offsets;
+  fp.B = s.B;
+  fp.H = s.H;
+  fp.Lq = s.Lq;
+  fp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+  fp.out = static_cast<__nv_bfloat16*>(out);
+  fp.lse = lse;
+  fp.hdr = hdr;
+  fp.err = ds->err;
+  fp.qb_items = items;
+  fp.kt_off = kt_off;
+  fp.part_o = reinterpret_cast<float*>(base + parto_off);
+  fp.part_lse = reinterpret_cast<float*>(base + partl_off);
+  if (e == cudaSuccess)
+    e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
+      return launch_fwd_bs(s.D, tq, tk, tv, fp, (int)std::min<long long>(ds->sms, cap), stream);
+    });
+  if (e == cudaSuccess)
+    e = run_kernel(JFA_KERNEL_FWD_COMBINE, stream,
+                   [&] { return launch_fwd_combine(s.D, fp, ds->sms, stream); });
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(stream);
+}
+
 jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
                   const int32_t* offsets, void* out, float* lse, cudaStream_t stream) {
   jfa_status st = check_common(s, q, k, v, offsets);
@@ -232,6 +292,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
     }
     return finish(stream);
   }
+  if (s.broadcast && fwd_bs_supported(s.Lq)) return do_fwd_bs(ds, s, q, k, v, offsets, out, lse, stream);
   const long long qt = s.broadcast ? cdivll(s.Lq, kFwdRows) : cdivll(s.max_len, kFwdRows);
   const long long cap = (long long)s.H * s.B * qt;
   if (cap >= (1LL << 31)) return fail(JFA_ERR_INVALID_ARG, "work list too large");

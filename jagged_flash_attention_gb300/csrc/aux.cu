@@ -11,6 +11,7 @@ namespace jfa {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+constexpr int kQbSmemOff = 8192;  // key-tile prefix entries kept in shared memory
 constexpr int kMaxBuckets = kSchedThreads;  // one bucket per thread in the scan
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -67,13 +68,20 @@ __device__ void scan_desc(const int* hist, int* base, int* warp_tot) {
 // first kPer of them stay in registers between the two passes, loaded
 // together so that their latencies overlap.
 constexpr int kPer = 8;
-__device__ void sched_body(const SchedParams& p) {
-  __shared__ int hist[kMaxBuckets];
-  __shared__ int base[kMaxBuckets];
-  __shared__ int cursor[kMaxBuckets];
-  __shared__ int warp_tot[32];
-  __shared__ int s_bad, s_nbig;
-  __shared__ int4 s_big[kSchedThreads];  // sequences with many items: {b, pos, tiles, items}
+struct SchedSmem {
+  int hist[kMaxBuckets], base[kMaxBuckets], cursor[kMaxBuckets];
+  int warp_tot[32];
+  int bad, nbig;
+  int4 big[kSchedThreads];  // sequences with many items: {b, pos, tiles, items}
+};
+__device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
+  int* hist = sm.hist;
+  int* base = sm.base;
+  int* cursor = sm.cursor;
+  int* warp_tot = sm.warp_tot;
+  int& s_bad = sm.bad;
+  int& s_nbig = sm.nbig;
+  int4* s_big = sm.big;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < kMaxBuckets; i += blockDim.x) hist[i] = 0, cursor[i] = 0;
   if (tid == 0) s_bad = (p.offsets[0] != 0);
@@ -200,7 +208,21 @@ __device__ void sched_body(const SchedParams& p) {
   }
 }
 
-__global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) { sched_body(p); }
+struct QbSmem {
+  int warp_tot[32];
+  int bad, carry;
+  int kt[kQbSmemOff];  // key-tile prefix, when B + 1 <= kQbSmemOff
+};
+// The two list builders never run in the same block: one static buffer.
+union SchedScratch {
+  SchedSmem s;
+  QbSmem q;
+};
+
+__global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedParams p) {
+  __shared__ SchedScratch sm;
+  sched_body(p, sm.s);
+}
 
 // A built work list copied out as 4 ints per item, with its item count
 // (and, for the broadcast dQ-pass list, its chunk count): list inspection
@@ -259,9 +281,10 @@ __device__ int block_incl_scan(int v, int* warp_tot) {
 // it is cut into nc equal chunks, and item (c, h, pair) at list index
 // (c * H + h) * pairs + pair starts at the sequence and tile where chunk c
 // starts.  kt_off[b] = key tiles of the sequences before b.
-__device__ void qb_sched_body(const QbSchedParams& p) {
-  __shared__ int warp_tot[32];
-  __shared__ int s_bad, s_carry;
+__device__ void qb_sched_body(const QbSchedParams& p, QbSmem& sm) {
+  int* warp_tot = sm.warp_tot;
+  int& s_bad = sm.bad;
+  int& s_carry = sm.carry;
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_bad = (p.offsets[0] != 0);
@@ -301,17 +324,25 @@ __device__ void qb_sched_body(const QbSchedParams& p) {
     }
     return;
   }
+  // Chunk starts: the last sequence b with kt_off[b] <= s0 (it is
+  // non-empty), by binary search over kt_off; a copy in shared memory when
+  // it fits.
+  int* s_kt = sm.kt;
+  const bool in_smem = p.B + 1 <= kQbSmemOff;
+  if (in_smem)
+    for (int b = tid; b <= p.B; b += blockDim.x) s_kt[b] = p.kt_off[b];
+  __syncthreads();
+  const int* kt = in_smem ? s_kt : p.kt_off;
   for (int idx = tid; idx < n_items; idx += blockDim.x) {
     const int c = idx / (p.H * pairs);
     const int rem = idx - c * (p.H * pairs);
     const int h = rem / pairs, pair = rem - h * pairs;
     const int s0 = static_cast<int>(static_cast<long long>(c) * total / nc);
     const int s1 = static_cast<int>(static_cast<long long>(c + 1) * total / nc);
-    // the last sequence b with kt_off[b] <= s0 (it is non-empty)
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.kt_off[mid] <= s0)
+      if (kt[mid] <= s0)
         lo = mid;
       else
         hi = mid - 1;
@@ -319,7 +350,7 @@ __device__ void qb_sched_body(const QbSchedParams& p) {
     QbItem it;
     it.hp = h | (pair << 16);
     it.b = lo;
-    it.j = s0 - p.kt_off[lo];
+    it.j = s0 - kt[lo];
     it.n = s1 - s0;
     p.items[idx] = it;
   }
@@ -452,14 +483,15 @@ __device__ void stats_body(const PrepParams& p, long long blk, long long nblk) {
 // sequence's last query tile) get {-inf, 0}, so that P = 0 there.
 __global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   if (blockIdx.x < p.n_sched) {
+    __shared__ SchedScratch sm;
     if (blockIdx.x == 0 && p.qb_only)
-      qb_sched_body(p.qb);
+      qb_sched_body(p.qb, sm.q);
     else if (blockIdx.x == 0)
-      sched_body(p.sched[0]);
+      sched_body(p.sched[0], sm.s);
     else if (p.broadcast)
-      qb_sched_body(p.qb);
+      qb_sched_body(p.qb, sm.q);
     else
-      sched_body(p.sched[1]);
+      sched_body(p.sched[1], sm.s);
     return;
   }
   const long long blk = blockIdx.x - p.n_sched, nblk = gridDim.x - p.n_sched;
@@ -476,7 +508,10 @@ __global__ void __launch_bounds__(kSchedThreads) bwd_prep_kernel(const __grid_co
   }
 }
 
-__global__ void __launch_bounds__(kSchedThreads) qb_sched_kernel(QbSchedParams p) { qb_sched_body(p); }
+__global__ void __launch_bounds__(kSchedThreads) qb_sched_kernel(QbSchedParams p) {
+  __shared__ SchedScratch sm;
+  qb_sched_body(p, sm.q);
+}
 
 // Broadcast dQ: dq[l, h, :] = bf16(scale * sum over the chunks c of the
 // partial of item (c, h, pair = l / 256)).  A block takes 32 four-column

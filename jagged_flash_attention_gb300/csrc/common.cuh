@@ -84,6 +84,13 @@ struct FwdParams {
   const Item* items;
   WorkHeader* hdr;
   int* err;
+  // Streamed broadcast forward (fwd_bs.cu): key-tile chunks, the key-tile
+  // prefix per sequence, and the partials of split sequences ([items][2]
+  // pieces x 128 rows: O / l fp32 [.., D] and the base-2 LSE).
+  const QbItem* qb_items;
+  const int* kt_off;
+  float* part_o;
+  float* part_lse;
 };
 
 struct BwdParams {
@@ -161,6 +168,12 @@ cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
                           int grid, cudaStream_t s);
+// Broadcast-Q forward for a short dense Q (q_len <= 128), streamed over
+// key-tile chunks (fwd_bs.cu), and the merge of split sequences.
+bool fwd_bs_supported(int Lq);
+cudaError_t launch_fwd_bs(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fwd_combine(int D, const FwdParams& p, int sms, cudaStream_t s);
 // Broadcast-Q backward in one pass for a short dense Q (bwd_bs.cu): dK, dV
 // and the dQ partials of the items of the dQ-pass list.
 bool bwd_bs_supported(int D, int Lq);

@@ -1,0 +1,634 @@
+// Broadcast-Q forward with a short dense Q (q_len <= 128) for sm_103a,
+// streamed over the key tiles of all sequences.
+//
+// In broadcast-Q mode ("Optimizing Jagged Flash Attention with TLX",
+// section 1) every sequence attends with the same dense Q.  When that Q is a
+// single 128-row tile, an item is a chunk of the concatenated key-tile
+// stream of all sequences (the dQ-pass chunks of the backward): the CTA
+// keeps Q in shared memory and streams K and V, the online softmax ("cuTile
+// Kernels - FMHA Implementation", "Flash Attention Algorithm"; base 2 with
+// the scale folded in) restarts at every sequence boundary, and each
+// sequence segment of the chunk ends with its O / LSE epilogue, run by its
+// own warpgroup on the other of two O accumulators while the next segment
+// computes.  Short sequences therefore cost neither a Q load nor a pipeline
+// drain.  A sequence cut by a chunk boundary (the TLX page's long-sequence
+// tail, section 2.2, "Scheduling jagged tiles across SMs") is split-KV: each
+// piece leaves its normalised O and base-2 LSE as an fp32 partial, and the
+// combine kernel merges the pieces with LSE weights.
+//
+// Per key tile u: S(u) = Q K_u^T (SS) into S[u % 2]; P = exp2(S * scale *
+// log2e - m) in bf16 over S's first 64 columns; O[seg % 2] += P V_u (TS).
+// Issue order: S(u) | PV(u - 1).
+//
+// CTA = 10 warps: warps 0-3 softmax (thread = query row = TMEM lane),
+// warps 4-7 epilogue of finished segments, warp 8 TMA producer, warp 9 MMA
+// issuer.  TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 after it.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8 (exact either way)
+
+template <int D>
+struct FsCfg {
+  static constexpr int NSK = (D == 128) ? 3 : 4;
+  static constexpr int NSV = (D == 128) ? 3 : 4;
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kTile;
+  static constexpr int kV = kK + NSK * kTile;
+  static constexpr int kSeg = kV + NSV * kTile;  // (m, l) per row, two parities: 2 KB
+  static constexpr int kCtl = kSeg + 2 * kBM * 8;
+  static constexpr int kSmem = kCtl + 512;
+  __host__ __device__ static constexpr uint32_t colS(int g) { return 128u * g; }
+  __host__ __device__ static constexpr uint32_t colO(int par) { return 256u + D * par; }
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct FsDec {
+  int b, j, n, h, slot;
+};
+
+struct Seg {
+  int b, j, nts, off0, L;
+};
+__device__ __forceinline__ void seg_load(Seg& s, const int32_t* off, int b, int j) {
+  s.b = b;
+  s.j = j;
+  s.off0 = off[b];
+  s.L = off[b + 1] - s.off0;
+  s.nts = cdiv(s.L, kBN);
+}
+__device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
+  if (++s.j < s.nts) return;
+  int b = s.b + 1;
+  while (b < B - 1 && off[b + 1] == off[b]) ++b;
+  seg_load(s, off, min(b, B - 1), 0);
+}
+
+struct KvTile {
+  int row, shift, nk;
+};
+__device__ __forceinline__ KvTile kv_tile(int off0, int L, int j, int T) {
+  KvTile k;
+  const int start = off0 + j * kBN;
+  k.shift = max(0, start + kBN - T);
+  k.row = start - k.shift;
+  k.nk = min(kBN, L - j * kBN);
+  return k;
+}
+
+struct FsCtl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_ready[2];  // o_ready[t % 2]: PV(t) complete
+  uint64_t o_done[2], o_free[2], seg_full[2], seg_empty[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  FsDec item[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > JFA_WAIT_LIMIT_CYCLES) {
+      atomicOr(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ bool next_item(FsCtl* c, uint32_t n, FsDec* f, bool* ok, int* err) {
+  const int slot = n & 1;
+  if (!mbar_wait_warp(&c->item_full[slot], (n >> 1) & 1, &c->abort, err)) {
+    *ok = false;
+    return false;
+  }
+  *f = c->item[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->item_empty[slot]);
+  return f->n >= 0;
+}
+
+template <int D>
+__device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                              const FwdParams& p, uint8_t* smem, FsCtl* c) {
+  using C = FsCfg<D>;
+  const int n_items = p.hdr->n_items;
+  const int T = p.hdr->T;
+  uint32_t itq = 0, nk = 0, nv = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    const int slot = n & 1;
+    if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
+    const int idx = atomicAdd(&p.hdr->ticket, 1);
+    FsDec f;
+    if (idx < n_items) {
+      const QbItem it = p.qb_items[idx];
+      f.h = it.hp & 0xffff;
+      f.b = it.b;
+      f.j = it.j;
+      f.n = it.n;
+      f.slot = idx;
+    } else {
+      f.n = -1;
+    }
+    c->item[slot] = f;
+    mbar_arrive(&c->item_full[slot]);
+    if (idx >= n_items) break;
+    if (f.n == 0) continue;
+    if (!mbar_wait(&c->q_empty, (itq & 1) ^ 1, &c->abort, p.err)) break;
+    mbar_arrive_expect_tx(&c->q_full, C::kTile);
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s)
+      tma_load_3d(smem + C::kQ + s * 16384, tq, &c->q_full, s * 64, f.h, 0);
+    ++itq;
+    Seg sg;
+    seg_load(sg, p.offsets, f.b, f.j);
+    for (int u = 0; u < f.n && ok; ++u) {
+      const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
+      {
+        const int st = nk % C::NSK;
+        if (!mbar_wait(&c->k_empty[st], ((nk / C::NSK) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
+#pragma unroll
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
+                      kt.row);
+        ++nk;
+      }
+      {
+        const int st = nv % C::NSV;
+        if (!mbar_wait(&c->v_empty[st], ((nv / C::NSV) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
+#pragma unroll
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
+                      kt.row);
+        ++nv;
+      }
+      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
+    }
+  }
+  if (itq > 0) drain_wait(&c->q_full, (itq - 1) & 1, p.err);
+  for (uint32_t g = nk > C::NSK ? nk - C::NSK : 0; g < nk; ++g)
+    drain_wait(&c->k_full[g % C::NSK], (g / C::NSK) & 1, p.err);
+  for (uint32_t g = nv > C::NSV ? nv - C::NSV : 0; g < nv; ++g)
+    drain_wait(&c->v_full[g % C::NSV], (g / C::NSV) & 1, p.err);
+}
+
+template <int D>
+__device__ void mma_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
+  using C = FsCfg<D>;
+  const uint32_t leader = elect_one();
+  const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);
+  const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
+  const uint64_t dq0 = smem_desc_sw128(smem_addr(smem + C::kQ), 16, 1024);
+  const uint64_t dk0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(smem_addr(smem + C::kV), 16384, 1024);
+  uint32_t itq = 0, nk = 0, nv = 0, g = 0, gseg = 0;
+  bool ok = true, issued = false;
+  for (uint32_t n = 0; ok; ++n) {
+    FsDec f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
+    if (f.n == 0) continue;
+    if (!mbar_wait_warp(&c->q_full, itq & 1, &c->abort, p.err)) break;
+    ++itq;
+    Seg sg;
+    seg_load(sg, p.offsets, f.b, f.j);
+    bool prev_start = false, prev_end = false;
+    for (int u = 0; u <= f.n && ok; ++u) {
+      const bool start = u < f.n && (u == 0 || sg.j == 0);
+      const bool end = u < f.n && (u == f.n - 1 || sg.j == sg.nts - 1);
+      if (u < f.n) {  // S(u) = Q K_u^T into S[(g + u) % 2]
+        const uint32_t kk = nk + u;
+        if (!mbar_wait_warp(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dk = desc_add(dk0, (kk % C::NSK) * C::kTile);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          if (leader)
+            mma_ss(tbase + C::colS((g + u) & 1), desc_add(dq0, off), desc_add(dk, off), id_s, k > 0);
+        }
+        if (leader) {
+          mma_commit(&c->s_full[(g + u) & 1]);
+          mma_commit(&c->k_empty[kk % C::NSK]);  // K is read by S only
+          if (u == f.n - 1) mma_commit(&c->q_empty);
+        }
+        issued = true;
+      }
+      if (u >= 1) {  // O[seg % 2] += P(u - 1) V_{u-1}
+        const uint32_t t = g + u - 1;
+        const uint32_t vv = nv + u - 1;
+        const int par = gseg & 1;
+        if (!mbar_wait_warp(&c->p_full[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&c->v_full[vv % C::NSV], (vv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (prev_start &&
+            !mbar_wait_warp(&c->o_free[par], ((gseg >> 1) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dv = desc_add(dv0, (vv % C::NSV) * C::kTile);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          if (leader)
+            mma_ts(tbase + C::colO(par), tbase + C::colS(t & 1) + k * 8, desc_add(dv, k * 2048),
+                   id_pv, !prev_start || k > 0);
+        if (leader) {
+          mma_commit(&c->o_ready[t & 1]);
+          mma_commit(&c->v_empty[vv % C::NSV]);
+          if (prev_end) mma_commit(&c->o_done[par]);
+        }
+        if (prev_end) ++gseg;
+      }
+      prev_start = start;
+      prev_end = end;
+      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
+    }
+    if (!ok) break;
+    g += f.n;
+    nk += f.n;
+    nv += f.n;
+  }
+  if (issued && leader) {
+    mma_commit(&c->drain);
+    drain_wait(&c->drain, 0, p.err);
+  }
+}
+
+template <int D>
+__device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
+  using C = FsCfg<D>;
+  const int r = threadIdx.x;  // query row == TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
+  const int T = p.hdr->T;
+  const float sl2 = p.scale_log2;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  float2* seg_ml = reinterpret_cast<float2*>(smem + C::kSeg);  // [parity][row] = (m, l)
+  uint32_t g = 0, gseg = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    FsDec f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
+    if (f.n == 0) continue;
+    Seg sg;
+    seg_load(sg, p.offsets, f.b, f.j);
+    float m_used = -INFINITY, l_run = 0.f;
+    for (int u = 0; u < f.n && ok; ++u) {
+      const uint32_t t = g + u;
+      const bool start = u == 0 || sg.j == 0;
+      const bool end = u == f.n - 1 || sg.j == sg.nts - 1;
+      if (start) {
+        m_used = -INFINITY;
+        l_run = 0.f;
+      }
+      if (!mbar_wait_warp(&c->s_full[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t ts = tbase + lane_base + C::colS(t & 1);
+      uint32_t raw[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(ts + ch * 32, raw[ch]);
+      tmem_wait_ld();
+      float s[128];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[ch][i]);
+      const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
+      if (kt.nk < kBN || kt.shift > 0) {  // ragged key tile: columns [shift, shift + nk)
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc)
+          s[cc] = (cc >= kt.shift && cc < kt.shift + kt.nk) ? s[cc] : -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int cc = 4; cc < 124; cc += 8) {
+        mx0 = fmax3(mx0, s[cc], s[cc + 1]);
+        mx1 = fmax3(mx1, s[cc + 2], s[cc + 3]);
+        mx2 = fmax3(mx2, s[cc + 4], s[cc + 5]);
+        mx3 = fmax3(mx3, s[cc + 6], s[cc + 7]);
+      }
+      mx0 = fmax3(mx0, s[124], s[125]);
+      mx1 = fmax3(mx1, s[126], s[127]);
+      const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+      const bool raise = m_tile > m_used + kRescaleLog2;
+      const float m_new = raise ? m_tile : m_used;
+      const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;
+      m_used = m_new;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const uint64_t negm = f2_pack(-m_use, -m_use);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const int cc = ch * 32 + i;
+          const float2 x0 = f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), sl2x2, negm));
+          const float2 x1 = f2_unpack(ffma2(f2_pack(s[cc + 2], s[cc + 3]), sl2x2, negm));
+          const float p0 = ex2_approx(x0.x), p1 = ex2_approx(x0.y);
+          const float p2 = ex2_approx(x1.x), p3 = ex2_approx(x1.y);
+          acc0 = fadd2(acc0, f2_pack(p0, p1));
+          acc1 = fadd2(acc1, f2_pack(p2, p3));
+          pk[i / 2] = pack_bf16x2(p0, p1);
+          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(ts + ch * 16, pk);
+      }
+      const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+      l_run = l_run * alpha + ((a0.x + a0.y) + (a1.x + a1.y));
+      if (!start && __any_sync(0xffffffffu, raise)) {
+        // A row raised its max: once PV(t - 1) has landed in this segment's
+        // O, scale O.  Only these tiles wait for the previous product; the
+        // per-parity barrier cannot run two phases ahead of this wait, since
+        // PV(t + 1) needs this tile's P first.
+        if (!mbar_wait_warp(&c->o_ready[(t - 1) & 1], ((t - 1) >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t to = tbase + lane_base + C::colO(gseg & 1);
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(to + ch * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(to + ch * 32, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&c->p_full[t & 1]);
+      if (end) {  // hand the segment's (m, l) to the epilogue warpgroup
+        const int par = gseg & 1;
+        if (!mbar_wait_warp(&c->seg_empty[par], ((gseg >> 1) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        seg_ml[par * kBM + r] = make_float2(m_used, l_run);
+        mbar_arrive(&c->seg_full[par]);
+        ++gseg;
+      }
+      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
+    }
+    if (!ok) break;
+    g += f.n;
+  }
+}
+
+// Epilogue of each finished segment: O / l in bf16 and the natural-log LSE
+// for a whole sequence; for a piece of a split sequence, O / l in fp32 and
+// the base-2 LSE m + log2(l) as a partial, in slot 0 (the piece starts
+// inside the sequence) or 1 (it starts at the sequence's first tile) of the
+// item.
+template <int D>
+__device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
+  using C = FsCfg<D>;
+  const int r = threadIdx.x - 128;
+  const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
+  const float2* seg_ml = reinterpret_cast<const float2*>(smem + C::kSeg);
+  uint32_t gseg = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    FsDec f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
+    if (f.n == 0) continue;
+    Seg sg;
+    seg_load(sg, p.offsets, f.b, f.j);
+    int seg_j0 = f.j;  // first tile of the current segment
+    for (int u = 0; u < f.n && ok; ++u) {
+      if (u > 0 && sg.j == 0) seg_j0 = 0;
+      const bool end = u == f.n - 1 || sg.j == sg.nts - 1;
+      if (end) {
+        const int par = gseg & 1;
+        const uint32_t ph = (gseg >> 1) & 1;
+        if (!mbar_wait_warp(&c->seg_full[par], ph, &c->abort, p.err)) { ok = false; break; }
+        const float2 ml = seg_ml[par * kBM + r];
+        mbar_arrive(&c->seg_empty[par]);
+        if (!mbar_wait_warp(&c->o_done[par], ph, &c->abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t o[D];
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch)
+          tmem_ld32(tbase + lane_base + C::colO(par) + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32 * ch));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&c->o_free[par]);
+        ++gseg;
+        const float inv_l = ml.y > 0.f ? 1.f / ml.y : 0.f;
+        const bool whole = seg_j0 == 0 && sg.j == sg.nts - 1;
+        if (r < p.Lq) {
+          if (whole) {
+            __nv_bfloat16* orow = p.out + ((static_cast<long long>(sg.b) * p.Lq + r) * p.H + f.h) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = pack_bf16x2(__uint_as_float(o[32 * ch + 2 * i]) * inv_l,
+                                   __uint_as_float(o[32 * ch + 2 * i + 1]) * inv_l);
+              st_global_64B(orow + ch * 32, w);
+            }
+            p.lse[(static_cast<long long>(sg.b) * p.H + f.h) * p.Lq + r] =
+                ml.y > 0.f ? (ml.x + lg2_approx(ml.y)) * kLn2 : -INFINITY;
+          } else {
+            const int slot = seg_j0 > 0 ? 0 : 1;
+            const long long prow = (static_cast<long long>(f.slot) * 2 + slot) * kBM + r;
+            float* dst = p.part_o + prow * D;
+#pragma unroll
+            for (int i = 0; i < D; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
+#pragma unroll
+            for (int q = 0; q < D / 8; ++q) st_global_v8(dst + 8 * q, o + 8 * q);
+            p.part_lse[prow] = ml.y > 0.f ? ml.x + lg2_approx(ml.y) : -INFINITY;
+          }
+        }
+      }
+      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bs_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = FsCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  FsCtl* c = reinterpret_cast<FsCtl*>(smem + C::kCtl);
+  const int warp = warp_id(), lane = lane_id();
+  if ((smem_addr(smem) & 1023) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&c->q_full, 1);
+    mbar_init(&c->q_empty, 1);
+    for (int i = 0; i < C::NSK; ++i) {
+      mbar_init(&c->k_full[i], 1);
+      mbar_init(&c->k_empty[i], 1);
+    }
+    for (int i = 0; i < C::NSV; ++i) {
+      mbar_init(&c->v_full[i], 1);
+      mbar_init(&c->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->s_full[i], 1);
+      mbar_init(&c->p_full[i], kBM);
+      mbar_init(&c->o_ready[i], 1);
+      mbar_init(&c->o_done[i], 1);
+      mbar_init(&c->o_free[i], kBM);
+      mbar_init(&c->seg_full[i], kBM);
+      mbar_init(&c->seg_empty[i], kBM);
+      mbar_init(&c->item_full[i], 1);
+      mbar_init(&c->item_empty[i], 9);  // 4 softmax + 4 epilogue warps + the MMA warp
+    }
+    mbar_init(&c->drain, 1);
+    c->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&c->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = c->tmem_base;
+  if (warp < 4) {
+    softmax_role<D>(p, smem, c, tbase);
+  } else if (warp < 8) {
+    epilogue_role<D>(p, smem, c, tbase);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer_role<D>(&tq, &tk, &tv, p, smem, c);
+  } else {
+    mma_role<D>(p, smem, c, tbase);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// Merge of the pieces of split sequences, and the outputs of empty ones.
+// One warp per (sequence b, head h), lanes over query rows.  A sequence
+// whose key tiles [kt_off[b], kt_off[b+1]) span chunks c0 < c1 has its first
+// piece in slot 1 of item (c0, h) and the others in slot 0 of items
+// (c0 + 1 .. c1, h): O = sum_i 2^(lse_i - lse) O_i with lse = log2 sum_i
+// 2^lse_i.  Empty sequences get O = 0 and LSE = -inf.
+template <int D>
+__global__ void fwd_combine_kernel(const FwdParams p) {
+  const WorkHeader* hdr = p.hdr;
+  if (!hdr->valid) return;
+  const int nc = hdr->n_chunks;
+  const long long total = p.kt_off[p.B];
+  const int lane = threadIdx.x & 31;
+  const long long nbh = static_cast<long long>(p.B) * p.H;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < nbh;
+       w += nwarps) {
+    const int h = static_cast<int>(w % p.H), b = static_cast<int>(w / p.H);
+    const long long s_first = p.kt_off[b], s_last = p.kt_off[b + 1] - 1;
+    float* lrow = p.lse + (static_cast<long long>(b) * p.H + h) * p.Lq;
+    if (s_last < s_first) {  // empty sequence
+      for (int r = lane; r < p.Lq; r += 32) {
+        __nv_bfloat16* orow = p.out + ((static_cast<long long>(b) * p.Lq + r) * p.H + h) * D;
+        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        lrow[r] = -INFINITY;
+      }
+      continue;
+    }
+    auto chunk_of = [&](long long s) {
+      int c = static_cast<int>(s * nc / total);
+      while (c + 1 < nc && (c + 1) * total / nc <= s) ++c;
+      while (c > 0 && c * total / nc > s) --c;
+      return c;
+    };
+    const int c0 = chunk_of(s_first), c1 = chunk_of(s_last);
+    if (c0 == c1) continue;  // whole: written by the forward kernel
+    for (int r = lane; r < p.Lq; r += 32) {
+      float lmax = -INFINITY;
+      for (int c = c0; c <= c1; ++c)
+        lmax = fmaxf(lmax, p.part_lse[((static_cast<long long>(c) * p.H + h) * 2 + (c == c0)) * kBM + r]);
+      float acc[D];
+#pragma unroll
+      for (int d = 0; d < D; ++d) acc[d] = 0.f;
+      float sw = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const long long prow = ((static_cast<long long>(c) * p.H + h) * 2 + (c == c0)) * kBM + r;
+        const float wgt = ex2_approx(p.part_lse[prow] - lmax);
+        sw += wgt;
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * D);
+#pragma unroll
+        for (int d4 = 0; d4 < D / 4; ++d4) {
+          const float4 v = src[d4];
+          acc[4 * d4] += wgt * v.x;
+          acc[4 * d4 + 1] += wgt * v.y;
+          acc[4 * d4 + 2] += wgt * v.z;
+          acc[4 * d4 + 3] += wgt * v.w;
+        }
+      }
+      const float inv = 1.f / sw;
+      __nv_bfloat16* orow = p.out + ((static_cast<long long>(b) * p.Lq + r) * p.H + h) * D;
+#pragma unroll
+      for (int d = 0; d < D; d += 8)
+        *reinterpret_cast<uint4*>(orow + d) =
+            make_uint4(pack_bf16x2(acc[d] * inv, acc[d + 1] * inv),
+                       pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv),
+                       pack_bf16x2(acc[d + 4] * inv, acc[d + 5] * inv),
+                       pack_bf16x2(acc[d + 6] * inv, acc[d + 7] * inv));
+      lrow[r] = (lmax + lg2_approx(sw)) * kLn2;
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const FwdParams& p, int grid, cudaStream_t s) {
+  using C = FsCfg<D>;
+  static_assert(C::kSmem <= 232448, "shared memory budget");
+  static_assert(sizeof(FsCtl) <= 512, "control block");
+  static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
+  auto kern = fwd_bs_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_bs_supported(int Lq) { return Lq >= 1 && Lq <= kBM; }
+
+cudaError_t launch_fwd_bs(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s) {
+  if (!fwd_bs_supported(p.Lq)) return cudaErrorInvalidValue;
+  if (D == 128) return launch_t<128>(tq, tk, tv, p, grid, s);
+  return launch_t<64>(tq, tk, tv, p, grid, s);
+}
+
+cudaError_t launch_fwd_combine(int D, const FwdParams& p, int sms, cudaStream_t s) {
+  const long long warps = static_cast<long long>(p.B) * p.H;
+  const int grid = static_cast<int>(std::min<long long>((warps + 7) / 8, 8LL * sms));
+  if (D == 128)
+    fwd_combine_kernel<128><<<grid > 0 ? grid : 1, 256, 0, s>>>(p);
+  else
+    fwd_combine_kernel<64><<<grid > 0 ? grid : 1, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

@@ -34,6 +34,11 @@ SMALL = {
                                   q_len=1),
     "bcast_d64_q200_two_pass": dict(name="skewed_broadcast_q", lengths=[3, 0, 300, 129, 1], H=2,
                                     q_len=200),
+    # q_len <= 128: the streamed forward; chunk boundaries split sequences
+    # into pieces that the combine kernel merges
+    "bcast_stream_split_one_long": dict(name="skewed_broadcast_q", lengths=[3000], H=2),
+    "bcast_stream_split_d128": dict(name="broadcast_q", lengths=[0, 900, 5, 1300, 0, 77], H=2,
+                                    q_len=100),
     "jagged_self_B6": dict(name="jagged_self", lengths=W.sample_lengths(
         W.WORKLOADS["jagged_self"], B=6)),
     "broadcast_q_B16": dict(name="broadcast_q", lengths=W.sample_lengths(
