@@ -43,18 +43,30 @@ def _stale(target, inputs) -> bool:
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def variant_path(name: str) -> str:
+    """Path of a library variant built by build(variant=name)."""
+    return os.path.join(PKG, f"libjfa_{name}.so")
+
+
+def build(verbose: bool = False, force: bool = False, variant: str | None = None,
+          defines: tuple = ()) -> str:
+    """Builds libjfa.so, or with `variant` a copy of the library compiled with
+    the extra preprocessor `defines` (e.g. a short wait limit for the timeout
+    test) into libjfa_<variant>.so, with its own object directory."""
+    build_dir = BUILD_DIR if variant is None else os.path.join(BUILD_DIR, variant)
+    lib_path = LIB_PATH if variant is None else variant_path(variant)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = _deps()
     objs = []
     jobs = []
+    extra = [f"-D{d}" for d in defines]
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
-            jobs.append([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])
 
     def run(cmd):
         if verbose:
@@ -66,9 +78,9 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB_PATH, objs):
-        run([nvcc, *ARCH, "-shared", "-o", LIB_PATH, *objs])
-    return LIB_PATH
+    if force or jobs or _stale(lib_path, objs):
+        run([nvcc, *ARCH, "-shared", "-o", lib_path, *objs])
+    return lib_path
 
 
 if __name__ == "__main__":

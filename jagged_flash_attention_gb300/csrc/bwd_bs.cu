@@ -63,22 +63,6 @@ struct BsDec {
   int b, j, n, h, slot;
 };
 
-struct Seg {
-  int b, j, nts, off0, L;
-};
-__device__ __forceinline__ void seg_load(Seg& s, const int32_t* off, int b, int j) {
-  s.b = b;
-  s.j = j;
-  s.off0 = off[b];
-  s.L = off[b + 1] - s.off0;
-  s.nts = cdiv(s.L, kBN);
-}
-__device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
-  if (++s.j < s.nts) return;
-  int b = s.b + 1;
-  while (b < B - 1 && off[b + 1] == off[b]) ++b;
-  seg_load(s, off, min(b, B - 1), 0);
-}
 
 struct KvTile {
   int row, shift, nk;
@@ -159,7 +143,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     tma_load_3d(smem + kQ, tq, &c->q_full, 0, f.h, 0);
     ++itq;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     for (int u = 0; u < f.n && ok; ++u) {
       const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
       {
@@ -233,7 +217,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, BsCtl* c, uint32_t t
     ++itq;
     const uint32_t k0 = nk, v0 = nv, t0 = gt;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     int st = 0;
     uint64_t do_m = do_m0, do_k = do_k0;
     for (int u = 0; u <= f.n && ok; ++u) {
@@ -370,7 +354,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, BsCtl* c, uint32_t 
     if (f.n == 0) continue;
     uint64_t nlse2 = 0, ndlt2 = 0;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     KvTile prev_kt = {0, 0, 0};
     int prev_off0 = 0, prev_j = 0;
     for (int u = 0; u < f.n && ok; ++u) {

@@ -207,7 +207,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   using C = KvCfg<D>;
   const int n_items = p.hdr->n_items;
   const int T = p.hdr->T;
-  uint32_t it = 0, gq = 0, nk = 0, nv = 0;
+  uint32_t it = 0, gq = 0, gdo = 0, nk = 0, nv = 0;  // gdo: stages whose dO was issued
   bool ok = true;
   // One-item lookahead: the next item is taken and decoded while this one's
   // loads go out, and its K, V and first Q / dO boxes are prefetched into
@@ -277,6 +277,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
           tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
                       f.h, qb.row);
       }
+      ++gdo;  // counted now: a wait below that gives up must not hide these copies from the drain
       if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
@@ -312,13 +313,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
     drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
   if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
-  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g) {
+  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) {
-      drain_wait(&c->q_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
-      drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
-    }
-  }
+    for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->q_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+  for (uint32_t g = gdo > C::NSQ ? gdo - C::NSQ : 0; g < gdo; ++g)
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
 }
 
 template <int D, bool CAUSAL>

@@ -67,27 +67,6 @@ struct QbDec {
   int nt;  // query tiles of the pair (1 or 2)
 };
 
-// Position in the key-tile stream: key tile j of sequence b.
-struct Seg {
-  int b, j, nts, off0, L;
-};
-
-__device__ __forceinline__ void seg_load(Seg& s, const int32_t* off, int b, int j) {
-  s.b = b;
-  s.j = j;
-  s.off0 = off[b];
-  s.L = off[b + 1] - s.off0;
-  s.nts = cdiv(s.L, kBN);
-}
-
-// Next key tile of the stream: the following tile of this sequence, else the
-// first tile of the next non-empty sequence (never past sequence B - 1).
-__device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
-  if (++s.j < s.nts) return;
-  int b = s.b + 1;
-  while (b < B - 1 && off[b + 1] == off[b]) ++b;
-  seg_load(s, off, min(b, B - 1), 0);
-}
 
 struct KvTile {
   int row, shift, nk;
@@ -177,7 +156,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
                     f.pair * kQbRows + g * kBM);
     ++itq;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     for (int u = 0; u < f.n && ok; ++u) {
       const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
       {
@@ -307,7 +286,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QbCtl* c, uint32_t t
     const int nt = f.nt;
     const uint32_t k0 = nk, v0 = nv;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     int st = 0;
     for (int u = 0; u <= f.n && ok; ++u) {
       bool k_ready = false;
@@ -453,7 +432,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, QbCtl* c, uint32_t 
       return true;
     };
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     for (int u = 0; u < f.n && ok; ++u) {
       if (u == 0 || sg.j == 0) {
         const int st = gs % C::NSDO;

@@ -64,6 +64,43 @@ struct QbItem {
 // Query rows per broadcast dQ-pass item (two 128-row tiles).
 constexpr int kQbRows = 256;
 
+// Position in the key-tile stream of the chunked broadcast kernels: key
+// tile j of sequence b (which has nts tiles, keys [off0, off0 + L)).  The
+// end offset of the next sequence is loaded when a sequence is entered, so
+// that the step into the next sequence needs no global load on the spot.
+struct Seg {
+  int b, j, nts, off0, L;
+  int nxt;  // offsets[b + 2] (or offsets[B] past the end)
+};
+
+__device__ __forceinline__ void seg_load(Seg& s, const int32_t* off, int B, int b, int j) {
+  s.b = b;
+  s.j = j;
+  s.off0 = off[b];
+  s.L = off[b + 1] - s.off0;
+  s.nts = (s.L + kBN - 1) / kBN;
+  s.nxt = b + 2 <= B ? off[b + 2] : s.off0 + s.L;
+}
+
+// Next key tile of the stream: the following tile of this sequence, else the
+// first tile of the next non-empty sequence (never past sequence B - 1).
+__device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
+  if (++s.j < s.nts) return;
+  const int b1 = s.b + 1, e1 = s.off0 + s.L;  // e1 = offsets[b1]
+  if (b1 < B && s.nxt > e1) {
+    s.b = b1;
+    s.j = 0;
+    s.off0 = e1;
+    s.L = s.nxt - e1;
+    s.nts = (s.L + kBN - 1) / kBN;
+    s.nxt = b1 + 2 <= B ? off[b1 + 2] : s.nxt;
+    return;
+  }
+  int b = b1;  // empty sequences follow
+  while (b < B - 1 && off[b + 1] == off[b]) ++b;
+  seg_load(s, off, B, b < B - 1 ? b : B - 1, 0);
+}
+
 struct SchedParams {
   const int32_t* offsets;
   int B, H, Lq, max_len;

@@ -16,39 +16,58 @@
 // piece leaves its normalised O and base-2 LSE as an fp32 partial, and the
 // combine kernel merges the pieces with LSE weights.
 //
-// Per key tile u: S(u) = Q K_u^T (SS) into S[u % 2]; P = exp2(S * scale *
+// Per key tile u: S(u) = Q K_u^T (SS) into S[u % NSB]; P = exp2(S * scale *
 // log2e - m) in bf16 over S's first 64 columns; O[seg % 2] += P V_u (TS).
-// Issue order: S(u) | PV(u - 1).
+// Issue order: S(u) | PV(u - NSB + 1): with three S buffers (D = 64) S runs
+// two tiles ahead of PV, so the softmax never waits for its next S behind
+// the previous tile's PV.
 //
-// CTA = 10 warps: warps 0-3 softmax (thread = query row = TMEM lane),
-// warps 4-7 epilogue of finished segments, warp 8 TMA producer, warp 9 MMA
-// issuer.  TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 after it.
+// CTA = 4 * SPLIT + 6 warps (SPLIT = 2: a four-way split measured slower,
+// the softmax being bound by latency rather than by its element count): warps
+// 0 .. 4*SPLIT-1 softmax (thread: query row r = TMEM lane, key columns
+// (128 / SPLIT) * (warp / 4)..; the SPLIT threads of a row exchange their
+// partial row max through shared memory each tile, so all apply the same
+// running max), then four epilogue warps for finished segments, the TMA
+// producer warp and the MMA issuer warp.  TMEM: S buffers at 128 * i, then
+// O0 and O1 (D columns each).
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// Column split of the softmax, warps and threads of the CTA.
+template <int D>
+struct FsRoles {
+  static constexpr int SPLIT = 2;
+  static constexpr int kCols = kBN / SPLIT;        // key columns per softmax thread
+  static constexpr int kSoftmax = kBM * SPLIT;     // softmax threads
+  static constexpr int kEpiWarp = 4 * SPLIT;       // first epilogue warp
+  static constexpr int kProducerWarp = kEpiWarp + 4;
+  static constexpr int kMmaWarp = kEpiWarp + 5;
+  static constexpr int kThreads = 32 * (kEpiWarp + 6);
+};
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8 (exact either way)
 
 template <int D>
 struct FsCfg {
   static constexpr int NSK = (D == 128) ? 3 : 4;
-  static constexpr int NSV = (D == 128) ? 3 : 4;
+  static constexpr int NSV = (D == 128) ? 2 : 4;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kSlabs = D / 64;
   static constexpr int kQ = 0;
   static constexpr int kK = kTile;
   static constexpr int kV = kK + NSK * kTile;
-  static constexpr int kSeg = kV + NSV * kTile;  // (m, l) per row, two parities: 2 KB
-  static constexpr int kCtl = kSeg + 2 * kBM * 8;
+  // (m, l) per row and column part, two segment parities
+  static constexpr int kSeg = kV + NSV * kTile;
+  // partial row max per row and column part, two tile parities
+  static constexpr int kXch = kSeg + 2 * FsRoles<D>::SPLIT * kBM * 8;
+  static constexpr int kCtl = kXch + 2 * FsRoles<D>::SPLIT * kBM * 4;
   static constexpr int kSmem = kCtl + 512;
-  __host__ __device__ static constexpr uint32_t colS(int g) { return 128u * g; }
-  __host__ __device__ static constexpr uint32_t colO(int par) { return 256u + D * par; }
+  static constexpr int NSB = (D == 64) ? 3 : 2;  // S buffers: 128 * NSB + 2 * D <= 512 columns
+  __host__ __device__ static constexpr uint32_t colS(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t colO(int par) { return 128u * NSB + D * par; }
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -57,22 +76,6 @@ struct FsDec {
   int b, j, n, h, slot;
 };
 
-struct Seg {
-  int b, j, nts, off0, L;
-};
-__device__ __forceinline__ void seg_load(Seg& s, const int32_t* off, int b, int j) {
-  s.b = b;
-  s.j = j;
-  s.off0 = off[b];
-  s.L = off[b + 1] - s.off0;
-  s.nts = cdiv(s.L, kBN);
-}
-__device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
-  if (++s.j < s.nts) return;
-  int b = s.b + 1;
-  while (b < B - 1 && off[b + 1] == off[b]) ++b;
-  seg_load(s, off, min(b, B - 1), 0);
-}
 
 struct KvTile {
   int row, shift, nk;
@@ -89,8 +92,9 @@ __device__ __forceinline__ KvTile kv_tile(int off0, int L, int j, int T) {
 struct FsCtl {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_ready[2];  // o_ready[t % 2]: PV(t) complete
+  uint64_t s_full[3], p_full[3], o_ready[2];  // o_ready[t % 2]: PV(t) complete
   uint64_t o_done[2], o_free[2], seg_full[2], seg_empty[2];
+  uint64_t xbar[2];  // the row-max exchange of tile t, t % 2
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   FsDec item[2];
@@ -154,7 +158,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       tma_load_3d(smem + C::kQ + s * 16384, tq, &c->q_full, s * 64, f.h, 0);
     ++itq;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     for (int u = 0; u < f.n && ok; ++u) {
       const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
       {
@@ -204,55 +208,55 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t t
     if (f.n == 0) continue;
     if (!mbar_wait_warp(&c->q_full, itq & 1, &c->abort, p.err)) break;
     ++itq;
+    // S runs LA tiles ahead of PV; the cursor follows the PV stream.
+    constexpr int LA = C::NSB - 1;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
-    bool prev_start = false, prev_end = false;
-    for (int u = 0; u <= f.n && ok; ++u) {
-      const bool start = u < f.n && (u == 0 || sg.j == 0);
-      const bool end = u < f.n && (u == f.n - 1 || sg.j == sg.nts - 1);
-      if (u < f.n) {  // S(u) = Q K_u^T into S[(g + u) % 2]
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
+    for (int u = 0; u < f.n + LA && ok; ++u) {
+      if (u < f.n) {  // S(u) = Q K_u^T into S[(g + u) % NSB]
         const uint32_t kk = nk + u;
+        const int sb = (g + u) % C::NSB;
         if (!mbar_wait_warp(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint64_t dk = desc_add(dk0, (kk % C::NSK) * C::kTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          if (leader)
-            mma_ss(tbase + C::colS((g + u) & 1), desc_add(dq0, off), desc_add(dk, off), id_s, k > 0);
+          if (leader) mma_ss(tbase + C::colS(sb), desc_add(dq0, off), desc_add(dk, off), id_s, k > 0);
         }
         if (leader) {
-          mma_commit(&c->s_full[(g + u) & 1]);
+          mma_commit(&c->s_full[sb]);
           mma_commit(&c->k_empty[kk % C::NSK]);  // K is read by S only
           if (u == f.n - 1) mma_commit(&c->q_empty);
         }
         issued = true;
       }
-      if (u >= 1) {  // O[seg % 2] += P(u - 1) V_{u-1}
-        const uint32_t t = g + u - 1;
-        const uint32_t vv = nv + u - 1;
+      if (u >= LA) {  // O[seg % 2] += P(v) V_v, v = u - LA
+        const int v = u - LA;
+        const bool start = v == 0 || sg.j == 0;
+        const bool end = v == f.n - 1 || sg.j == sg.nts - 1;
+        const uint32_t t = g + v;
+        const uint32_t vv = nv + v;
         const int par = gseg & 1;
-        if (!mbar_wait_warp(&c->p_full[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&c->p_full[t % C::NSB], (t / C::NSB) & 1, &c->abort, p.err)) { ok = false; break; }
         if (!mbar_wait_warp(&c->v_full[vv % C::NSV], (vv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
-        if (prev_start &&
+        if (start &&
             !mbar_wait_warp(&c->o_free[par], ((gseg >> 1) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint64_t dv = desc_add(dv0, (vv % C::NSV) * C::kTile);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
           if (leader)
-            mma_ts(tbase + C::colO(par), tbase + C::colS(t & 1) + k * 8, desc_add(dv, k * 2048),
-                   id_pv, !prev_start || k > 0);
+            mma_ts(tbase + C::colO(par), tbase + C::colS(t % C::NSB) + k * 8,
+                   desc_add(dv, k * 2048), id_pv, !start || k > 0);
         if (leader) {
           mma_commit(&c->o_ready[t & 1]);
           mma_commit(&c->v_empty[vv % C::NSV]);
-          if (prev_end) mma_commit(&c->o_done[par]);
+          if (end) mma_commit(&c->o_done[par]);
         }
-        if (prev_end) ++gseg;
+        if (end) ++gseg;
+        if (v + 1 < f.n) seg_next(sg, p.offsets, p.B);
       }
-      prev_start = start;
-      prev_end = end;
-      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
     }
     if (!ok) break;
     g += f.n;
@@ -268,12 +272,16 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t t
 template <int D>
 __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
   using C = FsCfg<D>;
-  const int r = threadIdx.x;  // query row == TMEM lane
+  using R = FsRoles<D>;
+  constexpr int NC = R::kCols;        // key columns of this thread
+  const int r = threadIdx.x & 127;    // query row == TMEM lane
+  const int part = threadIdx.x >> 7;  // key columns [NC * part, NC * part + NC)
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const int T = p.hdr->T;
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
-  float2* seg_ml = reinterpret_cast<float2*>(smem + C::kSeg);  // [parity][row] = (m, l)
+  float2* seg_ml = reinterpret_cast<float2*>(smem + C::kSeg);  // [parity][part][row] = (m, l)
+  float* xch = reinterpret_cast<float*>(smem + C::kXch);       // [tile parity][part][row]
   uint32_t g = 0, gseg = 0;
   bool ok = true;
   for (uint32_t n = 0; ok; ++n) {
@@ -281,8 +289,8 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
     if (!next_item(c, n, &f, &ok, p.err)) break;
     if (f.n == 0) continue;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
-    float m_used = -INFINITY, l_run = 0.f;
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
+    float m_used = -INFINITY, l_run = 0.f;  // l_run: this thread's columns
     for (int u = 0; u < f.n && ok; ++u) {
       const uint32_t t = g + u;
       const bool start = u == 0 || sg.j == 0;
@@ -291,35 +299,48 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
         m_used = -INFINITY;
         l_run = 0.f;
       }
-      if (!mbar_wait_warp(&c->s_full[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+      if (!mbar_wait_warp(&c->s_full[t % C::NSB], (t / C::NSB) & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t ts = tbase + lane_base + C::colS(t & 1);
-      uint32_t raw[4][32];
+      const uint32_t ts = tbase + lane_base + C::colS(t % C::NSB);
+      uint32_t raw[NC];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(ts + ch * 32, raw[ch]);
+      for (int ch = 0; ch < NC / 32; ++ch)
+        tmem_ld32(ts + NC * part + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * ch));
       tmem_wait_ld();
-      float s[128];
+      float s[NC];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[ch][i]);
+      for (int i = 0; i < NC; ++i) s[i] = __uint_as_float(raw[i]);
       const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
       if (kt.nk < kBN || kt.shift > 0) {  // ragged key tile: columns [shift, shift + nk)
+        const int c0 = NC * part;
 #pragma unroll
-        for (int cc = 0; cc < 128; ++cc)
-          s[cc] = (cc >= kt.shift && cc < kt.shift + kt.nk) ? s[cc] : -INFINITY;
+        for (int cc = 0; cc < NC; ++cc)
+          s[cc] = (c0 + cc >= kt.shift && c0 + cc < kt.shift + kt.nk) ? s[cc] : -INFINITY;
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int cc = 4; cc < 124; cc += 8) {
+      for (int cc = 4; cc < NC - 4; cc += 8) {
         mx0 = fmax3(mx0, s[cc], s[cc + 1]);
         mx1 = fmax3(mx1, s[cc + 2], s[cc + 3]);
         mx2 = fmax3(mx2, s[cc + 4], s[cc + 5]);
         mx3 = fmax3(mx3, s[cc + 6], s[cc + 7]);
       }
-      mx0 = fmax3(mx0, s[124], s[125]);
-      mx1 = fmax3(mx1, s[126], s[127]);
-      const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+      mx0 = fmax3(mx0, s[NC - 4], s[NC - 3]);
+      mx1 = fmax3(mx1, s[NC - 2], s[NC - 1]);
+      float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
+      // Exchange with the other parts of the row.  Every softmax thread has
+      // read its S columns before arriving, so the P writes below (part q
+      // packs into S columns NC/2 * q.., read by another part) come after
+      // all reads.
+      float* xt = xch + (t & 1) * R::SPLIT * kBM;
+      xt[part * kBM + r] = mx;
+      tc_fence_before();
+      mbar_arrive(&c->xbar[t & 1]);
+      if (!mbar_wait_warp(&c->xbar[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int q = 1; q < R::SPLIT; ++q) mx = fmaxf(mx, xt[((part + q) % R::SPLIT) * kBM + r]);
+      const float m_tile = mx * sl2;
       const bool raise = m_tile > m_used + kRescaleLog2;
       const float m_new = raise ? m_tile : m_used;
       const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;
@@ -328,7 +349,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
       const uint64_t negm = f2_pack(-m_use, -m_use);
       uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < NC / 32; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -342,37 +363,37 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
           pk[i / 2] = pack_bf16x2(p0, p1);
           pk[i / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        tmem_st16(ts + ch * 16, pk);
+        // keys NC*part + 32ch.. -> packed columns NC/2*part + 16ch..
+        tmem_st16(ts + (NC / 2) * part + ch * 16, pk);
       }
       const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
       l_run = l_run * alpha + ((a0.x + a0.y) + (a1.x + a1.y));
       if (!start && __any_sync(0xffffffffu, raise)) {
         // A row raised its max: once PV(t - 1) has landed in this segment's
-        // O, scale O.  Only these tiles wait for the previous product; the
-        // per-parity barrier cannot run two phases ahead of this wait, since
-        // PV(t + 1) needs this tile's P first.
+        // O, scale this thread's O columns.  Only these tiles wait for the
+        // previous product; the per-parity barrier cannot run two phases
+        // ahead of this wait, since PV(t + 1) needs this tile's P first.
         if (!mbar_wait_warp(&c->o_ready[(t - 1) & 1], ((t - 1) >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
-        {
-          const uint32_t to = tbase + lane_base + C::colO(gseg & 1);
+        constexpr int OC = D / R::SPLIT;  // O columns of this thread: 16 or 64
+        const uint32_t to = tbase + lane_base + C::colO(gseg & 1) + OC * part;
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(to + ch * 32, o);
-            tmem_wait_ld();
+        for (int ch = 0; ch < OC / 16; ++ch) {
+          uint32_t o[16];
+          tmem_ld16(to + ch * 16, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(to + ch * 32, o);
-          }
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(to + ch * 16, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&c->p_full[t & 1]);
-      if (end) {  // hand the segment's (m, l) to the epilogue warpgroup
+      mbar_arrive(&c->p_full[t % C::NSB]);
+      if (end) {  // hand the segment's (m, l of these columns) to the epilogue warpgroup
         const int par = gseg & 1;
         if (!mbar_wait_warp(&c->seg_empty[par], ((gseg >> 1) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
-        seg_ml[par * kBM + r] = make_float2(m_used, l_run);
+        seg_ml[(par * R::SPLIT + part) * kBM + r] = make_float2(m_used, l_run);
         mbar_arrive(&c->seg_full[par]);
         ++gseg;
       }
@@ -391,7 +412,8 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
 template <int D>
 __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
   using C = FsCfg<D>;
-  const int r = threadIdx.x - 128;
+  using R = FsRoles<D>;
+  const int r = threadIdx.x - R::kSoftmax;
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const float2* seg_ml = reinterpret_cast<const float2*>(smem + C::kSeg);
   uint32_t gseg = 0;
@@ -401,7 +423,7 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
     if (!next_item(c, n, &f, &ok, p.err)) break;
     if (f.n == 0) continue;
     Seg sg;
-    seg_load(sg, p.offsets, f.b, f.j);
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
     int seg_j0 = f.j;  // first tile of the current segment
     for (int u = 0; u < f.n && ok; ++u) {
       if (u > 0 && sg.j == 0) seg_j0 = 0;
@@ -410,43 +432,49 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
         const int par = gseg & 1;
         const uint32_t ph = (gseg >> 1) & 1;
         if (!mbar_wait_warp(&c->seg_full[par], ph, &c->abort, p.err)) { ok = false; break; }
-        const float2 ml = seg_ml[par * kBM + r];
+        const float m = seg_ml[(par * R::SPLIT) * kBM + r].x;
+        float l = 0.f;
+#pragma unroll
+        for (int q = 0; q < R::SPLIT; ++q) l += seg_ml[(par * R::SPLIT + q) * kBM + r].y;
         mbar_arrive(&c->seg_empty[par]);
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const bool whole = seg_j0 == 0 && sg.j == sg.nts - 1;
+        const bool store = r < p.Lq;
+        const int slot = seg_j0 > 0 ? 0 : 1;
+        const long long prow = (static_cast<long long>(f.slot) * 2 + slot) * kBM + r;
         if (!mbar_wait_warp(&c->o_done[par], ph, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
-        uint32_t o[D];
+        // 32 columns at a time out of TMEM: a whole sequence keeps bf16
+        // pairs until O is released; a piece is stored in fp32 at once.
+        uint32_t w[D / 2];
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch)
-          tmem_ld32(tbase + lane_base + C::colO(par) + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32 * ch));
-        tmem_wait_ld();
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tbase + lane_base + C::colO(par) + ch * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
+          if (whole) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[16 * ch + i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+          } else if (store) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_global_v8(p.part_o + prow * D + 32 * ch + 8 * q, o + 8 * q);
+          }
+        }
         tc_fence_before();
         mbar_arrive(&c->o_free[par]);
         ++gseg;
-        const float inv_l = ml.y > 0.f ? 1.f / ml.y : 0.f;
-        const bool whole = seg_j0 == 0 && sg.j == sg.nts - 1;
-        if (r < p.Lq) {
+        if (store) {
           if (whole) {
             __nv_bfloat16* orow = p.out + ((static_cast<long long>(sg.b) * p.Lq + r) * p.H + f.h) * D;
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t w[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                w[i] = pack_bf16x2(__uint_as_float(o[32 * ch + 2 * i]) * inv_l,
-                                   __uint_as_float(o[32 * ch + 2 * i + 1]) * inv_l);
-              st_global_64B(orow + ch * 32, w);
-            }
+            for (int ch = 0; ch < D / 32; ++ch) st_global_64B(orow + ch * 32, w + 16 * ch);
             p.lse[(static_cast<long long>(sg.b) * p.H + f.h) * p.Lq + r] =
-                ml.y > 0.f ? (ml.x + lg2_approx(ml.y)) * kLn2 : -INFINITY;
+                l > 0.f ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
           } else {
-            const int slot = seg_j0 > 0 ? 0 : 1;
-            const long long prow = (static_cast<long long>(f.slot) * 2 + slot) * kBM + r;
-            float* dst = p.part_o + prow * D;
-#pragma unroll
-            for (int i = 0; i < D; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
-#pragma unroll
-            for (int q = 0; q < D / 8; ++q) st_global_v8(dst + 8 * q, o + 8 * q);
-            p.part_lse[prow] = ml.y > 0.f ? ml.x + lg2_approx(ml.y) : -INFINITY;
+            p.part_lse[prow] = l > 0.f ? m + lg2_approx(l) : -INFINITY;
           }
         }
       }
@@ -456,10 +484,11 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FsRoles<D>::kThreads, 1)
     fwd_bs_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
   using C = FsCfg<D>;
+  using R = FsRoles<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   FsCtl* c = reinterpret_cast<FsCtl*>(smem + C::kCtl);
   const int warp = warp_id(), lane = lane_id();
@@ -478,27 +507,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c->v_full[i], 1);
       mbar_init(&c->v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&c->s_full[i], 1);
-      mbar_init(&c->p_full[i], kBM);
+      mbar_init(&c->p_full[i], R::kSoftmax);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&c->o_ready[i], 1);
       mbar_init(&c->o_done[i], 1);
       mbar_init(&c->o_free[i], kBM);
-      mbar_init(&c->seg_full[i], kBM);
+      mbar_init(&c->seg_full[i], R::kSoftmax);
       mbar_init(&c->seg_empty[i], kBM);
+      mbar_init(&c->xbar[i], R::kSoftmax);
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], 9);  // 4 softmax + 4 epilogue warps + the MMA warp
+      mbar_init(&c->item_empty[i], R::kEpiWarp + 5);  // softmax + epilogue warps + the MMA warp
     }
     mbar_init(&c->drain, 1);
     c->abort = 0;
     fence_barrier_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
+  if (warp == R::kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
   }
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc(&c->tmem_base, 512);
     tmem_relinquish();
   }
@@ -506,11 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
-  if (warp < 4) {
+  if (warp < R::kEpiWarp) {
     softmax_role<D>(p, smem, c, tbase);
-  } else if (warp < 8) {
+  } else if (warp < R::kEpiWarp + 4) {
     epilogue_role<D>(p, smem, c, tbase);
-  } else if (warp == kProducerWarp) {
+  } else if (warp == R::kProducerWarp) {
     if (lane == 0) producer_role<D>(&tq, &tk, &tv, p, smem, c);
   } else {
     mma_role<D>(p, smem, c, tbase);
@@ -518,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -606,7 +638,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = fwd_bs_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, p);
+  kern<<<grid, FsRoles<D>::kThreads, C::kSmem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,13 @@ namespace jfa {
 #ifndef JFA_WAIT_LIMIT_CYCLES
 #define JFA_WAIT_LIMIT_CYCLES (4000000000LL)  // about 2 s at 2 GHz
 #endif
+// Limit of the waits between the roles of a kernel (mbar_wait,
+// mbar_wait_warp).  The drain waits before a CTA exits keep
+// JFA_WAIT_LIMIT_CYCLES, so a build with a short role limit still lets every
+// copy and product it issued land (the timeout test builds such a copy).
+#ifndef JFA_ROLE_WAIT_LIMIT_CYCLES
+#define JFA_ROLE_WAIT_LIMIT_CYCLES JFA_WAIT_LIMIT_CYCLES
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -67,7 +74,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > JFA_WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > JFA_ROLE_WAIT_LIMIT_CYCLES) {
       *abort = 1;
       atomicOr(err, kErrTimeout);
       return false;
@@ -88,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
     if ((threadIdx.x & 31) == 0) {
       if (*abort) {
         give_up = 1;
-      } else if (clock64() - t0 > JFA_WAIT_LIMIT_CYCLES) {
+      } else if (clock64() - t0 > JFA_ROLE_WAIT_LIMIT_CYCLES) {
         *abort = 1;
         atomicOr(err, kErrTimeout);
         give_up = 1;
@@ -240,6 +247,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
