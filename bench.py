@@ -60,6 +60,8 @@ KERNEL_DESC = {
     "bwd_q": "self-attention backward dQ pass (S, dP, dQ += dS K)",
     "bwd_qb": "broadcast-Q backward dQ pass (S, dP, dQ += dS K over key-tile chunks)",
     "finalize": "broadcast-Q dQ: sum of the chunk partials, bf16",
+    "bwd_bs": "broadcast-Q backward in one pass (short dense Q): dK, dV and dQ partials",
+    "fwd_combine": "broadcast-Q forward: merge of split sequences",
 }
 
 
@@ -85,6 +87,9 @@ def kernel_model(x):
     if bq:
         m["bwd_qb"] = (6.0 * H * D * pairs, (2 * T + qrows + orows) * row + stat + 4 * Lq * H * D)
         m["finalize"] = (0.0, 6 * Lq * H * D)
+        # one-pass backward of a short dense Q: Q, K, V, dO read, dK, dV written once
+        m["bwd_bs"] = (10.0 * H * D * pairs, (4 * T + qrows + orows) * row + stat + 4 * Lq * H * D)
+        m["fwd_combine"] = (0.0, 0.0)
     else:
         m["bwd_q"] = (6.0 * H * D * pairs, (4 * T) * row + stat + T * row)
     return m
@@ -117,7 +122,8 @@ def _roof(flops, nbytes, seconds, peak_tf, hbm_gbs):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu"], "bwd_kv": ["bwd_kv.cu"], "bwd_q": ["bwd_q.cu"], "bwd_qb": ["bwd_qb.cu"],
-    "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"],
+    "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"], "bwd_bs": ["bwd_bs.cu"],
+    "fwd_combine": ["fwd_bs.cu"],
 }
 
 

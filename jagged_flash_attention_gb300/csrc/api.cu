@@ -325,7 +325,9 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
     fp.items = items;
     fp.hdr = hdr;
     fp.err = ds->err;
-    const int grid = (int)std::min<long long>(ds->sms, cap);
+    // One CTA per possible item: the forward takes work by cancelling CTAs
+    // that have not started (cluster launch control).
+    const int grid = (int)cap;
     e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
       return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
     });
@@ -930,7 +932,7 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   fp.items = items;
   fp.hdr = hdr;
   fp.err = d->err;
-  const int grid = (int)std::min<long long>(d->sms, cap);
+  const int grid = (int)cap;  // one CTA per possible item (cluster launch control)
   e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
     return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
   });

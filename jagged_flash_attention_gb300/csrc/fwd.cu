@@ -15,7 +15,12 @@
 //   warps 0-3, 4-7  softmax / correction / epilogue of query tile 0 and 1;
 //                   thread r owns row r of its tile (TMEM lane r)
 //   warp 8          TMA producer (the two Q tiles once per item, K and V
-//                   tiles into rings) and the dynamic work ticket
+//                   tiles into rings) and the work scheduling: the grid has
+//                   one CTA per possible item; a CTA takes its own item, then
+//                   the items of CTAs that have not started, cancelled through
+//                   Cluster Launch Control (the TLX page, section 2.2,
+//                   "Scheduling jagged tiles across SMs": CLC work stealing
+//                   over the precomputed longest-first list)
 //   warp 9          TMEM allocation and the tcgen05 issuer (the whole warp
 //                   waits; an elect.sync lane issues)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them.  P_t
@@ -81,6 +86,8 @@ struct FwdCtl {
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   FwdItem item[2];  // decoded by the producer; b < 0: no more items
+  uint64_t clc_bar;    // completion of the cluster-launch-control request in flight
+  uint4 clc_resp;      // its 16-byte response
   uint32_t tmem_base;
   int abort;
 };
@@ -162,18 +169,46 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   const int T = p.hdr->T;
   uint32_t itq = 0, nk = 0, nv = 0;
   bool ok = true;
+  // Items: this CTA's own index, then the indices of cancelled CTAs.  One
+  // request stays in flight while an item runs; after a request finds no CTA
+  // left, none is issued again.  Indices past the list (the host sizes the
+  // grid by the list's upper bound) only cancel further CTAs.
+  uint32_t nclc = 0;     // requests completed
+  bool pending = false;  // a request in flight
+  auto clc_issue = [&]() {
+    mbar_arrive_expect_tx(&c->clc_bar, 16);
+    clc_try_cancel(&c->clc_resp, &c->clc_bar);
+    pending = true;
+  };
+  auto clc_take = [&]() {
+    if (!pending) return -1;
+    pending = false;
+    if (!mbar_wait(&c->clc_bar, nclc & 1, &c->abort, p.err)) {
+      drain_wait(&c->clc_bar, nclc & 1, p.err);  // the response still lands in shared memory
+      ok = false;
+      return -1;
+    }
+    ++nclc;
+    int x;
+    if (!clc_query(&c->clc_resp, &x)) return -1;
+    clc_issue();
+    return x;
+  };
+  int idx = blockIdx.x;
+  clc_issue();
   for (uint32_t n = 0; ok; ++n) {
     const int slot = n & 1;
     if (!mbar_wait(&c->item_empty[slot], ((n >> 1) & 1) ^ 1, &c->abort, p.err)) break;
-    const int idx = atomicAdd(&p.hdr->ticket, 1);
+    while (idx >= n_items && ok) idx = clc_take();
     FwdItem f;
-    if (idx < n_items)
+    if (idx >= 0 && ok)
       f = decode<BCAST, CAUSAL>(p, idx, T);
     else
       f.b = -1;
     c->item[slot] = f;
     mbar_arrive(&c->item_full[slot]);
-    if (idx >= n_items) break;
+    if (f.b < 0) break;
+    idx = n_items;  // taken: the next index comes from the request in flight
     if (f.N == 0) continue;
     if (!mbar_wait(&c->q_empty, (itq & 1) ^ 1, &c->abort, p.err)) break;
     const int ntl = (f.t[0].n_kv > 0 ? 1 : 0) + (f.t[1].n_kv > 0 ? 1 : 0);
@@ -220,7 +255,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
     }
   }
-  // Drain: make sure every copy this CTA issued has landed before exit.
+  // Drain: every copy and request this CTA issued has landed before exit.
+  if (pending) drain_wait(&c->clc_bar, nclc & 1, p.err);
   if (itq > 0) drain_wait(&c->q_full, (itq - 1) & 1, p.err);
   for (uint32_t g = nk > C::NSK ? nk - C::NSK : 0; g < nk; ++g)
     for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->k_full[g % C::NSK][s], (g / C::NSK) & 1, p.err);
@@ -520,6 +556,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&c->item_empty[i], 9);  // 8 softmax warps + the MMA thread
     }
     mbar_init(&c->drain, 1);
+    mbar_init(&c->clc_bar, 1);
     c->abort = 0;
     fence_barrier_init();
   }

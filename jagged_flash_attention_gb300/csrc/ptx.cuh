@@ -292,6 +292,38 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ----------------------------------------------- cluster launch control
+
+// Asks the hardware to cancel a CTA of this grid that has not started yet; the
+// 16-byte response lands in shared memory at `resp` and completes 16 bytes
+// of transaction count on `bar` (arm it with mbar_arrive_expect_tx first).
+// Cluster size 1, no multicast.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_addr(resp)),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Reads a completed response: true and the x index of the cancelled CTA if
+// the request cancelled one, false if no CTA was left to cancel.
+__device__ __forceinline__ bool clc_query(const void* resp, int* ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+      "@!p mov.u32 %1, 0;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_addr(resp))
+      : "memory");
+  *ctaid_x = static_cast<int>(x);
+  return ok != 0;
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 form) for a 128-byte-swizzled
