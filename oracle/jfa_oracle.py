@@ -36,6 +36,16 @@ Readings where the pages are silent (each listed in the design notes):
   counted from the start of their sequence.
 * A sequence of length 0 contributes no rows in self-attention; in broadcast
   mode it yields O = 0, LSE = -inf and no dQ contribution.
+* GQA ("Optimizing Jagged Flash Attention with TLX", sections 3 and 4 name
+  it as a supported variant without defining it): k and v carry H_kv heads
+  with H_kv dividing the H query heads; query head h reads K/V head
+  h // (H / H_kv), consecutive query heads sharing one K/V head, and dK / dV
+  of a K/V head sum the contributions of its H / H_kv query heads.
+* Sliding window (same sections, also undefined there): window = (wl, wr)
+  keeps key j for query i iff i - wl <= j <= i + wr, positions counted from
+  the start of the sequence; None (or a negative value) leaves that side
+  unbounded.  Causal is the right bound wr = 0; windows apply to
+  self-attention only, as causal masking does.
 
 Parity pins (tests/test_oracle_pins.py): closed forms (length 1, constant V,
 a hand-derived two-key example in tests/golden), row-stochasticity, LSE by a
@@ -65,17 +75,32 @@ def _seq_bounds(offsets):
     return off
 
 
-def _scores(qc, kb, scale, causal, row0):
+def _window(causal, window):
+    """(wl, wr) with None for an unbounded side; causal bounds wr by 0."""
+    wl, wr = (None, None) if window is None else window
+    wl = None if wl is None or wl < 0 else int(wl)
+    wr = None if wr is None or wr < 0 else int(wr)
+    if causal:
+        wr = 0 if wr is None else min(wr, 0)
+    return wl, wr
+
+
+def _scores(qc, kb, scale, causal, row0, window=None):
     """Scaled scores of query rows [row0, row0+len(qc)) against all keys.
 
     Causal masking follows "cuTile Kernels - FMHA Implementation",
-    "Attention Basics": future keys (j > i) get -inf before the softmax.
+    "Attention Basics": future keys (j > i) get -inf before the softmax.  A
+    sliding window (wl, wr) also gives -inf to keys j < i - wl or j > i + wr.
     """
     s = scale * (qc @ kb.T)
-    if causal:
+    wl, wr = _window(causal, window)
+    if wl is not None or wr is not None:
         i = np.arange(row0, row0 + qc.shape[0])[:, None]
         j = np.arange(kb.shape[0])[None, :]
-        s = np.where(j > i, -np.inf, s)
+        if wr is not None:
+            s = np.where(j > i + wr, -np.inf, s)
+        if wl is not None:
+            s = np.where(j < i - wl, -np.inf, s)
     return s
 
 
@@ -103,40 +128,60 @@ def _grad_scores(p, dp):
     return p * (dp - delta[:, None])
 
 
-def _pairs(B, H, seqs, heads):
+def _pairs(B, H, seqs, heads, group=1):
+    """(sequence, query head) pairs to compute.  A sampled head brings in
+    every query head of its K/V head's group, so that sampled dK / dV hold
+    the whole sum."""
     bs = range(B) if seqs is None else seqs
-    hs = range(H) if heads is None else heads
+    if heads is None:
+        hs = range(H)
+    else:
+        hs = sorted({g * group + i for h in heads for g in [h // group] for i in range(group)})
     return [(b, h) for b in bs for h in hs]
 
 
+def _heads(q, k, broadcast_q):
+    """(H, H_kv, group): query heads, K/V heads, query heads per K/V head."""
+    H, Hkv = q.shape[1], k.shape[1]
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError("the K/V head count must divide the query head count")
+    return H, Hkv, H // Hkv
+
+
+def _check_mask_args(broadcast_q, causal, window):
+    if broadcast_q and (causal or _window(False, window) != (None, None)):
+        raise ValueError("causal and window masks are defined for self-attention only")
+
+
 def forward(q, k, v, offsets, scale, causal=False, broadcast_q=False,
-            seqs=None, heads=None):
+            seqs=None, heads=None, window=None):
     """Attention forward over packed sequences.
 
-    Returns (out, lse) in the layouts given in the module docstring.  With
-    `seqs` / `heads` only those (sequence, head) pairs are computed; the other
+    Returns (out, lse) in the layouts given in the module docstring, with H
+    query heads (k and v may carry fewer, see GQA above).  With `seqs` /
+    `heads` only those (sequence, head) pairs are computed; the other
     entries are NaN (used to sample outputs of large workloads).
     """
     q, k, v = _as64(q), _as64(k), _as64(v)
     off = _seq_bounds(offsets)
     B = off.size - 1
-    T, H, D = k.shape
+    T, Hkv, D = k.shape
+    H, Hkv, group = _heads(q, k, broadcast_q)
     if v.shape != k.shape or off[-1] != T:
-        raise ValueError("k, v must be [T, H, D] with T = offsets[B]")
-    if broadcast_q and causal:
-        raise ValueError("causal masking is defined for self-attention only")
+        raise ValueError("k, v must be [T, H_kv, D] with T = offsets[B]")
+    _check_mask_args(broadcast_q, causal, window)
     if broadcast_q:
         Lq = q.shape[0]
         out = np.full((B, Lq, H, D), np.nan)
         lse = np.full((B, H, Lq), np.nan)
     else:
-        if q.shape != k.shape:
+        if q.shape != (T, H, D):
             raise ValueError("self-attention q must be [T, H, D]")
         out = np.full((T, H, D), np.nan)
         lse = np.full((H, T), np.nan)
-    for b, h in _pairs(B, H, seqs, heads):
+    for b, h in _pairs(B, H, seqs, heads, group):
         s0, s1 = int(off[b]), int(off[b + 1])
-        kb, vb = k[s0:s1, h, :], v[s0:s1, h, :]
+        kb, vb = k[s0:s1, h // group, :], v[s0:s1, h // group, :]
         qb = q[:, h, :] if broadcast_q else q[s0:s1, h, :]
         nq = qb.shape[0]
         ob = np.zeros((nq, D))
@@ -144,7 +189,7 @@ def forward(q, k, v, offsets, scale, causal=False, broadcast_q=False,
         if s1 > s0:
             for r0 in range(0, nq, ROW_CHUNK):
                 r1 = min(nq, r0 + ROW_CHUNK)
-                s = _scores(qb[r0:r1], kb, scale, causal, r0)
+                s = _scores(qb[r0:r1], kb, scale, causal, r0, window)
                 l = _lse_rows(s)
                 ob[r0:r1] = _probs(s, l) @ vb
                 lb[r0:r1] = l
@@ -158,33 +203,39 @@ def forward(q, k, v, offsets, scale, causal=False, broadcast_q=False,
 
 
 def backward(q, k, v, offsets, dout, scale, causal=False, broadcast_q=False,
-             seqs=None, heads=None):
+             seqs=None, heads=None, window=None):
     """Gradients (dq, dk, dv) of sum(out * dout) for the forward above.
 
     In broadcast-Q mode dq is the sum over all sequences of the per-sequence
     dQ_b, as the TLX JFA page (section 1) describes; sampling with `seqs`
-    then sums only the sampled sequences.  Entries of unsampled pairs are NaN
-    in dk / dv (and in dq for self-attention).
+    then sums only the sampled sequences.  With GQA, dk / dv of a K/V head
+    sum over the query heads of its group.  Entries of unsampled pairs are
+    NaN in dk / dv (and in dq for self-attention).
     """
     q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
     off = _seq_bounds(offsets)
     B = off.size - 1
-    T, H, D = k.shape
-    if broadcast_q and causal:
-        raise ValueError("causal masking is defined for self-attention only")
-    dk = np.full((T, H, D), np.nan)
-    dv = np.full((T, H, D), np.nan)
+    T, Hkv, D = k.shape
+    H, Hkv, group = _heads(q, k, broadcast_q)
+    _check_mask_args(broadcast_q, causal, window)
+    pairs = _pairs(B, H, seqs, heads, group)
+    dk = np.full((T, Hkv, D), np.nan)
+    dv = np.full((T, Hkv, D), np.nan)
+    for b, h in pairs:
+        s0, s1 = int(off[b]), int(off[b + 1])
+        dk[s0:s1, h // group, :] = 0.0
+        dv[s0:s1, h // group, :] = 0.0
     if broadcast_q:
         dq = np.zeros_like(q)
         if heads is not None:
             dq[:] = np.nan
-            for h in heads:
+            for h in sorted({h for _, h in pairs}):
                 dq[:, h, :] = 0.0
     else:
         dq = np.full((T, H, D), np.nan)
-    for b, h in _pairs(B, H, seqs, heads):
+    for b, h in pairs:
         s0, s1 = int(off[b]), int(off[b + 1])
-        kb, vb = k[s0:s1, h, :], v[s0:s1, h, :]
+        kb, vb = k[s0:s1, h // group, :], v[s0:s1, h // group, :]
         if broadcast_q:
             qb, dob = q[:, h, :], dout[b, :, h, :]
         else:
@@ -196,7 +247,7 @@ def backward(q, k, v, offsets, dout, scale, causal=False, broadcast_q=False,
         if s1 > s0:
             for r0 in range(0, nq, ROW_CHUNK):
                 r1 = min(nq, r0 + ROW_CHUNK)
-                s = _scores(qb[r0:r1], kb, scale, causal, r0)
+                s = _scores(qb[r0:r1], kb, scale, causal, r0, window)
                 p = _probs(s, _lse_rows(s))
                 dp = dob[r0:r1] @ vb.T
                 ds = _grad_scores(p, dp)
@@ -207,8 +258,8 @@ def backward(q, k, v, offsets, dout, scale, causal=False, broadcast_q=False,
             dq[:, h, :] += dqb
         else:
             dq[s0:s1, h, :] = dqb
-        dk[s0:s1, h, :] = dkb
-        dv[s0:s1, h, :] = dvb
+        dk[s0:s1, h // group, :] += dkb
+        dv[s0:s1, h // group, :] += dvb
     return dq, dk, dv
 
 

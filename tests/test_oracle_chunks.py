@@ -119,8 +119,8 @@ def test_planted_row0_slip_is_caught(monkeypatch):
     """Score blocks always told they start at row 0 (the causal offset lost)."""
     orig = jfa_oracle._scores
 
-    def mutant(qc, kb, scale, causal, row0):
-        return orig(qc, kb, scale, causal, 0)
+    def mutant(qc, kb, scale, causal, row0, window=None):
+        return orig(qc, kb, scale, causal, 0, window)
     monkeypatch.setattr(jfa_oracle, "_scores", mutant)
     with pytest.raises(AssertionError):
         _check_self(jfa_oracle, True, 7, monkeypatch)

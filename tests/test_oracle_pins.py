@@ -326,11 +326,11 @@ def test_sampling_matches_full():
 
 # -------------------------------------------- planted mistakes are caught
 
-def _mutant_scores_no_scale(qc, kb, scale, causal, row0):
-    return _orig_scores(qc, kb, 1.0, causal, row0)
+def _mutant_scores_no_scale(qc, kb, scale, causal, row0, window=None):
+    return _orig_scores(qc, kb, 1.0, causal, row0, window)
 
 
-def _mutant_scores_flipped_causal(qc, kb, scale, causal, row0):
+def _mutant_scores_flipped_causal(qc, kb, scale, causal, row0, window=None):
     s = scale * (qc @ kb.T)
     if causal:
         i = np.arange(row0, row0 + qc.shape[0])[:, None]
