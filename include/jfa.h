@@ -61,7 +61,7 @@ extern "C" {
 typedef enum {
   JFA_OK = 0,
   JFA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or offsets */
-  JFA_ERR_UNSUPPORTED = 2, /* D not in {64,128}; causal with broadcast_q */
+  JFA_ERR_UNSUPPORTED = 2, /* D not in {64,128}; causal or a window with broadcast_q */
   JFA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
   JFA_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out */
   JFA_ERR_WORKSPACE = 5    /* scratch allocation failed */
@@ -101,6 +101,35 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
                       int H, int D, int max_len, int q_len, int broadcast_q, int causal,
                       float scale, const void* out, const float* lse, const void* dout, void* dq,
                       void* dk, void* dv, cudaStream_t stream);
+
+/* The attention variants that "Optimizing Jagged Flash Attention with TLX"
+ * (sections 3 and 4) names as supported by its kernels without defining
+ * them: GQA and sliding windows.  Same arguments as jfa_fwd_bq / jfa_bwd_bq
+ * plus:
+ * - H_kv: heads of k, v, dk, dv (H_kv divides H).  Layouts as above with
+ *   H_kv in place of H for k, v, dk, dv ([T, H_kv, D]); q, dq, out, dout and
+ *   lse keep H query heads.  Query head h reads K/V head h / (H / H_kv), so
+ *   consecutive query heads share one K/V head; dk and dv of a K/V head sum
+ *   over its H / H_kv query heads.  H_kv = H is multi-head attention.
+ * - window_left, window_right: query i attends to key j iff
+ *   i - window_left <= j <= i + window_right, positions counted from the
+ *   start of their sequence; -1 leaves that side unbounded (both -1: no
+ *   window).  causal = 1 is window_right = 0 (a window_right > 0 with causal
+ *   is JFA_ERR_INVALID_ARG).  Windows are self-attention only
+ *   (JFA_ERR_UNSUPPORTED with broadcast_q).  Every query row keeps at least
+ *   its own key.
+ * Key tiles outside a query tile's band are skipped (not loaded, no
+ * products), so the work follows the band's area.  Errors and ownership as
+ * for the other entry points. */
+jfa_status jfa_fwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int H_kv, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      int window_left, int window_right, float scale, void* out, float* lse,
+                      cudaStream_t stream);
+jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int H_kv, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      int window_left, int window_right, float scale, const void* out,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      cudaStream_t stream);
 
 /* Allocation-free forward pass.  The pages have no counterpart: this entry
  * point exists for callers that must not allocate device memory while the

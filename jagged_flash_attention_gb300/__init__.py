@@ -13,8 +13,8 @@ import os
 
 from .build import LIB_PATH
 
-__all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq",
-           "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
+__all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq", "jfa_fwd_ex",
+           "jfa_bwd_ex", "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
            "STATUS"]
 
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_CUDA",
@@ -45,7 +45,10 @@ def lib() -> ctypes.CDLL:
         L.jfa_bwd.argtypes = bwd
         L.jfa_fwd_bq.argtypes = fwd[:8] + [_I] + fwd[8:]
         L.jfa_bwd_bq.argtypes = bwd[:8] + [_I] + bwd[8:]
-        for f in (L.jfa_fwd, L.jfa_bwd, L.jfa_fwd_bq, L.jfa_bwd_bq):
+        # _ex: H_kv after H; window_left, window_right after causal
+        L.jfa_fwd_ex.argtypes = fwd[:6] + [_I] * 8 + fwd[10:]
+        L.jfa_bwd_ex.argtypes = bwd[:6] + [_I] * 8 + bwd[10:]
+        for f in (L.jfa_fwd, L.jfa_bwd, L.jfa_fwd_bq, L.jfa_bwd_bq, L.jfa_fwd_ex, L.jfa_bwd_ex):
             f.restype = _I
         L.jfa_sync_and_check.argtypes = [_P]
         L.jfa_sync_and_check.restype = _I
@@ -110,6 +113,22 @@ def jfa_bwd_bq(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, s
                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
+def jfa_fwd_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, causal,
+               window_left, window_right, scale, out, lse, stream=None):
+    _check(lib().jfa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len,
+                            q_len, int(broadcast_q), int(causal), int(window_left),
+                            int(window_right), float(scale), _ptr(out), _ptr(lse),
+                            _stream(stream)))
+
+
+def jfa_bwd_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, causal,
+               window_left, window_right, scale, out, lse, dout, dq, dk, dv, stream=None):
+    _check(lib().jfa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len,
+                            q_len, int(broadcast_q), int(causal), int(window_left),
+                            int(window_right), float(scale), _ptr(out), _ptr(lse), _ptr(dout),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
+
+
 def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale,
                        out, lse, stream=None):
     """Allocation-free forward (see include/jfa.h): for callers that must not
@@ -165,17 +184,26 @@ def profile_read():
 
 
 def _shapes(q, k, offsets, broadcast_q):
-    T, H, D = k.shape
+    """(B, H query heads, H_kv K/V heads, D, dense Q length or 0)."""
+    T, Hkv, D = k.shape
     B = offsets.numel() - 1
-    return B, H, D, (q.shape[0] if broadcast_q else 0)
+    return B, q.shape[1], Hkv, D, (q.shape[0] if broadcast_q else 0)
+
+
+def _window(window):
+    wl, wr = (-1, -1) if window is None else window
+    return (-1 if wl is None else int(wl)), (-1 if wr is None else int(wr))
 
 
 def forward(q, k, v, offsets, max_len, causal=False, broadcast_q=False, scale=None, out=None,
-            lse=None, stream=None):
+            lse=None, stream=None, window=None):
     """Allocate out / lse with torch and call the C ABI.  Tensors are CUDA
-    tensors in the layouts of include/jfa.h; offsets is int32 [B+1]."""
+    tensors in the layouts of include/jfa.h; offsets is int32 [B+1].  k and
+    v may carry fewer heads than q (GQA); window = (left, right) bounds the
+    keys of query i to [i - left, i + right] (None: unbounded side)."""
     import torch
-    B, H, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    wl, wr = _window(window)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     if out is None:
         out = torch.empty((B, Lq, H, D) if broadcast_q else tuple(q.shape), dtype=q.dtype,
@@ -183,7 +211,10 @@ def forward(q, k, v, offsets, max_len, causal=False, broadcast_q=False, scale=No
     if lse is None:
         lse = torch.empty((B, H, Lq) if broadcast_q else (H, k.shape[0]), dtype=torch.float32,
                           device=q.device)
-    if broadcast_q:
+    if Hkv != H or (wl, wr) != (-1, -1):
+        jfa_fwd_ex(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), causal, wl, wr,
+                   scale, out, lse, stream)
+    elif broadcast_q:
         jfa_fwd_bq(q, k, v, offsets, B, H, D, max_len, Lq, 1, causal, scale, out, lse, stream)
     else:
         jfa_fwd(q, k, v, offsets, B, H, D, max_len, 0, causal, scale, out, lse, stream)
@@ -191,15 +222,20 @@ def forward(q, k, v, offsets, max_len, causal=False, broadcast_q=False, scale=No
 
 
 def backward(q, k, v, offsets, max_len, out, lse, dout, causal=False, broadcast_q=False,
-             scale=None, dq=None, dk=None, dv=None, stream=None):
-    """Allocate dq / dk / dv with torch and call the C ABI."""
+             scale=None, dq=None, dk=None, dv=None, stream=None, window=None):
+    """Allocate dq / dk / dv with torch and call the C ABI (arguments as for
+    forward)."""
     import torch
-    B, H, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    wl, wr = _window(window)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    if broadcast_q:
+    if Hkv != H or (wl, wr) != (-1, -1):
+        jfa_bwd_ex(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), causal, wl, wr,
+                   scale, out, lse, dout, dq, dk, dv, stream)
+    elif broadcast_q:
         jfa_bwd_bq(q, k, v, offsets, B, H, D, max_len, Lq, 1, causal, scale, out, lse, dout,
                    dq, dk, dv, stream)
     else:

@@ -172,9 +172,21 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Shape {
   int B, H, D, max_len, Lq, broadcast, causal;
+  int Hkv, G;       // K/V heads; query heads per K/V head (GQA)
+  int wl, wr;       // window bounds as given (-1: unbounded)
+  int kwl, kwr;     // the kernels' bounds: kNoWindow when unbounded, causal: kwr = 0
+  int local;        // a local mask: causal or a window
   float scale;
   long long Tcap;  // upper bound of T used to size scratch and tensor maps
 };
+
+// GQA group and local mask of a kernel parameter block.
+template <class P>
+void set_variant(P& p, const Shape& s) {
+  p.G = s.G;
+  p.wl = s.kwl;
+  p.wr = s.kwr;
+}
 
 jfa_status check_common(const Shape& s, const void* q, const void* k, const void* v,
                         const int32_t* offsets) {
@@ -188,8 +200,17 @@ jfa_status check_common(const Shape& s, const void* q, const void* k, const void
     return fail(JFA_ERR_INVALID_ARG, "B * max_len must be < 2^31");
   if (!std::isfinite(s.scale) || !(s.scale > 0.f))
     return fail(JFA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (s.Hkv < 1 || s.Hkv > s.H || s.H % s.Hkv != 0)
+    return fail(JFA_ERR_INVALID_ARG, "H_kv must divide H (got H = %d, H_kv = %d)", s.H, s.Hkv);
+  if (s.wl < -1 || s.wr < -1)
+    return fail(JFA_ERR_INVALID_ARG, "window bounds must be >= -1 (-1: unbounded)");
+  if (s.causal && s.wr > 0)
+    return fail(JFA_ERR_INVALID_ARG, "causal masking bounds the window's right side by 0 (got %d)",
+                s.wr);
   if (s.broadcast && s.causal)
     return fail(JFA_ERR_UNSUPPORTED, "causal masking is supported for self-attention only");
+  if (s.broadcast && (s.wl >= 0 || s.wr >= 0))
+    return fail(JFA_ERR_UNSUPPORTED, "sliding windows are supported for self-attention only");
   if (s.broadcast && s.Lq < 1) return fail(JFA_ERR_INVALID_ARG, "q_len must be >= 1 in broadcast mode");
   if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 3u))
     return fail(JFA_ERR_INVALID_ARG, "offsets must be a non-null, 4-byte aligned device pointer");
@@ -232,8 +253,8 @@ jfa_status do_fwd_bs(DeviceState* ds, const Shape& s, const void* q, const void*
   off = align256(off + (size_t)cap * 2 * kBM * sizeof(float));
   CUtensorMap tq, tk, tv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q")) != JFA_OK) return st;
-  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
-  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -259,6 +280,7 @@ jfa_status do_fwd_bs(DeviceState* ds, const Shape& s, const void* q, const void*
   fp.kt_off = kt_off;
   fp.part_o = reinterpret_cast<float*>(base + parto_off);
   fp.part_lse = reinterpret_cast<float*>(base + partl_off);
+  set_variant(fp, s);
   if (e == cudaSuccess)
     e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
       return launch_fwd_bs(s.D, tq, tk, tv, fp, (int)std::min<long long>(ds->sms, cap), stream);
@@ -300,21 +322,23 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
   const size_t bytes = align256(items_off + cap * sizeof(Item));
   CUtensorMap tq, tk, tv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
-  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
-  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   void* scratch = nullptr;
   e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
   uint8_t* base = static_cast<uint8_t*>(scratch);
   WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
   Item* items = reinterpret_cast<Item*>(base + items_off);
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, s.broadcast, 0, kFwdRows,
-                 items, (int)cap, hdr, ds->err};
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.local, s.broadcast, 0, kFwdRows,
+                 items, (int)cap, hdr, ds->err, s.kwl, s.kwr};
   e = run_kernel(JFA_KERNEL_SCHED, stream, [&] {
     return launch_sched(sp, stream);
   });
   if (e == cudaSuccess) {
     FwdParams fp;
+    memset(&fp, 0, sizeof(fp));
+    set_variant(fp, s);
     fp.offsets = offsets;
     fp.B = s.B;
     fp.H = s.H;
@@ -329,7 +353,7 @@ jfa_status do_fwd(const Shape& s, const void* q, const void* k, const void* v,
     // that have not started (cluster launch control).
     const int grid = (int)cap;
     e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
-      return launch_fwd(s.D, s.causal, s.broadcast, tq, tk, tv, fp, grid, stream);
+      return launch_fwd(s.D, s.local, s.broadcast, tq, tk, tv, fp, grid, stream);
     });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
@@ -345,7 +369,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
                        const void* v, const int32_t* offsets, const void* out, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, cudaStream_t stream) {
   jfa_status st;
-  const long long cap_kv = (long long)s.H * s.B * cdivll(s.max_len, kBN);
+  const long long cap_kv = (long long)s.Hkv * s.B * cdivll(s.max_len, kBN);
   const long long cap_q = (long long)s.H * s.B * cdivll(s.max_len, kFwdRows);
   if (cap_kv >= (1LL << 31) || cap_q >= (1LL << 31))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
@@ -359,12 +383,12 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   off = align256(off + kStatCopies * stat_stride * sizeof(float));
   CUtensorMap tq, tk, tv, tdo;
   if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
-  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
-  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   if ((st = map_rows(&tdo, dout, s.D, s.H, s.Tcap, "dout")) != JFA_OK) return st;
   CUtensorMap tdk, tdv;
-  if ((st = map_rows(&tdk, dk, s.D, s.H, s.Tcap, "dk")) != JFA_OK) return st;
-  if ((st = map_rows(&tdv, dv, s.D, s.H, s.Tcap, "dv")) != JFA_OK) return st;
+  if ((st = map_rows(&tdk, dk, s.D, s.Hkv, s.Tcap, "dk")) != JFA_OK) return st;
+  if ((st = map_rows(&tdv, dv, s.D, s.Hkv, s.Tcap, "dv")) != JFA_OK) return st;
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -374,12 +398,15 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   WorkHeader* hdr_q = reinterpret_cast<WorkHeader*>(base + hq_off);
   Item* items_q = reinterpret_cast<Item*>(base + hq_off + 256);
   float* stat = reinterpret_cast<float*>(base + stat_off);
-  SchedParams sk{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 1, kBM,
-                 items_kv, (int)cap_kv, hdr_kv, ds->err};
-  SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.causal, 0, 0, kFwdRows,
-                 items_q, (int)cap_q, hdr_q, ds->err};
+  // dK/dV items over the K/V heads, dQ items over the query heads
+  SchedParams sk{offsets, s.B, s.Hkv, s.Lq, s.max_len, s.local, 0, 1, kBM,
+                 items_kv, (int)cap_kv, hdr_kv, ds->err, s.kwl, s.kwr};
+  SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.local, 0, 0, kFwdRows,
+                 items_q, (int)cap_q, hdr_q, ds->err, s.kwl, s.kwr};
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));
+  set_variant(bp, s);
+  bp.Hkv = s.Hkv;
   bp.offsets = offsets;
   bp.B = s.B;
   bp.H = s.H;
@@ -418,7 +445,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     bp.items = items_kv;
     bp.hdr = hdr_kv;
     e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
-      return launch_bwd_kv(s.D, s.causal, false, tq, tk, tv, tdo, tdk, tdv, bp,
+      return launch_bwd_kv(s.D, s.local, false, tq, tk, tv, tdo, tdk, tdv, bp,
                            (int)std::min<long long>(ds->sms, cap_kv), stream);
     });
   }
@@ -427,7 +454,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
     bp.hdr = hdr_q;
     e = run_kernel(JFA_KERNEL_BWD_Q, stream, [&] {
       return launch_bwd_q(
-          s.D, s.causal, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_q), stream);
+          s.D, s.local, tq, tk, tv, tdo, bp, (int)std::min<long long>(ds->sms, cap_q), stream);
     });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);
@@ -447,7 +474,7 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
                         const void* v, const int32_t* offsets, const void* out, const float* lse,
                         const void* dout, void* dq, void* dk, void* dv, cudaStream_t stream) {
   jfa_status st;
-  const long long cap_kv = (long long)s.H * s.B * cdivll(s.max_len, kBN);
+  const long long cap_kv = (long long)s.Hkv * s.B * cdivll(s.max_len, kBN);
   const long long pairs = cdivll(s.Lq, kQbRows);
   // chunks per (head, pair): about two items per SM in all
   const long long chunk_cap = std::max<long long>(1, cdivll(2LL * ds->sms, s.H * pairs));
@@ -455,8 +482,10 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   const long long lq_pad = cdivll(s.Lq, kBM) * kBM;
   if (cap_kv >= (1LL << 31) || (long long)s.B * s.H * lq_pad >= (1LL << 40))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
-  // A short dense Q (one tile, D = 64): dK, dV and dQ in one pass over K / V.
-  const bool one_pass = bwd_bs_supported(s.D, s.Lq);
+  // A short dense Q (one tile, D = 64): dK, dV and dQ in one pass over K / V
+  // (one query head per K/V head: with GQA, dK / dV sum over several query
+  // heads, which the two-pass path does in its dK/dV pass).
+  const bool one_pass = bwd_bs_supported(s.D, s.Lq) && s.G == 1;
   size_t off = 0;
   const size_t hkv_off = off;
   off = align256(off + 256 + (one_pass ? 0 : cap_kv) * sizeof(Item));
@@ -470,11 +499,11 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   off = align256(off + (size_t)cap_qb * 2 * kBM * s.D * sizeof(float));
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q")) != JFA_OK) return st;
-  if ((st = map_rows(&tk, k, s.D, s.H, s.Tcap, "k")) != JFA_OK) return st;
-  if ((st = map_rows(&tv, v, s.D, s.H, s.Tcap, "v")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   if ((st = map_bq(&tdo, dout, s.D, s.H, s.Lq, s.B, "dout")) != JFA_OK) return st;
-  if ((st = map_rows(&tdk, dk, s.D, s.H, s.Tcap, "dk")) != JFA_OK) return st;
-  if ((st = map_rows(&tdv, dv, s.D, s.H, s.Tcap, "dv")) != JFA_OK) return st;
+  if ((st = map_rows(&tdk, dk, s.D, s.Hkv, s.Tcap, "dk")) != JFA_OK) return st;
+  if ((st = map_rows(&tdv, dv, s.D, s.Hkv, s.Tcap, "dv")) != JFA_OK) return st;
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -501,7 +530,7 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
     pp.broadcast = 1;
     pp.n_sched = one_pass ? 1 : 2;
     pp.qb_only = one_pass ? 1 : 0;
-    pp.sched[0] = SchedParams{offsets, s.B, s.H, s.Lq, s.max_len, 0, 1, 1, kBM,
+    pp.sched[0] = SchedParams{offsets, s.B, s.Hkv, s.Lq, s.max_len, 0, 1, 1, kBM,
                               items_kv, (int)cap_kv, hdr_kv, ds->err};
     pp.qb = QbSchedParams{offsets, s.B, s.H, s.Lq, s.max_len, (int)chunk_cap, kt_off,
                           items_qb, (int)cap_qb, hdr_qb, ds->err};
@@ -511,6 +540,8 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   }
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));
+  set_variant(bp, s);
+  bp.Hkv = s.Hkv;
   bp.offsets = offsets;
   bp.B = s.B;
   bp.H = s.H;
@@ -595,16 +626,23 @@ jfa_status do_bwd(const Shape& s, const void* q, const void* k, const void* v,
   return do_bwd_bcast(ds, s, q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
 }
 
-Shape make_shape(int B, int H, int D, int max_len, int q_len, int broadcast_q, int causal,
-                 float scale) {
+Shape make_shape(int B, int H, int Hkv, int D, int max_len, int q_len, int broadcast_q,
+                 int causal, int window_left, int window_right, float scale) {
   Shape s;
   s.B = B;
   s.H = H;
+  s.Hkv = Hkv;
+  s.G = (Hkv > 0 && H % Hkv == 0) ? H / Hkv : 1;
   s.D = D;
   s.max_len = max_len;
   s.Lq = broadcast_q ? q_len : 0;
   s.broadcast = broadcast_q ? 1 : 0;
   s.causal = causal ? 1 : 0;
+  s.wl = window_left;
+  s.wr = window_right;
+  s.kwl = window_left >= 0 ? window_left : kNoWindow;
+  s.kwr = s.causal ? 0 : (window_right >= 0 ? window_right : kNoWindow);
+  s.local = (s.causal || window_left >= 0 || window_right >= 0) ? 1 : 0;
   s.scale = scale;
   s.Tcap = (long long)(B > 0 ? B : 0) * (max_len > 0 ? max_len : 0);
   return s;
@@ -621,8 +659,8 @@ jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* o
     return fail(JFA_ERR_INVALID_ARG,
                 "broadcast_q=1 needs the dense Q length: call jfa_fwd_bq with q_len");
   t_last_error.clear();
-  return do_fwd(make_shape(B, H, D, max_len, 0, 0, causal, scale), q, k, v, offsets, out, lse,
-                stream);
+  return do_fwd(make_shape(B, H, H, D, max_len, 0, 0, causal, -1, -1, scale), q, k, v, offsets,
+                out, lse, stream);
 }
 
 jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
@@ -633,16 +671,26 @@ jfa_status jfa_bwd(const void* q, const void* k, const void* v, const int32_t* o
     return fail(JFA_ERR_INVALID_ARG,
                 "broadcast_q=1 needs the dense Q length: call jfa_bwd_bq with q_len");
   t_last_error.clear();
-  return do_bwd(make_shape(B, H, D, max_len, 0, 0, causal, scale), q, k, v, offsets, out, lse,
-                dout, dq, dk, dv, stream);
+  return do_bwd(make_shape(B, H, H, D, max_len, 0, 0, causal, -1, -1, scale), q, k, v, offsets,
+                out, lse, dout, dq, dk, dv, stream);
 }
 
 jfa_status jfa_fwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
                       int H, int D, int max_len, int q_len, int broadcast_q, int causal,
                       float scale, void* out, float* lse, cudaStream_t stream) {
   t_last_error.clear();
-  return do_fwd(make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale), q, k, v, offsets,
-                out, lse, stream);
+  return do_fwd(make_shape(B, H, H, D, max_len, q_len, broadcast_q, causal, -1, -1, scale), q, k,
+                v, offsets, out, lse, stream);
+}
+
+jfa_status jfa_fwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int H_kv, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      int window_left, int window_right, float scale, void* out, float* lse,
+                      cudaStream_t stream) {
+  t_last_error.clear();
+  return do_fwd(make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, causal, window_left,
+                           window_right, scale),
+                q, k, v, offsets, out, lse, stream);
 }
 
 jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
@@ -650,8 +698,19 @@ jfa_status jfa_bwd_bq(const void* q, const void* k, const void* v, const int32_t
                       float scale, const void* out, const float* lse, const void* dout, void* dq,
                       void* dk, void* dv, cudaStream_t stream) {
   t_last_error.clear();
-  return do_bwd(make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale), q, k, v, offsets,
-                out, lse, dout, dq, dk, dv, stream);
+  return do_bwd(make_shape(B, H, H, D, max_len, q_len, broadcast_q, causal, -1, -1, scale), q, k,
+                v, offsets, out, lse, dout, dq, dk, dv, stream);
+}
+
+jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets, int B,
+                      int H, int H_kv, int D, int max_len, int q_len, int broadcast_q, int causal,
+                      int window_left, int window_right, float scale, const void* out,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      cudaStream_t stream) {
+  t_last_error.clear();
+  return do_bwd(make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, causal, window_left,
+                           window_right, scale),
+                q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
 }
 
 jfa_status jfa_worklist(const int32_t* offsets, int B, int H, int max_len, int q_len,
@@ -878,7 +937,7 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
                               int causal, float scale, void* out, float* lse,
                               cudaStream_t stream) {
   t_last_error.clear();
-  const Shape s = make_shape(B, H, D, max_len, q_len, broadcast_q, causal, scale);
+  const Shape s = make_shape(B, H, H, D, max_len, q_len, broadcast_q, causal, -1, -1, scale);
   jfa_status st = check_common(s, q, k, v, offsets);
   if (st != JFA_OK) return st;
   if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
@@ -922,6 +981,8 @@ jfa_status jfa_fwd_bq_noalloc(const void* q, const void* k, const void* v, const
   });
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
   FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  set_variant(fp, s);
   fp.offsets = offsets;
   fp.B = s.B;
   fp.H = s.H;

@@ -30,8 +30,13 @@ __device__ __forceinline__ int n_tiles(const SchedParams& p, int L) {
 // Cost bucket of sequence b: work of its longest item, in tile units.
 //  forward:  key tiles a query tile visits (causal: the last query tile's)
 //  backward: query tiles a key block visits (broadcast: all equal)
+// A sliding window bounds both by the band's width.
 __device__ __forceinline__ int bucket_of(const SchedParams& p, int L) {
   int c = p.backward ? (p.broadcast ? 0 : cdiv(L, kBM)) : cdiv(L, kBN);
+  if (p.causal) {
+    const long long w = static_cast<long long>(p.wl) + p.wr + (p.backward ? kBN : p.qrows);
+    if (w < L) c = min(c, static_cast<int>(w / kBN) + 2);
+  }
   return c < kMaxBuckets ? c : kMaxBuckets - 1;
 }
 

@@ -82,11 +82,14 @@ __device__ __forceinline__ RowBox row_box(int start, int remaining, int T) {
   return r;
 }
 
+// With GQA an item is a block of one K/V head, and its query tiles are the
+// tiles [t0, t0 + ntq) of each of the G query heads that read that K/V head,
+// head-major: tile i is query tile t0 + i % ntq of query head h * G + i / ntq.
 struct KvItem {
-  int b, h, kb;
+  int b, h, kb;  // sequence, K/V head, key block
   int off0, L;
-  RowBox kt;   // keys of this block
-  int t0, nt;  // first query tile and count
+  RowBox kt;        // keys of this block
+  int t0, ntq, nt;  // first query tile, tiles per query head, nt = G * ntq
 };
 
 // One staged output tensor for the store warp: which = 0: dV, 1: dK, -1:
@@ -125,7 +128,7 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ uint32_t pack_col(int k) { return 32 * (k >> 1) + 8 * (k & 1); }
 
 
-template <bool CAUSAL, bool BCAST>
+template <bool LOCAL, bool BCAST>
 __device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
   KvItem f;
   const Item it = p.items[idx];
@@ -137,13 +140,23 @@ __device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
   f.kt = row_box(f.off0 + f.kb * kBN, f.L - f.kb * kBN, T);
   if (BCAST) {
     f.t0 = 0;
-    f.nt = cdiv(p.Lq, kBM);
+    f.ntq = cdiv(p.Lq, kBM);
+  } else if (LOCAL) {  // the query tiles that admit a key of the block
+    const int ka = f.kb * kBN;
+    query_tiles(ka, ka + f.kt.n - 1, f.L, p.wl, p.wr, &f.t0, &f.ntq);
   } else {
-    f.t0 = CAUSAL ? (f.kb * kBN) / kBM : 0;
-    f.nt = cdiv(f.L, kBM) - f.t0;
+    f.t0 = 0;
+    f.ntq = cdiv(f.L, kBM);
   }
+  f.nt = p.G * f.ntq;
   return f;
 }
+
+// Query head and query tile of tile i of item f.
+__device__ __forceinline__ int q_head(const BwdParams& p, const KvItem& f, int i) {
+  return f.h * p.G + i / f.ntq;
+}
+__device__ __forceinline__ int q_tile(const KvItem& f, int i) { return f.t0 + i % f.ntq; }
 
 // Query tile t of item f: self-attention, rows of the sequence (moved back so
 // the box never reads past row T); broadcast, rows of the dense Q.
@@ -159,17 +172,18 @@ __device__ __forceinline__ RowBox q_box(const BwdParams& p, const KvItem& f, int
   return row_box(f.off0 + t * kBM, f.L - t * kBM, T);
 }
 
-// Statistics of the 128 rows of query tile t (1 KB, 32-byte aligned): self,
+// Statistics of the 128 rows of query tile t of query head qh (1 KB,
+// 32-byte aligned): self,
 // the copy in which the box's first row starts a group; broadcast, the
 // sequence's rows in the layout padded to whole tiles.
 template <bool BCAST>
-__device__ __forceinline__ const float* stat_src(const BwdParams& p, const KvItem& f,
+__device__ __forceinline__ const float* stat_src(const BwdParams& p, const KvItem& f, int qh,
                                                  const RowBox& qb, int t, int T) {
   if (BCAST) {
     const long long lq_pad = static_cast<long long>(cdiv(p.Lq, kBM)) * kBM;
-    return p.stat + stat_float((static_cast<long long>(f.b) * p.H + f.h) * lq_pad + t * kBM);
+    return p.stat + stat_float((static_cast<long long>(f.b) * p.H + qh) * lq_pad + t * kBM);
   }
-  const long long sidx = static_cast<long long>(f.h) * T + qb.row;
+  const long long sidx = static_cast<long long>(qh) * T + qb.row;
   const int sk = static_cast<int>((sidx + kStatPad) & 3);
   return p.stat + sk * p.stat_stride + stat_float(stat_pos(sidx, sk));
 }
@@ -200,7 +214,7 @@ __device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool*
   return f->b >= 0;
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tdo, const BwdParams& p, uint8_t* smem,
                               KvCtl* c) {
@@ -215,12 +229,13 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   auto fetch = [&](KvItem& f) {
     const int idx = atomicAdd(&p.hdr->ticket, 1);
     if (idx < n_items)
-      f = decode<CAUSAL, BCAST>(p, idx, T);
+      f = decode<LOCAL, BCAST>(p, idx, T);
     else
       f.b = -1;
   };
   auto prefetch = [&](const KvItem& f) {
     const RowBox qb = q_box<BCAST>(p, f, f.t0, T);
+    const int qh = f.h * p.G;  // the first tile's query head
 #pragma unroll
     for (int s = 0; s < C::kSlabs; ++s) {
       if (f.kt.row >= 0) {
@@ -228,10 +243,10 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         tma_prefetch_l2_3d(tv, s * 64, f.h, f.kt.row);
       }
       if (BCAST) {  // the dense Q stays in L2; the sequence's dO
-        tma_prefetch_l2_4d(tdo, s * 64, f.h, 0, f.b);
+        tma_prefetch_l2_4d(tdo, s * 64, qh, 0, f.b);
       } else if (qb.row >= 0) {
-        tma_prefetch_l2_3d(tq, s * 64, f.h, qb.row);
-        tma_prefetch_l2_3d(tdo, s * 64, f.h, qb.row);
+        tma_prefetch_l2_3d(tq, s * 64, qh, qb.row);
+        tma_prefetch_l2_3d(tdo, s * 64, qh, qb.row);
       }
     }
   };
@@ -265,17 +280,17 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         ok = false;
         break;
       }
-      const int t = f.t0 + i;
+      const int t = q_tile(f, i), qh = q_head(p, f, i);
       const RowBox qb = q_box<BCAST>(p, f, t, T);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
         mbar_arrive_expect_tx(&c->do_full[st][s], 16384);
         if (BCAST)
           tma_load_4d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
-                      f.h, qb.row, f.b);
+                      qh, qb.row, f.b);
         else
           tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
-                      f.h, qb.row);
+                      qh, qb.row);
       }
       ++gdo;  // counted now: a wait below that gives up must not hide these copies from the drain
       if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
@@ -283,13 +298,13 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         break;
       }
       // Row statistics of the box: 32 whole groups (1 KB).
-      const float* ssrc = stat_src<BCAST>(p, f, qb, t, T);
+      const float* ssrc = stat_src<BCAST>(p, f, qh, qb, t, T);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
         mbar_arrive_expect_tx(&c->q_full[st][s], 16384 + (s == 0 ? C::kStatBytes : 0));
         if (s == 0)
           bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->q_full[st][0]);
-        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st][s], s * 64, f.h,
+        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st][s], s * 64, qh,
                     qb.row);
       }
       ++gq;
@@ -321,7 +336,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
@@ -457,7 +472,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   const int r = threadIdx.x & 127;    // TMEM lane = key row of the block
@@ -476,7 +491,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
   // scale*log2e - LSE*log2e), kept as bf16 pairs of this thread's 32 columns.
   auto p_part = [&](const KvItem& f, int i, uint32_t g, uint32_t (&pk)[16]) {
     const int key = f.kb * kBN - f.kt.shift + r;  // local key index of this lane
-    const int t = f.t0 + i;
+    const int t = q_tile(f, i);
     const RowBox qb = q_box<BCAST>(p, f, t, T);
     const int q0 = t * kBM - qb.shift;  // local query index of column 0
     // (already complete once S^T is; waited on here for the statistics'
@@ -484,12 +499,14 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     if (!mbar_wait_warp(&c->q_full[g % C::NSQ][0], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
     const float4* st4 = stats(g);
     // Admissible query columns [lo, hi): the box's rows of the sequence
-    // and, causal, the queries at or after this key.
-    int lo = qb.shift;
-    const int hi = qb.shift + qb.n;
-    if (CAUSAL) lo = max(lo, key - q0);
+    // and, with a local mask, the queries in [key - wr, key + wl].
+    int lo = qb.shift, hi = qb.shift + qb.n;
+    if (LOCAL) {
+      lo = max(lo, key - p.wr - q0);
+      hi = min(hi, key + p.wl - q0 + 1);
+    }
     const bool ragged = qb.shift > 0 || qb.n < kBM;
-    const bool mask = ragged || (CAUSAL && __any_sync(0xffffffffu, lo > cbase));
+    const bool mask = ragged || (LOCAL && __any_sync(0xffffffffu, lo > cbase || hi < cbase + 32));
     const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
     if (!mbar_wait_warp(&c->s_full, g & 1, &c->abort, p.err)) return false;
     tc_fence_after();
@@ -512,7 +529,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         pk[2 * j] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
         pk[2 * j + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
       }
-      if (mask) {  // ragged or causal diagonal tile: zero inadmissible columns
+      if (mask) {  // ragged tile, or one a band edge crosses: zero inadmissible columns
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
           const int col = cbase + 2 * i2;
@@ -651,7 +668,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
                                                       ((ch ^ (row & (kCpr - 1))) * 16));
       if (row >= f.kt.shift && row < f.kt.shift + f.kt.n) {
         const long long tok = f.off0 + f.kb * kBN - f.kt.shift + row;
-        *reinterpret_cast<uint4*>(dst + (tok * p.H + f.h) * D + ch * 8) = v;
+        *reinterpret_cast<uint4*>(dst + (tok * p.Hkv + f.h) * D + ch * 8) = v;
       }
     }
     return true;
@@ -739,7 +756,7 @@ __device__ void store_role(const CUtensorMap* tdk, const CUtensorMap* tdv, uint8
   bulk_wait0();
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -804,13 +821,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
   if (warp < kMathWarps) {
-    math_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+    math_role<D, LOCAL, BCAST>(p, smem, c, tbase);
   } else if (warp == kStoreWarp) {
     if (lane == 0) store_role<D>(&tdk, &tdv, smem, c, p.err);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
+    if (lane == 0) producer_role<D, LOCAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
-    mma_role<D, CAUSAL>(p, smem, c, tbase);
+    mma_role<D, LOCAL>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();
@@ -821,15 +838,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                      const BwdParams& p, int grid, cudaStream_t s) {
   using C = KvCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(KvCtl) <= 512, "control block");
-  static_assert(!(CAUSAL && BCAST), "causal masking is self-attention only");
-  auto kern = bwd_kv_kernel<D, CAUSAL, BCAST>;
+  static_assert(!(LOCAL && BCAST), "causal masking is self-attention only");
+  auto kern = bwd_kv_kernel<D, LOCAL, BCAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p);

@@ -62,12 +62,13 @@ struct QTile {
   int nq;     // valid query rows (<= 0: tile absent)
   int shift;  // rows the box was moved back to stay inside [0, T)
   int row;    // TMA row coordinate
-  int n;      // key tiles this query tile visits (0: absent)
+  int j0;     // first key tile this query tile visits
+  int n;      // key tiles it visits, [j0, j0 + n) (0: absent)
 };
 
 struct QItem {
-  int b, h, off0, L;
-  int N;  // key tiles of the item = max over its two query tiles
+  int b, h, hk, off0, L;  // sequence, query head, K/V head
+  int J0, N;  // key tiles of the item: [J0, J0 + N), the union of its two tiles' ranges
   QTile t[2];
 };
 
@@ -83,15 +84,19 @@ struct QCtl {
   int abort;
 };
 
-template <bool CAUSAL>
+// LOCAL: a local mask (causal or a sliding window, bounds p.wl / p.wr): a
+// query tile visits only the key tiles holding admissible keys of its rows.
+template <bool LOCAL>
 __device__ __forceinline__ QItem decode(const BwdParams& p, int idx, int T) {
   QItem f;
   const Item it = p.items[idx];
   f.b = it.x;
   f.h = it.y >> 16;
+  f.hk = f.h / p.G;
   const int pair = it.y & 0xffff;
   f.off0 = p.offsets[f.b];
   f.L = p.offsets[f.b + 1] - f.off0;
+  int lo = 1 << 30, hi = 0;
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     QTile& q = f.t[g];
@@ -100,9 +105,19 @@ __device__ __forceinline__ QItem decode(const BwdParams& p, int idx, int T) {
     const int start = f.off0 + q.q_lo;
     q.shift = max(0, start + kBM - T);
     q.row = start - q.shift;
-    q.n = q.nq > 0 ? (CAUSAL ? cdiv(q.q_lo + q.nq, kBN) : cdiv(f.L, kBN)) : 0;
+    q.j0 = 0;
+    q.n = 0;
+    if (q.nq > 0) {
+      if (LOCAL)
+        key_tiles(q.q_lo, q.q_lo + q.nq - 1, f.L, p.wl, p.wr, &q.j0, &q.n);
+      else
+        q.n = cdiv(f.L, kBN);
+      lo = min(lo, q.j0);
+      hi = max(hi, q.j0 + q.n);
+    }
   }
-  f.N = max(f.t[0].n, f.t[1].n);
+  f.J0 = hi > 0 ? lo : 0;
+  f.N = hi > 0 ? hi - lo : 0;
   return f;
 }
 
@@ -142,7 +157,7 @@ __device__ __forceinline__ bool next_item(QCtl* c, uint32_t n, QItem* f, bool* o
   return f->b >= 0;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tdo, const BwdParams& p, uint8_t* smem,
                               QCtl* c) {
@@ -157,12 +172,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   auto fetch = [&](QItem& f) {
     const int idx = atomicAdd(&p.hdr->ticket, 1);
     if (idx < n_items)
-      f = decode<CAUSAL>(p, idx, T);
+      f = decode<LOCAL>(p, idx, T);
     else
       f.b = -1;
   };
   auto prefetch = [&](const QItem& f) {
-    const KvTile kt = kv_tile(f.off0, f.L, 0, T);
+    const KvTile kt = kv_tile(f.off0, f.L, f.J0, T);
 #pragma unroll
     for (int s = 0; s < C::kSlabs; ++s) {
 #pragma unroll
@@ -172,8 +187,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
           tma_prefetch_l2_3d(tdo, s * 64, f.h, f.t[g].row);
         }
       if (kt.row >= 0) {
-        tma_prefetch_l2_3d(tk, s * 64, f.h, kt.row);
-        tma_prefetch_l2_3d(tv, s * 64, f.h, kt.row);
+        tma_prefetch_l2_3d(tk, s * 64, f.hk, kt.row);
+        tma_prefetch_l2_3d(tv, s * 64, f.hk, kt.row);
       }
     }
   };
@@ -199,14 +214,14 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     }
     ++it;
     for (int j = 0; j < f.N; ++j) {
-      const KvTile kt = kv_tile(f.off0, f.L, j, T);
+      const KvTile kt = kv_tile(f.off0, f.L, (LOCAL ? f.J0 : 0) + j, T);
       {
         const int st = nk % C::NSK;
         if (!mbar_wait(&c->k_empty[st], ((nk / C::NSK) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
         mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.hk,
                       kt.row);
         ++nk;
       }
@@ -216,7 +231,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
+          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.hk,
                       kt.row);
         ++nv;
       }
@@ -233,7 +248,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     drain_wait(&c->v_full[g % C::NSV], (g / C::NSV) & 1, p.err);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tbase) {
   using C = QCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
@@ -281,21 +296,25 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
     if (!mbar_wait_warp(&c->qdo_full, it & 1, &c->abort, p.err)) break;
     const int N = f.N;
     const int nt[2] = {f.t[0].n, f.t[1].n};
+    // step j of the item is key tile J0 + j; for query tile g it is its own
+    // key tile lj = j + d[g] (active for 0 <= lj < nt[g])
+    const int d[2] = {LOCAL ? f.J0 - f.t[0].j0 : 0, LOCAL ? f.J0 - f.t[1].j0 : 0};
     const uint32_t k0 = nk, v0 = nv;
     // Step j: dQ_g(j-1) and S_g(j) for both tiles, then dP_0(j), dP_1(j).
     for (int j = 0; j <= N && ok; ++j) {
       bool k_ready = false;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        if (j >= 1 && j - 1 < nt[g]) {
-          const uint32_t u = gt[g] + j - 1;
+        const int lj = j + d[g];
+        if (lj >= 1 && lj - 1 < nt[g]) {
+          const uint32_t u = gt[g] + lj - 1;
           if (!mbar_wait_warp(&c->ds_full[g], u & 1, &c->abort, p.err)) { ok = false; break; }
-          if (j == 1 && !mbar_wait_warp(&c->dq_free[g], (gi[g] & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+          if (lj == 1 && !mbar_wait_warp(&c->dq_free[g], (gi[g] & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
           tc_fence_after();
-          issue_dq(g, k0 + j - 1, j > 1);
-          if (j == nt[g]) if (leader) mma_commit(&c->dq_full[g]);
+          issue_dq(g, k0 + j - 1, lj > 1);
+          if (lj == nt[g]) if (leader) mma_commit(&c->dq_full[g]);
         }
-        if (j < nt[g]) {
+        if (lj >= 0 && lj < nt[g]) {
           if (!k_ready) {
             const uint32_t kk = k0 + j;
             if (!mbar_wait_warp(&c->k_full[kk % C::NSK], (kk / C::NSK) & 1, &c->abort, p.err)) { ok = false; break; }
@@ -314,8 +333,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
         if (!mbar_wait_warp(&c->v_full[vv % C::NSV], (vv / C::NSV) & 1, &c->abort, p.err)) { ok = false; break; }
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          if (j < nt[g]) {
-            if (!mbar_wait_warp(&c->p_done[g], (gt[g] + j) & 1, &c->abort, p.err)) { ok = false; break; }
+          const int lj = j + d[g];
+          if (lj >= 0 && lj < nt[g]) {
+            if (!mbar_wait_warp(&c->p_done[g], (gt[g] + lj) & 1, &c->abort, p.err)) { ok = false; break; }
             tc_fence_after();
             issue_dp(g, vv);
             if (leader) mma_commit(&c->dp_full[g]);
@@ -341,7 +361,7 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, QCtl* c, uint32_t tb
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
   const int r = threadIdx.x & 127;    // query row of each tile == TMEM lane
   const int half = threadIdx.x >> 7;  // key columns [64*half, 64*half + 64)
@@ -375,7 +395,8 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
       nlse2[g] = f2_pack(nl, nl);
       ndlt2[g] = f2_pack(nd, nd);
     }
-    // P of tile g at key tile j: this thread's 64 columns -> 32 bf16 pairs.
+    // P of tile g at its key tile j (key tile t[g].j0 + j of the sequence):
+    // this thread's 64 columns -> 32 bf16 pairs.
     auto p_part = [&](int g, int j, uint32_t (&pk)[32]) {
       const uint32_t u = gt[g] + j;
       if (!mbar_wait_warp(&c->s_full[g], u & 1, &c->abort, p.err)) return false;
@@ -400,15 +421,23 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
         }
       }
       const QTile& q = f.t[g];
-      const KvTile kt = kv_tile(f.off0, f.L, j, T);
-      const int key0 = j * kBN - kt.shift;  // local key index of column 0
-      if (kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > q.q_lo - q.shift)) {
-        // Ragged or diagonal tile: zero the inadmissible columns.  The
-        // admissible ones are [lo, lo + span] (relative to this thread's
-        // first column); an empty range moves lo past every column.
-        const int last = CAUSAL ? min(kt.shift + kt.nk - 1, qi[g] - key0) : kt.shift + kt.nk - 1;
-        const int lo = (last >= kt.shift ? kt.shift : kBN) - 64 * half;
-        const uint32_t span = last >= kt.shift ? static_cast<uint32_t>(last - kt.shift) : 0u;
+      const int jk = LOCAL ? q.j0 + j : j;
+      const KvTile kt = kv_tile(f.off0, f.L, jk, T);
+      const int key0 = jk * kBN - kt.shift;  // local key index of column 0
+      const int qa = q.q_lo - q.shift;       // local query index of row 0 of the box
+      if (kt.nk < kBN || kt.shift > 0 ||
+          (LOCAL && (key0 + kBN - 1 > qa + p.wr || key0 < qa + kBM - 1 - p.wl))) {
+        // Ragged tile, or one that a band edge crosses: zero the
+        // inadmissible columns.  The admissible ones are [lo, lo + span]
+        // (relative to this thread's first column); an empty range moves lo
+        // past every column.
+        int first = kt.shift, last = kt.shift + kt.nk - 1;
+        if (LOCAL) {  // admissible keys [qi - wl, qi + wr]
+          first = max(first, qi[g] - p.wl - key0);
+          last = min(last, qi[g] + p.wr - key0);
+        }
+        const int lo = (last >= first ? first : kBN) - 64 * half;
+        const uint32_t span = last >= first ? static_cast<uint32_t>(last - first) : 0u;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const uint32_t keep = (static_cast<uint32_t>(2 * i - lo) <= span ? 0x0000ffffu : 0u) |
@@ -449,12 +478,15 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
     // Per key tile j: P of both tiles, then dS of both tiles (in the order
     // the MMA issuer produces S_0, S_1, dP_0, dP_1).
     const int n0 = f.t[0].n, n1 = f.t[1].n;
+    const int d0 = LOCAL ? f.J0 - f.t[0].j0 : 0, d1 = LOCAL ? f.J0 - f.t[1].j0 : 0;
     for (int j = 0; j < f.N && ok; ++j) {
       uint32_t p0[32], p1[32];
-      if (j < n0 && !p_part(0, j, p0)) { ok = false; break; }
-      if (j < n1 && !p_part(1, j, p1)) { ok = false; break; }
-      if (j < n0 && !ds_part(0, j, p0)) { ok = false; break; }
-      if (j < n1 && !ds_part(1, j, p1)) { ok = false; break; }
+      const int l0 = j + d0, l1 = j + d1;  // the step in each tile's own key tiles
+      const bool a0 = l0 >= 0 && l0 < n0, a1 = l1 >= 0 && l1 < n1;
+      if (a0 && !p_part(0, l0, p0)) { ok = false; break; }
+      if (a1 && !p_part(1, l1, p1)) { ok = false; break; }
+      if (a0 && !ds_part(0, l0, p0)) { ok = false; break; }
+      if (a1 && !ds_part(1, l1, p1)) { ok = false; break; }
     }
     if (!ok) break;
     // Epilogues: dQ = scale * acc in bf16 (this thread's half of the head dim).
@@ -486,7 +518,7 @@ __device__ void math_role(const BwdParams& p, QCtl* c, uint32_t tbase) {
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -541,11 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
   if (warp < 8) {
-    math_role<D, CAUSAL>(p, c, tbase);
+    math_role<D, LOCAL>(p, c, tbase);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, CAUSAL>(&tq, &tk, &tv, &tdo, p, smem, c);
+    if (lane == 0) producer_role<D, LOCAL>(&tq, &tk, &tv, &tdo, p, smem, c);
   } else {
-    mma_role<D, CAUSAL>(p, smem, c, tbase);
+    mma_role<D, LOCAL>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();
@@ -556,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool LOCAL>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t s) {
   using C = QCfg<D>;
@@ -564,7 +596,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   static_assert(sizeof(QCtl) <= 512, "control block");
   static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
   static_assert(128 + D <= 256, "TMEM columns per query tile");
-  auto kern = bwd_q_kernel<D, CAUSAL>;
+  auto kern = bwd_q_kernel<D, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, p);

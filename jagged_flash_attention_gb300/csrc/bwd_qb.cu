@@ -165,7 +165,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         mbar_arrive_expect_tx(&c->k_full[st], C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64, f.h,
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st], s * 64,
+                      f.h / p.G,
                       kt.row);
         ++nk;
       }
@@ -214,7 +215,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
+          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64,
+                      f.h / p.G,
                       kt.row);
         ++nv;
       }

@@ -16,6 +16,32 @@ constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;  // keys per tile
 constexpr int kFwdRows = 256;  // query rows per forward work item (two tiles)
 
+// Local (banded) attention: key j is admissible for query i, both counted
+// from the start of their sequence, iff i - wl <= j <= i + wr.  kNoWindow
+// leaves a side unbounded; causal masking is wl = kNoWindow, wr = 0.
+// Lengths are below 2^23 (at most 65535 tiles), so i + kNoWindow cannot
+// overflow.
+constexpr int kNoWindow = 1 << 30;
+
+// Key tiles [*j0, *j0 + *n) holding the admissible keys of query rows
+// [qa, qb] of a sequence of L > 0 keys.
+__host__ __device__ __forceinline__ void key_tiles(int qa, int qb, int L, int wl, int wr, int* j0,
+                                                   int* n) {
+  const int lo = qa - wl > 0 ? qa - wl : 0;
+  const int hi = qb + wr < L - 1 ? qb + wr : L - 1;
+  *j0 = lo / kBN;
+  *n = hi / kBN - *j0 + 1;
+}
+// Query tiles [*t0, *t0 + *n) holding the queries (of L) that admit some key
+// of rows [ka, kb].
+__host__ __device__ __forceinline__ void query_tiles(int ka, int kb, int L, int wl, int wr, int* t0,
+                                                     int* n) {
+  const int lo = ka - wr > 0 ? ka - wr : 0;
+  const int hi = kb + wl < L - 1 ? kb + wl : L - 1;
+  *t0 = lo / kBM;
+  *n = hi / kBM - *t0 + 1;
+}
+
 // Row statistics of the self-attention backward, {-LSE*log2e, -Delta} per
 // query row (h, t) at row index si = h*T + t, in a blocked layout: every
 // aligned group of 4 positions stores the 4 rows' -LSE*log2e (16 bytes),
@@ -103,18 +129,23 @@ __device__ __forceinline__ void seg_next(Seg& s, const int32_t* off, int B) {
 
 struct SchedParams {
   const int32_t* offsets;
-  int B, H, Lq, max_len;
-  int causal, broadcast, backward;
+  int B, H, Lq, max_len;  // H: heads of the list (K/V heads for the dK/dV list)
+  int causal, broadcast, backward;  // causal: any local mask (causal or a window)
   int qrows;  // query rows per item when backward == 0 (forward and dQ pass: 256)
   Item* items;
   int capacity;
   WorkHeader* hdr;
   int* err;
+  int wl = kNoWindow, wr = kNoWindow;  // the local mask, for the cost order
 };
 
+// Every parameter block below carries the GQA group G (query heads per K/V
+// head: query head h reads K/V head h / G) and the local mask (wl, wr); the
+// host sets them on every path.
 struct FwdParams {
   const int32_t* offsets;
   int B, H, Lq;
+  int G, wl, wr;
   float scale_log2;  // scale * log2(e)
   __nv_bfloat16* out;
   float* lse;
@@ -133,6 +164,7 @@ struct FwdParams {
 struct BwdParams {
   const int32_t* offsets;
   int B, H, Lq;
+  int Hkv, G, wl, wr;  // K/V heads (dK, dV are [T, Hkv, D]), group, local mask
   float scale_log2;
   float scale;
   const float* lse;    // caller's LSE (natural log)
@@ -198,6 +230,7 @@ struct FinParams {
 
 // Host-side launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
+// causal: any local mask (the kernels read wl, wr from the parameters).
 cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
 // tdk / tdv: the dK / dV outputs as maps like the inputs' (TMA stores).

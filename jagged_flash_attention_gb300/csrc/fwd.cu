@@ -67,14 +67,15 @@ struct QTile {
   int nq;     // valid query rows (<= 0: tile absent)
   int shift;  // rows the Q box was moved back to stay inside [0, T)
   int row;    // TMA row coordinate of the Q box
-  int n_kv;   // key tiles this query tile visits
+  int j0;     // first key tile this query tile visits
+  int n_kv;   // key tiles it visits: [j0, j0 + n_kv)
 };
 
 struct FwdItem {
-  int b, h;
+  int b, h, hk;  // sequence, query head, K/V head
   int off0, L;
   QTile t[2];
-  int N;  // key tiles loaded for the item (max over the two query tiles)
+  int J0, N;  // key tiles loaded for the item: [J0, J0 + N), the union of the tiles' ranges
 };
 
 struct FwdCtl {
@@ -92,19 +93,25 @@ struct FwdCtl {
   int abort;
 };
 
-template <bool BCAST, bool CAUSAL>
+// LOCAL: a local mask (causal or a sliding window, bounds p.wl / p.wr): a
+// query tile visits only the key tiles that hold admissible keys of its
+// rows, and the item streams the union of its two tiles' ranges.
+template <bool BCAST, bool LOCAL>
 __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
   FwdItem f;
   const Item it = p.items[idx];
   f.b = it.x;
   f.h = it.y >> 16;
+  f.hk = f.h / p.G;
   const int pair = it.y & 0xffff;
   f.off0 = p.offsets[f.b];
   f.L = p.offsets[f.b + 1] - f.off0;
+  int lo = 1 << 30, hi = 0;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     QTile& q = f.t[t];
     q.q_lo = (2 * pair + t) * kBM;
+    q.j0 = 0;
     if (BCAST) {
       q.nq = min(kBM, p.Lq - q.q_lo);
       q.shift = 0;
@@ -115,10 +122,21 @@ __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
       const int start = f.off0 + q.q_lo;
       q.shift = max(0, start + kBM - T);
       q.row = start - q.shift;
-      q.n_kv = q.nq > 0 ? (CAUSAL ? cdiv(q.q_lo + q.nq, kBN) : cdiv(f.L, kBN)) : 0;
+      q.n_kv = 0;
+      if (q.nq > 0) {
+        if (LOCAL)
+          key_tiles(q.q_lo, q.q_lo + q.nq - 1, f.L, p.wl, p.wr, &q.j0, &q.n_kv);
+        else
+          q.n_kv = cdiv(f.L, kBN);
+      }
+    }
+    if (q.n_kv > 0) {
+      lo = min(lo, q.j0);
+      hi = max(hi, q.j0 + q.n_kv);
     }
   }
-  f.N = max(f.t[0].n_kv, f.t[1].n_kv);
+  f.J0 = hi > 0 ? lo : 0;
+  f.N = hi > 0 ? hi - lo : 0;
   return f;
 }
 
@@ -161,7 +179,7 @@ __device__ __forceinline__ bool next_item(FwdCtl* c, uint32_t n, FwdItem* f, boo
   return f->b >= 0;
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const FwdParams& p, uint8_t* smem, FwdCtl* c) {
   using C = FwdCfg<D>;
@@ -202,7 +220,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     while (idx >= n_items && ok) idx = clc_take();
     FwdItem f;
     if (idx >= 0 && ok)
-      f = decode<BCAST, CAUSAL>(p, idx, T);
+      f = decode<BCAST, LOCAL>(p, idx, T);
     else
       f.b = -1;
     c->item[slot] = f;
@@ -222,11 +240,12 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
                     f.t[t].row);
     }
     ++itq;
-    // Order K0, K1, V0, K2, V1, ...: the MMA needs K(j) and V(j-1) together.
+    // Order K0, K1, V0, K2, V1, ... (of the item's key tiles J0, J0 + 1,
+    // ...): the MMA needs K(j) and V(j-1) together.
     for (int j = 0; j <= f.N && ok; ++j) {
       if (j < f.N) {
         const int st = nk % C::NSK;
-        const KvTile kt = kv_tile(f.off0, f.L, j, T);
+        const KvTile kt = kv_tile(f.off0, f.L, (LOCAL ? f.J0 : 0) + j, T);
         if (!mbar_wait(&c->k_empty[st], ((nk / C::NSK) & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -234,14 +253,14 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s) {
           mbar_arrive_expect_tx(&c->k_full[st][s], 16384);
-          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st][s], s * 64, f.h,
+          tma_load_3d(smem + C::kK + st * C::kTile + s * 16384, tk, &c->k_full[st][s], s * 64, f.hk,
                       kt.row);
         }
         ++nk;
       }
       if (j >= 1) {
         const int st = nv % C::NSV;
-        const KvTile kt = kv_tile(f.off0, f.L, j - 1, T);
+        const KvTile kt = kv_tile(f.off0, f.L, (LOCAL ? f.J0 : 0) + j - 1, T);
         if (!mbar_wait(&c->v_empty[st], ((nv / C::NSV) & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -249,7 +268,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         mbar_arrive_expect_tx(&c->v_full[st], C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.h,
+          tma_load_3d(smem + C::kV + st * C::kTile + s * 16384, tv, &c->v_full[st], s * 64, f.hk,
                       kt.row);
         ++nv;
       }
@@ -293,7 +312,7 @@ __device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t tbase, int t,
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
@@ -326,18 +345,19 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int nkv = f.t[t].n_kv;
-        if (j >= 1 && j - 1 < nkv) {  // O_t += P_t(j-1) V(j-1)
+        const int lj = LOCAL ? f.J0 + j - f.t[t].j0 : j;  // step j in query tile t's own key tiles
+        if (lj >= 1 && lj - 1 < nkv) {  // O_t += P_t V of the previous step
           if (!mbar_wait_warp(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
           ++np[t];
-          if (j == 1 && !mbar_wait_warp(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
+          if (lj == 1 && !mbar_wait_warp(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv<D>(leader, tbase, t, dv, j > 1);
+          issue_pv<D>(leader, tbase, t, dv, lj > 1);
           if (leader) mma_commit(&c->o_ready[t]);
         }
-        if (j < nkv) {  // S_t(j) = Q_t K(j)^T, slab 1 of K waited for between its halves
+        if (lj >= 0 && lj < nkv && j < f.N) {  // S_t = Q_t K^T, slab 1 of K waited for between its halves
           const uint64_t dq = desc_add(dq0, t * C::kTile);
 #pragma unroll
           for (int sl = 0; sl < C::kSlabs; ++sl) {
@@ -374,7 +394,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
   const int t = threadIdx.x >> 7;   // query tile of this warpgroup
@@ -423,18 +443,23 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[ch][i]);
-      const KvTile kt = kv_tile(f.off0, f.L, j, T);
-      const int key0 = j * kBN - kt.shift;  // local key index of column 0
-      const bool need_mask =
-          kt.nk < kBN || kt.shift > 0 || (CAUSAL && key0 + kBN - 1 > q.q_lo - q.shift);
+      const int jk = LOCAL ? q.j0 + j : j;  // key tile of the sequence
+      const KvTile kt = kv_tile(f.off0, f.L, jk, T);
+      const int key0 = jk * kBN - kt.shift;  // local key index of column 0
+      const int qa = q.q_lo - q.shift;       // local query index of row 0 of the box
+      const bool need_mask = kt.nk < kBN || kt.shift > 0 ||
+                             (LOCAL && (key0 + kBN - 1 > qa + p.wr || key0 < qa + kBM - 1 - p.wl));
       if (need_mask) {
-        // Peeled tail: only the ragged last tile (and the diagonal tile when
-        // causal) pays for the per-element mask.
-        const int c_lo = kt.shift, c_hi = kt.shift + kt.nk;
-        const int c_causal = qi - key0;  // last admissible column when causal
+        // Peeled tail: only the ragged last tile (and, with a local mask,
+        // the tiles a band edge crosses) pays for the per-element mask.
+        int c_lo = kt.shift, c_hi = kt.shift + kt.nk;
+        if (LOCAL) {  // admissible keys [qi - wl, qi + wr]
+          c_lo = max(c_lo, qi - p.wl - key0);
+          c_hi = min(c_hi, qi + p.wr - key0 + 1);
+        }
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) {
-          const bool keep = cc >= c_lo && cc < c_hi && (!CAUSAL || cc <= c_causal);
+          const bool keep = cc >= c_lo && cc < c_hi;
           s[cc] = keep ? s[cc] : -INFINITY;
         }
       }
@@ -523,7 +548,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -575,11 +600,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tbase = c->tmem_base;
 
   if (warp < 8) {
-    softmax_role<D, CAUSAL, BCAST>(p, c, tbase);
+    softmax_role<D, LOCAL, BCAST>(p, c, tbase);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, CAUSAL, BCAST>(&tq, &tk, &tv, p, smem, c);
+    if (lane == 0) producer_role<D, LOCAL, BCAST>(&tq, &tk, &tv, p, smem, c);
   } else {
-    mma_role<D, CAUSAL, BCAST>(p, smem, c, tbase);
+    mma_role<D, LOCAL, BCAST>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();
@@ -590,14 +615,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, int grid, cudaStream_t s) {
   using C = FwdCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(FwdCtl) <= 512, "control block");
   static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
-  auto kern = fwd_kernel<D, CAUSAL, BCAST>;
+  auto kern = fwd_kernel<D, LOCAL, BCAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kFwdThreads, C::kSmem, s>>>(tq, tk, tv, p);

@@ -36,6 +36,8 @@ class Workload:
     q_len: int  # dense Q length in broadcast mode, 0 otherwise
     lengths_desc: str
     extra: dict = field(default_factory=dict)
+    Hkv: int = 0  # K/V heads (GQA); 0: as many as query heads
+    window: tuple = (-1, -1)  # (left, right) band of a sliding window; -1: unbounded
 
 
 WORKLOADS = {
@@ -100,21 +102,35 @@ def make_inputs(w: Workload, lengths=None, seed=None):
     T = int(off[-1])
     B = L.size
     H, D = w.H, w.D
+    Hkv = w.Hkv or H
     if w.broadcast_q:
-        shapes = [(w.q_len, H, D), (T, H, D), (T, H, D), (B, w.q_len, H, D)]
+        shapes = [(w.q_len, H, D), (T, Hkv, D), (T, Hkv, D), (B, w.q_len, H, D)]
     else:
-        shapes = [(T, H, D)] * 4
+        shapes = [(T, H, D), (T, Hkv, D), (T, Hkv, D), (T, H, D)]
     q, k, v, do = draw_values(w.seed if seed is None else seed, shapes)
-    return dict(q=q, k=k, v=v, dout=do, offsets=off, lengths=L, B=B, H=H, D=D,
+    return dict(q=q, k=k, v=v, dout=do, offsets=off, lengths=L, B=B, H=H, Hkv=Hkv, D=D,
                 T=T, causal=w.causal, broadcast_q=w.broadcast_q, q_len=w.q_len,
-                max_len=int(L.max()) if L.size else 0, scale=1.0 / math.sqrt(D))
+                window=tuple(w.window), max_len=int(L.max()) if L.size else 0,
+                scale=1.0 / math.sqrt(D))
 
 
-def pairs(lengths, causal=False, q_len=0, broadcast_q=False) -> int:
-    """Number of (query, key) pairs attended: the useful-work count."""
+def pairs(lengths, causal=False, q_len=0, broadcast_q=False, window=(-1, -1)) -> int:
+    """Number of (query, key) pairs attended: the useful-work count.  A
+    window (left, right) keeps keys [i - left, i + right] of query i."""
     L = np.asarray(lengths, dtype=np.int64)
     if broadcast_q:
         return int(q_len * L.sum())
+    wl, wr = window
     if causal:
+        wr = 0
+    if wl < 0 and wr < 0:
+        return int((L * L).sum())
+    if wl < 0 and wr == 0:
         return int((L * (L + 1) // 2).sum())
-    return int((L * L).sum())
+    total = 0
+    for n in L.tolist():
+        i = np.arange(n, dtype=np.int64)
+        lo = np.maximum(0, i - wl) if wl >= 0 else np.zeros_like(i)
+        hi = np.minimum(n - 1, i + wr) if wr >= 0 else np.full_like(i, n - 1)
+        total += int((hi - lo + 1).sum())
+    return total

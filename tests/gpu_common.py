@@ -37,11 +37,14 @@ def run_gpu(x, stream=None, bwd=True):
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     off = torch.from_numpy(x["offsets"]).to(dev)
     res = {}
+    win = x.get("window", (-1, -1))
     out, lse = jfa.forward(q, k, v, off, x["max_len"], causal=x["causal"],
-                           broadcast_q=x["broadcast_q"], scale=x["scale"], stream=stream)
+                           broadcast_q=x["broadcast_q"], scale=x["scale"], stream=stream,
+                           window=win)
     if bwd:
         dq, dk, dv = jfa.backward(q, k, v, off, x["max_len"], out, lse, do, causal=x["causal"],
-                                  broadcast_q=x["broadcast_q"], scale=x["scale"], stream=stream)
+                                  broadcast_q=x["broadcast_q"], scale=x["scale"], stream=stream,
+                                  window=win)
     jfa.jfa_sync_and_check(stream)
     res["out"], res["lse"] = f64(out), f64(lse)
     if bwd:
@@ -51,13 +54,14 @@ def run_gpu(x, stream=None, bwd=True):
 
 def run_oracle(x, seqs=None, heads=None, bwd=True):
     q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "dout"))
+    win = x.get("window", (-1, -1))
     out, lse = orc.forward(q, k, v, x["offsets"], x["scale"], x["causal"], x["broadcast_q"],
-                           seqs=seqs, heads=heads)
+                           seqs=seqs, heads=heads, window=win)
     res = {"out": out, "lse": lse}
     if bwd:
         res["dq"], res["dk"], res["dv"] = orc.backward(q, k, v, x["offsets"], do, x["scale"],
                                                        x["causal"], x["broadcast_q"],
-                                                       seqs=seqs, heads=heads)
+                                                       seqs=seqs, heads=heads, window=win)
     return res
 
 

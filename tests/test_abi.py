@@ -127,3 +127,33 @@ def test_worklist_argument_errors(L):
     assert fn(16, 4, 2, 100, 64, 1, 1, 1, 16, 100, 16, 0) == 1
     assert fn(16, 4, 2, 100, 0, 0, 0, 0, 8, 100, 16, 0) == 1  # items not 16-byte aligned
     assert b"16-byte" in L.jfa_last_error()
+
+
+def _fwd_ex(L, **kw):
+    a = dict(H=4, Hkv=2, q_len=0, bq=0, causal=0, wl=-1, wr=-1)
+    a.update(kw)
+    return L.jfa_fwd_ex(16, 16, 16, 16, 2, a["H"], a["Hkv"], 128, 10, a["q_len"], a["bq"],
+                        a["causal"], a["wl"], a["wr"], 0.1, 16, 16, 0)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(Hkv=3), 1, "H_kv must divide H"),
+    (dict(Hkv=0), 1, "H_kv must divide H"),
+    (dict(Hkv=8), 1, "H_kv must divide H"),
+    (dict(wl=-2), 1, "window bounds"),
+    (dict(wr=-3), 1, "window bounds"),
+    (dict(causal=1, wr=5), 1, "right side by 0"),
+    (dict(bq=1, q_len=64, wl=16), 2, "self-attention only"),
+    (dict(bq=1, q_len=64, wr=0), 2, "self-attention only"),
+])
+def test_variant_argument_errors(L, kw, status, needle):
+    """GQA / window arguments of jfa_fwd_ex and jfa_bwd_ex are checked on the
+    host before anything touches a GPU."""
+    import jagged_flash_attention_gb300  # noqa: F401  (sets the argument types)
+    assert _fwd_ex(L, **kw) == status
+    assert needle in L.jfa_last_error().decode()
+    a = dict(H=4, Hkv=2, q_len=0, bq=0, causal=0, wl=-1, wr=-1)
+    a.update(kw)
+    st = L.jfa_bwd_ex(16, 16, 16, 16, 2, a["H"], a["Hkv"], 128, 10, a["q_len"], a["bq"],
+                      a["causal"], a["wl"], a["wr"], 0.1, 16, 16, 16, 16, 16, 16, 0)
+    assert st == status and needle in L.jfa_last_error().decode()
