@@ -46,8 +46,13 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def _pairs(x):
+    return W.pairs(x["lengths"], x["causal"], x["q_len"], x["broadcast_q"],
+                   x.get("window", (-1, -1)))
+
+
 def _flops(x):
-    p = W.pairs(x["lengths"], x["causal"], x["q_len"], x["broadcast_q"])
+    p = _pairs(x)
     f = 4.0 * x["H"] * x["D"] * p
     return f, 2.5 * f, p
 
@@ -70,28 +75,31 @@ def kernel_model(x):
     {kind: (tensor FLOPs, DRAM bytes)}.  FLOPs count true (query, key) pairs
     (2 * D per pair and product); bytes count each tensor the kernel must
     read or write once: Q rows are T (self) or q_len (broadcast), O / dO rows
-    T or B * q_len, K / V rows T; bf16 tensors, fp32 LSE and statistics
-    (8 bytes per row and head; self-attention keeps four copies)."""
+    T or B * q_len, K / V rows T (with H_kv heads); bf16 tensors, fp32 LSE
+    and statistics (8 bytes per row and head; self-attention keeps four
+    copies).  A window counts only the pairs inside the band."""
     H, D, T, B, Lq = x["H"], x["D"], x["T"], x["B"], x["q_len"]
     bq = x["broadcast_q"]
-    pairs = W.pairs(x["lengths"], x["causal"], Lq, bq)
-    row = H * D * 2
+    pairs = _pairs(x)
+    row, rkv = H * D * 2, x.get("Hkv", H) * D * 2
     qrows, orows = (Lq, B * Lq) if bq else (T, T)
     stat = 8 * H * orows
     m = {
         "sched": (0.0, 4.0 * (B + 1)),
-        "fwd": (4.0 * H * D * pairs, (qrows + 2 * T + orows) * row + 4 * H * orows),
+        "fwd": (4.0 * H * D * pairs, (qrows + orows) * row + 2 * T * rkv + 4 * H * orows),
         "prep": (0.0, 2 * orows * row + 4 * H * orows + (stat if bq else 4 * stat)),
-        "bwd_kv": (8.0 * H * D * pairs, (4 * T + qrows + orows) * row + stat),
+        "bwd_kv": (8.0 * H * D * pairs, (qrows + orows) * row + 4 * T * rkv + stat),
     }
     if bq:
-        m["bwd_qb"] = (6.0 * H * D * pairs, (2 * T + qrows + orows) * row + stat + 4 * Lq * H * D)
+        m["bwd_qb"] = (6.0 * H * D * pairs,
+                       (qrows + orows) * row + 2 * T * rkv + stat + 4 * Lq * H * D)
         m["finalize"] = (0.0, 6 * Lq * H * D)
         # one-pass backward of a short dense Q: Q, K, V, dO read, dK, dV written once
-        m["bwd_bs"] = (10.0 * H * D * pairs, (4 * T + qrows + orows) * row + stat + 4 * Lq * H * D)
+        m["bwd_bs"] = (10.0 * H * D * pairs,
+                       (qrows + orows) * row + 4 * T * rkv + stat + 4 * Lq * H * D)
         m["fwd_combine"] = (0.0, 0.0)
     else:
-        m["bwd_q"] = (6.0 * H * D * pairs, (4 * T) * row + stat + T * row)
+        m["bwd_q"] = (6.0 * H * D * pairs, 3 * T * row + 2 * T * rkv + stat)
     return m
 
 
@@ -102,10 +110,10 @@ def step_model(x):
     LSE, Delta, and dQ, dK, dV written."""
     H, D, T, B, Lq = x["H"], x["D"], x["T"], x["B"], x["q_len"]
     fwd_f, bwd_f, _ = _flops(x)
-    row = H * D * 2
+    row, rkv = H * D * 2, x.get("Hkv", H) * D * 2
     qrows, orows = (Lq, B * Lq) if x["broadcast_q"] else (T, T)
-    fwd_b = (qrows + 2 * T + orows) * row + 4 * H * orows
-    bwd_b = (2 * qrows + 4 * T + 3 * orows) * row + 8 * H * orows
+    fwd_b = (qrows + orows) * row + 2 * T * rkv + 4 * H * orows
+    bwd_b = (2 * qrows + 3 * orows) * row + 4 * T * rkv + 8 * H * orows
     return (fwd_f, fwd_b), (bwd_f, bwd_b)
 
 
@@ -254,10 +262,11 @@ def _oracle_sample(x, budget_s, max_seqs=None):
         k, v = f64(x["k"][s0:s1]), f64(x["v"][s0:s1])
         sub = [0, s1 - s0]
         t0 = time.perf_counter()
-        orc.forward(q, k, v, sub, x["scale"], x["causal"], x["broadcast_q"])
-        orc.backward(q, k, v, sub, do, x["scale"], x["causal"], x["broadcast_q"])
+        win = x.get("window", (-1, -1))
+        orc.forward(q, k, v, sub, x["scale"], x["causal"], x["broadcast_q"], window=win)
+        orc.backward(q, k, v, sub, do, x["scale"], x["causal"], x["broadcast_q"], window=win)
         tot_t += time.perf_counter() - t0
-        p = W.pairs([s1 - s0], x["causal"], x["q_len"], x["broadcast_q"])
+        p = W.pairs([s1 - s0], x["causal"], x["q_len"], x["broadcast_q"], win)
         tot_f += 14.0 * x["H"] * x["D"] * p
         n += 1
         if tot_t >= budget_s:
@@ -272,14 +281,19 @@ def _l2_note(x):
     return "inputs fit in L2: a 256 MB buffer is written between timed steps (flush)"
 
 
+def _workload_def(wname):
+    return W.WORKLOADS[wname] if wname in W.WORKLOADS else W.variant(wname)
+
+
 def _config(x, wname, ws=1):
     """The workload description both arms print (same keys)."""
-    return {"workload": wname, "B": int(x["B"]), "H": x["H"], "D": x["D"], "T": x["T"],
-            "causal": x["causal"], "broadcast_q": x["broadcast_q"], "q_len": x["q_len"],
-            "max_len": x["max_len"], "lengths": W.WORKLOADS[wname].lengths_desc,
-            "seed": W.WORKLOADS[wname].seed,
-            "pairs": W.pairs(x["lengths"], x["causal"], x["q_len"], x["broadcast_q"]),
-            "l2": _l2_note(x), "parallelism": "replicas" if ws > 1 else "single GPU"}
+    w = _workload_def(wname)
+    return {"workload": wname, "B": int(x["B"]), "H": x["H"], "H_kv": x.get("Hkv", x["H"]),
+            "D": x["D"], "T": x["T"], "causal": x["causal"], "broadcast_q": x["broadcast_q"],
+            "q_len": x["q_len"], "window": list(x.get("window", (-1, -1))),
+            "max_len": x["max_len"], "lengths": w.lengths_desc, "seed": w.seed,
+            "pairs": _pairs(x), "l2": _l2_note(x),
+            "parallelism": "replicas" if ws > 1 else "single GPU"}
 
 
 def run_reference(args, x, wname):
@@ -341,19 +355,22 @@ def _time_steps(jfa, torch, x, steps, warmup, stream, dev, min_seconds=0.15):
     bq, causal, scale, max_len = x["broadcast_q"], x["causal"], x["scale"], x["max_len"]
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     off = torch.from_numpy(x["offsets"]).to(dev)
-    out, lse = jfa.forward(q, k, v, off, max_len, causal=causal, broadcast_q=bq, scale=scale)
+    out, lse = jfa.forward(q, k, v, off, max_len, causal=causal, broadcast_q=bq, scale=scale,
+                           window=x.get("window", (-1, -1)))
     dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
     flush = None
     if x["k"].numel() * 2 <= L2_BYTES:
         flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
 
+    win = x.get("window", (-1, -1))
+
     def fwd():
         jfa.forward(q, k, v, off, max_len, causal=causal, broadcast_q=bq, scale=scale, out=out,
-                    lse=lse)
+                    lse=lse, window=win)
 
     def bwd():
         jfa.backward(q, k, v, off, max_len, out, lse, do, causal=causal, broadcast_q=bq,
-                     scale=scale, dq=dq, dk=dk, dv=dv)
+                     scale=scale, dq=dq, dk=dk, dv=dv, window=win)
 
     for _ in range(warmup):
         fwd()
@@ -550,7 +567,7 @@ def run_ours(args, x, wname):
 
     # The other workloads (rank 0 of a single-GPU run, unless --only): each
     # device-timed over a few steps through the same public API.
-    workloads = {}
+    workloads, variants = {}, {}
     if ws == 1 and not args.only:
         workloads[wname] = (x, fwd_ms, bwd_ms, kprof, windows[0], args.steps)
         for other in W.ORDER:
@@ -564,11 +581,22 @@ def run_ours(args, x, wname):
             workloads[other] = (xo, f_ms, b_ms, kp, win, steps)
             del xo
             torch.cuda.empty_cache()
+        # GQA and sliding-window variants, the same way
+        for vname in W.VARIANTS:
+            xo = W.make_inputs(W.variant(vname))
+            steps = max(3, min(args.steps, args.workload_steps))
+            f_ms, b_ms, kp, _, win, steps = _time_steps(jfa, torch, xo, steps,
+                                                        max(3, args.warmup), stream, dev)
+            windows.append(win)
+            variants[vname] = (xo, f_ms, b_ms, kp, win, steps)
+            del xo
+            torch.cuda.empty_cache()
     clk.__exit__(None, None, None)
-    for other, entry in list(workloads.items()):
-        if isinstance(entry, tuple):
-            xo, f_ms, b_ms, kp, win, steps = entry
-            workloads[other] = _workload_entry(xo, other, f_ms, b_ms, kp, peak, hbm, clk, win,
+    for group in (workloads, variants):
+        for other, entry in list(group.items()):
+            if isinstance(entry, tuple):
+                xo, f_ms, b_ms, kp, win, steps = entry
+                group[other] = _workload_entry(xo, other, f_ms, b_ms, kp, peak, hbm, clk, win,
                                                steps)
 
     if rank != 0:
@@ -617,6 +645,8 @@ def run_ours(args, x, wname):
     }
     if workloads:
         line["workloads"] = workloads
+    if variants:
+        line["variants"] = variants
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -54,6 +54,21 @@ WORKLOADS = {
 }
 ORDER = ["tiny_self", "jagged_self", "broadcast_q", "causal_self", "skewed_broadcast_q"]
 
+# The GQA and sliding-window variants ("Optimizing Jagged Flash Attention with
+# TLX", sections 3 and 4 name both as supported), measured on the lengths and
+# values of two workloads above (same seeds): four query heads per K/V head on
+# jagged_self, a 1024-key causal band on causal_self.
+VARIANTS = {
+    "jagged_self_gqa4": dict(base="jagged_self", Hkv=2),
+    "causal_self_window1024": dict(base="causal_self", window=(1024, -1)),
+}
+
+
+def variant(name: str) -> Workload:
+    import dataclasses
+    v = dict(VARIANTS[name])
+    return dataclasses.replace(WORKLOADS[v.pop("base")], **v)
+
 
 def sample_lengths(w: Workload, B: int | None = None) -> np.ndarray:
     """Sequence lengths of workload `w` (optionally with a different B)."""
