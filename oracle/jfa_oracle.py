@@ -55,7 +55,9 @@ differences of the gradients, broadcast = stacked per-sequence attention, and
 permutation invariants.  The query-row chunking (ROW_CHUNK) is pinned in
 tests/test_oracle_chunks.py: blocks of 3 and 7 rows against the same torch
 float64 routes, with planted slips (causal offset lost, dK / dV overwritten
-instead of summed, block rows taken from the wrong place) caught.
+instead of summed, block rows taken from the wrong place) caught.  GQA and
+windows are pinned in tests/test_oracle_variants.py, the block-sparse
+selection and forward (end of this file) in tests/test_oracle_sparse.py.
 """
 from __future__ import annotations
 
@@ -272,3 +274,100 @@ def delta_rowsum(out, dout, broadcast_q=False):
     o, do = _as64(out), _as64(dout)
     d = np.sum(o * do, axis=-1)
     return np.moveaxis(d, -1, -2) if broadcast_q else d.T.copy()
+
+
+# ------------------------------------------------------- block-sparse variant
+#
+# "Optimizing Jagged Flash Attention with TLX", section 3 ("Block-sparse
+# attention"): a scoring step average-pools each Q block and each K block,
+# keeps per Q block the top-k K/V blocks (k from a selection ratio), and the
+# attention then runs over the selected blocks only.  Readings where the page
+# is silent (listed in the design notes): K blocks are 128 keys, Q blocks 256
+# query rows, both counted from the start of their sequence (the last one
+# ragged); a block's pooled vector is the mean of its valid rows, per head
+# (K/V head h // group for query head h); the block score is the dot product
+# of the two pooled vectors; k = max(1, ceil(permille * n / 1000)) of the
+# sequence's n K blocks, in integer arithmetic; ties go to the lower block
+# index; the list is stored in ascending order.  Self-attention without a
+# causal mask.
+
+SPARSE_Q_BLOCK = 256
+SPARSE_K_BLOCK = 128
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def sparse_k_count(n_blocks, permille):
+    """Selected K blocks out of n: max(1, ceil(permille * n / 1000)), at most n."""
+    if n_blocks == 0:
+        return 0
+    return min(n_blocks, max(1, (permille * n_blocks + 999) // 1000))
+
+
+def block_select(q, k, offsets, permille):
+    """Top-k K blocks per (sequence, query head, Q block) by pooled scores.
+
+    Returns (blocks, counts, scores): blocks int64 [B, H, nqb, kcap] holding
+    the selected K block indices in ascending order in the first counts
+    entries (-1 after them), counts int64 [B, H, nqb], and the fp64 block
+    scores [B, H, nqb, kcap] (NaN where there is no block), with nqb =
+    ceil(max_len / 256) and kcap = ceil(max_len / 128).
+    """
+    q, k = _as64(q), _as64(k)
+    off = _seq_bounds(offsets)
+    B = off.size - 1
+    H, Hkv, group = _heads(q, k, False)
+    L = np.diff(off)
+    max_len = int(L.max()) if B else 0
+    nqb, kcap = _cdiv(max_len, SPARSE_Q_BLOCK), _cdiv(max_len, SPARSE_K_BLOCK)
+    blocks = np.full((B, H, nqb, kcap), -1, dtype=np.int64)
+    counts = np.zeros((B, H, nqb), dtype=np.int64)
+    scores = np.full((B, H, nqb, kcap), np.nan)
+    for b in range(B):
+        s0, n = int(off[b]), int(L[b])
+        nk, nq = _cdiv(n, SPARSE_K_BLOCK), _cdiv(n, SPARSE_Q_BLOCK)
+        kk = sparse_k_count(nk, permille)
+        for h in range(H):
+            kbar = np.stack([k[s0 + j * SPARSE_K_BLOCK: s0 + min(n, (j + 1) * SPARSE_K_BLOCK),
+                               h // group, :].mean(axis=0) for j in range(nk)]) if nk else None
+            for i in range(nq):
+                qbar = q[s0 + i * SPARSE_Q_BLOCK: s0 + min(n, (i + 1) * SPARSE_Q_BLOCK), h, :]
+                sc = kbar @ qbar.mean(axis=0)
+                scores[b, h, i, :nk] = sc
+                order = np.argsort(-sc, kind="stable")  # descending, ties: lower index first
+                blocks[b, h, i, :kk] = np.sort(order[:kk])
+                counts[b, h, i] = kk
+    return blocks, counts, scores
+
+
+def forward_sparse(q, k, v, offsets, scale, blocks, counts):
+    """Attention in which query row i of a sequence sees only the keys of the
+    K blocks listed for its Q block (i // 256): blocks[b, h, i // 256,
+    :counts[b, h, i // 256]].  A row with no key gets O = 0, LSE = -inf.
+    Layouts as forward (self-attention)."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    off = _seq_bounds(offsets)
+    B = off.size - 1
+    T, Hkv, D = k.shape
+    H, Hkv, group = _heads(q, k, False)
+    out = np.zeros((T, H, D))
+    lse = np.full((H, T), -np.inf)
+    for b in range(B):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        n = s1 - s0
+        if n == 0:
+            continue
+        kblock = np.arange(n) // SPARSE_K_BLOCK
+        for h in range(H):
+            kb, vb = k[s0:s1, h // group, :], v[s0:s1, h // group, :]
+            for i in range(_cdiv(n, SPARSE_Q_BLOCK)):
+                r0, r1 = i * SPARSE_Q_BLOCK, min(n, (i + 1) * SPARSE_Q_BLOCK)
+                keep = np.isin(kblock, blocks[b, h, i, :counts[b, h, i]])
+                s = scale * (q[s0 + r0:s0 + r1, h, :] @ kb.T)
+                s = np.where(keep[None, :], s, -np.inf)
+                l = _lse_rows(s)
+                out[s0 + r0:s0 + r1, h, :] = _probs(s, l) @ vb
+                lse[h, s0 + r0:s0 + r1] = l
+    return out, lse

@@ -1,0 +1,197 @@
+"""Pins for the oracle's block-sparse variant ("Optimizing Jagged Flash
+Attention with TLX", section 3, "Block-sparse attention"): block scores from
+mean-pooled Q (256-row) and K (128-key) blocks, top-k K blocks per Q block,
+and attention over the selected blocks only.  CPU only.
+
+* a full selection (permille = 1000) is dense attention;
+* the sparse forward equals torch's float64 scaled_dot_product_attention with
+  a boolean mask expanded (by torch) from the block list;
+* brute force: selection by explicit loops (pooled sums, dot products, a
+  sort keyed on (-score, index)); attention rows by explicit sums;
+* invariants: a positive scale of Q, a constant added to every key row (the
+  scores of one Q block all move by the same amount only for means, not for
+  sums over ragged blocks), a permutation of rows inside a K block;
+* the count rule k = max(1, ceil(permille * n / 1000));
+* planted slips (sum for mean, lowest scores kept, 128-row Q blocks, head
+  map h % H_kv) that these catch.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import jfa_oracle
+
+QB, KB = 256, 128
+
+
+def _case(lengths, H, Hkv, D, seed):
+    rng = np.random.default_rng(seed)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    T = int(off[-1])
+    return (rng.standard_normal((T, H, D)), rng.standard_normal((T, Hkv, D)),
+            rng.standard_normal((T, Hkv, D)), off)
+
+
+def test_count_rule():
+    for n in (1, 2, 3, 7, 16, 64, 65):
+        for p in (1, 100, 333, 500, 999, 1000):
+            assert jfa_oracle.sparse_k_count(n, p) == min(n, max(1, math.ceil(p * n / 1000)))
+    assert jfa_oracle.sparse_k_count(0, 500) == 0
+
+
+def test_full_selection_is_dense():
+    q, k, v, off = _case([300, 1, 513, 129], 4, 2, 8, seed=51)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 1000)
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.3, blocks, counts)
+    ref_out, ref_lse = jfa_oracle.forward(q, k, v, off, 0.3)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def _torch_block_masked(q, k, v, off, scale, blocks, counts):
+    """Per sequence: SDPA (enable_gqa) with a mask expanded by torch from the
+    block-level selection matrix."""
+    out = np.zeros(q.shape)
+    H = q.shape[1]
+    for b in range(len(off) - 1):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        n = s1 - s0
+        if n == 0:
+            continue
+        nqb, nkb = -(-n // QB), -(-n // KB)
+        sel = torch.zeros(H, nqb, nkb, dtype=torch.bool)
+        for h in range(H):
+            for i in range(nqb):
+                for j in blocks[b, h, i, :counts[b, h, i]]:
+                    sel[h, i, int(j)] = True
+        mask = sel.repeat_interleave(QB, dim=1)[:, :n].repeat_interleave(KB, dim=2)[:, :, :n]
+        Q = torch.from_numpy(q[s0:s1]).permute(1, 0, 2)
+        K = torch.from_numpy(k[s0:s1]).permute(1, 0, 2)
+        V = torch.from_numpy(v[s0:s1]).permute(1, 0, 2)
+        O = torch.nn.functional.scaled_dot_product_attention(
+            Q, K, V, attn_mask=mask, scale=scale, enable_gqa=K.shape[0] != Q.shape[0])
+        out[s0:s1] = O.permute(1, 0, 2).numpy()
+    return out
+
+
+@pytest.mark.parametrize("permille", [250, 500, 750])
+def test_sparse_forward_equals_torch_block_mask(permille):
+    q, k, v, off = _case([700, 129, 1000, 5], 4, 2, 8, seed=52)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, permille)
+    out, _ = jfa_oracle.forward_sparse(q, k, v, off, 0.25, blocks, counts)
+    ref = _torch_block_masked(q, k, v, off, 0.25, blocks, counts)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+
+
+def test_sparse_forward_brute_force_rows():
+    q, k, v, off = _case([600], 2, 1, 4, seed=53)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 400)
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.5, blocks, counts)
+    rng = np.random.default_rng(0)
+    for i in rng.choice(600, 12, replace=False):
+        for h in range(2):
+            keys = [j for j in range(600) if j // KB in set(blocks[0, h, i // QB, :counts[0, h, i // QB]].tolist())]
+            e = [math.exp(0.5 * float(np.dot(q[i, h], k[j, 0]))) for j in keys]
+            den = sum(e)
+            o = sum(w * v[j, 0] for w, j in zip(e, keys)) / den
+            np.testing.assert_allclose(out[i, h], o, atol=1e-12)
+            assert abs(lse[h, i] - math.log(den)) < 1e-12
+
+
+def _select_by_loops(q, k, off, permille, group):
+    """Selection written with explicit loops and a sort keyed on (-score, j)."""
+    res = {}
+    H, D = q.shape[1], q.shape[2]
+    for b in range(len(off) - 1):
+        s0, n = int(off[b]), int(off[b + 1] - off[b])
+        nk = -(-n // KB)
+        kk = 0 if nk == 0 else min(nk, max(1, -(-(permille * nk) // 1000)))
+        for h in range(H):
+            kbar = []
+            for j in range(nk):
+                rows = range(s0 + j * KB, s0 + min(n, (j + 1) * KB))
+                kbar.append([sum(k[r, h // group, d] for r in rows) / len(rows) for d in range(D)])
+            for i in range(-(-n // QB)):
+                rows = range(s0 + i * QB, s0 + min(n, (i + 1) * QB))
+                qbar = [sum(q[r, h, d] for r in rows) / len(rows) for d in range(D)]
+                sc = [sum(a * c for a, c in zip(qbar, kbar[j])) for j in range(nk)]
+                best = sorted(range(nk), key=lambda j: (-sc[j], j))[:kk]
+                res[(b, h, i)] = sorted(best)
+    return res
+
+
+def test_selection_brute_force():
+    q, k, v, off = _case([300, 1, 700, 129], 4, 2, 6, seed=54)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 500)
+    ref = _select_by_loops(q, k, off, 500, 2)
+    for (b, h, i), sel in ref.items():
+        assert list(blocks[b, h, i, :counts[b, h, i]]) == sel, (b, h, i)
+
+
+def test_selection_invariants():
+    q, k, v, off = _case([900, 333, 1025], 2, 2, 8, seed=55)
+    base, counts, _ = jfa_oracle.block_select(q, k, off, 400)
+    # a positive scale of Q keeps the order of every score row
+    b2, _, _ = jfa_oracle.block_select(3.5 * q, k, off, 400)
+    np.testing.assert_array_equal(base, b2)
+    # a constant added to every key row moves all scores of a Q block alike
+    c = np.random.default_rng(1).standard_normal(8) * 5
+    b3, _, _ = jfa_oracle.block_select(q, k + c, off, 400)
+    np.testing.assert_array_equal(base, b3)
+    # rows permuted inside each K block
+    perm = np.arange(k.shape[0])
+    for b in range(3):
+        s0, s1 = off[b], off[b + 1]
+        for j0 in range(s0, s1, KB):
+            seg = perm[j0:min(s1, j0 + KB)]
+            perm[j0:min(s1, j0 + KB)] = seg[::-1]
+    b4, _, _ = jfa_oracle.block_select(q, k[perm], off, 400)
+    np.testing.assert_array_equal(base, b4)
+
+
+# ------------------------------------------------------ planted slips caught
+
+def _mutant_module(replace_from, replace_to):
+    import importlib.util
+    import inspect
+    src = inspect.getsource(jfa_oracle)
+    assert replace_from in src, replace_from
+    spec = importlib.util.spec_from_loader("jfa_oracle_sparse_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    exec(compile(src.replace(replace_from, replace_to), "jfa_oracle_sparse_mutant", "exec"),
+         mod.__dict__)
+    return mod
+
+
+def _check(mod):
+    q, k, v, off = _case([300, 1, 700, 129], 4, 2, 6, seed=54)
+    blocks, counts, _ = mod.block_select(q, k, off, 500)
+    ref = _select_by_loops(q, k, off, 500, 2)
+    for (b, h, i), sel in ref.items():
+        assert list(blocks[b, h, i, :counts[b, h, i]]) == sel, (b, h, i)
+    # the invariant that separates means from sums over ragged blocks
+    c = np.full(6, 3.0)
+    b3, _, _ = mod.block_select(q, k + c, off, 500)
+    np.testing.assert_array_equal(blocks, b3)
+    out, _ = mod.forward_sparse(q, k, v, off, 0.25, blocks, counts)
+    np.testing.assert_allclose(out, _torch_block_masked(q, k, v, off, 0.25, blocks, counts),
+                               atol=1e-12)
+
+
+def test_unmutated_copy_passes():
+    _check(_mutant_module("", ""))
+
+
+@pytest.mark.parametrize("slip", [
+    ("h // group, :].mean(axis=0) for j in range(nk)", "h // group, :].sum(axis=0) for j in range(nk)"),
+    ("order = np.argsort(-sc, kind=\"stable\")", "order = np.argsort(sc, kind=\"stable\")"),
+    ("keep = np.isin(kblock, blocks[b, h, i, :counts[b, h, i]])",
+     "keep = np.isin(kblock, blocks[b, h, min(i * 2, blocks.shape[2] - 1), :counts[b, h, i]])"),
+    ("                                h // group, :].mean(axis=0)",
+     "                                h % Hkv, :].mean(axis=0)"),
+])
+def test_planted_sparse_slips_are_caught(slip):
+    with pytest.raises(AssertionError):
+        _check(_mutant_module(*slip))
