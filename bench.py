@@ -67,6 +67,8 @@ KERNEL_DESC = {
     "finalize": "broadcast-Q dQ: sum of the chunk partials, bf16",
     "bwd_bs": "broadcast-Q backward in one pass (short dense Q): dK, dV and dQ partials",
     "fwd_combine": "broadcast-Q forward: merge of split sequences",
+    "sparse_pool": "block-sparse selection: K-block and Q-block means",
+    "sparse_select": "block-sparse selection: scores and top-k per Q block",
 }
 
 
@@ -100,6 +102,9 @@ def kernel_model(x):
         m["fwd_combine"] = (0.0, 0.0)
     else:
         m["bwd_q"] = (6.0 * H * D * pairs, 3 * T * row + 2 * T * rkv + stat)
+    # block-sparse selection: K and Q read once (the means are small)
+    m["sparse_pool"] = (0.0, T * rkv + T * row)
+    m["sparse_select"] = (0.0, 0.0)
     return m
 
 
@@ -131,7 +136,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu"], "bwd_kv": ["bwd_kv.cu"], "bwd_q": ["bwd_q.cu"], "bwd_qb": ["bwd_qb.cu"],
     "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"], "bwd_bs": ["bwd_bs.cu"],
-    "fwd_combine": ["fwd_bs.cu"],
+    "fwd_combine": ["fwd_bs.cu"], "sparse_pool": ["sparse.cu"], "sparse_select": ["sparse.cu"],
 }
 
 
@@ -409,6 +414,54 @@ def _time_steps(jfa, torch, x, steps, warmup, stream, dev, min_seconds=0.15):
     return fwd_ms, bwd_ms, kprof, launches, (t0, t1), steps
 
 
+def _time_sparse(jfa, torch, x, permille, steps, warmup, stream, dev, min_seconds=0.15):
+    """Block-sparse forward (selection + attention over the selected blocks)
+    of workload x, device-timed; returns (ms per step, kernel profile,
+    selected (query, key) pairs summed over the heads, host window, steps)."""
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    off = torch.from_numpy(x["offsets"]).to(dev)
+    ml, scale = x["max_len"], x["scale"]
+    blocks, counts = jfa.block_select(q, k, off, ml, permille)
+    out, lse = jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale)
+
+    def step():
+        jfa.block_select(q, k, off, ml, permille, blocks=blocks, counts=counts)
+        jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale, out=out, lse=lse)
+
+    for _ in range(warmup):
+        step()
+    jfa.jfa_sync_and_check()
+    torch.cuda.synchronize()
+    t_probe = time.time()
+    step()
+    torch.cuda.synchronize()
+    steps = int(min(max(steps, round(min_seconds / max(time.time() - t_probe, 1e-6))), 500))
+    jfa.profile_read()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    jfa.profile_enable(True)
+    h0 = time.time()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    jfa.profile_enable(False)
+    win = (h0, time.time())
+    kprof = jfa.profile_read()
+    jfa.jfa_sync_and_check()
+    # selected pairs, summed over heads: per (sequence, head, Q block) its rows
+    # times the keys of its blocks
+    bl, ct = blocks.cpu().numpy(), counts.cpu().numpy()
+    pairs = 0
+    for b, n in enumerate(x["lengths"].tolist()):
+        for i in range(-(-n // 256)):
+            rows = min(256, n - 256 * i)
+            for h in range(x["H"]):
+                sel = bl[b, h, i, :ct[b, h, i]]
+                pairs += rows * int(sum(min(128, n - 128 * int(j)) for j in sel))
+    return e0.elapsed_time(e1) / steps, kprof, pairs, win, steps
+
+
 def _workload_entry(x, wname, fwd_ms, bwd_ms, kprof, peak, hbm, clk, window, steps):
     fwd_f, bwd_f, pairs = _flops(x)
     (ff, fb), (bf, bb) = step_model(x)
@@ -568,6 +621,7 @@ def run_ours(args, x, wname):
     # The other workloads (rank 0 of a single-GPU run, unless --only): each
     # device-timed over a few steps through the same public API.
     workloads, variants = {}, {}
+    sparse_entry = None
     if ws == 1 and not args.only:
         workloads[wname] = (x, fwd_ms, bwd_ms, kprof, windows[0], args.steps)
         for other in W.ORDER:
@@ -581,6 +635,15 @@ def run_ours(args, x, wname):
             workloads[other] = (xo, f_ms, b_ms, kp, win, steps)
             del xo
             torch.cuda.empty_cache()
+        # block-sparse forward at a 0.5 selection ratio, against the dense forward
+        xs = W.make_inputs(W.WORKLOADS["jagged_self"])
+        sp_ms, sp_prof, sp_pairs, win, sp_steps = _time_sparse(
+            jfa, torch, xs, 500, max(3, min(args.steps, args.workload_steps)),
+            max(3, args.warmup), stream, dev)
+        windows.append(win)
+        sparse_entry = (xs, sp_ms, sp_prof, sp_pairs, win, sp_steps)
+        del xs
+        torch.cuda.empty_cache()
         # GQA and sliding-window variants, the same way
         for vname in W.VARIANTS:
             xo = W.make_inputs(W.variant(vname))
@@ -592,6 +655,29 @@ def run_ours(args, x, wname):
             del xo
             torch.cuda.empty_cache()
     clk.__exit__(None, None, None)
+    if sparse_entry is not None:
+        xs, sp_ms, sp_prof, sp_pairs, win, sp_steps = sparse_entry
+        dense_fwd_ms = workloads["jagged_self"][1]  # (x, fwd ms, ...) of the dense run
+        kern = _kernels_entry(xs, sp_prof, peak, hbm, "jagged_self")
+        fl = 4.0 * xs["D"] * sp_pairs  # sp_pairs counts every head
+        for kk in ("fwd",):  # the attention kernel's work is the selected pairs
+            if kk in kern:
+                ms = kern[kk]["ms_per_launch"]
+                kern[kk]["tflops"] = fl / (ms * 1e-3) / 1e12
+                kern[kk]["roofline_frac"] = kern[kk]["tflops"] / peak
+        dense_pairs = W.pairs(xs["lengths"])
+        variants["jagged_self_block_sparse500"] = {
+            "config": {k: v for k, v in _config(xs, "jagged_self").items()
+                       if k not in ("parallelism",)} | {"permille": 500},
+            "steps": sp_steps,
+            "fwd": {"ms": sp_ms, "tflops": fl / (sp_ms * 1e-3) / 1e12,
+                    "selected_fraction": sp_pairs / (xs["H"] * dense_pairs),
+                    "dense_fwd_ms": dense_fwd_ms,
+                    "speedup_vs_dense": (dense_fwd_ms / sp_ms) if dense_fwd_ms else None},
+            "kernels": kern,
+            "clocks": clk.summary([win]),
+        }
+        del xs
     for group in (workloads, variants):
         for other, entry in list(group.items()):
             if isinstance(entry, tuple):

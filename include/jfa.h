@@ -131,6 +131,46 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
                       cudaStream_t stream);
 
+/* Block-sparse attention ("Optimizing Jagged Flash Attention with TLX",
+ * section 3, "Block-sparse attention"): a cheap scoring step average-pools
+ * each Q block and each K block and keeps the top-k K/V blocks per Q block;
+ * the attention then runs over the selected blocks only.  Self-attention
+ * without a causal mask or window; GQA as for jfa_fwd_ex.
+ *
+ * Blocks: K block j of a sequence = its keys [128 j, 128 j + 128), Q block i
+ * = its query rows [256 i, 256 i + 256) (the last ones ragged).  With
+ * nqb = ceil(max_len / 256) and kcap = ceil(max_len / 128):
+ * - blocks: device int32 [B, H, nqb, kcap]; entry (b, h, i) lists the K
+ *   blocks that query head h of Q block i of sequence b attends to, strictly
+ *   ascending, in its first counts[b, h, i] slots;
+ * - counts: device int32 [B, H, nqb]; 0 for Q blocks past the sequence.
+ *
+ * jfa_block_select (stage 1) fills blocks and counts: the score of K block j
+ * for Q block i is the dot product (fp32) of the mean of the Q block's rows
+ * (query head h) with the mean of the K block's rows (K/V head h / (H /
+ * H_kv)); the k = max(1, ceil(permille * n / 1000)) highest scores of the
+ * sequence's n K blocks are kept (1 <= permille <= 1000), ties to the lower
+ * index; slots after the count are set to -1.  Two kernels that read K and
+ * Q once each; scratch: B * H_kv * kcap * D floats from the pool.  max_len
+ * must be <= 262144 (kcap <= 2048) and B <= 65535.
+ *
+ * jfa_fwd_sparse (stage 2) writes out and lse like jfa_fwd, with query row r
+ * of a sequence attending only to the keys of the K blocks listed for its Q
+ * block r / 256; a row whose list is empty gets out = 0 and lse = -inf.  The
+ * lists may come from jfa_block_select or from the caller; they are checked
+ * on the device (a count above the sequence's K blocks, or entries not
+ * strictly ascending below it, sets the device error word, reported by
+ * jfa_sync_and_check as JFA_ERR_INVALID_ARG, and nothing is written).  The
+ * forward kernel is the dense one following each item's list instead of all
+ * key tiles, so its time scales with the selected fraction. */
+jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
+                            int H_kv, int D, int max_len, int permille, int32_t* blocks,
+                            int32_t* counts, cudaStream_t stream);
+jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int32_t* offsets,
+                          int B, int H, int H_kv, int D, int max_len, float scale,
+                          const int32_t* blocks, const int32_t* counts, void* out, float* lse,
+                          cudaStream_t stream);
+
 /* Allocation-free forward pass.  The pages have no counterpart: this entry
  * point exists for callers that must not allocate device memory while the
  * library runs (memory owned and pre-partitioned by a host framework, for
@@ -208,7 +248,9 @@ typedef enum {
   JFA_KERNEL_FILL = 7,      /* outputs of an all-empty broadcast batch */
   JFA_KERNEL_BWD_BCAST_ONEPASS = 8, /* broadcast-Q backward, one pass (D = 64, q_len <= 128) */
   JFA_KERNEL_FWD_COMBINE = 9, /* broadcast-Q forward (q_len <= 128): merge of split sequences */
-  JFA_KERNEL_KINDS = 10
+  JFA_KERNEL_SPARSE_POOL = 10,   /* block-sparse selection: K-block means */
+  JFA_KERNEL_SPARSE_SELECT = 11, /* block-sparse selection: Q-block means, scores, top-k */
+  JFA_KERNEL_KINDS = 12
 } jfa_kernel_kind;
 
 /* Kernels enqueued by this library since the process started (all threads,

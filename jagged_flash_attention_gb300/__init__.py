@@ -14,7 +14,8 @@ import os
 from .build import LIB_PATH
 
 __all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq", "jfa_fwd_ex",
-           "jfa_bwd_ex", "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
+           "jfa_bwd_ex", "jfa_block_select", "jfa_fwd_sparse", "block_select", "forward_sparse",
+           "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
            "STATUS"]
 
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_CUDA",
@@ -129,6 +130,26 @@ def jfa_bwd_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, cau
                             _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
+def jfa_block_select(q, k, offsets, B, H, H_kv, D, max_len, permille, blocks, counts,
+                     stream=None):
+    fn = lib().jfa_block_select
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(q), _ptr(k), _ptr(offsets), B, H, H_kv, D, max_len, int(permille),
+              _ptr(blocks), _ptr(counts), _stream(stream)))
+
+
+def jfa_fwd_sparse(q, k, v, offsets, B, H, H_kv, D, max_len, scale, blocks, counts, out, lse,
+                   stream=None):
+    fn = lib().jfa_fwd_sparse
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len, float(scale),
+              _ptr(blocks), _ptr(counts), _ptr(out), _ptr(lse), _stream(stream)))
+
+
 def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale,
                        out, lse, stream=None):
     """Allocation-free forward (see include/jfa.h): for callers that must not
@@ -162,7 +183,7 @@ def jfa_sync_and_check(stream=None):
 
 
 KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill",
-                "bwd_bs", "fwd_combine")
+                "bwd_bs", "fwd_combine", "sparse_pool", "sparse_select")
 
 
 def launch_count() -> int:
@@ -242,3 +263,32 @@ def backward(q, k, v, offsets, max_len, out, lse, dout, causal=False, broadcast_
         jfa_bwd(q, k, v, offsets, B, H, D, max_len, 0, causal, scale, out, lse, dout, dq, dk, dv,
                 stream)
     return dq, dk, dv
+
+
+def block_select(q, k, offsets, max_len, permille, blocks=None, counts=None, stream=None):
+    """Top-k K blocks per (sequence, query head, 256-row Q block) (see
+    jfa_block_select in include/jfa.h); returns int32 (blocks [B, H, nqb,
+    kcap], counts [B, H, nqb])."""
+    import torch
+    B, H, Hkv, D, _ = _shapes(q, k, offsets, False)
+    nqb, kcap = -(-max_len // 256), -(-max_len // 128)
+    if blocks is None:
+        blocks = torch.empty((B, H, nqb, kcap), dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.empty((B, H, nqb), dtype=torch.int32, device=q.device)
+    jfa_block_select(q, k, offsets, B, H, Hkv, D, max_len, permille, blocks, counts, stream)
+    return blocks, counts
+
+
+def forward_sparse(q, k, v, offsets, max_len, blocks, counts, scale=None, out=None, lse=None,
+                   stream=None):
+    """Attention over the listed K blocks of each Q block (jfa_fwd_sparse)."""
+    import torch
+    B, H, Hkv, D, _ = _shapes(q, k, offsets, False)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((H, k.shape[0]), dtype=torch.float32, device=q.device)
+    jfa_fwd_sparse(q, k, v, offsets, B, H, Hkv, D, max_len, scale, blocks, counts, out, lse,
+                   stream)
+    return out, lse

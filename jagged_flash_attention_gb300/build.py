@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libjfa.so")
 SOURCES = ["aux.cu", "fwd.cu", "fwd_bs.cu", "bwd_kv.cu", "bwd_q.cu", "bwd_qb.cu", "bwd_bs.cu",
-           "api.cu"]
+           "sparse.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

@@ -713,6 +713,128 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
                 q, k, v, offsets, out, lse, dout, dq, dk, dv, stream);
 }
 
+jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
+                            int H_kv, int D, int max_len, int permille, int32_t* blocks,
+                            int32_t* counts, cudaStream_t stream) {
+  t_last_error.clear();
+  Shape s = make_shape(B, H, H_kv, D, max_len, 0, 0, 0, -1, -1, 1.f);
+  jfa_status st = check_common(s, q, k, k, offsets);
+  if (st != JFA_OK) return st;
+  if (permille < 1 || permille > 1000)
+    return fail(JFA_ERR_INVALID_ARG, "permille must be in [1, 1000] (got %d)", permille);
+  if (B > 65535) return fail(JFA_ERR_INVALID_ARG, "block-sparse: B must be <= 65535");
+  const long long kcap = cdivll(max_len, kBN), nqb = cdivll(max_len, kFwdRows);
+  if (kcap > kSparseMaxKBlocks)
+    return fail(JFA_ERR_INVALID_ARG, "block-sparse: max_len must be <= %d", kSparseMaxKBlocks * kBN);
+  if (!blocks || !counts || (reinterpret_cast<uintptr_t>(blocks) & 3u) ||
+      (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "blocks and counts must be non-null, 4-byte aligned");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != JFA_OK) return st;
+  if (max_len == 0) {  // no Q block anywhere: nothing to write
+    return finish(stream);
+  }
+  const size_t kbar_bytes = align256((size_t)B * H_kv * kcap * D * sizeof(float));
+  const size_t bytes = kbar_bytes + align256((size_t)B * H * nqb * D * sizeof(float));
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  SparseParams sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.q = static_cast<const __nv_bfloat16*>(q);
+  sp.k = static_cast<const __nv_bfloat16*>(k);
+  sp.offsets = offsets;
+  sp.B = B;
+  sp.H = H;
+  sp.Hkv = H_kv;
+  sp.G = s.G;
+  sp.D = D;
+  sp.max_len = max_len;
+  sp.permille = permille;
+  sp.nqb = (int)nqb;
+  sp.kcap = (int)kcap;
+  sp.kbar = static_cast<float*>(scratch);
+  sp.qbar = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kbar_bytes);
+  sp.blocks = blocks;
+  sp.counts = counts;
+  sp.err = ds->err;
+  e = run_kernel(JFA_KERNEL_SPARSE_POOL, stream, [&] { return launch_sparse_pool(sp, stream); });
+  if (e == cudaSuccess)
+    e = run_kernel(JFA_KERNEL_SPARSE_SELECT, stream, [&] { return launch_sparse_select(sp, stream); });
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "block selection launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(stream);
+}
+
+jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int32_t* offsets,
+                          int B, int H, int H_kv, int D, int max_len, float scale,
+                          const int32_t* blocks, const int32_t* counts, void* out, float* lse,
+                          cudaStream_t stream) {
+  t_last_error.clear();
+  const Shape s = make_shape(B, H, H_kv, D, max_len, 0, 0, 0, -1, -1, scale);
+  jfa_status st = check_common(s, q, k, v, offsets);
+  if (st != JFA_OK) return st;
+  if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "lse must be non-null, 4-byte aligned");
+  if (!blocks || !counts || (reinterpret_cast<uintptr_t>(blocks) & 3u) ||
+      (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return fail(JFA_ERR_INVALID_ARG, "blocks and counts must be non-null, 4-byte aligned");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != JFA_OK) return st;
+  if (s.max_len == 0) return finish(stream);
+  const long long kcap = cdivll(s.max_len, kBN), nqb = cdivll(s.max_len, kFwdRows);
+  const long long cap = (long long)s.H * s.B * nqb;
+  if (cap >= (1LL << 31) || (long long)s.B * s.H * nqb * kcap >= (1LL << 40))
+    return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  const size_t items_off = 256;
+  const size_t bytes = align256(items_off + cap * sizeof(Item));
+  CUtensorMap tq, tk, tv;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
+  if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
+  if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
+  Item* items = reinterpret_cast<Item*>(base + items_off);
+  // The scheduler also checks every list before the forward follows it.
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, 0, 0, 0, kFwdRows, items, (int)cap, hdr,
+                 ds->err};
+  sp.blocks = blocks;
+  sp.counts = counts;
+  sp.nqb = (int)nqb;
+  sp.kcap = (int)kcap;
+  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] { return launch_sched(sp, stream); });
+  if (e == cudaSuccess) {
+    FwdParams fp;
+    memset(&fp, 0, sizeof(fp));
+    set_variant(fp, s);
+    fp.offsets = offsets;
+    fp.B = s.B;
+    fp.H = s.H;
+    fp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.lse = lse;
+    fp.items = items;
+    fp.hdr = hdr;
+    fp.err = ds->err;
+    fp.blocks = blocks;
+    fp.counts = counts;
+    fp.nqb = (int)nqb;
+    fp.kcap = (int)kcap;
+    e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
+      return launch_fwd(s.D, false, false, tq, tk, tv, fp, (int)cap, stream, true);
+    });
+  }
+  cudaError_t e2 = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch free");
+  return finish(stream);
+}
+
 jfa_status jfa_worklist(const int32_t* offsets, int B, int H, int max_len, int q_len,
                         int broadcast_q, int causal, int list, int32_t* items, int capacity,
                         int32_t* count, cudaStream_t stream) {
@@ -840,6 +962,11 @@ jfa_status sync_and_read_error_word(cudaStream_t stream) {
     cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
     if (word & kErrTimeout)
       return fail(JFA_ERR_TIMEOUT, "a device-side bounded wait ran out (error bits 0x%x)", word);
+    if (word & kErrBadBlocks)
+      return fail(JFA_ERR_INVALID_ARG,
+                  "a block-sparse list failed device checks: a count above the sequence's key "
+                  "tiles, or entries not strictly ascending below it (error bits 0x%x)",
+                  word);
     if (word & kErrBadOffsets)
       return fail(JFA_ERR_INVALID_ARG,
                   "offsets failed device checks: offsets[0] != 0, decreasing, or a length above "

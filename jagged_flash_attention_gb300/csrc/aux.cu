@@ -76,7 +76,7 @@ constexpr int kPer = 8;
 struct SchedSmem {
   int hist[kMaxBuckets], base[kMaxBuckets], cursor[kMaxBuckets];
   int warp_tot[32];
-  int bad, nbig;
+  int bad, badblk, nbig;
   int4 big[kSchedThreads];  // sequences with many items: {b, pos, tiles, items}
 };
 __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
@@ -89,7 +89,10 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
   int4* s_big = sm.big;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < kMaxBuckets; i += blockDim.x) hist[i] = 0, cursor[i] = 0;
-  if (tid == 0) s_bad = (p.offsets[0] != 0);
+  if (tid == 0) {
+    s_bad = (p.offsets[0] != 0);
+    sm.badblk = 0;
+  }
   int Lr[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -127,14 +130,36 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       if (lane == __ffs(peers) - 1) atomicAdd(&hist[key], tot);
     }
   }
+  // Block lists of the sparse forward: per (sequence, head, 256-row query
+  // block) a count of at most the sequence's key tiles and strictly
+  // ascending key tiles below it.
+  if (p.blocks != nullptr) {
+    const long long n_lists = static_cast<long long>(p.B) * p.H * p.nqb;
+    for (long long r = tid; r < n_lists; r += blockDim.x) {
+      const int i = static_cast<int>(r % p.nqb);
+      const int b = static_cast<int>(r / p.nqb / p.H);
+      const int L = p.offsets[b + 1] - p.offsets[b];
+      if (L < 0 || L > p.max_len || i * kFwdRows >= L) continue;
+      const int nk = cdiv(L, kBN);
+      const int c = p.counts[r];
+      bool ok = c >= 0 && c <= nk;
+      const int32_t* lst = p.blocks + r * p.kcap;
+      for (int e = 0, prev = -1; ok && e < c; ++e) {
+        const int v = lst[e];
+        ok = v > prev && v < nk;
+        prev = v;
+      }
+      if (!ok) sm.badblk = 1;
+    }
+  }
   __syncthreads();
-  if (s_bad) {
+  if (s_bad || sm.badblk) {
     if (tid == 0) {
       p.hdr->n_items = 0;
       p.hdr->T = 0;
       p.hdr->ticket = 0;
       p.hdr->valid = 0;
-      atomicOr(p.err, kErrBadOffsets);
+      atomicOr(p.err, s_bad ? kErrBadOffsets : kErrBadBlocks);
     }
     return;
   }

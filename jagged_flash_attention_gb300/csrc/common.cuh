@@ -137,6 +137,11 @@ struct SchedParams {
   WorkHeader* hdr;
   int* err;
   int wl = kNoWindow, wr = kNoWindow;  // the local mask, for the cost order
+  // Block-sparse forward: the lists the forward will follow, checked here
+  // (nullptr: none).
+  const int32_t* blocks = nullptr;
+  const int32_t* counts = nullptr;
+  int nqb = 0, kcap = 0;
 };
 
 // Every parameter block below carries the GQA group G (query heads per K/V
@@ -159,6 +164,10 @@ struct FwdParams {
   const int* kt_off;
   float* part_o;
   float* part_lse;
+  // Block-sparse forward: key-tile lists [B][H][nqb][kcap] and their counts.
+  const int32_t* blocks;
+  const int32_t* counts;
+  int nqb, kcap;
 };
 
 struct BwdParams {
@@ -228,11 +237,31 @@ struct FinParams {
   const WorkHeader* hdr;  // header of the dQ-pass list (n_chunks, valid)
 };
 
+// Block-sparse attention, stage 1 (sparse.cu): K-block means, then per
+// (sequence, query head, 256-row Q block) the top-k of its sequence's
+// 128-key K blocks by the dot product of the two means.  Lists: blocks
+// [B][H][nqb][kcap] (ascending, -1 after counts), counts [B][H][nqb].
+constexpr int kSparseMaxKBlocks = 2048;  // kcap limit: max_len <= 262144
+struct SparseParams {
+  const __nv_bfloat16* q;  // [T, H, D]
+  const __nv_bfloat16* k;  // [T, Hkv, D]
+  const int32_t* offsets;
+  int B, H, Hkv, G, D, max_len, permille;
+  int nqb, kcap;  // ceil(max_len / 256), ceil(max_len / 128)
+  float* kbar;     // scratch fp32 [B][Hkv][kcap][D]: K-block means
+  float* qbar;     // scratch fp32 [B][H][nqb][D]: Q-block means
+  int32_t* blocks;
+  int32_t* counts;
+  int* err;
+};
+
 // Host-side launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
 // causal: any local mask (the kernels read wl, wr from the parameters).
+// sparse: the block-sparse forward (self-attention, no mask; p.blocks).
 cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s,
+                       bool sparse = false);
 // tdk / tdv: the dK / dV outputs as maps like the inputs' (TMA stores).
 cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
@@ -262,6 +291,8 @@ cudaError_t launch_qb_sched(const QbSchedParams& p, cudaStream_t s);
 cudaError_t launch_export_list(const WorkHeader* hdr, const void* items, int qb, int32_t* out,
                                int capacity, int32_t* count, cudaStream_t s);
 cudaError_t launch_finalize(const FinParams& p, int sms, cudaStream_t s);
+cudaError_t launch_sparse_pool(const SparseParams& p, cudaStream_t s);
+cudaError_t launch_sparse_select(const SparseParams& p, cudaStream_t s);
 cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, long long rows, int D,
                               cudaStream_t s);
 cudaError_t prepare_kernels(int device);

@@ -96,7 +96,10 @@ struct FwdCtl {
 // LOCAL: a local mask (causal or a sliding window, bounds p.wl / p.wr): a
 // query tile visits only the key tiles that hold admissible keys of its
 // rows, and the item streams the union of its two tiles' ranges.
-template <bool BCAST, bool LOCAL>
+// SPARSE: block-sparse attention (self-attention, no mask): both query tiles
+// of the item visit the key tiles of the item's block list, in its
+// (ascending) order.
+template <bool BCAST, bool LOCAL, bool SPARSE>
 __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
   FwdItem f;
   const Item it = p.items[idx];
@@ -124,7 +127,9 @@ __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
       q.row = start - q.shift;
       q.n_kv = 0;
       if (q.nq > 0) {
-        if (LOCAL)
+        if (SPARSE)
+          q.n_kv = p.counts[(static_cast<long long>(f.b) * p.H + f.h) * p.nqb + pair];
+        else if (LOCAL)
           key_tiles(q.q_lo, q.q_lo + q.nq - 1, f.L, p.wl, p.wr, &q.j0, &q.n_kv);
         else
           q.n_kv = cdiv(f.L, kBN);
@@ -138,6 +143,19 @@ __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
   f.J0 = hi > 0 ? lo : 0;
   f.N = hi > 0 ? hi - lo : 0;
   return f;
+}
+
+// Block list of a sparse item: key tiles in ascending order.
+__device__ __forceinline__ const int32_t* sparse_list(const FwdParams& p, const FwdItem& f) {
+  const long long row = (static_cast<long long>(f.b) * p.H + f.h) * p.nqb + f.t[0].q_lo / kFwdRows;
+  return p.blocks + row * p.kcap;
+}
+
+// Key tile of step j of the item's key-tile stream.
+template <bool LOCAL, bool SPARSE>
+__device__ __forceinline__ int stream_tile(const FwdParams& p, const FwdItem& f, int j) {
+  if (SPARSE) return sparse_list(p, f)[j];
+  return (LOCAL ? f.J0 : 0) + j;
 }
 
 // Key tile j of a sequence: box row coordinate, shift and valid key count.
@@ -179,7 +197,7 @@ __device__ __forceinline__ bool next_item(FwdCtl* c, uint32_t n, FwdItem* f, boo
   return f->b >= 0;
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool SPARSE>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const FwdParams& p, uint8_t* smem, FwdCtl* c) {
   using C = FwdCfg<D>;
@@ -220,7 +238,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     while (idx >= n_items && ok) idx = clc_take();
     FwdItem f;
     if (idx >= 0 && ok)
-      f = decode<BCAST, LOCAL>(p, idx, T);
+      f = decode<BCAST, LOCAL, SPARSE>(p, idx, T);
     else
       f.b = -1;
     c->item[slot] = f;
@@ -245,7 +263,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     for (int j = 0; j <= f.N && ok; ++j) {
       if (j < f.N) {
         const int st = nk % C::NSK;
-        const KvTile kt = kv_tile(f.off0, f.L, (LOCAL ? f.J0 : 0) + j, T);
+        const KvTile kt = kv_tile(f.off0, f.L, stream_tile<LOCAL, SPARSE>(p, f, j), T);
         if (!mbar_wait(&c->k_empty[st], ((nk / C::NSK) & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -260,7 +278,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       if (j >= 1) {
         const int st = nv % C::NSV;
-        const KvTile kt = kv_tile(f.off0, f.L, (LOCAL ? f.J0 : 0) + j - 1, T);
+        const KvTile kt = kv_tile(f.off0, f.L, stream_tile<LOCAL, SPARSE>(p, f, j - 1), T);
         if (!mbar_wait(&c->v_empty[st], ((nv / C::NSV) & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -394,7 +412,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
   }
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool SPARSE>
 __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   using C = FwdCfg<D>;
   const int t = threadIdx.x >> 7;   // query tile of this warpgroup
@@ -431,6 +449,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       continue;
     }
     float m_used = -INFINITY, l_run = 0.f;
+    const int32_t* lst = SPARSE ? sparse_list(p, f) : nullptr;
     for (int j = 0; j < q.n_kv; ++j, ++u) {
       if (!mbar_wait_warp(&c->s_full[t], u & 1, &c->abort, p.err)) { ok = false; break; }
       tc_fence_after();
@@ -443,7 +462,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
       for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[ch][i]);
-      const int jk = LOCAL ? q.j0 + j : j;  // key tile of the sequence
+      const int jk = SPARSE ? lst[j] : (LOCAL ? q.j0 + j : j);  // key tile of the sequence
       const KvTile kt = kv_tile(f.off0, f.L, jk, T);
       const int key0 = jk * kBN - kt.shift;  // local key index of column 0
       const int qa = q.q_lo - q.shift;       // local query index of row 0 of the box
@@ -548,7 +567,7 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
   }
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool SPARSE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -600,9 +619,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tbase = c->tmem_base;
 
   if (warp < 8) {
-    softmax_role<D, LOCAL, BCAST>(p, c, tbase);
+    softmax_role<D, LOCAL, BCAST, SPARSE>(p, c, tbase);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, LOCAL, BCAST>(&tq, &tk, &tv, p, smem, c);
+    if (lane == 0) producer_role<D, LOCAL, BCAST, SPARSE>(&tq, &tk, &tv, p, smem, c);
   } else {
     mma_role<D, LOCAL, BCAST>(p, smem, c, tbase);
   }
@@ -615,14 +634,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool SPARSE = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, int grid, cudaStream_t s) {
   using C = FwdCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(FwdCtl) <= 512, "control block");
   static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
-  auto kern = fwd_kernel<D, LOCAL, BCAST>;
+  auto kern = fwd_kernel<D, LOCAL, BCAST, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kFwdThreads, C::kSmem, s>>>(tq, tk, tv, p);
@@ -632,7 +651,13 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s) {
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s,
+                       bool sparse) {
+  if (sparse) {
+    if (causal || bcast) return cudaErrorInvalidValue;
+    if (D == 128) return launch_fwd_t<128, false, false, true>(tq, tk, tv, p, grid, s);
+    return launch_fwd_t<64, false, false, true>(tq, tk, tv, p, grid, s);
+  }
   if (D == 128) {
     if (bcast) return launch_fwd_t<128, false, true>(tq, tk, tv, p, grid, s);
     if (causal) return launch_fwd_t<128, true, false>(tq, tk, tv, p, grid, s);

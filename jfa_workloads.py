@@ -149,3 +149,29 @@ def pairs(lengths, causal=False, q_len=0, broadcast_q=False, window=(-1, -1)) ->
         hi = np.minimum(n - 1, i + wr) if wr >= 0 else np.full_like(i, n - 1)
         total += int((hi - lo + 1).sum())
     return total
+
+
+def random_block_lists(lengths, H, max_len, seed, p_keep=0.5, p_empty=0.0):
+    """Seeded random block lists in the layout of the block-sparse forward:
+    blocks int32 [B, H, nqb, kcap] (ascending K-block indices, -1 after the
+    count) and counts int32 [B, H, nqb], nqb = ceil(max_len / 256), kcap =
+    ceil(max_len / 128).  Each K block of the sequence is kept with
+    probability p_keep (at least one unless the list is drawn empty, with
+    probability p_empty); Q blocks past a sequence get count 0."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(lengths, dtype=np.int64)
+    nqb, kcap = -(-max_len // 256), -(-max_len // 128)
+    blocks = np.full((L.size, H, nqb, kcap), -1, dtype=np.int32)
+    counts = np.zeros((L.size, H, nqb), dtype=np.int32)
+    for b, n in enumerate(L.tolist()):
+        nk = -(-n // 128)
+        for h in range(H):
+            for i in range(-(-n // 256)):
+                if rng.random() < p_empty:
+                    continue
+                keep = np.flatnonzero(rng.random(nk) < p_keep)
+                if keep.size == 0:
+                    keep = np.array([rng.integers(0, nk)])
+                blocks[b, h, i, :keep.size] = keep
+                counts[b, h, i] = keep.size
+    return blocks, counts

@@ -1,0 +1,174 @@
+"""GPU parity of the block-sparse variant ("Optimizing Jagged Flash Attention
+with TLX", section 3, "Block-sparse attention") against the fp64 oracle.
+
+* Stage 2 (jfa_fwd_sparse) on seeded random block lists drawn by the input
+  generator, element by element: ragged sequences, lists with one block, all
+  blocks, none (O = 0, LSE = -inf), D = 64 and 128, GQA.
+* Stage 1 (jfa_block_select): counts exactly; the selected set equals the
+  oracle's wherever the oracle's scores separate the k-th and (k+1)-th best
+  by more than the fp32 rounding of the GPU's scores, and is valid (no
+  unselected block scores clearly higher than a selected one) everywhere;
+  unused slots hold -1.
+* Both stages together against the oracle's own selection and forward, on
+  inputs whose selections are unambiguous.
+* A bad list is caught on the device and nothing is written.
+"""
+import numpy as np
+import pytest
+import torch
+
+import jfa_workloads as W
+from oracle import jfa_oracle as orc
+from tests.gpu_common import compare, f64, inputs
+
+pytestmark = pytest.mark.gpu
+
+GAP = 1e-4  # fp32 score rounding is far below this
+
+
+def _dev(x):
+    dev = torch.device("cuda")
+    return ((x[n].to(dev) for n in ("q", "k", "v")), torch.from_numpy(x["offsets"]).to(dev))
+
+
+def _gpu_sparse(x, blocks, counts):
+    import jagged_flash_attention_gb300 as jfa
+    (q, k, v), off = _dev(x)
+    bl = torch.from_numpy(np.ascontiguousarray(blocks, dtype=np.int32)).cuda()
+    ct = torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).cuda()
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], bl, ct, scale=x["scale"])
+    jfa.jfa_sync_and_check()
+    return {"out": f64(out), "lse": f64(lse)}
+
+
+def _oracle_sparse(x, blocks, counts):
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    out, lse = orc.forward_sparse(q, k, v, x["offsets"], x["scale"], blocks, counts)
+    return {"out": out, "lse": lse}
+
+
+LIST_CASES = {
+    "d128_edges_half": (dict(name="jagged_self", lengths=[1, 127, 128, 129, 255, 256, 257, 700],
+                             H=2), 0.5, 0.0),
+    "d128_one_block": (dict(name="jagged_self", lengths=[300, 1000, 40], H=2), 0.0, 0.0),
+    "d128_all_blocks": (dict(name="jagged_self", lengths=[513, 2], H=2), 1.0, 0.0),
+    "d128_some_empty": (dict(name="jagged_self", lengths=[600, 260, 5], H=2), 0.4, 0.3),
+    "d64_gqa": (dict(name="tiny_self", lengths=[900, 3, 385], H=4, Hkv=2), 0.5, 0.1),
+    "d128_gqa_long": (dict(name="jagged_self", lengths=[3000, 129], H=4, Hkv=1), 0.3, 0.0),
+}
+
+
+@pytest.mark.parametrize("case", list(LIST_CASES), ids=list(LIST_CASES))
+def test_sparse_forward_on_given_lists(case):
+    spec, p_keep, p_empty = LIST_CASES[case]
+    spec = dict(spec)
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    blocks, counts = W.random_block_lists(x["lengths"], x["H"], x["max_len"], seed=7,
+                                          p_keep=p_keep, p_empty=p_empty)
+    g = _gpu_sparse(x, blocks, counts)
+    r = _oracle_sparse(x, blocks, counts)
+    print(case, compare(g, r, ("out", "lse")))
+
+
+def _gpu_select(x, permille):
+    import jagged_flash_attention_gb300 as jfa
+    (q, k, _), off = _dev(x)
+    blocks, counts = jfa.block_select(q, k, off, x["max_len"], permille)
+    jfa.jfa_sync_and_check()
+    return blocks.cpu().numpy(), counts.cpu().numpy()
+
+
+@pytest.mark.parametrize("permille,spec", [
+    (500, dict(name="jagged_self", lengths=[1, 300, 1000, 129, 2048], H=4, Hkv=2)),
+    (250, dict(name="tiny_self", lengths=[700, 64, 1500], H=3)),
+    (1000, dict(name="jagged_self", lengths=[500, 130], H=2)),
+    (1, dict(name="jagged_self", lengths=[900, 17], H=2)),
+])
+def test_block_select(permille, spec):
+    spec = dict(spec)
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    gb, gc = _gpu_select(x, permille)
+    rb, rc, rs = orc.block_select(f64(x["q"]), f64(x["k"]), x["offsets"], permille)
+    np.testing.assert_array_equal(gc, rc)
+    exact = 0
+    for b in range(gc.shape[0]):
+        for h in range(gc.shape[1]):
+            for i in range(gc.shape[2]):
+                c = int(gc[b, h, i])
+                assert np.all(gb[b, h, i, c:] == -1)
+                if c == 0:
+                    continue
+                sel = gb[b, h, i, :c]
+                assert np.all(np.diff(sel) > 0)
+                sc = rs[b, h, i]
+                nk = int(np.sum(~np.isnan(sc)))
+                assert sel.min() >= 0 and sel.max() < nk
+                unsel = np.setdiff1d(np.arange(nk), sel)
+                if unsel.size:  # valid: nothing left out scores clearly above a kept block
+                    assert sc[unsel].max() <= sc[sel].min() + GAP
+                srt = np.sort(sc[:nk])[::-1]
+                if c == nk or srt[c - 1] - srt[c] > GAP:
+                    np.testing.assert_array_equal(sel, rb[b, h, i, :c])
+                    exact += 1
+    assert exact > 0
+    print(permille, "exactly compared lists:", exact)
+
+
+def test_select_then_forward_matches_oracle():
+    """Stage 1 then stage 2 on the GPU against the oracle's own selection and
+    sparse forward (inputs whose selections are unambiguous)."""
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs("jagged_self", [1500, 700, 257], H=2)
+    q64, k64 = f64(x["q"]), f64(x["k"])
+    rb, rc, rs = orc.block_select(q64, k64, x["offsets"], 500)
+    # the seeded inputs separate the k-th and (k+1)-th scores clearly
+    for idx in np.ndindex(rc.shape):
+        c = int(rc[idx])
+        if c == 0:
+            continue
+        srt = np.sort(rs[idx][~np.isnan(rs[idx])])[::-1]
+        assert c == srt.size or srt[c - 1] - srt[c] > GAP, idx
+    (q, k, v), off = _dev(x)
+    blocks, counts = jfa.block_select(q, k, off, x["max_len"], 500)
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], blocks, counts, scale=x["scale"])
+    jfa.jfa_sync_and_check()
+    g = {"out": f64(out), "lse": f64(lse)}
+    r = _oracle_sparse(x, rb, rc)
+    print(compare(g, r, ("out", "lse")))
+
+
+def test_full_selection_equals_dense():
+    x = inputs("jagged_self", [1000, 129, 3], H=2)
+    blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=1, p_keep=1.0)
+    g = _gpu_sparse(x, blocks, counts)
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    out, lse = orc.forward(q, k, v, x["offsets"], x["scale"])
+    compare(g, {"out": out, "lse": lse}, ("out", "lse"))
+
+
+def test_bad_list_is_caught_on_the_device():
+    import jagged_flash_attention_gb300 as jfa
+    x = inputs("jagged_self", [600, 300], H=2)
+    blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=3, p_keep=1.0)
+    blocks[0, 1, 1, :2] = [3, 2]  # not ascending
+    (q, k, v), off = _dev(x)
+    bl = torch.from_numpy(blocks).cuda()
+    ct = torch.from_numpy(counts).cuda()
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((2, x["T"]), 7.0, device="cuda")
+    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], x["scale"], bl, ct, out, lse)
+    with pytest.raises(jfa.JfaError, match="block-sparse list"):
+        jfa.jfa_sync_and_check()
+    assert torch.isnan(out).all() and (lse == 7.0).all()
+    # a count above the sequence's K blocks
+    blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=3, p_keep=1.0)
+    counts[1, 0, 0] = 4  # sequence 1 has 3 K blocks
+    blocks[1, 0, 0, 3] = 3
+    bl = torch.from_numpy(blocks).cuda()
+    ct = torch.from_numpy(counts).cuda()
+    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], x["scale"], bl, ct, out, lse)
+    with pytest.raises(jfa.JfaError, match="block-sparse list"):
+        jfa.jfa_sync_and_check()
+    # the library still works afterwards
+    blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=4)
+    compare(_gpu_sparse(x, blocks, counts), _oracle_sparse(x, blocks, counts), ("out", "lse"))
