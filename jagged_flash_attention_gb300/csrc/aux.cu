@@ -183,6 +183,16 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
   // over items.  Heads outer, tiles inner, so that consecutive items share
   // K/V (or Q) in L2; forward causal: longest query tile first.
   const bool reverse = !p.backward && p.causal;
+  // Broadcast dK/dV list: heads outermost over the whole list (every item
+  // costs the same), so that a CTA's consecutive items share the head and
+  // with it the dense Q tiles its shared memory still holds.  Every
+  // sequence's block of items is H * tiles long, so pos / H is the offset of
+  // its tiles within one head's part.
+  const bool head_outer = p.broadcast && p.backward;
+  const int per_head = total / p.H;
+  auto slot = [&](int pos, int h, int t, int nt) {
+    return head_outer ? h * per_head + pos / p.H + t : pos + h * nt + t;
+  };
   constexpr int kOwnItems = 32;  // at most this many: written by the thread itself
   for (int i = 0; i * static_cast<int>(blockDim.x) < p.B; ++i) {
     if (tid == 0) s_nbig = 0;
@@ -213,10 +223,9 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       pos = base[key] + first + pre;
     }
     if (n > 0 && n <= kOwnItems) {
-      int j = pos;
       for (int h = 0; h < p.H; ++h)
-        for (int t = 0; t < nt; ++t, ++j)
-          p.items[j] = make_int2(b, (h << 16) | (reverse ? nt - 1 - t : t));
+        for (int t = 0; t < nt; ++t)
+          p.items[slot(pos, h, t, nt)] = make_int2(b, (h << 16) | (reverse ? nt - 1 - t : t));
     } else if (n > kOwnItems) {
       s_big[atomicAdd(&s_nbig, 1)] = make_int4(b, pos, nt, n);
     }
@@ -225,7 +234,7 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       const int4 g = s_big[k];
       for (int j = lane; j < g.w; j += 32) {
         const int h = j / g.z, t = j - h * g.z;
-        p.items[g.y + j] = make_int2(g.x, (h << 16) | (reverse ? g.z - 1 - t : t));
+        p.items[slot(g.y, h, t, g.z)] = make_int2(g.x, (h << 16) | (reverse ? g.z - 1 - t : t));
       }
     }
     __syncthreads();

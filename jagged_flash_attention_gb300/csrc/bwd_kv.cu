@@ -105,6 +105,10 @@ struct KvCtl {
   // full barriers are per 64-column slab ([stage][slab]; the statistics
   // ride with slab 0), so that a product's first K steps need only slab 0.
   uint64_t q_full[2][2], q_empty[2], do_full[2][2], do_empty[2];
+  // Row statistics of a stage: loaded as soon as the math's dS part of the
+  // stage's previous tile has read them (before its Q is free), so that a Q
+  // box a stage already holds needs no copy on the issuer's path.
+  uint64_t stat_full[2], stat_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dkdv_full, dv_empty, dk_empty;
   uint64_t epi;  // math-warp sync of the staged epilogue stores
@@ -221,8 +225,15 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   using C = KvCfg<D>;
   const int n_items = p.hdr->n_items;
   const int T = p.hdr->T;
-  uint32_t it = 0, gq = 0, gdo = 0, nk = 0, nv = 0;  // gdo: stages whose dO was issued
+  // gdo / gst: stages whose dO / statistics copy was issued
+  uint32_t it = 0, gq = 0, gdo = 0, gst = 0, nk = 0, nv = 0;
   bool ok = true;
+  // Q box each ring stage holds (query head, row; -1: none).  When the next
+  // tile of a stage is the same box (broadcast: consecutive items of one head
+  // walk the same dense-Q tiles) it is not loaded again; only its row
+  // statistics are.  Nothing but these loads writes a Q stage.
+  static_assert(C::NSQ == 2, "held boxes: two stages");
+  long long held0 = -1, held1 = -1;
   // One-item lookahead: the next item is taken and decoded while this one's
   // loads go out, and its K, V and first Q / dO boxes are prefetched into
   // L2, so that at the item boundary they come from L2 rather than HBM.
@@ -293,24 +304,41 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
                       qh, qb.row);
       }
       ++gdo;  // counted now: a wait below that gives up must not hide these copies from the drain
+      // Row statistics of the box: 32 whole groups (1 KB).
+      if (!mbar_wait(&c->stat_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&c->stat_full[st], C::kStatBytes);
+      bulk_load(smem + C::kStat + st * C::kStatBytes, stat_src<BCAST>(p, f, qh, qb, t, T),
+                C::kStatBytes, &c->stat_full[st]);
+      ++gst;
       if (!mbar_wait(&c->q_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
         ok = false;
         break;
       }
-      // Row statistics of the box: 32 whole groups (1 KB).
-      const float* ssrc = stat_src<BCAST>(p, f, qh, qb, t, T);
+      const long long tag = (static_cast<long long>(qh) << 32) | static_cast<uint32_t>(qb.row);
+      const bool reuse = (st == 0 ? held0 : held1) == tag;
+      if (st == 0)
+        held0 = tag;
+      else
+        held1 = tag;
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s) {
-        mbar_arrive_expect_tx(&c->q_full[st][s], 16384 + (s == 0 ? C::kStatBytes : 0));
-        if (s == 0)
-          bulk_load(smem + C::kStat + st * C::kStatBytes, ssrc, C::kStatBytes, &c->q_full[st][0]);
+        if (reuse) {  // Q already in the stage: the phase completes at once
+          mbar_arrive(&c->q_full[st][s]);
+          continue;
+        }
+        mbar_arrive_expect_tx(&c->q_full[st][s], 16384);
         tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st][s], s * 64, qh,
                     qb.row);
       }
       ++gq;
       if (i == 0) {
-        fetch(nx);
-        if (nx.b >= 0) prefetch(nx);
+        // V first: the item's first dP^T waits for it.  The next item's
+        // ticket is taken before the wait and decoded (two dependent global
+        // loads) only once V's copy is out.
+        const int nidx = atomicAdd(&p.hdr->ticket, 1);
         if (!mbar_wait(&c->v_empty, (it & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
@@ -320,6 +348,10 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         for (int s = 0; s < C::kSlabs; ++s)
           tma_load_3d(smem + C::kV + s * 16384, tv, &c->v_full, s * 64, f.h, f.kt.row);
         ++nv;
+        if (nidx < n_items) {
+          nx = decode<LOCAL, BCAST>(p, nidx, T);
+          prefetch(nx);
+        }
       }
     }
     ++it;
@@ -334,6 +366,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   for (uint32_t g = gdo > C::NSQ ? gdo - C::NSQ : 0; g < gdo; ++g)
 #pragma unroll
     for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+  for (uint32_t g = gst > C::NSQ ? gst - C::NSQ : 0; g < gst; ++g)
+    drain_wait(&c->stat_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
 }
 
 template <int D, bool LOCAL>
@@ -494,9 +528,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     const int t = q_tile(f, i);
     const RowBox qb = q_box<BCAST>(p, f, t, T);
     const int q0 = t * kBM - qb.shift;  // local query index of column 0
-    // (already complete once S^T is; waited on here for the statistics'
-    // visibility)
-    if (!mbar_wait_warp(&c->q_full[g % C::NSQ][0], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
+    if (!mbar_wait_warp(&c->stat_full[g % C::NSQ], (g / C::NSQ) & 1, &c->abort, p.err)) return false;
     const float4* st4 = stats(g);
     // Admissible query columns [lo, hi): the box's rows of the sequence
     // and, with a local mask, the queries in [key - wr, key + wl].
@@ -574,6 +606,9 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&c->ds_full);
+    // this warp's reads of the stage's statistics are done
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&c->stat_empty[g % C::NSQ]);
     return true;
   };
   uint32_t it = 0, gq = 0, ep = 0;
@@ -786,6 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c->do_full[i][0], 1);
       mbar_init(&c->do_full[i][1], 1);
       mbar_init(&c->do_empty[i], 1);
+      mbar_init(&c->stat_full[i], 1);
+      mbar_init(&c->stat_empty[i], kMathWarps);  // after each math warp's dS part
       mbar_init(&c->item_full[i], 1);
       mbar_init(&c->item_empty[i], kMathWarps + 1);  // math warps + the MMA warp
     }

@@ -99,6 +99,8 @@ def test_broadcast_lists(case):
     expect = collections.Counter((b, h, t) for b in range(B) for h in range(H)
                                  for t in range(_cdiv(int(L[b]), 128)))
     assert collections.Counter(map(tuple, items[:, :3].tolist())) == expect
+    # heads outermost over the whole list (consecutive items share the dense Q)
+    assert np.all(np.diff(items[:, 1]) >= 0)
     # dQ pass: equal chunks of the key-tile stream of every (head, pair)
     items, nc, sms = _run(L, H, BCAST_Q, q_len=q_len)
     pairs = _cdiv(q_len, 256)
