@@ -83,7 +83,9 @@ struct FwdCtl {
   // K stages have one full barrier per 64-column slab ([stage][slab]): S's
   // first K steps need only slab 0.
   uint64_t k_full[4][2], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
+  // P_t in two halves (keys 0-63, 64-127): PV_t's first four K steps start
+  // while the softmax writes the second half.
+  uint64_t s_full[2], p_half[2], p_full[2], o_ready[2], o_free[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   FwdItem item[2];  // decoded by the producer; b < 0: no more items
@@ -316,14 +318,15 @@ __device__ __forceinline__ void issue_s(uint32_t leader, uint32_t tbase, int t, 
   }
 }
 
-// O_t += P_t V: dv is the MN-major descriptor of the V stage.
+// O_t += P_t V, K steps [k0, k1) (16 keys each): dv is the MN-major
+// descriptor of the V stage.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t tbase, int t, uint64_t dv,
-                                         bool accumulate) {
+                                         bool accumulate, int k0, int k1) {
   using C = FwdCfg<D>;
   const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
 #pragma unroll
-  for (int k = 0; k < kBN / 16; ++k) {
+  for (int k = k0; k < k1; ++k) {
     if (leader)
       mma_ts(tbase + C::colO(t), tbase + C::colS(t) + k * 8, desc_add(dv, k * 2048), id_pv,
              accumulate || (k > 0));
@@ -364,15 +367,18 @@ __device__ void mma_role(const FwdParams& p, uint8_t* smem, FwdCtl* c, uint32_t 
       for (int t = 0; t < 2; ++t) {
         const int nkv = f.t[t].n_kv;
         const int lj = LOCAL ? f.J0 + j - f.t[t].j0 : j;  // step j in query tile t's own key tiles
-        if (lj >= 1 && lj - 1 < nkv) {  // O_t += P_t V of the previous step
-          if (!mbar_wait_warp(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
-          ++np[t];
+        if (lj >= 1 && lj - 1 < nkv) {  // O_t += P_t V of the previous step, by halves of P
+          if (!mbar_wait_warp(&c->p_half[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
           if (lj == 1 && !mbar_wait_warp(&c->o_free[t], (ito[t] & 1) ^ 1, &c->abort, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv<D>(leader, tbase, t, dv, lj > 1);
+          issue_pv<D>(leader, tbase, t, dv, lj > 1, 0, kBN / 32);
+          if (!mbar_wait_warp(&c->p_full[t], np[t] & 1, &c->abort, p.err)) { ok = false; break; }
+          ++np[t];
+          tc_fence_after();
+          issue_pv<D>(leader, tbase, t, dv, true, kBN / 32, kBN / 16);
           if (leader) mma_commit(&c->o_ready[t]);
         }
         if (lj >= 0 && lj < nkv && j < f.N) {  // S_t = Q_t K^T, slab 1 of K waited for between its halves
@@ -521,26 +527,34 @@ __device__ void softmax_role(const FwdParams& p, FwdCtl* c, uint32_t tbase) {
           pk[i / 2 + 1] = pack_bf16x2(p2, p3);
         }
         tmem_st16(ts + ch * 16, pk);
-      }
-      const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
-      l_run = l_run * alpha + ((a0.x + a0.y) + (a1.x + a1.y));
-      if (j > 0) {
-        // PV of the previous tile has landed before S of this one (issue
-        // order); observe it, then correct O if any row raised its max.
-        if (!mbar_wait_warp(&c->o_ready[t], (u - 1) & 1, &c->abort, p.err)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, raise)) {
+        if (ch == 1) {
+          // Keys 0-63 of P are stored (and their scores dead).  PV of the
+          // previous tile was issued before S of this one, so it has
+          // completed by now (MMAs complete in issue order): observe it and
+          // correct O before the first half of P is handed over.
+          if (j > 0) {
+            if (!mbar_wait_warp(&c->o_ready[t], (u - 1) & 1, &c->abort, p.err)) { ok = false; break; }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(to + ch * 32, o);
-            tmem_wait_ld();
+              for (int oc = 0; oc < D / 32; ++oc) {
+                uint32_t o[32];
+                tmem_ld32(to + oc * 32, o);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(to + ch * 32, o);
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(to + oc * 32, o);
+              }
+            }
           }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&c->p_half[t]);
         }
       }
+      if (!ok) break;
+      const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+      l_run = l_run * alpha + ((a0.x + a0.y) + (a1.x + a1.y));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c->p_full[t]);
@@ -593,6 +607,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->s_full[i], 1);
+      mbar_init(&c->p_half[i], kBM);
       mbar_init(&c->p_full[i], kBM);
       mbar_init(&c->o_ready[i], 1);
       mbar_init(&c->o_free[i], kBM);
