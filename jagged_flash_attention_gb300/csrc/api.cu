@@ -135,12 +135,14 @@ jfa_status device_state(DeviceState** out) {
   return JFA_OK;
 }
 
-// [rows, H, D] bf16 tensor viewed as a 3-D map (D, H, rows), box 64 x 1 x 128,
-// 128-byte swizzle: one TMA copy fills one 16 KB swizzle-atom slab.
-jfa_status map_rows(CUtensorMap* m, const void* ptr, int D, int H, long long rows, const char* nm) {
+// [rows, H, D] bf16 tensor viewed as a 3-D map (D, H, rows), box 64 x 1 x
+// box_rows (128 by default), 128-byte swizzle: one TMA copy of 128 rows
+// fills one 16 KB swizzle-atom slab.
+jfa_status map_rows(CUtensorMap* m, const void* ptr, int D, int H, long long rows, const char* nm,
+                    unsigned box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -252,7 +254,9 @@ jfa_status do_fwd_bs(DeviceState* ds, const Shape& s, const void* q, const void*
   const size_t partl_off = off;
   off = align256(off + (size_t)cap * 2 * kBM * sizeof(float));
   CUtensorMap tq, tk, tv;
-  if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q")) != JFA_OK) return st;
+  // a dense Q of at most 64 rows is loaded in 16-row boxes (the spread layout)
+  if ((st = map_rows(&tq, q, s.D, s.H, s.Lq, "q", fwd_bs_spread(s.Lq) ? 16 : 128)) != JFA_OK)
+    return st;
   if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
   if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   void* scratch = nullptr;

@@ -270,6 +270,8 @@ cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
 // Broadcast-Q forward for a short dense Q (q_len <= 128), streamed over
 // key-tile chunks (fwd_bs.cu), and the merge of split sequences.
 bool fwd_bs_supported(int Lq);
+// q_len <= 64: the spread layout (the Q map's box must then be 16 rows high).
+bool fwd_bs_spread(int Lq);
 cudaError_t launch_fwd_bs(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fwd_combine(int D, const FwdParams& p, int sms, cudaStream_t s);

@@ -124,7 +124,9 @@ __device__ __forceinline__ bool next_item(FsCtl* c, uint32_t n, FsDec* f, bool* 
   return f->n >= 0;
 }
 
-template <int D>
+// SPREAD: the Q map's box is 16 rows, and query rows [16 k, 16 k + 16) go to
+// tile rows [32 k, 32 k + 16) (the other rows are never read as queries).
+template <int D, bool SPREAD>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const FwdParams& p, uint8_t* smem, FsCtl* c) {
   using C = FsCfg<D>;
@@ -152,10 +154,19 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     if (idx >= n_items) break;
     if (f.n == 0) continue;
     if (!mbar_wait(&c->q_empty, (itq & 1) ^ 1, &c->abort, p.err)) break;
-    mbar_arrive_expect_tx(&c->q_full, C::kTile);
+    if (SPREAD) {
+      const int nbox = min(4, cdiv(p.Lq, 16));
+      mbar_arrive_expect_tx(&c->q_full, nbox * C::kSlabs * 16 * 128);
+      for (int k = 0; k < nbox; ++k)
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s)
-      tma_load_3d(smem + C::kQ + s * 16384, tq, &c->q_full, s * 64, f.h, 0);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d(smem + C::kQ + s * 16384 + k * 32 * 128, tq, &c->q_full, s * 64, f.h, 16 * k);
+    } else {
+      mbar_arrive_expect_tx(&c->q_full, C::kTile);
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_load_3d(smem + C::kQ + s * 16384, tq, &c->q_full, s * 64, f.h, 0);
+    }
     ++itq;
     Seg sg;
     seg_load(sg, p.offsets, p.B, f.b, f.j);
@@ -406,16 +417,185 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32
   }
 }
 
+// Softmax of the spread layout (q_len <= 64): query i sits at tile row
+// 32 * (i / 16) + i % 16, so that the valid rows fill lanes 0-15 of all four
+// TMEM lane quadrants and every sub-partition's warps work on them.  Warp w
+// takes quadrant w % 4 and key columns [64 * (w / 4), + 64); through the
+// 16-lane load shapes thread t holds rows t/4 and t/4 + 8 of its quadrant,
+// two adjacent key columns in every eight, so P packs into bf16 pairs in
+// place and four threads share a row (row max and sum over two shuffles).
+template <int D>
+__device__ void softmax_spread(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
+  using C = FsCfg<D>;
+  using R = FsRoles<D>;
+  static_assert(R::SPLIT == 2, "two key-column halves");
+  const int warp = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  const int quad = warp & 3, part = warp >> 2;
+  const int r0 = 32 * quad + (ln >> 2), r1 = r0 + 8;  // tile rows (TMEM lanes) of this thread
+  const int cq = 2 * (ln & 3);                         // its first column in every eight
+  const bool active = 16 * quad < p.Lq;                // the quadrant holds queries (warp-uniform)
+  const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
+  const int T = p.hdr->T;
+  const float sl2 = p.scale_log2;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  float2* seg_ml = reinterpret_cast<float2*>(smem + C::kSeg);  // [parity][part][row] = (m, l)
+  float* xch = reinterpret_cast<float*>(smem + C::kXch);       // [tile parity][part][row]
+  uint32_t g = 0, gseg = 0;
+  bool ok = true;
+  for (uint32_t n = 0; ok; ++n) {
+    FsDec f;
+    if (!next_item(c, n, &f, &ok, p.err)) break;
+    if (f.n == 0) continue;
+    Seg sg;
+    seg_load(sg, p.offsets, p.B, f.b, f.j);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows r0, r1; l: this thread's columns
+    for (int u = 0; u < f.n && ok; ++u) {
+      const uint32_t t = g + u;
+      const bool start = u == 0 || sg.j == 0;
+      const bool end = u == f.n - 1 || sg.j == sg.nts - 1;
+      if (start) {
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+      }
+      if (!mbar_wait_warp(&c->s_full[t % C::NSB], (t / C::NSB) & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t ts = tbase + lane_base + C::colS(t % C::NSB);
+      // s[4i + e]: e = 0, 1 row r0 and e = 2, 3 row r1, key columns
+      // 64 * part + 8 i + cq + (e & 1)
+      float s[32];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (active) {
+        uint32_t raw[32];
+        tmem_ld_16x256b_x8(ts + 64 * part, raw);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
+        const KvTile kt = kv_tile(sg.off0, sg.L, sg.j, T);
+        if (kt.nk < kBN || kt.shift > 0) {  // ragged key tile: columns [shift, shift + nk)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = 64 * part + 8 * (i >> 2) + cq + (i & 1);
+            s[i] = (col >= kt.shift && col < kt.shift + kt.nk) ? s[i] : -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mx0 = fmax3(mx0, s[4 * i], s[4 * i + 1]);
+          mx1 = fmax3(mx1, s[4 * i + 2], s[4 * i + 3]);
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      }
+      // Exchange with the other column half.  Every softmax thread has read
+      // its S columns before arriving, so the P writes below (half q packs
+      // into S columns 32 q.., read by half 0) come after all reads.
+      float* xt = xch + (t & 1) * R::SPLIT * kBM;
+      if (active && (ln & 3) == 0) {
+        xt[part * kBM + r0] = mx0;
+        xt[part * kBM + r1] = mx1;
+      }
+      tc_fence_before();
+      mbar_arrive(&c->xbar[t & 1]);
+      if (!mbar_wait_warp(&c->xbar[t & 1], (t >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      if (active) {
+        mx0 = fmaxf(mx0, xt[(1 - part) * kBM + r0]);
+        mx1 = fmaxf(mx1, xt[(1 - part) * kBM + r1]);
+        const float mt0 = mx0 * sl2, mt1 = mx1 * sl2;
+        const bool raise0 = mt0 > m0 + kRescaleLog2, raise1 = mt1 > m1 + kRescaleLog2;
+        const float mn0 = raise0 ? mt0 : m0, mn1 = raise1 ? mt1 : m1;
+        const float alpha0 = raise0 ? ex2_approx(m0 - mn0) : 1.f;
+        const float alpha1 = raise1 ? ex2_approx(m1 - mn1) : 1.f;
+        m0 = mn0;
+        m1 = mn1;
+        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const uint64_t negm0 = f2_pack(-mu0, -mu0), negm1 = f2_pack(-mu1, -mu1);
+        uint64_t acc0 = 0, acc1 = 0;
+        uint32_t pk[16];  // 16x128b: pk[2 i] row r0, pk[2 i + 1] row r1, packed column 4 i + t % 4
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 xa = f2_unpack(ffma2(f2_pack(s[4 * i], s[4 * i + 1]), sl2x2, negm0));
+          const float2 xb = f2_unpack(ffma2(f2_pack(s[4 * i + 2], s[4 * i + 3]), sl2x2, negm1));
+          const float pa = ex2_approx(xa.x), pb = ex2_approx(xa.y);
+          const float pc = ex2_approx(xb.x), pd = ex2_approx(xb.y);
+          acc0 = fadd2(acc0, f2_pack(pa, pb));
+          acc1 = fadd2(acc1, f2_pack(pc, pd));
+          pk[2 * i] = pack_bf16x2(pa, pb);
+          pk[2 * i + 1] = pack_bf16x2(pc, pd);
+        }
+        // keys 64 * part.. -> packed columns 32 * part..
+        tmem_st_16x128b_x8(ts + 32 * part, pk);
+        const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+        l0 = l0 * alpha0 + (a0.x + a0.y);
+        l1 = l1 * alpha1 + (a1.x + a1.y);
+        if (!start && __any_sync(0xffffffffu, raise0 || raise1)) {
+          // A row raised its max: once PV(t - 1) has landed in this segment's
+          // O, scale this thread's O entries (rows r0, r1; columns of this
+          // half).  The per-parity barrier cannot run two phases ahead of
+          // this wait, since PV(t + 1) needs this tile's P first.
+          if (!mbar_wait_warp(&c->o_ready[(t - 1) & 1], ((t - 1) >> 1) & 1, &c->abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t to = tbase + lane_base + C::colO(gseg & 1) + (D / 2) * part;
+          if (D == 64) {
+            uint32_t o[16];
+            tmem_ld_16x256b_x4(to, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * ((i & 2) ? alpha1 : alpha0));
+            tmem_st_16x256b_x4(to, o);
+          } else {
+            uint32_t o[32];
+            tmem_ld_16x256b_x8(to, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * ((i & 2) ? alpha1 : alpha0));
+            tmem_st_16x256b_x8(to, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&c->p_full[t % C::NSB]);
+      if (end) {  // hand the segment's (m, l of this half) to the epilogue warpgroup
+        const int par = gseg & 1;
+        if (!mbar_wait_warp(&c->seg_empty[par], ((gseg >> 1) & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+        if (active) {
+          float s0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+          float s1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+          s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+          if ((ln & 3) == 0) {
+            seg_ml[(par * R::SPLIT + part) * kBM + r0] = make_float2(m0, s0);
+            seg_ml[(par * R::SPLIT + part) * kBM + r1] = make_float2(m1, s1);
+          }
+        }
+        mbar_arrive(&c->seg_full[par]);
+        ++gseg;
+      }
+      if (u + 1 < f.n) seg_next(sg, p.offsets, p.B);
+    }
+    if (!ok) break;
+    g += f.n;
+  }
+}
+
 // Epilogue of each finished segment: O / l in bf16 and the natural-log LSE
 // for a whole sequence; for a piece of a split sequence, O / l in fp32 and
 // the base-2 LSE m + log2(l) as a partial, in slot 0 (the piece starts
 // inside the sequence) or 1 (it starts at the sequence's first tile) of the
 // item.
-template <int D>
+template <int D, bool SPREAD>
 __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint32_t tbase) {
   using C = FsCfg<D>;
   using R = FsRoles<D>;
-  const int r = threadIdx.x - R::kSoftmax;
+  const int r = threadIdx.x - R::kSoftmax;  // tile row == TMEM lane
+  // the query of this row (spread layout: row 32 k + i holds query 16 k + i, i < 16)
+  const int qr = SPREAD ? 16 * (r >> 5) + (r & 31) : r;
+  const bool qrow_valid = (SPREAD ? (r & 31) < 16 : true) && qr < p.Lq;
   const uint32_t lane_base = static_cast<uint32_t>((r >> 5) * 32) << 16;
   const float2* seg_ml = reinterpret_cast<const float2*>(smem + C::kSeg);
   uint32_t gseg = 0;
@@ -441,9 +621,9 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
         mbar_arrive(&c->seg_empty[par]);
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const bool whole = seg_j0 == 0 && sg.j == sg.nts - 1;
-        const bool store = r < p.Lq;
+        const bool store = qrow_valid;
         const int slot = seg_j0 > 0 ? 0 : 1;
-        const long long prow = (static_cast<long long>(f.slot) * 2 + slot) * kBM + r;
+        const long long prow = (static_cast<long long>(f.slot) * 2 + slot) * kBM + qr;
         if (!mbar_wait_warp(&c->o_done[par], ph, &c->abort, p.err)) { ok = false; break; }
         tc_fence_after();
         // 32 columns at a time out of TMEM: a whole sequence keeps bf16
@@ -470,10 +650,10 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
         ++gseg;
         if (store) {
           if (whole) {
-            __nv_bfloat16* orow = p.out + ((static_cast<long long>(sg.b) * p.Lq + r) * p.H + f.h) * D;
+            __nv_bfloat16* orow = p.out + ((static_cast<long long>(sg.b) * p.Lq + qr) * p.H + f.h) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) st_global_64B(orow + ch * 32, w + 16 * ch);
-            p.lse[(static_cast<long long>(sg.b) * p.H + f.h) * p.Lq + r] =
+            p.lse[(static_cast<long long>(sg.b) * p.H + f.h) * p.Lq + qr] =
                 l > 0.f ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
           } else {
             p.part_lse[prow] = l > 0.f ? m + lg2_approx(l) : -INFINITY;
@@ -485,7 +665,7 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* smem, FsCtl* c, uint3
   }
 }
 
-template <int D>
+template <int D, bool SPREAD>
 __global__ void __launch_bounds__(FsRoles<D>::kThreads, 1)
     fwd_bs_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -541,11 +721,14 @@ __global__ void __launch_bounds__(FsRoles<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
   if (warp < R::kEpiWarp) {
-    softmax_role<D>(p, smem, c, tbase);
+    if (SPREAD)
+      softmax_spread<D>(p, smem, c, tbase);
+    else
+      softmax_role<D>(p, smem, c, tbase);
   } else if (warp < R::kEpiWarp + 4) {
-    epilogue_role<D>(p, smem, c, tbase);
+    epilogue_role<D, SPREAD>(p, smem, c, tbase);
   } else if (warp == R::kProducerWarp) {
-    if (lane == 0) producer_role<D>(&tq, &tk, &tv, p, smem, c);
+    if (lane == 0) producer_role<D, SPREAD>(&tq, &tk, &tv, p, smem, c);
   } else {
     mma_role<D>(p, smem, c, tbase);
   }
@@ -630,14 +813,14 @@ __global__ void fwd_combine_kernel(const FwdParams p) {
   }
 }
 
-template <int D>
+template <int D, bool SPREAD>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int grid, cudaStream_t s) {
   using C = FsCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(FsCtl) <= 512, "control block");
   static_assert(C::NSK <= 4 && C::NSV <= 4, "ring depth");
-  auto kern = fwd_bs_kernel<D>;
+  auto kern = fwd_bs_kernel<D, SPREAD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<grid, FsRoles<D>::kThreads, C::kSmem, s>>>(tq, tk, tv, p);
@@ -647,12 +830,17 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }  // namespace
 
 bool fwd_bs_supported(int Lq) { return Lq >= 1 && Lq <= kBM; }
+bool fwd_bs_spread(int Lq) { return Lq >= 1 && Lq <= 64; }
 
 cudaError_t launch_fwd_bs(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s) {
   if (!fwd_bs_supported(p.Lq)) return cudaErrorInvalidValue;
-  if (D == 128) return launch_t<128>(tq, tk, tv, p, grid, s);
-  return launch_t<64>(tq, tk, tv, p, grid, s);
+  if (fwd_bs_spread(p.Lq)) {
+    if (D == 128) return launch_t<128, true>(tq, tk, tv, p, grid, s);
+    return launch_t<64, true>(tq, tk, tv, p, grid, s);
+  }
+  if (D == 128) return launch_t<128, false>(tq, tk, tv, p, grid, s);
+  return launch_t<64, false>(tq, tk, tv, p, grid, s);
 }
 
 cudaError_t launch_fwd_combine(int D, const FwdParams& p, int sms, cudaStream_t s) {

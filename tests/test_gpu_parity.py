@@ -39,6 +39,13 @@ SMALL = {
     "bcast_stream_split_one_long": dict(name="skewed_broadcast_q", lengths=[3000], H=2),
     "bcast_stream_split_d128": dict(name="broadcast_q", lengths=[0, 900, 5, 1300, 0, 77], H=2,
                                     q_len=100),
+    # q_len <= 64: the queries spread over the four TMEM lane quadrants
+    "bcast_stream_spread_d128_q40": dict(name="broadcast_q", lengths=[0, 900, 5, 1300, 129], H=2,
+                                         q_len=40),
+    "bcast_stream_spread_d64_q17": dict(name="skewed_broadcast_q", lengths=[3000, 1, 0, 129, 64],
+                                        H=2, q_len=17),
+    "bcast_stream_spread_d64_q49": dict(name="skewed_broadcast_q", lengths=[700, 2, 300], H=3,
+                                        q_len=49),
     "jagged_self_B6": dict(name="jagged_self", lengths=W.sample_lengths(
         W.WORKLOADS["jagged_self"], B=6)),
     "broadcast_q_B16": dict(name="broadcast_q", lengths=W.sample_lengths(
