@@ -742,73 +742,78 @@ __global__ void __launch_bounds__(FsRoles<D>::kThreads, 1)
 }
 
 // Merge of the pieces of split sequences, and the outputs of empty ones.
-// One warp per (sequence b, head h), lanes over query rows.  A sequence
-// whose key tiles [kt_off[b], kt_off[b+1]) span chunks c0 < c1 has its first
-// piece in slot 1 of item (c0, h) and the others in slot 0 of items
-// (c0 + 1 .. c1, h): O = sum_i 2^(lse_i - lse) O_i with lse = log2 sum_i
-// 2^lse_i.  Empty sequences get O = 0 and LSE = -inf.
+// One block per chunk boundary (item (c, h), c >= 1): the item starts inside
+// sequence b (tile j > 0) when the boundary cuts b, and the block of b's
+// first such boundary merges it: its first piece is in slot 1 of item
+// (c - 1, h), the others in slot 0 of items (c .. c1, h), where c1 is the
+// last consecutive item that starts inside b.  Threads take (query row, 8
+// head-dim columns): O = sum_i 2^(lse_i - lse) O_i with lse = log2 sum_i
+// 2^lse_i.  Every thread of the grid then checks one (sequence, head) and
+// writes O = 0, LSE = -inf when the sequence is empty.
+constexpr int kCombineThreads = 256;
 template <int D>
-__global__ void fwd_combine_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kCombineThreads) fwd_combine_kernel(const FwdParams p) {
   const WorkHeader* hdr = p.hdr;
   if (!hdr->valid) return;
   const int nc = hdr->n_chunks;
-  const long long total = p.kt_off[p.B];
-  const int lane = threadIdx.x & 31;
-  const long long nbh = static_cast<long long>(p.B) * p.H;
-  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < nbh;
-       w += nwarps) {
-    const int h = static_cast<int>(w % p.H), b = static_cast<int>(w / p.H);
-    const long long s_first = p.kt_off[b], s_last = p.kt_off[b + 1] - 1;
-    float* lrow = p.lse + (static_cast<long long>(b) * p.H + h) * p.Lq;
-    if (s_last < s_first) {  // empty sequence
-      for (int r = lane; r < p.Lq; r += 32) {
-        __nv_bfloat16* orow = p.out + ((static_cast<long long>(b) * p.Lq + r) * p.H + h) * D;
-        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
-        lrow[r] = -INFINITY;
+  const long long idx = blockIdx.x + static_cast<long long>(p.H);  // items of chunks 1..
+  if (idx < static_cast<long long>(nc) * p.H) {
+    const int h = static_cast<int>(idx % p.H), c = static_cast<int>(idx / p.H);
+    const QbItem it = p.qb_items[idx];
+    const QbItem prev = p.qb_items[idx - p.H];
+    // cut here, and by no earlier boundary
+    if (it.j > 0 && !(prev.b == it.b && prev.j > 0)) {
+      const int b = it.b, c0 = c - 1;
+      int c1 = c;
+      while (c1 + 1 < nc) {
+        const QbItem nx = p.qb_items[static_cast<long long>(c1 + 1) * p.H + h];
+        if (nx.b != b || nx.j == 0) break;
+        ++c1;
       }
-      continue;
-    }
-    auto chunk_of = [&](long long s) {
-      int c = static_cast<int>(s * nc / total);
-      while (c + 1 < nc && (c + 1) * total / nc <= s) ++c;
-      while (c > 0 && c * total / nc > s) --c;
-      return c;
-    };
-    const int c0 = chunk_of(s_first), c1 = chunk_of(s_last);
-    if (c0 == c1) continue;  // whole: written by the forward kernel
-    for (int r = lane; r < p.Lq; r += 32) {
-      float lmax = -INFINITY;
-      for (int c = c0; c <= c1; ++c)
-        lmax = fmaxf(lmax, p.part_lse[((static_cast<long long>(c) * p.H + h) * 2 + (c == c0)) * kBM + r]);
-      float acc[D];
-#pragma unroll
-      for (int d = 0; d < D; ++d) acc[d] = 0.f;
-      float sw = 0.f;
-      for (int c = c0; c <= c1; ++c) {
-        const long long prow = ((static_cast<long long>(c) * p.H + h) * 2 + (c == c0)) * kBM + r;
-        const float wgt = ex2_approx(p.part_lse[prow] - lmax);
-        sw += wgt;
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * D);
-#pragma unroll
-        for (int d4 = 0; d4 < D / 4; ++d4) {
-          const float4 v = src[d4];
-          acc[4 * d4] += wgt * v.x;
-          acc[4 * d4 + 1] += wgt * v.y;
-          acc[4 * d4 + 2] += wgt * v.z;
-          acc[4 * d4 + 3] += wgt * v.w;
+      constexpr int kGroups = D / 8;
+      for (int w = threadIdx.x; w < p.Lq * kGroups; w += kCombineThreads) {
+        const int r = w / kGroups, d0 = 8 * (w % kGroups);
+        float lmax = -INFINITY;
+        for (int cc = c0; cc <= c1; ++cc)
+          lmax = fmaxf(lmax, p.part_lse[((static_cast<long long>(cc) * p.H + h) * 2 + (cc == c0)) * kBM + r]);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float sw = 0.f;
+        for (int cc = c0; cc <= c1; ++cc) {
+          const long long prow = ((static_cast<long long>(cc) * p.H + h) * 2 + (cc == c0)) * kBM + r;
+          const float wgt = ex2_approx(p.part_lse[prow] - lmax);
+          sw += wgt;
+          const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * D + d0);
+          const float4 v0 = src[0], v1 = src[1];
+          acc[0] += wgt * v0.x;
+          acc[1] += wgt * v0.y;
+          acc[2] += wgt * v0.z;
+          acc[3] += wgt * v0.w;
+          acc[4] += wgt * v1.x;
+          acc[5] += wgt * v1.y;
+          acc[6] += wgt * v1.z;
+          acc[7] += wgt * v1.w;
         }
+        const float inv = 1.f / sw;
+        __nv_bfloat16* orow = p.out + ((static_cast<long long>(b) * p.Lq + r) * p.H + h) * D + d0;
+        *reinterpret_cast<uint4*>(orow) =
+            make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                       pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+        if (d0 == 0) p.lse[(static_cast<long long>(b) * p.H + h) * p.Lq + r] = (lmax + lg2_approx(sw)) * kLn2;
       }
-      const float inv = 1.f / sw;
+    }
+  }
+  // empty sequences
+  const long long nbh = static_cast<long long>(p.B) * p.H;
+  const long long nthreads = static_cast<long long>(gridDim.x) * kCombineThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kCombineThreads + threadIdx.x; i < nbh;
+       i += nthreads) {
+    const int h = static_cast<int>(i % p.H), b = static_cast<int>(i / p.H);
+    if (p.offsets[b + 1] != p.offsets[b]) continue;
+    float* lrow = p.lse + (static_cast<long long>(b) * p.H + h) * p.Lq;
+    for (int r = 0; r < p.Lq; ++r) {
       __nv_bfloat16* orow = p.out + ((static_cast<long long>(b) * p.Lq + r) * p.H + h) * D;
-#pragma unroll
-      for (int d = 0; d < D; d += 8)
-        *reinterpret_cast<uint4*>(orow + d) =
-            make_uint4(pack_bf16x2(acc[d] * inv, acc[d + 1] * inv),
-                       pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv),
-                       pack_bf16x2(acc[d + 4] * inv, acc[d + 5] * inv),
-                       pack_bf16x2(acc[d + 6] * inv, acc[d + 7] * inv));
-      lrow[r] = (lmax + lg2_approx(sw)) * kLn2;
+      for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+      lrow[r] = -INFINITY;
     }
   }
 }
@@ -844,12 +849,16 @@ cudaError_t launch_fwd_bs(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_fwd_combine(int D, const FwdParams& p, int sms, cudaStream_t s) {
-  const long long warps = static_cast<long long>(p.B) * p.H;
-  const int grid = static_cast<int>(std::min<long long>((warps + 7) / 8, 8LL * sms));
+  // one block per chunk boundary (the chunk list holds at most chunk_cap =
+  // ceil(2 * sms / H) chunks per head), and at least one thread per
+  // (sequence, head) for the empty-sequence pass
+  const long long boundaries = std::max<long long>(1, ((2LL * sms + p.H - 1) / p.H) * p.H);
+  const long long for_empty = (static_cast<long long>(p.B) * p.H + kCombineThreads - 1) / kCombineThreads;
+  const int grid = static_cast<int>(std::max(boundaries, std::min<long long>(for_empty, 4LL * sms)));
   if (D == 128)
-    fwd_combine_kernel<128><<<grid > 0 ? grid : 1, 256, 0, s>>>(p);
+    fwd_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
   else
-    fwd_combine_kernel<64><<<grid > 0 ? grid : 1, 256, 0, s>>>(p);
+    fwd_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
