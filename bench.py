@@ -658,7 +658,7 @@ def run_ours(args, x, wname):
     if sparse_entry is not None:
         xs, sp_ms, sp_prof, sp_pairs, win, sp_steps = sparse_entry
         dense_fwd_ms = workloads["jagged_self"][1]  # (x, fwd ms, ...) of the dense run
-        kern = _kernels_entry(xs, sp_prof, peak, hbm, "jagged_self")
+        kern = _kernels_entry(xs, sp_prof, peak, hbm, "jagged_self_block_sparse500")
         fl = 4.0 * xs["D"] * sp_pairs  # sp_pairs counts every head
         for kk in ("fwd",):  # the attention kernel's work is the selected pairs
             if kk in kern:
@@ -738,6 +738,38 @@ def run_ours(args, x, wname):
         torch.distributed.destroy_process_group()
 
 
+def run_variant(args):
+    """One variant alone, device-timed like the bench line's `variants`
+    entries (the block-sparse forward: selection + attention per step)."""
+    import torch
+    import jagged_flash_attention_gb300 as jfa
+    dev = torch.device("cuda")
+    jfa.lib()
+    peak, _, hbm, _ = _peaks()
+    stream = torch.cuda.current_stream()
+    steps, warmup = max(3, args.steps), max(3, args.warmup)
+    if args.variant == "jagged_self_block_sparse500":
+        w = W.WORKLOADS["jagged_self"]
+        lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
+        x = W.make_inputs(w, lengths=lengths)
+        ms, kprof, pairs, _, steps = _time_sparse(jfa, torch, x, 500, steps, warmup, stream, dev)
+        fl = 4.0 * x["D"] * pairs
+        entry = {"fwd": {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                         "selected_fraction": pairs / (x["H"] * W.pairs(x["lengths"]))},
+                 "kernels": _kernels_entry(x, kprof, peak, hbm, "jagged_self_block_sparse500")}
+    else:
+        w = W.variant(args.variant)
+        lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
+        x = W.make_inputs(w, lengths=lengths)
+        f_ms, b_ms, kprof, _, _, steps = _time_steps(jfa, torch, x, steps, warmup, stream, dev)
+        fwd_f, bwd_f, _ = _flops(x)
+        entry = {"fwd": {"ms": f_ms, "tflops": fwd_f / (f_ms * 1e-3) / 1e12},
+                 "bwd": {"ms": b_ms, "tflops": bwd_f / (b_ms * 1e-3) / 1e12},
+                 "kernels": _kernels_entry(x, kprof, peak, hbm, args.variant)}
+    print(json.dumps({"variant": args.variant, "steps": steps, "B": int(x["B"]), **entry}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -752,10 +784,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default=None,
+                    choices=list(W.VARIANTS) + ["jagged_self_block_sparse500"],
+                    help="time one GQA / window / block-sparse variant alone (one JSON line "
+                         "with that variant's entry; for profiling captures)")
     ap.add_argument("--batch", type=int, default=None,
                     help="draw this many sequences instead of the workload's B "
                          "(same length distribution; for profiling captures)")
     args = ap.parse_args()
+    if args.variant is not None:
+        run_variant(args)
+        return
     w = W.WORKLOADS[args.workload]
     lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
     x = W.make_inputs(w, lengths=lengths)
