@@ -26,14 +26,22 @@
 // sub-partition, so that each part's TMEM load -> math -> TMEM store chain
 // is hidden by the others) and the dK/dV epilogue, warp 16 TMA producer
 // (decodes items one ahead, publishes them in shared memory, prefetches the
-// next item's first boxes into L2; each Q stage carries its tile's row
-// statistics, and Q and dO of a stage have their own barriers), warp 17 MMA
-// issuer, warp 18 the store warp (TMA stores of full dK/dV blocks).
+// next item's first boxes into L2; Q, dO and the row statistics of a stage
+// have their own barriers, the statistics freed by the math right after
+// their dS part; a Q box a stage still holds is not loaded again; V is
+// loaded before the next item is decoded), warp 17 MMA issuer, warp 18 the
+// store warp (TMA stores of full dK/dV blocks).
+// Variants: with a local mask (causal or a sliding window) a key block
+// visits only the query tiles of its band; with GQA an item is a block of
+// one K/V head and its query tiles are those of the G query heads that read
+// it, so dK and dV sum over the group without leaving the CTA.
 // Broadcast-Q ("Optimizing Jagged Flash Attention with TLX", section 1):
 // the query tiles of every item are the tiles of the one dense Q, dO is the
 // sequence's own [q_len, D] block of the [B, q_len, H, D] tensor (a 4-D
 // tensor map zero-fills rows past q_len), and the row statistics come from
 // a per-sequence layout padded to whole tiles (padding rows give P = 0).
+// Its work list is head-outer, so a CTA's consecutive items usually share
+// the dense-Q tiles its stages hold.
 // At an item boundary the math warps compute the next item's first P part,
 // then the item's dV epilogue, the next item's first dS part, and only then
 // the item's dK epilogue, so that the first products of the next item wait

@@ -25,10 +25,19 @@
 //                   waits; an elect.sync lane issues)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them.  P_t
 // (bf16) overwrites the first 64 columns of S_t and is read from TMEM by the
-// PV MMA.  Issue order per K/V tile j: PV0(j-1), S0(j), PV1(j-1), S1(j), so
-// each softmax group has the time of two MMAs to turn S into P.  S_t(j)
-// overwrites the columns that PV_t(j-1), issued just before it, reads P from;
-// tcgen05 MMAs of one CTA execute in issue order.
+// PV MMA, in two halves: keys 0-63 are handed over (with any O rescale
+// already done) while keys 64-127 are still being written, so PV's first
+// four K steps overlap the rest of the softmax.  Issue order per K/V tile j:
+// PV0(j-1), S0(j), PV1(j-1), S1(j), so each softmax group has the time of two
+// MMAs to turn S into P.  S_t(j) overwrites the columns that PV_t(j-1),
+// issued just before it, reads P from; tcgen05 MMAs of one CTA execute in
+// issue order.
+//
+// Variants: with a local mask (causal or a sliding window, the LOCAL
+// instantiation) each query tile visits only the key tiles of its band and
+// the item streams the union of its two tiles' ranges; with GQA the K/V
+// tiles are those of head h / G; the SPARSE instantiation streams the key
+// tiles of the item's block list (block-sparse attention).
 #include "common.cuh"
 #include "ptx.cuh"
 

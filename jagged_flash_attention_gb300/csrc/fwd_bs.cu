@@ -22,6 +22,10 @@
 // two tiles ahead of PV, so the softmax never waits for its next S behind
 // the previous tile's PV.
 //
+// q_len <= 64 uses the spread layout (softmax_spread): the queries sit in
+// rows 0-15 of each 32-row lane quadrant of the tile, so that the softmax of
+// the rows that count runs on all four SM sub-partitions.
+//
 // CTA = 4 * SPLIT + 6 warps (SPLIT = 2: a four-way split measured slower,
 // the softmax being bound by latency rather than by its element count): warps
 // 0 .. 4*SPLIT-1 softmax (thread: query row r = TMEM lane, key columns
