@@ -288,8 +288,10 @@ def delta_rowsum(out, dout, broadcast_q=False):
 # (K/V head h // group for query head h); the block score is the dot product
 # of the two pooled vectors; k = max(1, ceil(permille * n / 1000)) of the
 # sequence's n K blocks, in integer arithmetic; ties go to the lower block
-# index; the list is stored in ascending order.  Self-attention without a
-# causal mask.
+# index; the list is stored in ascending order.  Without a causal mask or
+# window.  In broadcast-Q mode the Q blocks are the 256-row blocks of the
+# one dense Q (the same for every sequence); a sequence without keys gets
+# an empty list (O = 0, LSE = -inf).
 
 SPARSE_Q_BLOCK = 256
 SPARSE_K_BLOCK = 128
@@ -306,34 +308,42 @@ def sparse_k_count(n_blocks, permille):
     return min(n_blocks, max(1, (permille * n_blocks + 999) // 1000))
 
 
-def block_select(q, k, offsets, permille):
+def block_select(q, k, offsets, permille, broadcast_q=False):
     """Top-k K blocks per (sequence, query head, Q block) by pooled scores.
 
     Returns (blocks, counts, scores): blocks int64 [B, H, nqb, kcap] holding
     the selected K block indices in ascending order in the first counts
     entries (-1 after them), counts int64 [B, H, nqb], and the fp64 block
     scores [B, H, nqb, kcap] (NaN where there is no block), with nqb =
-    ceil(max_len / 256) and kcap = ceil(max_len / 128).
+    ceil(max_len / 256) (broadcast: ceil(q_len / 256)) and kcap =
+    ceil(max_len / 128).
     """
     q, k = _as64(q), _as64(k)
     off = _seq_bounds(offsets)
     B = off.size - 1
-    H, Hkv, group = _heads(q, k, False)
+    H, Hkv, group = _heads(q, k, broadcast_q)
     L = np.diff(off)
     max_len = int(L.max()) if B else 0
-    nqb, kcap = _cdiv(max_len, SPARSE_Q_BLOCK), _cdiv(max_len, SPARSE_K_BLOCK)
+    nqb = _cdiv(q.shape[0] if broadcast_q else max_len, SPARSE_Q_BLOCK)
+    kcap = _cdiv(max_len, SPARSE_K_BLOCK)
     blocks = np.full((B, H, nqb, kcap), -1, dtype=np.int64)
     counts = np.zeros((B, H, nqb), dtype=np.int64)
     scores = np.full((B, H, nqb, kcap), np.nan)
     for b in range(B):
         s0, n = int(off[b]), int(L[b])
-        nk, nq = _cdiv(n, SPARSE_K_BLOCK), _cdiv(n, SPARSE_Q_BLOCK)
+        nk = _cdiv(n, SPARSE_K_BLOCK)
+        nq = nqb if broadcast_q else _cdiv(n, SPARSE_Q_BLOCK)
+        if nk == 0:
+            continue  # no keys: empty lists
         kk = sparse_k_count(nk, permille)
         for h in range(H):
             kbar = np.stack([k[s0 + j * SPARSE_K_BLOCK: s0 + min(n, (j + 1) * SPARSE_K_BLOCK),
-                               h // group, :].mean(axis=0) for j in range(nk)]) if nk else None
+                               h // group, :].mean(axis=0) for j in range(nk)])
             for i in range(nq):
-                qbar = q[s0 + i * SPARSE_Q_BLOCK: s0 + min(n, (i + 1) * SPARSE_Q_BLOCK), h, :]
+                if broadcast_q:
+                    qbar = q[i * SPARSE_Q_BLOCK: min(q.shape[0], (i + 1) * SPARSE_Q_BLOCK), h, :]
+                else:
+                    qbar = q[s0 + i * SPARSE_Q_BLOCK: s0 + min(n, (i + 1) * SPARSE_Q_BLOCK), h, :]
                 sc = kbar @ qbar.mean(axis=0)
                 scores[b, h, i, :nk] = sc
                 order = np.argsort(-sc, kind="stable")  # descending, ties: lower index first
@@ -342,32 +352,44 @@ def block_select(q, k, offsets, permille):
     return blocks, counts, scores
 
 
-def forward_sparse(q, k, v, offsets, scale, blocks, counts):
+def forward_sparse(q, k, v, offsets, scale, blocks, counts, broadcast_q=False):
     """Attention in which query row i of a sequence sees only the keys of the
     K blocks listed for its Q block (i // 256): blocks[b, h, i // 256,
     :counts[b, h, i // 256]].  A row with no key gets O = 0, LSE = -inf.
-    Layouts as forward (self-attention)."""
+    Layouts as forward (self-attention, or broadcast-Q: row i of the dense
+    Q, out [B, q_len, H, D], lse [B, H, q_len])."""
     q, k, v = _as64(q), _as64(k), _as64(v)
     off = _seq_bounds(offsets)
     B = off.size - 1
     T, Hkv, D = k.shape
-    H, Hkv, group = _heads(q, k, False)
-    out = np.zeros((T, H, D))
-    lse = np.full((H, T), -np.inf)
+    H, Hkv, group = _heads(q, k, broadcast_q)
+    if broadcast_q:
+        Lq = q.shape[0]
+        out = np.zeros((B, Lq, H, D))
+        lse = np.full((B, H, Lq), -np.inf)
+    else:
+        out = np.zeros((T, H, D))
+        lse = np.full((H, T), -np.inf)
     for b in range(B):
         s0, s1 = int(off[b]), int(off[b + 1])
         n = s1 - s0
         if n == 0:
             continue
         kblock = np.arange(n) // SPARSE_K_BLOCK
+        nrows = q.shape[0] if broadcast_q else n
         for h in range(H):
             kb, vb = k[s0:s1, h // group, :], v[s0:s1, h // group, :]
-            for i in range(_cdiv(n, SPARSE_Q_BLOCK)):
-                r0, r1 = i * SPARSE_Q_BLOCK, min(n, (i + 1) * SPARSE_Q_BLOCK)
+            for i in range(_cdiv(nrows, SPARSE_Q_BLOCK)):
+                r0, r1 = i * SPARSE_Q_BLOCK, min(nrows, (i + 1) * SPARSE_Q_BLOCK)
                 keep = np.isin(kblock, blocks[b, h, i, :counts[b, h, i]])
-                s = scale * (q[s0 + r0:s0 + r1, h, :] @ kb.T)
+                qrows = q[r0:r1, h, :] if broadcast_q else q[s0 + r0:s0 + r1, h, :]
+                s = scale * (qrows @ kb.T)
                 s = np.where(keep[None, :], s, -np.inf)
                 l = _lse_rows(s)
-                out[s0 + r0:s0 + r1, h, :] = _probs(s, l) @ vb
-                lse[h, s0 + r0:s0 + r1] = l
+                if broadcast_q:
+                    out[b, r0:r1, h, :] = _probs(s, l) @ vb
+                    lse[b, h, r0:r1] = l
+                else:
+                    out[s0 + r0:s0 + r1, h, :] = _probs(s, l) @ vb
+                    lse[h, s0 + r0:s0 + r1] = l
     return out, lse

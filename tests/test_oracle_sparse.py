@@ -195,3 +195,76 @@ def test_unmutated_copy_passes():
 def test_planted_sparse_slips_are_caught(slip):
     with pytest.raises(AssertionError):
         _check(_mutant_module(*slip))
+
+
+# ------------------------------------------------------------ broadcast-Q
+
+def _bq_case(lengths, Lq, H, Hkv, D, seed):
+    rng = np.random.default_rng(seed)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    T = int(off[-1])
+    return (rng.standard_normal((Lq, H, D)), rng.standard_normal((T, Hkv, D)),
+            rng.standard_normal((T, Hkv, D)), off)
+
+
+def test_broadcast_full_selection_is_dense():
+    q, k, v, off = _bq_case([300, 0, 513, 129], 300, 4, 2, 8, seed=61)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 1000, broadcast_q=True)
+    assert blocks.shape[2] == 2 and np.all(counts[1] == 0)  # q_len 300: two Q blocks
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.3, blocks, counts, broadcast_q=True)
+    ref_out, ref_lse = jfa_oracle.forward(q, k, v, off, 0.3, broadcast_q=True)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], atol=1e-12)
+
+
+@pytest.mark.parametrize("permille", [250, 600])
+def test_broadcast_sparse_equals_torch_block_mask(permille):
+    Lq, H = 300, 4
+    q, k, v, off = _bq_case([700, 5, 0, 1000], Lq, H, 2, 8, seed=62)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, permille, broadcast_q=True)
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.25, blocks, counts, broadcast_q=True)
+    for b in range(len(off) - 1):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        n = s1 - s0
+        if n == 0:
+            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        nqb, nkb = -(-Lq // QB), -(-n // KB)
+        sel = torch.zeros(H, nqb, nkb, dtype=torch.bool)
+        for h in range(H):
+            for i in range(nqb):
+                for j in blocks[b, h, i, :counts[b, h, i]]:
+                    sel[h, i, int(j)] = True
+        mask = sel.repeat_interleave(QB, dim=1)[:, :Lq].repeat_interleave(KB, dim=2)[:, :, :n]
+        Q = torch.from_numpy(q).permute(1, 0, 2)
+        K = torch.from_numpy(k[s0:s1]).permute(1, 0, 2)
+        V = torch.from_numpy(v[s0:s1]).permute(1, 0, 2)
+        O = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=0.25,
+                                                             enable_gqa=True)
+        np.testing.assert_allclose(out[b], O.permute(1, 0, 2).numpy(), atol=1e-12)
+
+
+def test_broadcast_selection_brute_force():
+    Lq, H, D = 260, 2, 5
+    q, k, v, off = _bq_case([300, 1, 0, 700], Lq, H, 1, D, seed=63)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 400, broadcast_q=True)
+    for b in range(len(off) - 1):
+        s0, n = int(off[b]), int(off[b + 1] - off[b])
+        nk = -(-n // KB)
+        for h in range(H):
+            for i in range(-(-Lq // QB)):
+                if nk == 0:
+                    assert counts[b, h, i] == 0
+                    continue
+                kk = min(nk, max(1, -(-(400 * nk) // 1000)))
+                rows = range(i * QB, min(Lq, (i + 1) * QB))
+                qbar = [sum(q[r, h, d] for r in rows) / len(rows) for d in range(D)]
+                sc = []
+                for j in range(nk):
+                    kr = range(s0 + j * KB, s0 + min(n, (j + 1) * KB))
+                    kbar = [sum(k[r, 0, d] for r in kr) / len(kr) for d in range(D)]
+                    sc.append(sum(a * c for a, c in zip(qbar, kbar)))
+                best = sorted(sorted(range(nk), key=lambda j: (-sc[j], j))[:kk])
+                assert list(blocks[b, h, i, :counts[b, h, i]]) == best
