@@ -134,16 +134,20 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
 /* Block-sparse attention ("Optimizing Jagged Flash Attention with TLX",
  * section 3, "Block-sparse attention"): a cheap scoring step average-pools
  * each Q block and each K block and keeps the top-k K/V blocks per Q block;
- * the attention then runs over the selected blocks only.  Self-attention
- * without a causal mask or window; GQA as for jfa_fwd_ex.
+ * the attention then runs over the selected blocks only.  Without a causal
+ * mask or window; GQA as for jfa_fwd_ex; self-attention, or broadcast-Q
+ * (broadcast_q = 1, q_len as for jfa_fwd_bq, layouts of broadcast-Q).
  *
  * Blocks: K block j of a sequence = its keys [128 j, 128 j + 128), Q block i
- * = its query rows [256 i, 256 i + 256) (the last ones ragged).  With
- * nqb = ceil(max_len / 256) and kcap = ceil(max_len / 128):
+ * = its query rows [256 i, 256 i + 256) (broadcast: rows of the dense Q,
+ * the same blocks for every sequence; the last ones ragged).  With
+ * nqb = ceil(max_len / 256) (broadcast: ceil(q_len / 256)) and
+ * kcap = ceil(max_len / 128):
  * - blocks: device int32 [B, H, nqb, kcap]; entry (b, h, i) lists the K
  *   blocks that query head h of Q block i of sequence b attends to, strictly
  *   ascending, in its first counts[b, h, i] slots;
- * - counts: device int32 [B, H, nqb]; 0 for Q blocks past the sequence.
+ * - counts: device int32 [B, H, nqb]; 0 for Q blocks past the sequence and,
+ *   in broadcast mode, for sequences without keys.
  *
  * jfa_block_select (stage 1) fills blocks and counts: the score of K block j
  * for Q block i is the dot product (fp32) of the mean of the Q block's rows
@@ -154,8 +158,8 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
  * Q once each; scratch: B * H_kv * kcap * D floats from the pool.  max_len
  * must be <= 262144 (kcap <= 2048) and B <= 65535.
  *
- * jfa_fwd_sparse (stage 2) writes out and lse like jfa_fwd, with query row r
- * of a sequence attending only to the keys of the K blocks listed for its Q
+ * jfa_fwd_sparse (stage 2) writes out and lse like jfa_fwd / jfa_fwd_bq, with
+ * query row r attending only to the keys of the K blocks listed for its Q
  * block r / 256; a row whose list is empty gets out = 0 and lse = -inf.  The
  * lists may come from jfa_block_select or from the caller; they are checked
  * on the device (a count above the sequence's K blocks, or entries not
@@ -164,12 +168,12 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
  * forward kernel is the dense one following each item's list instead of all
  * key tiles, so its time scales with the selected fraction. */
 jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
-                            int H_kv, int D, int max_len, int permille, int32_t* blocks,
-                            int32_t* counts, cudaStream_t stream);
+                            int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                            int permille, int32_t* blocks, int32_t* counts, cudaStream_t stream);
 jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int32_t* offsets,
-                          int B, int H, int H_kv, int D, int max_len, float scale,
-                          const int32_t* blocks, const int32_t* counts, void* out, float* lse,
-                          cudaStream_t stream);
+                          int B, int H, int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                          float scale, const int32_t* blocks, const int32_t* counts, void* out,
+                          float* lse, cudaStream_t stream);
 
 /* Allocation-free forward pass.  The pages have no counterpart: this entry
  * point exists for callers that must not allocate device memory while the

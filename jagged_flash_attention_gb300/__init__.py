@@ -130,24 +130,25 @@ def jfa_bwd_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, cau
                             _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
-def jfa_block_select(q, k, offsets, B, H, H_kv, D, max_len, permille, blocks, counts,
-                     stream=None):
+def jfa_block_select(q, k, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, permille,
+                     blocks, counts, stream=None):
     fn = lib().jfa_block_select
     if fn.argtypes is None:
-        fn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]
+        fn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         fn.restype = _I
-    _check(fn(_ptr(q), _ptr(k), _ptr(offsets), B, H, H_kv, D, max_len, int(permille),
-              _ptr(blocks), _ptr(counts), _stream(stream)))
+    _check(fn(_ptr(q), _ptr(k), _ptr(offsets), B, H, H_kv, D, max_len, q_len, int(broadcast_q),
+              int(permille), _ptr(blocks), _ptr(counts), _stream(stream)))
 
 
-def jfa_fwd_sparse(q, k, v, offsets, B, H, H_kv, D, max_len, scale, blocks, counts, out, lse,
-                   stream=None):
+def jfa_fwd_sparse(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, scale, blocks,
+                   counts, out, lse, stream=None):
     fn = lib().jfa_fwd_sparse
     if fn.argtypes is None:
-        fn.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]
+        fn.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]
         fn.restype = _I
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len, float(scale),
-              _ptr(blocks), _ptr(counts), _ptr(out), _ptr(lse), _stream(stream)))
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len, q_len,
+              int(broadcast_q), float(scale), _ptr(blocks), _ptr(counts), _ptr(out), _ptr(lse),
+              _stream(stream)))
 
 
 def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale,
@@ -265,30 +266,35 @@ def backward(q, k, v, offsets, max_len, out, lse, dout, causal=False, broadcast_
     return dq, dk, dv
 
 
-def block_select(q, k, offsets, max_len, permille, blocks=None, counts=None, stream=None):
+def block_select(q, k, offsets, max_len, permille, blocks=None, counts=None, stream=None,
+                 broadcast_q=False):
     """Top-k K blocks per (sequence, query head, 256-row Q block) (see
     jfa_block_select in include/jfa.h); returns int32 (blocks [B, H, nqb,
     kcap], counts [B, H, nqb])."""
     import torch
-    B, H, Hkv, D, _ = _shapes(q, k, offsets, False)
-    nqb, kcap = -(-max_len // 256), -(-max_len // 128)
+    B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
+    nqb, kcap = -(-(Lq if broadcast_q else max_len) // 256), -(-max_len // 128)
     if blocks is None:
         blocks = torch.empty((B, H, nqb, kcap), dtype=torch.int32, device=q.device)
     if counts is None:
         counts = torch.empty((B, H, nqb), dtype=torch.int32, device=q.device)
-    jfa_block_select(q, k, offsets, B, H, Hkv, D, max_len, permille, blocks, counts, stream)
+    jfa_block_select(q, k, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), permille,
+                     blocks, counts, stream)
     return blocks, counts
 
 
 def forward_sparse(q, k, v, offsets, max_len, blocks, counts, scale=None, out=None, lse=None,
-                   stream=None):
+                   stream=None, broadcast_q=False):
     """Attention over the listed K blocks of each Q block (jfa_fwd_sparse)."""
     import torch
-    B, H, Hkv, D, _ = _shapes(q, k, offsets, False)
+    B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    out = torch.empty_like(q) if out is None else out
+    if out is None:
+        out = torch.empty((B, Lq, H, D) if broadcast_q else tuple(q.shape), dtype=q.dtype,
+                          device=q.device)
     if lse is None:
-        lse = torch.empty((H, k.shape[0]), dtype=torch.float32, device=q.device)
-    jfa_fwd_sparse(q, k, v, offsets, B, H, Hkv, D, max_len, scale, blocks, counts, out, lse,
-                   stream)
+        lse = torch.empty((B, H, Lq) if broadcast_q else (H, k.shape[0]), dtype=torch.float32,
+                          device=q.device)
+    jfa_fwd_sparse(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), scale, blocks,
+                   counts, out, lse, stream)
     return out, lse

@@ -718,16 +718,16 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
 }
 
 jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
-                            int H_kv, int D, int max_len, int permille, int32_t* blocks,
-                            int32_t* counts, cudaStream_t stream) {
+                            int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                            int permille, int32_t* blocks, int32_t* counts, cudaStream_t stream) {
   t_last_error.clear();
-  Shape s = make_shape(B, H, H_kv, D, max_len, 0, 0, 0, -1, -1, 1.f);
+  Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1, 1.f);
   jfa_status st = check_common(s, q, k, k, offsets);
   if (st != JFA_OK) return st;
   if (permille < 1 || permille > 1000)
     return fail(JFA_ERR_INVALID_ARG, "permille must be in [1, 1000] (got %d)", permille);
   if (B > 65535) return fail(JFA_ERR_INVALID_ARG, "block-sparse: B must be <= 65535");
-  const long long kcap = cdivll(max_len, kBN), nqb = cdivll(max_len, kFwdRows);
+  const long long kcap = cdivll(max_len, kBN), nqb = cdivll(s.broadcast ? s.Lq : max_len, kFwdRows);
   if (kcap > kSparseMaxKBlocks)
     return fail(JFA_ERR_INVALID_ARG, "block-sparse: max_len must be <= %d", kSparseMaxKBlocks * kBN);
   if (!blocks || !counts || (reinterpret_cast<uintptr_t>(blocks) & 3u) ||
@@ -739,7 +739,8 @@ jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets
     return finish(stream);
   }
   const size_t kbar_bytes = align256((size_t)B * H_kv * kcap * D * sizeof(float));
-  const size_t bytes = kbar_bytes + align256((size_t)B * H * nqb * D * sizeof(float));
+  const size_t bytes =
+      kbar_bytes + align256((size_t)(s.broadcast ? 1 : B) * H * nqb * D * sizeof(float));
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -755,6 +756,8 @@ jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets
   sp.D = D;
   sp.max_len = max_len;
   sp.permille = permille;
+  sp.Lq = s.Lq;
+  sp.broadcast = s.broadcast;
   sp.nqb = (int)nqb;
   sp.kcap = (int)kcap;
   sp.kbar = static_cast<float*>(scratch);
@@ -772,11 +775,11 @@ jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets
 }
 
 jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int32_t* offsets,
-                          int B, int H, int H_kv, int D, int max_len, float scale,
-                          const int32_t* blocks, const int32_t* counts, void* out, float* lse,
-                          cudaStream_t stream) {
+                          int B, int H, int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                          float scale, const int32_t* blocks, const int32_t* counts, void* out,
+                          float* lse, cudaStream_t stream) {
   t_last_error.clear();
-  const Shape s = make_shape(B, H, H_kv, D, max_len, 0, 0, 0, -1, -1, scale);
+  const Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1, scale);
   jfa_status st = check_common(s, q, k, v, offsets);
   if (st != JFA_OK) return st;
   if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
@@ -787,15 +790,25 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
     return fail(JFA_ERR_INVALID_ARG, "blocks and counts must be non-null, 4-byte aligned");
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != JFA_OK) return st;
-  if (s.max_len == 0) return finish(stream);
-  const long long kcap = cdivll(s.max_len, kBN), nqb = cdivll(s.max_len, kFwdRows);
+  if (s.max_len == 0) {  // no keys anywhere (broadcast: every row O = 0, LSE = -inf)
+    if (s.broadcast) {
+      cudaError_t e = run_kernel(JFA_KERNEL_FILL, stream, [&] {
+        return launch_fill_empty(
+            static_cast<__nv_bfloat16*>(out), lse, (long long)s.B * s.Lq * s.H, s.D, stream);
+      });
+      if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+    }
+    return finish(stream);
+  }
+  const long long kcap = cdivll(s.max_len, kBN);
+  const long long nqb = cdivll(s.broadcast ? s.Lq : s.max_len, kFwdRows);
   const long long cap = (long long)s.H * s.B * nqb;
   if (cap >= (1LL << 31) || (long long)s.B * s.H * nqb * kcap >= (1LL << 40))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
   const size_t items_off = 256;
   const size_t bytes = align256(items_off + cap * sizeof(Item));
   CUtensorMap tq, tk, tv;
-  if ((st = map_rows(&tq, q, s.D, s.H, s.Tcap, "q")) != JFA_OK) return st;
+  if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
   if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
   if ((st = map_rows(&tv, v, s.D, s.Hkv, s.Tcap, "v")) != JFA_OK) return st;
   void* scratch = nullptr;
@@ -805,8 +818,8 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
   WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
   Item* items = reinterpret_cast<Item*>(base + items_off);
   // The scheduler also checks every list before the forward follows it.
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, 0, 0, 0, kFwdRows, items, (int)cap, hdr,
-                 ds->err};
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, 0, s.broadcast, 0, kFwdRows, items, (int)cap,
+                 hdr, ds->err};
   sp.blocks = blocks;
   sp.counts = counts;
   sp.nqb = (int)nqb;
@@ -819,6 +832,7 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
     fp.offsets = offsets;
     fp.B = s.B;
     fp.H = s.H;
+    fp.Lq = s.Lq;
     fp.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
     fp.out = static_cast<__nv_bfloat16*>(out);
     fp.lse = lse;
@@ -830,7 +844,7 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
     fp.nqb = (int)nqb;
     fp.kcap = (int)kcap;
     e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
-      return launch_fwd(s.D, false, false, tq, tk, tv, fp, (int)cap, stream, true);
+      return launch_fwd(s.D, false, s.broadcast, tq, tk, tv, fp, (int)cap, stream, true);
     });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);

@@ -139,7 +139,8 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       const int i = static_cast<int>(r % p.nqb);
       const int b = static_cast<int>(r / p.nqb / p.H);
       const int L = p.offsets[b + 1] - p.offsets[b];
-      if (L < 0 || L > p.max_len || i * kFwdRows >= L) continue;
+      // Q blocks of the sequence (broadcast: of the dense Q, for every sequence)
+      if (L < 0 || L > p.max_len || i * kFwdRows >= (p.broadcast ? p.Lq : L)) continue;
       const int nk = cdiv(L, kBN);
       const int c = p.counts[r];
       bool ok = c >= 0 && c <= nk;

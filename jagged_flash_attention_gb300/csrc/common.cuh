@@ -247,9 +247,10 @@ struct SparseParams {
   const __nv_bfloat16* k;  // [T, Hkv, D]
   const int32_t* offsets;
   int B, H, Hkv, G, D, max_len, permille;
-  int nqb, kcap;  // ceil(max_len / 256), ceil(max_len / 128)
+  int Lq, broadcast;  // broadcast-Q: the Q blocks are the dense Q's (q is [Lq, H, D])
+  int nqb, kcap;  // ceil(max_len / 256) (broadcast: ceil(Lq / 256)), ceil(max_len / 128)
   float* kbar;     // scratch fp32 [B][Hkv][kcap][D]: K-block means
-  float* qbar;     // scratch fp32 [B][H][nqb][D]: Q-block means
+  float* qbar;     // scratch fp32 [B][H][nqb][D]: Q-block means (broadcast: [1][H][nqb][D])
   int32_t* blocks;
   int32_t* counts;
   int* err;

@@ -107,9 +107,9 @@ struct FwdCtl {
 // LOCAL: a local mask (causal or a sliding window, bounds p.wl / p.wr): a
 // query tile visits only the key tiles that hold admissible keys of its
 // rows, and the item streams the union of its two tiles' ranges.
-// SPARSE: block-sparse attention (self-attention, no mask): both query tiles
-// of the item visit the key tiles of the item's block list, in its
-// (ascending) order.
+// SPARSE: block-sparse attention (no mask; self-attention or broadcast-Q):
+// both query tiles of the item visit the key tiles of the item's block list,
+// in its (ascending) order.
 template <bool BCAST, bool LOCAL, bool SPARSE>
 __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
   FwdItem f;
@@ -130,7 +130,9 @@ __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
       q.nq = min(kBM, p.Lq - q.q_lo);
       q.shift = 0;
       q.row = q.q_lo;
-      q.n_kv = q.nq > 0 ? cdiv(f.L, kBN) : 0;
+      q.n_kv = q.nq > 0 ? (SPARSE ? p.counts[(static_cast<long long>(f.b) * p.H + f.h) * p.nqb + pair]
+                                  : cdiv(f.L, kBN))
+                        : 0;
     } else {
       q.nq = min(kBM, f.L - q.q_lo);
       const int start = f.off0 + q.q_lo;
@@ -678,8 +680,12 @@ cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, co
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s,
                        bool sparse) {
   if (sparse) {
-    if (causal || bcast) return cudaErrorInvalidValue;
-    if (D == 128) return launch_fwd_t<128, false, false, true>(tq, tk, tv, p, grid, s);
+    if (causal) return cudaErrorInvalidValue;
+    if (D == 128) {
+      if (bcast) return launch_fwd_t<128, false, true, true>(tq, tk, tv, p, grid, s);
+      return launch_fwd_t<128, false, false, true>(tq, tk, tv, p, grid, s);
+    }
+    if (bcast) return launch_fwd_t<64, false, true, true>(tq, tk, tv, p, grid, s);
     return launch_fwd_t<64, false, false, true>(tq, tk, tv, p, grid, s);
   }
   if (D == 128) {

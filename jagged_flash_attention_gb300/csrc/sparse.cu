@@ -93,7 +93,8 @@ __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0,
 
 // One CTA per (block j, sequence b, tensor z): z = 0, K block j (128 keys)
 // for every K/V head into kbar [B][Hkv][kcap][D]; z = 1, Q block j (256
-// rows) for every query head into qbar [B][H][nqb][D].
+// rows) for every query head into qbar [B][H][nqb][D] (broadcast-Q: the
+// dense Q's block j, once, into qbar [H][nqb][D]).
 __global__ void __launch_bounds__(kPoolThreads) sparse_pool_kernel(SparseParams p) {
   __shared__ float part[kPoolThreads * 8];
   const int j = blockIdx.x, b = blockIdx.y;
@@ -106,6 +107,11 @@ __global__ void __launch_bounds__(kPoolThreads) sparse_pool_kernel(SparseParams 
     pool_rows(p.k, p.Hkv, p.D, off0 + r0, min(kBN, L - r0),
               p.kbar + (static_cast<long long>(b) * p.Hkv * p.kcap + j) * p.D,
               static_cast<long long>(p.kcap) * p.D, part);
+  } else if (p.broadcast) {  // the dense Q's blocks, once (by the CTAs of sequence 0)
+    const int r0 = j * kFwdRows;
+    if (b != 0 || j >= p.nqb) return;
+    pool_rows(p.q, p.H, p.D, r0, min(kFwdRows, p.Lq - r0), p.qbar + static_cast<long long>(j) * p.D,
+              static_cast<long long>(p.nqb) * p.D, part);
   } else {
     const int r0 = j * kFwdRows;
     if (j >= p.nqb || r0 >= L) return;
@@ -127,7 +133,8 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseParams
   const long long row = (static_cast<long long>(b) * p.H + h) * p.nqb + i;
   int32_t* list = p.blocks + row * p.kcap;
   const int q0 = i * kFwdRows;
-  if (!seq_ok(p, off0, L) || q0 >= L) {  // no such Q block (or bad offsets: an empty list)
+  // no such Q block, a sequence without keys (broadcast), or bad offsets: an empty list
+  if (!seq_ok(p, off0, L) || (p.broadcast ? L == 0 : q0 >= L)) {
     for (int c = t; c < p.kcap; c += kSelThreads) list[c] = -1;
     if (t == 0) p.counts[row] = 0;
     return;
@@ -135,7 +142,8 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseParams
   const int D = p.D;
   const int nk = cdiv(L, kBN);
   const int hk = h / p.G;
-  const float* qm = p.qbar + row * D;  // the Q block's mean (row = (b * H + h) * nqb + i)
+  // the Q block's mean (row = (b * H + h) * nqb + i; broadcast: one dense Q for all b)
+  const float* qm = p.qbar + (p.broadcast ? static_cast<long long>(h) * p.nqb + i : row) * D;
   // Scores: one warp per K block, lanes over the head dimension.
   const float* kb = p.kbar + (static_cast<long long>(b) * p.Hkv + hk) * p.kcap * D;
   for (int j = warp; j < nk; j += kSelThreads / 32) {

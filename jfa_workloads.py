@@ -151,22 +151,26 @@ def pairs(lengths, causal=False, q_len=0, broadcast_q=False, window=(-1, -1)) ->
     return total
 
 
-def random_block_lists(lengths, H, max_len, seed, p_keep=0.5, p_empty=0.0):
+def random_block_lists(lengths, H, max_len, seed, p_keep=0.5, p_empty=0.0, q_len=0):
     """Seeded random block lists in the layout of the block-sparse forward:
     blocks int32 [B, H, nqb, kcap] (ascending K-block indices, -1 after the
-    count) and counts int32 [B, H, nqb], nqb = ceil(max_len / 256), kcap =
-    ceil(max_len / 128).  Each K block of the sequence is kept with
-    probability p_keep (at least one unless the list is drawn empty, with
-    probability p_empty); Q blocks past a sequence get count 0."""
+    count) and counts int32 [B, H, nqb], nqb = ceil(max_len / 256) (with
+    q_len > 0, broadcast-Q: ceil(q_len / 256)), kcap = ceil(max_len / 128).
+    Each K block of the sequence is kept with probability p_keep (at least
+    one unless the list is drawn empty, with probability p_empty); Q blocks
+    past a sequence, and every Q block of a sequence without keys, get count
+    0."""
     rng = np.random.default_rng(seed)
     L = np.asarray(lengths, dtype=np.int64)
-    nqb, kcap = -(-max_len // 256), -(-max_len // 128)
+    nqb, kcap = -(-(q_len if q_len > 0 else max_len) // 256), -(-max_len // 128)
     blocks = np.full((L.size, H, nqb, kcap), -1, dtype=np.int32)
     counts = np.zeros((L.size, H, nqb), dtype=np.int32)
     for b, n in enumerate(L.tolist()):
         nk = -(-n // 128)
+        if nk == 0:
+            continue
         for h in range(H):
-            for i in range(-(-n // 256)):
+            for i in range(nqb if q_len > 0 else -(-n // 256)):
                 if rng.random() < p_empty:
                     continue
                 keep = np.flatnonzero(rng.random(nk) < p_keep)

@@ -163,18 +163,19 @@ def test_sparse_argument_errors(L):
     """Block selection and the sparse forward reject bad arguments on the host."""
     import jagged_flash_attention_gb300 as jfa
     sel = lambda **kw: jfa.lib().jfa_block_select(
-        16, 16, 16, 2, 4, kw.get("Hkv", 2), 128, kw.get("max_len", 1000), kw.get("permille", 500),
-        kw.get("blocks", 16), kw.get("counts", 16), 0)
-    L.jfa_block_select.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 3
+        16, 16, 16, 2, 4, kw.get("Hkv", 2), 128, kw.get("max_len", 1000), kw.get("q_len", 0),
+        kw.get("bq", 0), kw.get("permille", 500), kw.get("blocks", 16), kw.get("counts", 16), 0)
+    L.jfa_block_select.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 8 + [ctypes.c_void_p] * 3
     assert sel(permille=0) == 1 and b"permille" in L.jfa_last_error()
     assert sel(permille=1001) == 1 and b"permille" in L.jfa_last_error()
     assert sel(max_len=300000) == 1 and b"max_len must be <=" in L.jfa_last_error()
     assert sel(blocks=0) == 1 and b"blocks and counts" in L.jfa_last_error()
     assert sel(counts=18) == 1 and b"blocks and counts" in L.jfa_last_error()
     assert sel(Hkv=3) == 1 and b"H_kv must divide H" in L.jfa_last_error()
-    L.jfa_fwd_sparse.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [ctypes.c_float]
+    assert sel(bq=1, q_len=0) == 1 and b"q_len" in L.jfa_last_error()
+    L.jfa_fwd_sparse.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 7 + [ctypes.c_float]
                                  + [ctypes.c_void_p] * 5)
-    st = L.jfa_fwd_sparse(16, 16, 16, 16, 2, 4, 2, 128, 1000, 0.1, 0, 16, 16, 16, 0)
+    st = L.jfa_fwd_sparse(16, 16, 16, 16, 2, 4, 2, 128, 1000, 0, 0, 0.1, 0, 16, 16, 16, 0)
     assert st == 1 and b"blocks and counts" in L.jfa_last_error()
-    st = L.jfa_fwd_sparse(16, 16, 16, 16, 2, 4, 2, 96, 1000, 0.1, 16, 16, 16, 16, 0)
+    st = L.jfa_fwd_sparse(16, 16, 16, 16, 2, 4, 2, 96, 1000, 0, 0, 0.1, 16, 16, 16, 16, 0)
     assert st == 2 and b"D must be" in L.jfa_last_error()

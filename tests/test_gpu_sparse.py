@@ -156,7 +156,8 @@ def test_bad_list_is_caught_on_the_device():
     ct = torch.from_numpy(counts).cuda()
     out = torch.full_like(q, float("nan"))
     lse = torch.full((2, x["T"]), 7.0, device="cuda")
-    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], x["scale"], bl, ct, out, lse)
+    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], 0, 0, x["scale"], bl, ct, out,
+                       lse)
     with pytest.raises(jfa.JfaError, match="block-sparse list"):
         jfa.jfa_sync_and_check()
     assert torch.isnan(out).all() and (lse == 7.0).all()
@@ -166,9 +167,82 @@ def test_bad_list_is_caught_on_the_device():
     blocks[1, 0, 0, 3] = 3
     bl = torch.from_numpy(blocks).cuda()
     ct = torch.from_numpy(counts).cuda()
-    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], x["scale"], bl, ct, out, lse)
+    jfa.jfa_fwd_sparse(q, k, v, off, 2, 2, 2, 128, x["max_len"], 0, 0, x["scale"], bl, ct, out,
+                       lse)
     with pytest.raises(jfa.JfaError, match="block-sparse list"):
         jfa.jfa_sync_and_check()
     # the library still works afterwards
     blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=4)
     compare(_gpu_sparse(x, blocks, counts), _oracle_sparse(x, blocks, counts), ("out", "lse"))
+
+
+# ------------------------------------------------------------ broadcast-Q
+
+def _gpu_sparse_bq(x, blocks, counts):
+    import jagged_flash_attention_gb300 as jfa
+    (q, k, v), off = _dev(x)
+    bl = torch.from_numpy(np.ascontiguousarray(blocks, dtype=np.int32)).cuda()
+    ct = torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).cuda()
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], bl, ct, scale=x["scale"],
+                                  broadcast_q=True)
+    jfa.jfa_sync_and_check()
+    return {"out": f64(out), "lse": f64(lse)}
+
+
+def _oracle_sparse_bq(x, blocks, counts):
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    out, lse = orc.forward_sparse(q, k, v, x["offsets"], x["scale"], blocks, counts,
+                                  broadcast_q=True)
+    return {"out": out, "lse": lse}
+
+
+BQ_CASES = {
+    "bq_d128_q300_gqa": dict(name="broadcast_q", lengths=[0, 1, 300, 700, 129], H=4, Hkv=2,
+                             q_len=300),
+    "bq_d64_q64": dict(name="skewed_broadcast_q", lengths=[1000, 0, 5, 257], H=2),
+}
+
+
+@pytest.mark.parametrize("case", list(BQ_CASES), ids=list(BQ_CASES))
+def test_broadcast_sparse_forward_on_given_lists(case):
+    spec = dict(BQ_CASES[case])
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    blocks, counts = W.random_block_lists(x["lengths"], x["H"], x["max_len"], seed=9,
+                                          p_keep=0.5, p_empty=0.1, q_len=x["q_len"])
+    print(case, compare(_gpu_sparse_bq(x, blocks, counts), _oracle_sparse_bq(x, blocks, counts),
+                        ("out", "lse")))
+
+
+@pytest.mark.parametrize("case", list(BQ_CASES), ids=list(BQ_CASES))
+def test_broadcast_select_then_forward(case):
+    """Both stages on the GPU against the oracle's selection and forward, where
+    the oracle's scores separate the boundary; the lists valid everywhere."""
+    import jagged_flash_attention_gb300 as jfa
+    spec = dict(BQ_CASES[case])
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    (q, k, v), off = _dev(x)
+    blocks, counts = jfa.block_select(q, k, off, x["max_len"], 500, broadcast_q=True)
+    jfa.jfa_sync_and_check()
+    gb, gc = blocks.cpu().numpy(), counts.cpu().numpy()
+    rb, rc, rs = orc.block_select(f64(x["q"]), f64(x["k"]), x["offsets"], 500, broadcast_q=True)
+    np.testing.assert_array_equal(gc, rc)
+    same = True
+    for idx in np.ndindex(gc.shape):
+        c = int(gc[idx])
+        if c == 0:
+            continue
+        sel = gb[idx][:c]
+        sc = rs[idx]
+        nk = int(np.sum(~np.isnan(sc)))
+        assert np.all(np.diff(sel) > 0) and sel.max() < nk
+        unsel = np.setdiff1d(np.arange(nk), sel)
+        if unsel.size:
+            assert sc[unsel].max() <= sc[sel].min() + GAP
+        srt = np.sort(sc[:nk])[::-1]
+        if c == nk or srt[c - 1] - srt[c] > GAP:
+            np.testing.assert_array_equal(sel, rb[idx][:c])
+        else:
+            same = False
+    g = _gpu_sparse_bq(x, gb, gc)  # the GPU's own lists, through the public call
+    if same:  # every list is the oracle's: compare the outputs with the oracle's stages
+        print(case, compare(g, _oracle_sparse_bq(x, rb, rc), ("out", "lse")))
