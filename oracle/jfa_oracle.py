@@ -288,10 +288,14 @@ def delta_rowsum(out, dout, broadcast_q=False):
 # (K/V head h // group for query head h); the block score is the dot product
 # of the two pooled vectors; k = max(1, ceil(permille * n / 1000)) of the
 # sequence's n K blocks, in integer arithmetic; ties go to the lower block
-# index; the list is stored in ascending order.  Without a causal mask or
-# window.  In broadcast-Q mode the Q blocks are the 256-row blocks of the
-# one dense Q (the same for every sequence); a sequence without keys gets
-# an empty list (O = 0, LSE = -inf).
+# index; the list is stored in ascending order.  In broadcast-Q mode the Q
+# blocks are the 256-row blocks of the one dense Q (the same for every
+# sequence); a sequence without keys gets an empty list (O = 0, LSE =
+# -inf).  With a causal mask or a window (self-attention), the candidates
+# are the K blocks that hold an admissible key of some row of the Q block,
+# k counts from them, and the attention keeps a key only when it is both
+# in a listed block and in the row's band (a row can then be left with no
+# key: O = 0, LSE = -inf).
 
 SPARSE_Q_BLOCK = 256
 SPARSE_K_BLOCK = 128
@@ -308,7 +312,7 @@ def sparse_k_count(n_blocks, permille):
     return min(n_blocks, max(1, (permille * n_blocks + 999) // 1000))
 
 
-def block_select(q, k, offsets, permille, broadcast_q=False):
+def block_select(q, k, offsets, permille, broadcast_q=False, causal=False, window=None):
     """Top-k K blocks per (sequence, query head, Q block) by pooled scores.
 
     Returns (blocks, counts, scores): blocks int64 [B, H, nqb, kcap] holding
@@ -322,6 +326,8 @@ def block_select(q, k, offsets, permille, broadcast_q=False):
     off = _seq_bounds(offsets)
     B = off.size - 1
     H, Hkv, group = _heads(q, k, broadcast_q)
+    _check_mask_args(broadcast_q, causal, window)
+    wl, wr = _window(causal, window)
     L = np.diff(off)
     max_len = int(L.max()) if B else 0
     nqb = _cdiv(q.shape[0] if broadcast_q else max_len, SPARSE_Q_BLOCK)
@@ -335,7 +341,6 @@ def block_select(q, k, offsets, permille, broadcast_q=False):
         nq = nqb if broadcast_q else _cdiv(n, SPARSE_Q_BLOCK)
         if nk == 0:
             continue  # no keys: empty lists
-        kk = sparse_k_count(nk, permille)
         for h in range(H):
             kbar = np.stack([k[s0 + j * SPARSE_K_BLOCK: s0 + min(n, (j + 1) * SPARSE_K_BLOCK),
                                h // group, :].mean(axis=0) for j in range(nk)])
@@ -346,13 +351,20 @@ def block_select(q, k, offsets, permille, broadcast_q=False):
                     qbar = q[s0 + i * SPARSE_Q_BLOCK: s0 + min(n, (i + 1) * SPARSE_Q_BLOCK), h, :]
                 sc = kbar @ qbar.mean(axis=0)
                 scores[b, h, i, :nk] = sc
-                order = np.argsort(-sc, kind="stable")  # descending, ties: lower index first
+                # candidates: K blocks holding an admissible key of a row of the Q block
+                r0, r1 = i * SPARSE_Q_BLOCK, min(n, (i + 1) * SPARSE_Q_BLOCK) - 1
+                lo = 0 if wl is None else max(0, r0 - wl)
+                hi = n - 1 if wr is None else min(n - 1, r1 + wr)
+                cand = np.arange(lo // SPARSE_K_BLOCK, hi // SPARSE_K_BLOCK + 1)
+                kk = sparse_k_count(cand.size, permille)
+                order = cand[np.argsort(-sc[cand], kind="stable")]  # descending, ties: lower first
                 blocks[b, h, i, :kk] = np.sort(order[:kk])
                 counts[b, h, i] = kk
     return blocks, counts, scores
 
 
-def forward_sparse(q, k, v, offsets, scale, blocks, counts, broadcast_q=False):
+def forward_sparse(q, k, v, offsets, scale, blocks, counts, broadcast_q=False, causal=False,
+                   window=None):
     """Attention in which query row i of a sequence sees only the keys of the
     K blocks listed for its Q block (i // 256): blocks[b, h, i // 256,
     :counts[b, h, i // 256]].  A row with no key gets O = 0, LSE = -inf.
@@ -363,6 +375,7 @@ def forward_sparse(q, k, v, offsets, scale, blocks, counts, broadcast_q=False):
     B = off.size - 1
     T, Hkv, D = k.shape
     H, Hkv, group = _heads(q, k, broadcast_q)
+    _check_mask_args(broadcast_q, causal, window)
     if broadcast_q:
         Lq = q.shape[0]
         out = np.zeros((B, Lq, H, D))
@@ -383,7 +396,7 @@ def forward_sparse(q, k, v, offsets, scale, blocks, counts, broadcast_q=False):
                 r0, r1 = i * SPARSE_Q_BLOCK, min(nrows, (i + 1) * SPARSE_Q_BLOCK)
                 keep = np.isin(kblock, blocks[b, h, i, :counts[b, h, i]])
                 qrows = q[r0:r1, h, :] if broadcast_q else q[s0 + r0:s0 + r1, h, :]
-                s = scale * (qrows @ kb.T)
+                s = _scores(qrows, kb, scale, causal, r0, window)  # the band, if any
                 s = np.where(keep[None, :], s, -np.inf)
                 l = _lse_rows(s)
                 if broadcast_q:

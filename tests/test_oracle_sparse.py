@@ -13,7 +13,13 @@ and attention over the selected blocks only.  CPU only.
   sums over ragged blocks), a permutation of rows inside a K block;
 * the count rule k = max(1, ceil(permille * n / 1000));
 * planted slips (sum for mean, lowest scores kept, 128-row Q blocks, head
-  map h % H_kv) that these catch.
+  map h % H_kv) that these catch;
+* with a causal mask or a sliding window: a full selection is dense local
+  attention; candidates found by testing every (row, key) pair; the forward
+  against SDPA with the block mask AND a torch.tril / torch.triu band; a
+  causal row whose listed blocks hold no admissible key (O = 0, LSE =
+  -inf); slips (band ignored by the candidates or the attention, k counted
+  from all blocks) caught.
 """
 import math
 
@@ -157,7 +163,8 @@ def _mutant_module(replace_from, replace_to):
     import importlib.util
     import inspect
     src = inspect.getsource(jfa_oracle)
-    assert replace_from in src, replace_from
+    if replace_from not in src:  # a stale slip must not pass as a caught one
+        raise LookupError(replace_from)
     spec = importlib.util.spec_from_loader("jfa_oracle_sparse_mutant", loader=None)
     mod = importlib.util.module_from_spec(spec)
     exec(compile(src.replace(replace_from, replace_to), "jfa_oracle_sparse_mutant", "exec"),
@@ -186,11 +193,10 @@ def test_unmutated_copy_passes():
 
 @pytest.mark.parametrize("slip", [
     ("h // group, :].mean(axis=0) for j in range(nk)", "h // group, :].sum(axis=0) for j in range(nk)"),
-    ("order = np.argsort(-sc, kind=\"stable\")", "order = np.argsort(sc, kind=\"stable\")"),
+    ("order = cand[np.argsort(-sc[cand]", "order = cand[np.argsort(sc[cand]"),
     ("keep = np.isin(kblock, blocks[b, h, i, :counts[b, h, i]])",
      "keep = np.isin(kblock, blocks[b, h, min(i * 2, blocks.shape[2] - 1), :counts[b, h, i]])"),
-    ("                                h // group, :].mean(axis=0)",
-     "                                h % Hkv, :].mean(axis=0)"),
+    ("h // group, :].mean(axis=0) for j in range(nk)", "h % Hkv, :].mean(axis=0) for j in range(nk)"),
 ])
 def test_planted_sparse_slips_are_caught(slip):
     with pytest.raises(AssertionError):
@@ -268,3 +274,175 @@ def test_broadcast_selection_brute_force():
                     sc.append(sum(a * c for a, c in zip(qbar, kbar)))
                 best = sorted(sorted(range(nk), key=lambda j: (-sc[j], j))[:kk])
                 assert list(blocks[b, h, i, :counts[b, h, i]]) == best
+
+
+# ------------------------------------------- causal and sliding-window masks
+# The TLX page keeps windowing in the sparse variant.  Reading: a Q block's
+# candidates are the K blocks holding an admissible key of one of its rows,
+# k counts from them, and the attention keeps a key only when it is both
+# listed and admissible (a row left without one: O = 0, LSE = -inf).
+
+LOCAL_MASKS = [(True, None), (False, (64, 0)), (False, (300, 200)), (True, (200, None)),
+               (False, (0, 130))]
+
+
+def _admissible(i, j, causal, window):
+    wl, wr = (None, None) if window is None else window
+    if causal and not (j <= i):
+        return False
+    if wl is not None and j < i - wl:
+        return False
+    if wr is not None and j > i + wr:
+        return False
+    return True
+
+
+def _select_local_by_loops(q, k, off, permille, group, causal, window):
+    """Candidates by testing every (row, key) pair of the Q block against
+    every K block, then the pooled scores and a sort keyed on (-score, j)."""
+    res = {}
+    H, D = q.shape[1], q.shape[2]
+    for b in range(len(off) - 1):
+        s0, n = int(off[b]), int(off[b + 1] - off[b])
+        nk = -(-n // KB)
+        for h in range(H):
+            kbar = []
+            for j in range(nk):
+                rows = range(s0 + j * KB, s0 + min(n, (j + 1) * KB))
+                kbar.append([sum(k[r, h // group, d] for r in rows) / len(rows) for d in range(D)])
+            for i in range(-(-n // QB)):
+                qrows = range(i * QB, min(n, (i + 1) * QB))
+                cand = [j for j in range(nk)
+                        if any(_admissible(r, c, causal, window)
+                               for r in qrows for c in range(j * KB, min(n, (j + 1) * KB)))]
+                kk = min(len(cand), max(1, -(-(permille * len(cand)) // 1000)))
+                qbar = [sum(q[s0 + r, h, d] for r in qrows) / len(qrows) for d in range(D)]
+                sc = {j: sum(a * c for a, c in zip(qbar, kbar[j])) for j in cand}
+                res[(b, h, i)] = sorted(sorted(cand, key=lambda j: (-sc[j], j))[:kk])
+    return res
+
+
+@pytest.mark.parametrize("causal,window", LOCAL_MASKS)
+def test_local_full_selection_is_dense_local(causal, window):
+    q, k, v, off = _case([300, 1, 700, 129], 4, 2, 8, seed=61)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 1000, causal=causal, window=window)
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.3, blocks, counts, causal=causal,
+                                         window=window)
+    ref_out, ref_lse = jfa_oracle.forward(q, k, v, off, 0.3, causal, window=window)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", LOCAL_MASKS[:3])
+def test_local_selection_brute_force(causal, window):
+    q, k, v, off = _case([300, 1, 700], 2, 1, 4, seed=62)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, 400, causal=causal, window=window)
+    ref = _select_local_by_loops(q, k, off, 400, 2, causal, window)
+    for (b, h, i), sel in ref.items():
+        assert list(blocks[b, h, i, :counts[b, h, i]]) == sel, (b, h, i)
+
+
+def _torch_local_block_masked(q, k, v, off, scale, blocks, counts, causal, window):
+    """SDPA with the block mask AND the band (torch.tril / torch.triu on a
+    ones matrix); rows whose mask is all False are set to O = 0, LSE = -inf."""
+    out = np.zeros(q.shape)
+    H = q.shape[1]
+    lse = np.full((H, q.shape[0]), -np.inf)
+    wl, wr = (None, None) if window is None else window
+    if causal:
+        wr = 0 if wr is None else min(wr, 0)
+    for b in range(len(off) - 1):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        n = s1 - s0
+        if n == 0:
+            continue
+        nqb, nkb = -(-n // QB), -(-n // KB)
+        sel = torch.zeros(H, nqb, nkb, dtype=torch.bool)
+        for h in range(H):
+            for i in range(nqb):
+                for j in blocks[b, h, i, :counts[b, h, i]]:
+                    sel[h, i, int(j)] = True
+        mask = sel.repeat_interleave(QB, dim=1)[:, :n].repeat_interleave(KB, dim=2)[:, :, :n]
+        band = torch.ones(n, n, dtype=torch.bool)
+        if wr is not None:
+            band = torch.tril(band, diagonal=wr)
+        if wl is not None:
+            band = torch.triu(band, diagonal=-wl)
+        mask = mask & band
+        Q = torch.from_numpy(q[s0:s1]).permute(1, 0, 2)
+        K = torch.from_numpy(k[s0:s1]).permute(1, 0, 2)
+        V = torch.from_numpy(v[s0:s1]).permute(1, 0, 2)
+        grp = Q.shape[0] // K.shape[0]
+        O = torch.nn.functional.scaled_dot_product_attention(
+            Q, K, V, attn_mask=mask, scale=scale, enable_gqa=grp != 1)
+        S = (Q @ K.repeat_interleave(grp, dim=0).transpose(1, 2)) * scale
+        L = torch.logsumexp(S.masked_fill(~mask, -math.inf), dim=-1)
+        empty = ~mask.any(dim=-1)
+        O = O.masked_fill(empty[..., None], 0.0)
+        out[s0:s1] = O.permute(1, 0, 2).numpy()
+        lse[:, s0:s1] = L.numpy()
+    return out, lse
+
+
+@pytest.mark.parametrize("causal,window", LOCAL_MASKS)
+@pytest.mark.parametrize("permille", [250, 500])
+def test_local_sparse_forward_equals_torch_masks(causal, window, permille):
+    q, k, v, off = _case([700, 129, 1000, 5], 4, 2, 8, seed=63)
+    blocks, counts, _ = jfa_oracle.block_select(q, k, off, permille, causal=causal, window=window)
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.25, blocks, counts, causal=causal,
+                                         window=window)
+    ref_out, ref_lse = _torch_local_block_masked(q, k, v, off, 0.25, blocks, counts, causal,
+                                                 window)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def test_causal_row_without_listed_key():
+    """Causal, one 300-key sequence, Q block 0 lists K block 1 only: rows
+    0-127 see no admissible listed key (O = 0, LSE = -inf); row r in 128-255
+    sees keys 128..r; Q block 1 lists K blocks 0 and 2."""
+    q, k, v, off = _case([300], 1, 1, 4, seed=64)
+    blocks = np.full((1, 1, 2, 3), -1, dtype=np.int64)
+    counts = np.array([[[1, 2]]], dtype=np.int64)
+    blocks[0, 0, 0, 0] = 1
+    blocks[0, 0, 1, :2] = [0, 2]
+    out, lse = jfa_oracle.forward_sparse(q, k, v, off, 0.5, blocks, counts, causal=True)
+    assert np.all(out[:128] == 0.0) and np.all(np.isneginf(lse[0, :128]))
+    for r in (128, 129, 200, 255, 256, 257, 299):
+        keys = list(range(128, r + 1)) if r < 256 else list(range(0, 128)) + list(range(256, r + 1))
+        e = [math.exp(0.5 * float(np.dot(q[r, 0], k[j, 0]))) for j in keys]
+        o = sum(w * v[j, 0] for w, j in zip(e, keys)) / sum(e)
+        np.testing.assert_allclose(out[r, 0], o, atol=1e-12)
+        assert abs(lse[0, r] - math.log(sum(e))) < 1e-12
+
+
+def _check_local(mod):
+    causal, window = False, (300, 200)
+    q, k, v, off = _case([300, 1, 700], 2, 1, 4, seed=62)
+    blocks, counts, _ = mod.block_select(q, k, off, 400, causal=causal, window=window)
+    ref = _select_local_by_loops(q, k, off, 400, 2, causal, window)
+    for (b, h, i), sel in ref.items():
+        assert list(blocks[b, h, i, :counts[b, h, i]]) == sel, (b, h, i)
+    out, lse = mod.forward_sparse(q, k, v, off, 0.25, blocks, counts, causal=causal, window=window)
+    ref_out, ref_lse = _torch_local_block_masked(q, k, v, off, 0.25, blocks, counts, causal,
+                                                 window)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+
+
+def test_unmutated_copy_passes_local():
+    _check_local(_mutant_module("", ""))
+
+
+@pytest.mark.parametrize("slip", [
+    # the band ignored when choosing candidates
+    ("hi = n - 1 if wr is None else min(n - 1, r1 + wr)", "hi = n - 1"),
+    ("lo = 0 if wl is None else max(0, r0 - wl)", "lo = 0"),
+    # k counted from all the sequence's K blocks
+    ("kk = sparse_k_count(cand.size, permille)", "kk = min(cand.size, sparse_k_count(nk, permille))"),
+    # the band ignored by the attention
+    ("s = _scores(qrows, kb, scale, causal, r0, window)  # the band, if any",
+     "s = _scores(qrows, kb, scale, causal, r0)"),
+])
+def test_planted_local_sparse_slips_are_caught(slip):
+    with pytest.raises(AssertionError):
+        _check_local(_mutant_module(*slip))

@@ -225,7 +225,8 @@ def _mutant_module(replace_from, replace_to):
     import importlib.util
     import inspect
     src = inspect.getsource(jfa_oracle)
-    assert replace_from in src, replace_from
+    if replace_from not in src:  # a stale slip must not pass as a caught one
+        raise LookupError(replace_from)
     spec = importlib.util.spec_from_loader("jfa_oracle_variant_mutant", loader=None)
     mod = importlib.util.module_from_spec(spec)
     exec(compile(src.replace(replace_from, replace_to), "jfa_oracle_variant_mutant", "exec"),
