@@ -414,19 +414,45 @@ def _time_steps(jfa, torch, x, steps, warmup, stream, dev, min_seconds=0.15):
     return fwd_ms, bwd_ms, kprof, launches, (t0, t1), steps
 
 
+def _sparse_pairs(lengths, H, bl, ct, causal, window):
+    """Computed (query, key) pairs of the block-sparse forward, summed over
+    the heads: per (sequence, head, Q block) and listed K block, the keys of
+    the block inside each row's band (all of them without a local mask)."""
+    big = 1 << 40
+    wl = big if window is None or window[0] is None or window[0] < 0 else window[0]
+    wr = big if window is None or window[1] is None or window[1] < 0 else window[1]
+    if causal:
+        wr = min(wr, 0)
+    pairs = 0
+    for b, n in enumerate(np.asarray(lengths).tolist()):
+        for i in range(-(-n // 256)):
+            rows = np.arange(256 * i, min(n, 256 * i + 256))[:, None]
+            for h in range(H):
+                sel = bl[b, h, i, :ct[b, h, i]].astype(np.int64)[None, :]
+                lo = np.maximum(sel * 128, rows - wl)
+                hi = np.minimum(np.minimum(sel * 128 + 127, n - 1), rows + wr)
+                pairs += int(np.clip(hi - lo + 1, 0, None).sum())
+    return pairs
+
+
 def _time_sparse(jfa, torch, x, permille, steps, warmup, stream, dev, min_seconds=0.15):
     """Block-sparse forward (selection + attention over the selected blocks)
-    of workload x, device-timed; returns (ms per step, kernel profile,
-    selected (query, key) pairs summed over the heads, host window, steps)."""
+    of workload x (with its causal mask and window, if any), device-timed;
+    returns (ms per step, kernel profile, computed (query, key) pairs summed
+    over the heads, host window, steps)."""
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     off = torch.from_numpy(x["offsets"]).to(dev)
     ml, scale = x["max_len"], x["scale"]
-    blocks, counts = jfa.block_select(q, k, off, ml, permille)
-    out, lse = jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale)
+    causal, window = bool(x["causal"]), x.get("window")
+    blocks, counts = jfa.block_select(q, k, off, ml, permille, causal=causal, window=window)
+    out, lse = jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale, causal=causal,
+                                  window=window)
 
     def step():
-        jfa.block_select(q, k, off, ml, permille, blocks=blocks, counts=counts)
-        jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale, out=out, lse=lse)
+        jfa.block_select(q, k, off, ml, permille, blocks=blocks, counts=counts, causal=causal,
+                         window=window)
+        jfa.forward_sparse(q, k, v, off, ml, blocks, counts, scale=scale, out=out, lse=lse,
+                           causal=causal, window=window)
 
     for _ in range(warmup):
         step()
@@ -449,17 +475,37 @@ def _time_sparse(jfa, torch, x, permille, steps, warmup, stream, dev, min_second
     win = (h0, time.time())
     kprof = jfa.profile_read()
     jfa.jfa_sync_and_check()
-    # selected pairs, summed over heads: per (sequence, head, Q block) its rows
-    # times the keys of its blocks
-    bl, ct = blocks.cpu().numpy(), counts.cpu().numpy()
-    pairs = 0
-    for b, n in enumerate(x["lengths"].tolist()):
-        for i in range(-(-n // 256)):
-            rows = min(256, n - 256 * i)
-            for h in range(x["H"]):
-                sel = bl[b, h, i, :ct[b, h, i]]
-                pairs += rows * int(sum(min(128, n - 128 * int(j)) for j in sel))
+    pairs = _sparse_pairs(x["lengths"], x["H"], blocks.cpu().numpy(), counts.cpu().numpy(),
+                          causal, window)
     return e0.elapsed_time(e1) / steps, kprof, pairs, win, steps
+
+
+# Block-sparse variants of the bench line: name -> the workload they run on.
+SPARSE_VARIANTS = {"jagged_self_block_sparse500": "jagged_self",
+                   "causal_self_block_sparse500": "causal_self"}
+
+
+def _sparse_entry(xs, base, sname, sp_ms, sp_prof, sp_pairs, sp_steps, peak, hbm, dense_fwd_ms):
+    """Bench entry of a block-sparse variant: selection + attention per step;
+    the attention kernel's work is the computed pairs."""
+    kern = _kernels_entry(xs, sp_prof, peak, hbm, sname)
+    fl = 4.0 * xs["D"] * sp_pairs  # sp_pairs counts every head
+    if "fwd" in kern:
+        ms = kern["fwd"]["ms_per_launch"]
+        kern["fwd"]["tflops"] = fl / (ms * 1e-3) / 1e12
+        kern["fwd"]["roofline_frac"] = kern["fwd"]["tflops"] / peak
+    dense_pairs = W.pairs(xs["lengths"], xs["causal"], xs["q_len"], xs["broadcast_q"],
+                          xs.get("window", (-1, -1)))
+    return {
+        "config": {k: v for k, v in _config(xs, base).items()
+                   if k not in ("parallelism",)} | {"permille": 500},
+        "steps": sp_steps,
+        "fwd": {"ms": sp_ms, "tflops": fl / (sp_ms * 1e-3) / 1e12,
+                "selected_fraction": sp_pairs / (xs["H"] * dense_pairs),
+                "dense_fwd_ms": dense_fwd_ms,
+                "speedup_vs_dense": (dense_fwd_ms / sp_ms) if dense_fwd_ms else None},
+        "kernels": kern,
+    }
 
 
 def _workload_entry(x, wname, fwd_ms, bwd_ms, kprof, peak, hbm, clk, window, steps):
@@ -621,7 +667,7 @@ def run_ours(args, x, wname):
     # The other workloads (rank 0 of a single-GPU run, unless --only): each
     # device-timed over a few steps through the same public API.
     workloads, variants = {}, {}
-    sparse_entry = None
+    sparse_entries = {}
     if ws == 1 and not args.only:
         workloads[wname] = (x, fwd_ms, bwd_ms, kprof, windows[0], args.steps)
         for other in W.ORDER:
@@ -635,15 +681,17 @@ def run_ours(args, x, wname):
             workloads[other] = (xo, f_ms, b_ms, kp, win, steps)
             del xo
             torch.cuda.empty_cache()
-        # block-sparse forward at a 0.5 selection ratio, against the dense forward
-        xs = W.make_inputs(W.WORKLOADS["jagged_self"])
-        sp_ms, sp_prof, sp_pairs, win, sp_steps = _time_sparse(
-            jfa, torch, xs, 500, max(3, min(args.steps, args.workload_steps)),
-            max(3, args.warmup), stream, dev)
-        windows.append(win)
-        sparse_entry = (xs, sp_ms, sp_prof, sp_pairs, win, sp_steps)
-        del xs
-        torch.cuda.empty_cache()
+        # block-sparse forward at a 0.5 selection ratio, against the dense
+        # forward of the same workload (causal_self: with its causal mask)
+        for sname, base in SPARSE_VARIANTS.items():
+            xs = W.make_inputs(W.WORKLOADS[base])
+            sp_ms, sp_prof, sp_pairs, win, sp_steps = _time_sparse(
+                jfa, torch, xs, 500, max(3, min(args.steps, args.workload_steps)),
+                max(3, args.warmup), stream, dev)
+            windows.append(win)
+            sparse_entries[sname] = (base, sp_ms, sp_prof, sp_pairs, win, sp_steps, xs)
+            del xs
+            torch.cuda.empty_cache()
         # GQA and sliding-window variants, the same way
         for vname in W.VARIANTS:
             xo = W.make_inputs(W.variant(vname))
@@ -655,29 +703,11 @@ def run_ours(args, x, wname):
             del xo
             torch.cuda.empty_cache()
     clk.__exit__(None, None, None)
-    if sparse_entry is not None:
-        xs, sp_ms, sp_prof, sp_pairs, win, sp_steps = sparse_entry
-        dense_fwd_ms = workloads["jagged_self"][1]  # (x, fwd ms, ...) of the dense run
-        kern = _kernels_entry(xs, sp_prof, peak, hbm, "jagged_self_block_sparse500")
-        fl = 4.0 * xs["D"] * sp_pairs  # sp_pairs counts every head
-        for kk in ("fwd",):  # the attention kernel's work is the selected pairs
-            if kk in kern:
-                ms = kern[kk]["ms_per_launch"]
-                kern[kk]["tflops"] = fl / (ms * 1e-3) / 1e12
-                kern[kk]["roofline_frac"] = kern[kk]["tflops"] / peak
-        dense_pairs = W.pairs(xs["lengths"])
-        variants["jagged_self_block_sparse500"] = {
-            "config": {k: v for k, v in _config(xs, "jagged_self").items()
-                       if k not in ("parallelism",)} | {"permille": 500},
-            "steps": sp_steps,
-            "fwd": {"ms": sp_ms, "tflops": fl / (sp_ms * 1e-3) / 1e12,
-                    "selected_fraction": sp_pairs / (xs["H"] * dense_pairs),
-                    "dense_fwd_ms": dense_fwd_ms,
-                    "speedup_vs_dense": (dense_fwd_ms / sp_ms) if dense_fwd_ms else None},
-            "kernels": kern,
-            "clocks": clk.summary([win]),
-        }
-        del xs
+    for sname, (base, sp_ms, sp_prof, sp_pairs, win, sp_steps, xs) in sparse_entries.items():
+        dense_fwd_ms = workloads[base][1]  # (x, fwd ms, ...) of the dense run
+        variants[sname] = _sparse_entry(xs, base, sname, sp_ms, sp_prof, sp_pairs, sp_steps,
+                                        peak, hbm, dense_fwd_ms) | {"clocks": clk.summary([win])}
+    sparse_entries.clear()
     for group in (workloads, variants):
         for other, entry in list(group.items()):
             if isinstance(entry, tuple):
@@ -748,15 +778,13 @@ def run_variant(args):
     peak, _, hbm, _ = _peaks()
     stream = torch.cuda.current_stream()
     steps, warmup = max(3, args.steps), max(3, args.warmup)
-    if args.variant == "jagged_self_block_sparse500":
-        w = W.WORKLOADS["jagged_self"]
+    if args.variant in SPARSE_VARIANTS:
+        base = SPARSE_VARIANTS[args.variant]
+        w = W.WORKLOADS[base]
         lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
         x = W.make_inputs(w, lengths=lengths)
         ms, kprof, pairs, _, steps = _time_sparse(jfa, torch, x, 500, steps, warmup, stream, dev)
-        fl = 4.0 * x["D"] * pairs
-        entry = {"fwd": {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
-                         "selected_fraction": pairs / (x["H"] * W.pairs(x["lengths"]))},
-                 "kernels": _kernels_entry(x, kprof, peak, hbm, "jagged_self_block_sparse500")}
+        entry = _sparse_entry(x, base, args.variant, ms, kprof, pairs, steps, peak, hbm, None)
     else:
         w = W.variant(args.variant)
         lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
@@ -785,7 +813,7 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default=None,
-                    choices=list(W.VARIANTS) + ["jagged_self_block_sparse500"],
+                    choices=list(W.VARIANTS) + list(SPARSE_VARIANTS),
                     help="time one GQA / window / block-sparse variant alone (one JSON line "
                          "with that variant's entry; for profiling captures)")
     ap.add_argument("--batch", type=int, default=None,

@@ -134,9 +134,11 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
 /* Block-sparse attention ("Optimizing Jagged Flash Attention with TLX",
  * section 3, "Block-sparse attention"): a cheap scoring step average-pools
  * each Q block and each K block and keeps the top-k K/V blocks per Q block;
- * the attention then runs over the selected blocks only.  Without a causal
- * mask or window; GQA as for jfa_fwd_ex; self-attention, or broadcast-Q
- * (broadcast_q = 1, q_len as for jfa_fwd_bq, layouts of broadcast-Q).
+ * the attention then runs over the selected blocks only.  GQA as for
+ * jfa_fwd_ex; self-attention, or broadcast-Q (broadcast_q = 1, q_len as for
+ * jfa_fwd_bq, layouts of broadcast-Q).  The pages keep windowing in the
+ * sparse variant: the _ex forms take a causal mask and a sliding window as
+ * jfa_fwd_ex does (self-attention only).
  *
  * Blocks: K block j of a sequence = its keys [128 j, 128 j + 128), Q block i
  * = its query rows [256 i, 256 i + 256) (broadcast: rows of the dense Q,
@@ -166,7 +168,16 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
  * strictly ascending below it, sets the device error word, reported by
  * jfa_sync_and_check as JFA_ERR_INVALID_ARG, and nothing is written).  The
  * forward kernel is the dense one following each item's list instead of all
- * key tiles, so its time scales with the selected fraction. */
+ * key tiles, so its time scales with the selected fraction.
+ *
+ * jfa_block_select_ex / jfa_fwd_sparse_ex add causal, window_left and
+ * window_right, with the meaning and checks of jfa_fwd_ex; the plain forms
+ * are these with causal = 0 and window_left = window_right = -1.  With a
+ * local mask (admissible keys [i - wl, i + wr] for row i), the candidates
+ * of Q block i are the K blocks that hold an admissible key of one of its
+ * rows, and k counts from those candidates instead of all n; the forward
+ * keeps a key only when it is both in a listed block and admissible, so a
+ * row whose band misses every listed block gets out = 0 and lse = -inf. */
 jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
                             int H_kv, int D, int max_len, int q_len, int broadcast_q,
                             int permille, int32_t* blocks, int32_t* counts, cudaStream_t stream);
@@ -174,6 +185,15 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
                           int B, int H, int H_kv, int D, int max_len, int q_len, int broadcast_q,
                           float scale, const int32_t* blocks, const int32_t* counts, void* out,
                           float* lse, cudaStream_t stream);
+jfa_status jfa_block_select_ex(const void* q, const void* k, const int32_t* offsets, int B, int H,
+                               int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                               int causal, int window_left, int window_right, int permille,
+                               int32_t* blocks, int32_t* counts, cudaStream_t stream);
+jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const int32_t* offsets,
+                             int B, int H, int H_kv, int D, int max_len, int q_len,
+                             int broadcast_q, int causal, int window_left, int window_right,
+                             float scale, const int32_t* blocks, const int32_t* counts, void* out,
+                             float* lse, cudaStream_t stream);
 
 /* Allocation-free forward pass.  The pages have no counterpart: this entry
  * point exists for callers that must not allocate device memory while the

@@ -14,7 +14,8 @@ import os
 from .build import LIB_PATH
 
 __all__ = ["JfaError", "lib", "jfa_fwd", "jfa_bwd", "jfa_fwd_bq", "jfa_bwd_bq", "jfa_fwd_ex",
-           "jfa_bwd_ex", "jfa_block_select", "jfa_fwd_sparse", "block_select", "forward_sparse",
+           "jfa_bwd_ex", "jfa_block_select", "jfa_fwd_sparse", "jfa_block_select_ex",
+           "jfa_fwd_sparse_ex", "block_select", "forward_sparse",
            "jfa_fwd_bq_noalloc", "jfa_worklist", "jfa_sync_and_check", "forward", "backward",
            "STATUS"]
 
@@ -151,6 +152,28 @@ def jfa_fwd_sparse(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q,
               _stream(stream)))
 
 
+def jfa_block_select_ex(q, k, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, causal,
+                        window_left, window_right, permille, blocks, counts, stream=None):
+    fn = lib().jfa_block_select_ex
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _P, _P] + [_I] * 11 + [_P, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(q), _ptr(k), _ptr(offsets), B, H, H_kv, D, max_len, q_len, int(broadcast_q),
+              int(causal), int(window_left), int(window_right), int(permille), _ptr(blocks),
+              _ptr(counts), _stream(stream)))
+
+
+def jfa_fwd_sparse_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, causal,
+                      window_left, window_right, scale, blocks, counts, out, lse, stream=None):
+    fn = lib().jfa_fwd_sparse_ex
+    if fn.argtypes is None:
+        fn.argtypes = [_P, _P, _P, _P] + [_I] * 10 + [_F, _P, _P, _P, _P, _P]
+        fn.restype = _I
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), B, H, H_kv, D, max_len, q_len,
+              int(broadcast_q), int(causal), int(window_left), int(window_right), float(scale),
+              _ptr(blocks), _ptr(counts), _ptr(out), _ptr(lse), _stream(stream)))
+
+
 def jfa_fwd_bq_noalloc(q, k, v, offsets, B, H, D, max_len, q_len, broadcast_q, causal, scale,
                        out, lse, stream=None):
     """Allocation-free forward (see include/jfa.h): for callers that must not
@@ -267,10 +290,11 @@ def backward(q, k, v, offsets, max_len, out, lse, dout, causal=False, broadcast_
 
 
 def block_select(q, k, offsets, max_len, permille, blocks=None, counts=None, stream=None,
-                 broadcast_q=False):
+                 broadcast_q=False, causal=False, window=None):
     """Top-k K blocks per (sequence, query head, 256-row Q block) (see
     jfa_block_select in include/jfa.h); returns int32 (blocks [B, H, nqb,
-    kcap], counts [B, H, nqb])."""
+    kcap], counts [B, H, nqb]).  causal / window restrict the candidates to
+    the blocks inside each Q block's band (jfa_block_select_ex)."""
     import torch
     B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
     nqb, kcap = -(-(Lq if broadcast_q else max_len) // 256), -(-max_len // 128)
@@ -278,14 +302,21 @@ def block_select(q, k, offsets, max_len, permille, blocks=None, counts=None, str
         blocks = torch.empty((B, H, nqb, kcap), dtype=torch.int32, device=q.device)
     if counts is None:
         counts = torch.empty((B, H, nqb), dtype=torch.int32, device=q.device)
-    jfa_block_select(q, k, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), permille,
-                     blocks, counts, stream)
+    wl, wr = _window(window)
+    if causal or (wl, wr) != (-1, -1):
+        jfa_block_select_ex(q, k, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), causal,
+                            wl, wr, permille, blocks, counts, stream)
+    else:
+        jfa_block_select(q, k, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), permille,
+                         blocks, counts, stream)
     return blocks, counts
 
 
 def forward_sparse(q, k, v, offsets, max_len, blocks, counts, scale=None, out=None, lse=None,
-                   stream=None, broadcast_q=False):
-    """Attention over the listed K blocks of each Q block (jfa_fwd_sparse)."""
+                   stream=None, broadcast_q=False, causal=False, window=None):
+    """Attention over the listed K blocks of each Q block (jfa_fwd_sparse;
+    with causal / window, over the admissible keys of those blocks:
+    jfa_fwd_sparse_ex)."""
     import torch
     B, H, Hkv, D, Lq = _shapes(q, k, offsets, broadcast_q)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
@@ -295,6 +326,11 @@ def forward_sparse(q, k, v, offsets, max_len, blocks, counts, scale=None, out=No
     if lse is None:
         lse = torch.empty((B, H, Lq) if broadcast_q else (H, k.shape[0]), dtype=torch.float32,
                           device=q.device)
-    jfa_fwd_sparse(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), scale, blocks,
-                   counts, out, lse, stream)
+    wl, wr = _window(window)
+    if causal or (wl, wr) != (-1, -1):
+        jfa_fwd_sparse_ex(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), causal,
+                          wl, wr, scale, blocks, counts, out, lse, stream)
+    else:
+        jfa_fwd_sparse(q, k, v, offsets, B, H, Hkv, D, max_len, Lq, int(broadcast_q), scale,
+                       blocks, counts, out, lse, stream)
     return out, lse

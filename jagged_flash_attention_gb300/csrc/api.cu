@@ -720,8 +720,17 @@ jfa_status jfa_bwd_ex(const void* q, const void* k, const void* v, const int32_t
 jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets, int B, int H,
                             int H_kv, int D, int max_len, int q_len, int broadcast_q,
                             int permille, int32_t* blocks, int32_t* counts, cudaStream_t stream) {
+  return jfa_block_select_ex(q, k, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1,
+                             permille, blocks, counts, stream);
+}
+
+jfa_status jfa_block_select_ex(const void* q, const void* k, const int32_t* offsets, int B, int H,
+                               int H_kv, int D, int max_len, int q_len, int broadcast_q,
+                               int causal, int window_left, int window_right, int permille,
+                               int32_t* blocks, int32_t* counts, cudaStream_t stream) {
   t_last_error.clear();
-  Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1, 1.f);
+  Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, causal, window_left,
+                       window_right, 1.f);
   jfa_status st = check_common(s, q, k, k, offsets);
   if (st != JFA_OK) return st;
   if (permille < 1 || permille > 1000)
@@ -760,6 +769,8 @@ jfa_status jfa_block_select(const void* q, const void* k, const int32_t* offsets
   sp.broadcast = s.broadcast;
   sp.nqb = (int)nqb;
   sp.kcap = (int)kcap;
+  sp.wl = s.kwl;
+  sp.wr = s.kwr;
   sp.kbar = static_cast<float*>(scratch);
   sp.qbar = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kbar_bytes);
   sp.blocks = blocks;
@@ -778,8 +789,18 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
                           int B, int H, int H_kv, int D, int max_len, int q_len, int broadcast_q,
                           float scale, const int32_t* blocks, const int32_t* counts, void* out,
                           float* lse, cudaStream_t stream) {
+  return jfa_fwd_sparse_ex(q, k, v, offsets, B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1,
+                           scale, blocks, counts, out, lse, stream);
+}
+
+jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const int32_t* offsets,
+                             int B, int H, int H_kv, int D, int max_len, int q_len,
+                             int broadcast_q, int causal, int window_left, int window_right,
+                             float scale, const int32_t* blocks, const int32_t* counts, void* out,
+                             float* lse, cudaStream_t stream) {
   t_last_error.clear();
-  const Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, 0, -1, -1, scale);
+  const Shape s = make_shape(B, H, H_kv, D, max_len, q_len, broadcast_q, causal, window_left,
+                             window_right, scale);
   jfa_status st = check_common(s, q, k, v, offsets);
   if (st != JFA_OK) return st;
   if (!out || !aligned16(out)) return fail(JFA_ERR_INVALID_ARG, "out must be non-null, 16-byte aligned");
@@ -818,8 +839,8 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
   WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
   Item* items = reinterpret_cast<Item*>(base + items_off);
   // The scheduler also checks every list before the forward follows it.
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, 0, s.broadcast, 0, kFwdRows, items, (int)cap,
-                 hdr, ds->err};
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.local, s.broadcast, 0, kFwdRows, items,
+                 (int)cap, hdr, ds->err, s.kwl, s.kwr};
   sp.blocks = blocks;
   sp.counts = counts;
   sp.nqb = (int)nqb;
@@ -844,7 +865,7 @@ jfa_status jfa_fwd_sparse(const void* q, const void* k, const void* v, const int
     fp.nqb = (int)nqb;
     fp.kcap = (int)kcap;
     e = run_kernel(JFA_KERNEL_FWD, stream, [&] {
-      return launch_fwd(s.D, false, s.broadcast, tq, tk, tv, fp, (int)cap, stream, true);
+      return launch_fwd(s.D, s.local, s.broadcast, tq, tk, tv, fp, (int)cap, stream, true);
     });
   }
   cudaError_t e2 = cudaFreeAsync(scratch, stream);

@@ -249,6 +249,7 @@ struct SparseParams {
   int B, H, Hkv, G, D, max_len, permille;
   int Lq, broadcast;  // broadcast-Q: the Q blocks are the dense Q's (q is [Lq, H, D])
   int nqb, kcap;  // ceil(max_len / 256) (broadcast: ceil(Lq / 256)), ceil(max_len / 128)
+  int wl, wr;     // local mask [i - wl, i + wr] (kNoWindow: unbounded side)
   float* kbar;     // scratch fp32 [B][Hkv][kcap][D]: K-block means
   float* qbar;     // scratch fp32 [B][H][nqb][D]: Q-block means (broadcast: [1][H][nqb][D])
   int32_t* blocks;

@@ -107,9 +107,11 @@ struct FwdCtl {
 // LOCAL: a local mask (causal or a sliding window, bounds p.wl / p.wr): a
 // query tile visits only the key tiles that hold admissible keys of its
 // rows, and the item streams the union of its two tiles' ranges.
-// SPARSE: block-sparse attention (no mask; self-attention or broadcast-Q):
-// both query tiles of the item visit the key tiles of the item's block list,
-// in its (ascending) order.
+// SPARSE: block-sparse attention (self-attention or broadcast-Q): both query
+// tiles of the item visit the key tiles of the item's block list, in its
+// (ascending) order; with LOCAL as well (self-attention) the band masks the
+// listed tiles, and a row left without an admissible key ends with O = 0,
+// LSE = -inf.
 template <bool BCAST, bool LOCAL, bool SPARSE>
 __device__ __forceinline__ FwdItem decode(const FwdParams& p, int idx, int T) {
   FwdItem f;
@@ -680,7 +682,11 @@ cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, co
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s,
                        bool sparse) {
   if (sparse) {
-    if (causal) return cudaErrorInvalidValue;
+    if (causal) {  // a local mask on top of the lists (self-attention only)
+      if (bcast) return cudaErrorInvalidValue;
+      if (D == 128) return launch_fwd_t<128, true, false, true>(tq, tk, tv, p, grid, s);
+      return launch_fwd_t<64, true, false, true>(tq, tk, tv, p, grid, s);
+    }
     if (D == 128) {
       if (bcast) return launch_fwd_t<128, false, true, true>(tq, tk, tv, p, grid, s);
       return launch_fwd_t<128, false, false, true>(tq, tk, tv, p, grid, s);

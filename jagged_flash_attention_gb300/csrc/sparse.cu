@@ -16,7 +16,10 @@
 //   sparse_select_kernel   per (Q block, query head, sequence): the dot
 //                          products of the Q-block mean with the sequence's
 //                          K-block means, the rank of every score, the
-//                          selected blocks in ascending order.
+//                          selected blocks in ascending order.  With a local
+//                          mask (causal or a window) only the K blocks that
+//                          hold an admissible key of some row of the Q block
+//                          are candidates, and k counts from them.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -142,11 +145,16 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseParams
   const int D = p.D;
   const int nk = cdiv(L, kBN);
   const int hk = h / p.G;
+  // Candidates: K blocks [jlo, jhi) holding keys of [q0 - wl, q_last + wr]
+  // (all of them without a local mask; kNoWindow keeps the sums in range).
+  const int q_last = (p.broadcast ? min(p.Lq, q0 + kFwdRows) : min(L, q0 + kFwdRows)) - 1;
+  const int jlo = max(0, q0 - p.wl) / kBN;
+  const int jhi = min(L - 1, q_last + p.wr) / kBN + 1;
   // the Q block's mean (row = (b * H + h) * nqb + i; broadcast: one dense Q for all b)
   const float* qm = p.qbar + (p.broadcast ? static_cast<long long>(h) * p.nqb + i : row) * D;
   // Scores: one warp per K block, lanes over the head dimension.
   const float* kb = p.kbar + (static_cast<long long>(b) * p.Hkv + hk) * p.kcap * D;
-  for (int j = warp; j < nk; j += kSelThreads / 32) {
+  for (int j = jlo + warp; j < jhi; j += kSelThreads / 32) {
     float s = 0.f;
     for (int d = lane; d < D; d += 32) s += qm[d] * kb[static_cast<long long>(j) * D + d];
 #pragma unroll
@@ -156,15 +164,20 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseParams
   __syncthreads();
   // Rank of every score (larger first, ties to the lower index); the k best
   // are selected.
-  const int k = min(nk, max(1, (p.permille * nk + 999) / 1000));
+  const int nc = jhi - jlo;
+  const int k = min(nc, max(1, (p.permille * nc + 999) / 1000));
   for (int j = t; j < nk; j += kSelThreads) {
-    const float sj = score[j];
-    int rank = 0;
-    for (int m = 0; m < nk; ++m) {
-      const float sm = score[m];
-      rank += (sm > sj || (sm == sj && m < j)) ? 1 : 0;
+    int f = 0;
+    if (j >= jlo && j < jhi) {
+      const float sj = score[j];
+      int rank = 0;
+      for (int m = jlo; m < jhi; ++m) {
+        const float sm = score[m];
+        rank += (sm > sj || (sm == sj && m < j)) ? 1 : 0;
+      }
+      f = rank < k ? 1 : 0;
     }
-    flag[j] = rank < k ? 1 : 0;
+    flag[j] = f;
   }
   __syncthreads();
   // Selected blocks in ascending order: a block-wide prefix count per chunk

@@ -179,3 +179,30 @@ def test_sparse_argument_errors(L):
     assert st == 1 and b"blocks and counts" in L.jfa_last_error()
     st = L.jfa_fwd_sparse(16, 16, 16, 16, 2, 4, 2, 96, 1000, 0, 0, 0.1, 16, 16, 16, 16, 0)
     assert st == 2 and b"D must be" in L.jfa_last_error()
+
+
+def test_local_sparse_argument_errors(L):
+    """The _ex forms of the block-sparse calls check the mask arguments like
+    jfa_fwd_ex does, on the host."""
+    L.jfa_block_select_ex.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int] * 11
+                                      + [ctypes.c_void_p] * 3)
+    L.jfa_fwd_sparse_ex.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 10 + [ctypes.c_float]
+                                    + [ctypes.c_void_p] * 5)
+
+    def both(bq, q_len, causal, wl, wr):
+        s1 = L.jfa_block_select_ex(16, 16, 16, 2, 4, 2, 128, 1000, q_len, bq, causal, wl, wr, 500,
+                                   16, 16, 0)
+        e1 = L.jfa_last_error().decode()
+        s2 = L.jfa_fwd_sparse_ex(16, 16, 16, 16, 2, 4, 2, 128, 1000, q_len, bq, causal, wl, wr,
+                                 0.1, 16, 16, 16, 16, 0)
+        e2 = L.jfa_last_error().decode()
+        return (s1, e1), (s2, e2)
+
+    for (st, err) in both(0, 0, 1, -1, 4):
+        assert st == 1 and "right side by 0" in err
+    for (st, err) in both(0, 0, 0, -2, -1):
+        assert st == 1 and "window bounds" in err
+    for (st, err) in both(1, 64, 1, -1, -1):
+        assert st == 2 and "self-attention only" in err
+    for (st, err) in both(1, 64, 0, 32, -1):
+        assert st == 2 and "self-attention only" in err

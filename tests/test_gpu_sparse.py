@@ -246,3 +246,105 @@ def test_broadcast_select_then_forward(case):
     g = _gpu_sparse_bq(x, gb, gc)  # the GPU's own lists, through the public call
     if same:  # every list is the oracle's: compare the outputs with the oracle's stages
         print(case, compare(g, _oracle_sparse_bq(x, rb, rc), ("out", "lse")))
+
+
+# ------------------------------------------- causal and sliding-window masks
+
+def _gpu_sparse_local(x, blocks, counts, causal, window):
+    import jagged_flash_attention_gb300 as jfa
+    (q, k, v), off = _dev(x)
+    bl = torch.from_numpy(np.ascontiguousarray(blocks, dtype=np.int32)).cuda()
+    ct = torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).cuda()
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], bl, ct, scale=x["scale"],
+                                  causal=causal, window=window)
+    jfa.jfa_sync_and_check()
+    return {"out": f64(out), "lse": f64(lse)}
+
+
+def _oracle_sparse_local(x, blocks, counts, causal, window):
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    out, lse = orc.forward_sparse(q, k, v, x["offsets"], x["scale"], blocks, counts,
+                                  causal=causal, window=window)
+    return {"out": out, "lse": lse}
+
+
+LOCAL_CASES = {
+    "causal_d128_edges": (dict(name="causal_self", lengths=[1, 127, 128, 129, 255, 256, 257, 700],
+                               H=2), True, None, 0.5),
+    "causal_d128_sparse_lists": (dict(name="causal_self", lengths=[1500, 300], H=2), True, None,
+                                 0.25),
+    "window_d64_gqa": (dict(name="tiny_self", lengths=[900, 3, 385], H=4, Hkv=2), False, (64, 0),
+                       0.5),
+    "window_d128_two_sided": (dict(name="jagged_self", lengths=[1000, 129, 600], H=2), False,
+                              (300, 200), 0.6),
+    "window_d128_right_only": (dict(name="jagged_self", lengths=[700, 260], H=2), False, (0, 130),
+                               0.7),
+}
+
+
+@pytest.mark.parametrize("case", list(LOCAL_CASES), ids=list(LOCAL_CASES))
+def test_local_sparse_forward_on_given_lists(case):
+    """Random lists (also with blocks outside the band, and causal rows left
+    without a listed admissible key) under a causal mask or a window."""
+    spec, causal, window, p_keep = LOCAL_CASES[case]
+    spec = dict(spec)
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    blocks, counts = W.random_block_lists(x["lengths"], x["H"], x["max_len"], seed=11,
+                                          p_keep=p_keep, p_empty=0.1)
+    r = _oracle_sparse_local(x, blocks, counts, causal, window)
+    g = _gpu_sparse_local(x, blocks, counts, causal, window)
+    print(case, compare(g, r, ("out", "lse")),
+          "rows without a key:", int(np.isinf(r["lse"]).sum()))
+
+
+@pytest.mark.parametrize("case", list(LOCAL_CASES)[1:4], ids=list(LOCAL_CASES)[1:4])
+def test_local_select_and_forward(case):
+    """Stage 1 under a local mask: counts exact, every list inside the
+    candidates (the oracle's full selection), valid against the oracle's
+    scores and equal to the oracle's list where the boundary is separated;
+    then stage 2 on the GPU's lists against the oracle's forward on them."""
+    import jagged_flash_attention_gb300 as jfa
+    spec, causal, window, _ = LOCAL_CASES[case]
+    spec = dict(spec)
+    x = inputs(spec.pop("name"), spec.pop("lengths"), **spec)
+    (q, k, v), off = _dev(x)
+    blocks, counts = jfa.block_select(q, k, off, x["max_len"], 400, causal=causal, window=window)
+    jfa.jfa_sync_and_check()
+    gb, gc = blocks.cpu().numpy(), counts.cpu().numpy()
+    q64, k64 = f64(x["q"]), f64(x["k"])
+    rb, rc, rs = orc.block_select(q64, k64, x["offsets"], 400, causal=causal, window=window)
+    cb, cc, _ = orc.block_select(q64, k64, x["offsets"], 1000, causal=causal, window=window)
+    np.testing.assert_array_equal(gc, rc)
+    exact = 0
+    for idx in np.ndindex(gc.shape):
+        c = int(gc[idx])
+        assert np.all(gb[idx][c:] == -1)
+        if c == 0:
+            continue
+        sel = gb[idx][:c]
+        cand = cb[idx][:int(cc[idx])]
+        assert np.all(np.diff(sel) > 0) and np.isin(sel, cand).all(), idx
+        sc = rs[idx]
+        unsel = np.setdiff1d(cand, sel)
+        if unsel.size:
+            assert sc[unsel].max() <= sc[sel].min() + GAP
+        srt = np.sort(sc[cand])[::-1]
+        if c == cand.size or srt[c - 1] - srt[c] > GAP:
+            np.testing.assert_array_equal(sel, rb[idx][:c])
+            exact += 1
+    assert exact > 0
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], blocks, counts, scale=x["scale"],
+                                  causal=causal, window=window)
+    jfa.jfa_sync_and_check()
+    r = _oracle_sparse_local(x, gb, gc, causal, window)
+    print(case, "exact lists:", exact, compare({"out": f64(out), "lse": f64(lse)}, r,
+                                               ("out", "lse")))
+
+
+def test_local_full_selection_equals_dense_local():
+    x = inputs("causal_self", [1000, 129, 3], H=2)
+    blocks, counts = W.random_block_lists(x["lengths"], 2, x["max_len"], seed=1, p_keep=1.0)
+    g = _gpu_sparse_local(x, blocks, counts, True, (300, None))
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    out, lse = orc.forward(q, k, v, x["offsets"], x["scale"], True, window=(300, None))
+    compare(g, {"out": out, "lse": lse}, ("out", "lse"))

@@ -40,3 +40,27 @@ def test_values_deterministic_bf16():
     assert x["q"].shape == (x["T"], 2, 64)
     b = W.make_inputs(W.WORKLOADS["broadcast_q"], lengths=[3, 4])
     assert b["q"].shape == (256, 4, 128) and b["dout"].shape == (2, 256, 4, 128)
+
+
+def test_sparse_pair_count_by_enumeration():
+    """The block-sparse bench's computed-pair count equals the number of
+    (row, key) entries of the block mask AND the band, enumerated."""
+    import bench
+    rng = np.random.default_rng(5)
+    lengths = np.array([1, 300, 700, 129])
+    for causal, window in ((False, (-1, -1)), (True, (-1, -1)), (False, (100, 40)),
+                           (True, (300, -1))):
+        bl, ct = W.random_block_lists(lengths, 2, 700, seed=int(rng.integers(100)), p_keep=0.5)
+        wl = None if window[0] < 0 else window[0]
+        wr = None if window[1] < 0 else window[1]
+        want = 0
+        for b, n in enumerate(lengths.tolist()):
+            for h in range(2):
+                for r in range(n):
+                    i = r // 256
+                    listed = set(bl[b, h, i, :ct[b, h, i]].tolist())
+                    for c in range(n):
+                        ok = (c // 128 in listed and (not causal or c <= r)
+                              and (wl is None or c >= r - wl) and (wr is None or c <= r + wr))
+                        want += ok
+        assert bench._sparse_pairs(lengths, 2, bl, ct, causal, window) == want
