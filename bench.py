@@ -16,6 +16,7 @@ per-kernel roofline fractions.  Prints ONE JSON line (rank 0).
 of the same workload); there is no GPU reference implementation.
 """
 import argparse
+import contextlib
 import datetime
 import hashlib
 import json
@@ -69,6 +70,7 @@ KERNEL_DESC = {
     "fwd_combine": "broadcast-Q forward: merge of split sequences",
     "sparse_pool": "block-sparse selection: K-block and Q-block means",
     "sparse_select": "block-sparse selection: scores and top-k per Q block",
+    "bwd_kv_pair": "backward dK/dV pass on CTA pairs (cta_group::2 products over two key blocks)",
 }
 
 
@@ -92,6 +94,7 @@ def kernel_model(x):
         "prep": (0.0, 2 * orows * row + 4 * H * orows + (stat if bq else 4 * stat)),
         "bwd_kv": (8.0 * H * D * pairs, (qrows + orows) * row + 4 * T * rkv + stat),
     }
+    m["bwd_kv_pair"] = m["bwd_kv"]
     if bq:
         m["bwd_qb"] = (6.0 * H * D * pairs,
                        (qrows + orows) * row + 2 * T * rkv + stat + 4 * Lq * H * D)
@@ -137,6 +140,7 @@ KERNEL_SOURCES = {
     "fwd": ["fwd.cu"], "bwd_kv": ["bwd_kv.cu"], "bwd_q": ["bwd_q.cu"], "bwd_qb": ["bwd_qb.cu"],
     "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"], "bwd_bs": ["bwd_bs.cu"],
     "fwd_combine": ["fwd_bs.cu"], "sparse_pool": ["sparse.cu"], "sparse_select": ["sparse.cu"],
+    "bwd_kv_pair": ["bwd_kv.cu"],
 }
 
 
@@ -480,6 +484,25 @@ def _time_sparse(jfa, torch, x, permille, steps, warmup, stream, dev, min_second
     return e0.elapsed_time(e1) / steps, kprof, pairs, win, steps
 
 
+# The dK/dV pass on pairs of CTAs (cta_group::2 products over two key
+# blocks; the library runs it under JFA_KV_PAIR=1): name -> workload.
+PAIR_VARIANTS = {"jagged_self_kv_pair": "jagged_self", "broadcast_q_kv_pair": "broadcast_q"}
+
+
+class _kv_pair:
+    """JFA_KV_PAIR=1 inside the block (the library reads it on every call)."""
+
+    def __enter__(self):
+        self.old = os.environ.get("JFA_KV_PAIR")
+        os.environ["JFA_KV_PAIR"] = "1"
+
+    def __exit__(self, *exc):
+        if self.old is None:
+            os.environ.pop("JFA_KV_PAIR", None)
+        else:
+            os.environ["JFA_KV_PAIR"] = self.old
+
+
 # Block-sparse variants of the bench line: name -> the workload they run on.
 SPARSE_VARIANTS = {"jagged_self_block_sparse500": "jagged_self",
                    "causal_self_block_sparse500": "causal_self"}
@@ -702,6 +725,17 @@ def run_ours(args, x, wname):
             variants[vname] = (xo, f_ms, b_ms, kp, win, steps)
             del xo
             torch.cuda.empty_cache()
+        # the dK/dV pass on CTA pairs (cta_group::2), the same way
+        for vname, base in PAIR_VARIANTS.items():
+            xo = W.make_inputs(W.WORKLOADS[base])
+            steps = max(3, min(args.steps, args.workload_steps))
+            with _kv_pair():
+                f_ms, b_ms, kp, _, win, steps = _time_steps(jfa, torch, xo, steps,
+                                                            max(3, args.warmup), stream, dev)
+            windows.append(win)
+            variants[vname] = (xo, f_ms, b_ms, kp, win, steps)
+            del xo
+            torch.cuda.empty_cache()
     clk.__exit__(None, None, None)
     for sname, (base, sp_ms, sp_prof, sp_pairs, win, sp_steps, xs) in sparse_entries.items():
         dense_fwd_ms = workloads[base][1]  # (x, fwd ms, ...) of the dense run
@@ -786,10 +820,13 @@ def run_variant(args):
         ms, kprof, pairs, _, steps = _time_sparse(jfa, torch, x, 500, steps, warmup, stream, dev)
         entry = _sparse_entry(x, base, args.variant, ms, kprof, pairs, steps, peak, hbm, None)
     else:
-        w = W.variant(args.variant)
+        pair = args.variant in PAIR_VARIANTS
+        w = W.WORKLOADS[PAIR_VARIANTS[args.variant]] if pair else W.variant(args.variant)
         lengths = None if args.batch is None else W.sample_lengths(w, B=args.batch)
         x = W.make_inputs(w, lengths=lengths)
-        f_ms, b_ms, kprof, _, _, steps = _time_steps(jfa, torch, x, steps, warmup, stream, dev)
+        with (_kv_pair() if pair else contextlib.nullcontext()):
+            f_ms, b_ms, kprof, _, _, steps = _time_steps(jfa, torch, x, steps, warmup, stream,
+                                                         dev)
         fwd_f, bwd_f, _ = _flops(x)
         entry = {"fwd": {"ms": f_ms, "tflops": fwd_f / (f_ms * 1e-3) / 1e12},
                  "bwd": {"ms": b_ms, "tflops": bwd_f / (b_ms * 1e-3) / 1e12},
@@ -813,7 +850,7 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default=None,
-                    choices=list(W.VARIANTS) + list(SPARSE_VARIANTS),
+                    choices=list(W.VARIANTS) + list(SPARSE_VARIANTS) + list(PAIR_VARIANTS),
                     help="time one GQA / window / block-sparse variant alone (one JSON line "
                          "with that variant's entry; for profiling captures)")
     ap.add_argument("--batch", type=int, default=None,

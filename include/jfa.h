@@ -272,9 +272,10 @@ typedef enum {
   JFA_KERNEL_FILL = 7,      /* outputs of an all-empty broadcast batch */
   JFA_KERNEL_BWD_BCAST_ONEPASS = 8, /* broadcast-Q backward, one pass (D = 64, q_len <= 128) */
   JFA_KERNEL_FWD_COMBINE = 9, /* broadcast-Q forward (q_len <= 128): merge of split sequences */
-  JFA_KERNEL_SPARSE_POOL = 10,   /* block-sparse selection: K-block means */
-  JFA_KERNEL_SPARSE_SELECT = 11, /* block-sparse selection: Q-block means, scores, top-k */
-  JFA_KERNEL_KINDS = 12
+  JFA_KERNEL_SPARSE_POOL = 10,   /* block-sparse selection: K-block and Q-block means */
+  JFA_KERNEL_SPARSE_SELECT = 11, /* block-sparse selection: scores, top-k */
+  JFA_KERNEL_BWD_KV_PAIR = 12,   /* backward dK / dV pass on pairs of CTAs (JFA_KV_PAIR=1) */
+  JFA_KERNEL_KINDS = 13
 } jfa_kernel_kind;
 
 /* Kernels enqueued by this library since the process started (all threads,

@@ -152,11 +152,12 @@ jfa_status map_rows(CUtensorMap* m, const void* ptr, int D, int H, long long row
   return JFA_OK;
 }
 
-// [B, Lq, H, D] bf16 tensor as a 4-D map (D, H, Lq, B), box 64 x 1 x 128 x 1.
-jfa_status map_bq(CUtensorMap* m, const void* ptr, int D, int H, int Lq, int B, const char* nm) {
+// [B, Lq, H, D] bf16 tensor as a 4-D map (D, H, Lq, B), box 64 x 1 x box_rows x 1.
+jfa_status map_bq(CUtensorMap* m, const void* ptr, int D, int H, int Lq, int B, const char* nm,
+                  unsigned box_rows = 128) {
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Lq, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)Lq * H * D * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, 1, box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -181,6 +182,14 @@ struct Shape {
   float scale;
   long long Tcap;  // upper bound of T used to size scratch and tensor maps
 };
+
+// dK/dV pass on pairs of CTAs (cta_group::2 products over two key blocks):
+// JFA_KV_PAIR=1 selects it where it applies (D = 128, no local mask; for
+// broadcast-Q, the two-pass backward); read on every call.
+bool kv_pair_mode(const Shape& s) {
+  const char* e = std::getenv("JFA_KV_PAIR");
+  return e != nullptr && e[0] == '1' && s.D == 128 && !s.local;
+}
 
 // GQA group and local mask of a kernel parameter block.
 template <class P>
@@ -393,6 +402,13 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   CUtensorMap tdk, tdv;
   if ((st = map_rows(&tdk, dk, s.D, s.Hkv, s.Tcap, "dk")) != JFA_OK) return st;
   if ((st = map_rows(&tdv, dv, s.D, s.Hkv, s.Tcap, "dv")) != JFA_OK) return st;
+  // the pair variant also reads half-tiles of Q and dO (64-row boxes)
+  const bool pair = kv_pair_mode(s);
+  CUtensorMap tq_h, tdo_h;
+  if (pair) {
+    if ((st = map_rows(&tq_h, q, s.D, s.H, s.Tcap, "q", 64)) != JFA_OK) return st;
+    if ((st = map_rows(&tdo_h, dout, s.D, s.H, s.Tcap, "dout", 64)) != JFA_OK) return st;
+  }
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -405,6 +421,7 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   // dK/dV items over the K/V heads, dQ items over the query heads
   SchedParams sk{offsets, s.B, s.Hkv, s.Lq, s.max_len, s.local, 0, 1, kBM,
                  items_kv, (int)cap_kv, hdr_kv, ds->err, s.kwl, s.kwr};
+  sk.kpair = pair ? 2 : 1;
   SchedParams sq{offsets, s.B, s.H, s.Lq, s.max_len, s.local, 0, 0, kFwdRows,
                  items_q, (int)cap_q, hdr_q, ds->err, s.kwl, s.kwr};
   BwdParams bp;
@@ -448,9 +465,10 @@ jfa_status do_bwd_self(DeviceState* ds, const Shape& s, const void* q, const voi
   if (e == cudaSuccess) {
     bp.items = items_kv;
     bp.hdr = hdr_kv;
-    e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
+    e = run_kernel(pair ? JFA_KERNEL_BWD_KV_PAIR : JFA_KERNEL_BWD_KV, stream, [&] {
       return launch_bwd_kv(s.D, s.local, false, tq, tk, tv, tdo, tdk, tdv, bp,
-                           (int)std::min<long long>(ds->sms, cap_kv), stream);
+                           (int)std::min<long long>(ds->sms, pair ? 2 * cap_kv : cap_kv), stream,
+                           pair ? &tq_h : nullptr, pair ? &tdo_h : nullptr);
     });
   }
   if (e == cudaSuccess) {
@@ -508,6 +526,12 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   if ((st = map_bq(&tdo, dout, s.D, s.H, s.Lq, s.B, "dout")) != JFA_OK) return st;
   if ((st = map_rows(&tdk, dk, s.D, s.Hkv, s.Tcap, "dk")) != JFA_OK) return st;
   if ((st = map_rows(&tdv, dv, s.D, s.Hkv, s.Tcap, "dv")) != JFA_OK) return st;
+  const bool pair = !one_pass && kv_pair_mode(s);
+  CUtensorMap tq_h, tdo_h;
+  if (pair) {
+    if ((st = map_rows(&tq_h, q, s.D, s.H, s.Lq, "q", 64)) != JFA_OK) return st;
+    if ((st = map_bq(&tdo_h, dout, s.D, s.H, s.Lq, s.B, "dout", 64)) != JFA_OK) return st;
+  }
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, off, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -536,6 +560,7 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
     pp.qb_only = one_pass ? 1 : 0;
     pp.sched[0] = SchedParams{offsets, s.B, s.Hkv, s.Lq, s.max_len, 0, 1, 1, kBM,
                               items_kv, (int)cap_kv, hdr_kv, ds->err};
+    pp.sched[0].kpair = pair ? 2 : 1;
     pp.qb = QbSchedParams{offsets, s.B, s.H, s.Lq, s.max_len, (int)chunk_cap, kt_off,
                           items_qb, (int)cap_qb, hdr_qb, ds->err};
     e = run_kernel(JFA_KERNEL_PREP, stream, [&] {
@@ -568,9 +593,10 @@ jfa_status do_bwd_bcast(DeviceState* ds, const Shape& s, const void* q, const vo
   if (e == cudaSuccess && !one_pass) {
     bp.items = items_kv;
     bp.hdr = hdr_kv;
-    e = run_kernel(JFA_KERNEL_BWD_KV, stream, [&] {
+    e = run_kernel(pair ? JFA_KERNEL_BWD_KV_PAIR : JFA_KERNEL_BWD_KV, stream, [&] {
       return launch_bwd_kv(s.D, false, true, tq, tk, tv, tdo, tdk, tdv, bp,
-                           (int)std::min<long long>(ds->sms, cap_kv), stream);
+                           (int)std::min<long long>(ds->sms, pair ? 2 * cap_kv : cap_kv), stream,
+                           pair ? &tq_h : nullptr, pair ? &tdo_h : nullptr);
     });
   }
   if (e == cudaSuccess && !one_pass) {

@@ -20,9 +20,9 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //  query items: tiles of `qrows` query rows (forward: 256 = two 128-row MMA
 //            tiles; self-attention dQ pass: 128); self: of the sequence,
 //            broadcast: of the dense Q
-//  backward: key/value blocks of the sequence
+//  backward: key/value blocks of the sequence (pairs of them for CTA pairs)
 __device__ __forceinline__ int n_tiles(const SchedParams& p, int L) {
-  if (p.backward) return cdiv(L, kBN);
+  if (p.backward) return cdiv(L, kBN * p.kpair);
   // broadcast: every sequence, even an empty one, owns its output rows
   return p.broadcast ? cdiv(p.Lq, p.qrows) : cdiv(L, p.qrows);
 }

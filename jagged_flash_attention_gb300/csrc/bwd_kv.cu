@@ -46,6 +46,23 @@
 // then the item's dV epilogue, the next item's first dS part, and only then
 // the item's dK epilogue, so that the first products of the next item wait
 // for one TMEM load each rather than for the epilogue.
+//
+// PAIR ("Optimizing Jagged Flash Attention with TLX", "2-CTA collaborative
+// MMA (backward)"): a cluster of two CTAs takes two adjacent key blocks of
+// one (sequence, head), CTA r block 2j + r, and the pair's products are
+// cta_group::2 products with M = 256 (the two key blocks) issued by CTA 0:
+// each CTA keeps its key block's K, V and accumulators and holds half of
+// every B operand.  Per query tile CTA r loads query rows [64r, 64r + 64) of
+// Q and dO with all head-dim columns (the N half of S^T and dP^T) and all
+// 128 rows of head-dim columns [64r, 64r + 64) (the N half of dK and dV):
+// [rows-half slab 0 | rows-half slab 1 | columns-half slab], 32 KB like the
+// single-CTA stage.  Both CTAs' loads complete on CTA 0's full barriers
+// (CTA 0 expects both CTAs' bytes), the commits arrive on both CTAs'
+// barriers, and each CTA's math warps report P^T / dS^T and the freed
+// accumulators to CTA 0's issuer, one arrive per warp.  Items are the key
+// block pairs of the work list, taken by the pairs in a fixed stride (both
+// CTAs walk the same items without exchanging tickets).  Self-attention
+// without a local mask and broadcast-Q, D = 128.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -140,13 +157,15 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ uint32_t pack_col(int k) { return 32 * (k >> 1) + 8 * (k & 1); }
 
 
-template <bool LOCAL, bool BCAST>
-__device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T) {
+template <bool LOCAL, bool BCAST, bool PAIR>
+__device__ __forceinline__ KvItem decode(const BwdParams& p, int idx, int T, int rank) {
   KvItem f;
   const Item it = p.items[idx];
   f.b = it.x;
   f.h = it.y >> 16;
-  f.kb = it.y & 0xffff;
+  // a pair item is a pair of key blocks; CTA r of the pair takes block 2j + r
+  // (past the sequence for the second CTA of an odd count: nothing stored)
+  f.kb = PAIR ? 2 * (it.y & 0xffff) + rank : it.y & 0xffff;
   f.off0 = p.offsets[f.b];
   f.L = p.offsets[f.b + 1] - f.off0;
   f.kt = row_box(f.off0 + f.kb * kBN, f.L - f.kb * kBN, T);
@@ -226,13 +245,73 @@ __device__ __forceinline__ bool next_item(KvCtl* c, uint32_t n, KvItem* f, bool*
   return f->b >= 0;
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool PAIR>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                              const CUtensorMap* tdo, const BwdParams& p, uint8_t* smem,
+                              const CUtensorMap* tdo, const CUtensorMap* tq_h,
+                              const CUtensorMap* tdo_h, const BwdParams& p, uint8_t* smem,
                               KvCtl* c) {
   using C = KvCfg<D>;
   const int n_items = p.hdr->n_items;
   const int T = p.hdr->T;
+  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
+  const bool lead = rank == 0;
+  // Items: the shared ticket; a pair walks the list in a fixed stride.
+  uint32_t ki = 0;
+  auto take = [&]() -> int {
+    if (PAIR) return static_cast<int>((blockIdx.x >> 1) + (ki++) * (gridDim.x >> 1));
+    return atomicAdd(&p.hdr->ticket, 1);
+  };
+  // A pair's loads complete on CTA 0's barriers, which expect both CTAs'
+  // bytes; CTA 1 only issues its copies.
+  auto expect = [&](uint64_t* bar, uint32_t bytes) {
+    if (!PAIR)
+      mbar_arrive_expect_tx(bar, bytes);
+    else if (lead)
+      mbar_arrive_expect_tx(bar, 2 * bytes);
+  };
+  auto load3 = [&](void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
+    if (PAIR && !lead)
+      tma_load_3d_pair(dst, m, smem_in_cta(bar, 0), c0, c1, c2);
+    else
+      tma_load_3d(dst, m, bar, c0, c1, c2);
+  };
+  auto load4 = [&](void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2, int c3) {
+    if (PAIR && !lead)
+      tma_load_4d_pair(dst, m, smem_in_cta(bar, 0), c0, c1, c2, c3);
+    else
+      tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  };
+  // Q or dO tile of query head qh at box row `row` into ring stage `st` of
+  // buffer `buf`, slab barriers full[0..1]; dO of broadcast-Q is the 4-D
+  // [B, q_len, H, D] tensor (coordinate b), everything else 3-D.
+  auto load_tile = [&](int buf, int st, const CUtensorMap* m, const CUtensorMap* m_h,
+                       uint64_t* full, int qh, int row, int b, bool four_d) {
+    uint8_t* dst = smem + buf + st * C::kTile;
+    if (!PAIR) {
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s) {
+        mbar_arrive_expect_tx(&full[s], 16384);
+        if (four_d)
+          tma_load_4d(dst + s * 16384, m, &full[s], s * 64, qh, row, b);
+        else
+          tma_load_3d(dst + s * 16384, m, &full[s], s * 64, qh, row);
+      }
+      return;
+    }
+    // [rows-half slab 0 | rows-half slab 1 | columns-half]: slab 0 of the
+    // row half on barrier 0, the rest on barrier 1
+    expect(&full[0], 8192);
+    expect(&full[1], 8192 + 16384);
+    if (four_d) {
+      load4(dst, m_h, &full[0], 0, qh, row + 64 * rank, b);
+      load4(dst + 8192, m_h, &full[1], 64, qh, row + 64 * rank, b);
+      load4(dst + 16384, m, &full[1], 64 * rank, qh, row, b);
+    } else {
+      load3(dst, m_h, &full[0], 0, qh, row + 64 * rank);
+      load3(dst + 8192, m_h, &full[1], 64, qh, row + 64 * rank);
+      load3(dst + 16384, m, &full[1], 64 * rank, qh, row);
+    }
+  };
   // gdo / gst: stages whose dO / statistics copy was issued
   uint32_t it = 0, gq = 0, gdo = 0, gst = 0, nk = 0, nv = 0;
   bool ok = true;
@@ -246,9 +325,9 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
   // loads go out, and its K, V and first Q / dO boxes are prefetched into
   // L2, so that at the item boundary they come from L2 rather than HBM.
   auto fetch = [&](KvItem& f) {
-    const int idx = atomicAdd(&p.hdr->ticket, 1);
+    const int idx = take();
     if (idx < n_items)
-      f = decode<LOCAL, BCAST>(p, idx, T);
+      f = decode<LOCAL, BCAST, PAIR>(p, idx, T, rank);
     else
       f.b = -1;
   };
@@ -283,11 +362,10 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     // previous item's last dP^T), then the other Q / dO tiles.
     const int ks = it & 1;
     if (!mbar_wait(&c->k_empty[ks], ((it >> 1) & 1) ^ 1, &c->abort, p.err)) break;
-    mbar_arrive_expect_tx(&c->k_full[ks], C::kTile);
+    expect(&c->k_full[ks], C::kTile);
 #pragma unroll
     for (int s = 0; s < C::kSlabs; ++s)
-      tma_load_3d(smem + C::kK + ks * C::kTile + s * 16384, tk, &c->k_full[ks], s * 64, f.h,
-                  f.kt.row);
+      load3(smem + C::kK + ks * C::kTile + s * 16384, tk, &c->k_full[ks], s * 64, f.h, f.kt.row);
     ++nk;
     for (int i = 0; i < f.nt; ++i) {
       const uint32_t g = gq;
@@ -301,16 +379,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
       }
       const int t = q_tile(f, i), qh = q_head(p, f, i);
       const RowBox qb = q_box<BCAST>(p, f, t, T);
-#pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s) {
-        mbar_arrive_expect_tx(&c->do_full[st][s], 16384);
-        if (BCAST)
-          tma_load_4d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
-                      qh, qb.row, f.b);
-        else
-          tma_load_3d(smem + C::kDO + st * C::kTile + s * 16384, tdo, &c->do_full[st][s], s * 64,
-                      qh, qb.row);
-      }
+      load_tile(C::kDO, st, tdo, tdo_h, c->do_full[st], qh, qb.row, f.b, BCAST);
       ++gdo;  // counted now: a wait below that gives up must not hide these copies from the drain
       // Row statistics of the box: 32 whole groups (1 KB).
       if (!mbar_wait(&c->stat_empty[st], ((g / C::NSQ) & 1) ^ 1, &c->abort, p.err)) {
@@ -331,33 +400,31 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         held0 = tag;
       else
         held1 = tag;
+      if (reuse) {  // Q already in the stage: the phases complete at once
+        if (!PAIR || lead) {
 #pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s) {
-        if (reuse) {  // Q already in the stage: the phase completes at once
-          mbar_arrive(&c->q_full[st][s]);
-          continue;
+          for (int s = 0; s < C::kSlabs; ++s) mbar_arrive(&c->q_full[st][s]);
         }
-        mbar_arrive_expect_tx(&c->q_full[st][s], 16384);
-        tma_load_3d(smem + C::kQ + st * C::kTile + s * 16384, tq, &c->q_full[st][s], s * 64, qh,
-                    qb.row);
+      } else {
+        load_tile(C::kQ, st, tq, tq_h, c->q_full[st], qh, qb.row, f.b, false);
       }
       ++gq;
       if (i == 0) {
         // V first: the item's first dP^T waits for it.  The next item's
         // ticket is taken before the wait and decoded (two dependent global
         // loads) only once V's copy is out.
-        const int nidx = atomicAdd(&p.hdr->ticket, 1);
+        const int nidx = take();
         if (!mbar_wait(&c->v_empty, (it & 1) ^ 1, &c->abort, p.err)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&c->v_full, C::kTile);
+        expect(&c->v_full, C::kTile);
 #pragma unroll
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(smem + C::kV + s * 16384, tv, &c->v_full, s * 64, f.h, f.kt.row);
+          load3(smem + C::kV + s * 16384, tv, &c->v_full, s * 64, f.h, f.kt.row);
         ++nv;
         if (nidx < n_items) {
-          nx = decode<LOCAL, BCAST>(p, nidx, T);
+          nx = decode<LOCAL, BCAST, PAIR>(p, nidx, T, rank);
           prefetch(nx);
         }
       }
@@ -365,26 +432,60 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     ++it;
     f = nx;
   }
-  for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
-    drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
-  if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
-  for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
+  // A pair's copies complete on CTA 0's barriers: CTA 0 drains both CTAs'
+  // (the pair's closing cluster barrier keeps CTA 1 until then).
+  if (!PAIR || lead) {
+    for (uint32_t j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
+      drain_wait(&c->k_full[j & 1], (j >> 1) & 1, p.err);
+    if (nv > 0) drain_wait(&c->v_full, (nv - 1) & 1, p.err);
+    for (uint32_t g = gq > C::NSQ ? gq - C::NSQ : 0; g < gq; ++g)
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->q_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
-  for (uint32_t g = gdo > C::NSQ ? gdo - C::NSQ : 0; g < gdo; ++g)
+      for (int s = 0; s < C::kSlabs; ++s)
+        drain_wait(&c->q_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+    for (uint32_t g = gdo > C::NSQ ? gdo - C::NSQ : 0; g < gdo; ++g)
 #pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+      for (int s = 0; s < C::kSlabs; ++s)
+        drain_wait(&c->do_full[g % C::NSQ][s], (g / C::NSQ) & 1, p.err);
+  }
   for (uint32_t g = gst > C::NSQ ? gst - C::NSQ : 0; g < gst; ++g)
     drain_wait(&c->stat_full[g % C::NSQ], (g / C::NSQ) & 1, p.err);
 }
 
-template <int D, bool LOCAL>
+template <int D, bool LOCAL, bool PAIR>
 __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
   // Run by the whole warp; the elected lane issues products and commits.
+  // PAIR: run by CTA 0 only; M = 256 covers both CTAs' key blocks.
   const uint32_t leader = elect_one();
-  const uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-  const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
+  constexpr int kM = PAIR ? 256 : 128;
+  const uint32_t id_st = idesc_bf16_f32(kM, 128, false, false);  // S^T, dP^T
+  const uint32_t id_kv = idesc_bf16_f32(kM, D, false, true);     // dV, dK (A in TMEM)
+  // Offsets in a query-tile stage: single CTA, 64-column slab k at 16 KB k;
+  // pair, the row half's slab k at 8 KB k and the column half at 16 KB.
+  constexpr uint32_t kSlabN = PAIR ? 8192 : 16384, kColsM = PAIR ? 16384 : 0;
+  auto ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    if (PAIR)
+      mma_ss_pair(d, a, b, id, acc);
+    else
+      mma_ss(d, a, b, id, acc);
+  };
+  auto ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    if (PAIR)
+      mma_ts_pair(d, a, b, id, acc);
+    else
+      mma_ts(d, a, b, id, acc);
+  };
+  auto commit = [&](uint64_t* bar) {
+    if (!leader) return;
+    if (PAIR)
+      mma_commit_pair(bar);
+    else
+      mma_commit(bar);
+  };
+  // Barriers the math warps arrive on (both CTAs' warps for a pair).
+  auto wait_math = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait_warp(bar, parity, &c->abort, p.err);
+  };
   // Descriptors built once; per tile and K step only adds remain.
   const uint64_t dk_k0 = smem_desc_sw128(smem_addr(smem + C::kK), 16, 1024);
   const uint64_t dv_k = smem_desc_sw128(smem_addr(smem + C::kV), 16, 1024);
@@ -409,8 +510,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
         if (!wait_slab(c->q_full, g, k / 4)) return false;
         tc_fence_after();
       }
-      const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      if (leader) mma_ss(tS, desc_add(dk_k, off), desc_add(dq_k, off), id_st, k > 0);
+      const uint32_t off_a = (k / 4) * 16384 + (k % 4) * 32;
+      const uint32_t off_b = (k / 4) * kSlabN + (k % 4) * 32;
+      if (leader) ss(tS, desc_add(dk_k, off_a), desc_add(dq_k, off_b), id_st, k > 0);
     }
     return true;
   };
@@ -422,8 +524,9 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
         if (!wait_slab(c->do_full, g, k / 4)) return false;
         tc_fence_after();
       }
-      const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-      if (leader) mma_ss(tDP, desc_add(dv_k, off), desc_add(ddo_k, off), id_st, k > 0);
+      const uint32_t off_a = (k / 4) * 16384 + (k % 4) * 32;
+      const uint32_t off_b = (k / 4) * kSlabN + (k % 4) * 32;
+      if (leader) ss(tDP, desc_add(dv_k, off_a), desc_add(ddo_k, off_b), id_st, k > 0);
     }
     return true;
   };
@@ -433,18 +536,18 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     const uint64_t ddo_m = desc_add(ddo_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBM / 16; ++k)
-      if (leader) mma_ts(tDV, tS + pack_col(k), desc_add(ddo_m, k * 2048), id_kv, acc || (k > 0));
+      if (leader) ts(tDV, tS + pack_col(k), desc_add(ddo_m, kColsM + k * 2048), id_kv, acc || (k > 0));
   };
   auto issue_dk = [&](uint32_t g, bool acc) {
     const uint64_t dq_m = desc_add(dq_m0, (g % C::NSQ) * C::kTile);
 #pragma unroll
     for (int k = 0; k < kBM / 16; ++k)
-      if (leader) mma_ts(tDK, tDP + pack_col(k), desc_add(dq_m, k * 2048), id_kv, acc || (k > 0));
+      if (leader) ts(tDK, tDP + pack_col(k), desc_add(dq_m, kColsM + k * 2048), id_kv, acc || (k > 0));
   };
   auto wait_q = [&](uint32_t g) { return wait_slab(c->q_full, g, 0); };
   auto wait_do = [&](uint32_t g) { return wait_slab(c->do_full, g, 0); };
-  auto wait_p = [&](uint32_t g) { return mbar_wait_warp(&c->p_full, g & 1, &c->abort, p.err); };
-  auto wait_ds = [&](uint32_t g) { return mbar_wait_warp(&c->ds_full, g & 1, &c->abort, p.err); };
+  auto wait_p = [&](uint32_t g) { return wait_math(&c->p_full, g & 1); };
+  auto wait_ds = [&](uint32_t g) { return wait_math(&c->ds_full, g & 1); };
   uint32_t it = 0, gq = 0;
   bool ok = true, issued = false;
   for (uint32_t n = 0; ok; ++n) {
@@ -458,18 +561,18 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
     tc_fence_after();
     issued = true;
     if (!issue_s(g0, dk_k)) break;
-    if (leader) mma_commit(&c->s_full);
+    commit(&c->s_full);
     // V is released after the item's last dP^T; K after the item epilogue,
     // which stages its stores in the K buffer.
     if (!mbar_wait_warp(&c->v_full, it & 1, &c->abort, p.err)) break;
     if (!wait_do(g0)) break;
     tc_fence_after();
     if (!issue_dp(g0)) break;
-    if (leader) mma_commit(&c->dp_full);
-    if (f.nt == 1 && leader) mma_commit(&c->v_empty);
+    commit(&c->dp_full);
+    if (f.nt == 1) commit(&c->v_empty);
     // dV(g0) restarts the accumulator the previous item's epilogue reads
     // (dK(g0) waits below for the dK one).
-    if (!mbar_wait_warp(&c->dv_empty, (it & 1) ^ 1, &c->abort, p.err)) break;
+    if (!wait_math(&c->dv_empty, (it & 1) ^ 1)) break;
     // Order per tile g: dV(g), S(g+1), dK(g), dP(g+1).  Every product is
     // committed whole, and the issuer waits only before a product that reads
     // what the math produced (P^T before dV, dS^T before dK) or for the query
@@ -483,40 +586,58 @@ __device__ void mma_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t t
       if (!wait_p(g)) { ok = false; break; }
       tc_fence_after();
       issue_dv(g, i > 0);
-      if (leader) mma_commit(&c->do_empty[g % C::NSQ]);
+      commit(&c->do_empty[g % C::NSQ]);
       if (more) {
         if (!wait_q(g + 1)) { ok = false; break; }
         tc_fence_after();
         if (!issue_s(g + 1, dk_k)) { ok = false; break; }
-        if (leader) mma_commit(&c->s_full);
+        commit(&c->s_full);
       }
       if (!wait_ds(g)) { ok = false; break; }
-      if (i == 0 && !mbar_wait_warp(&c->dk_empty, (it & 1) ^ 1, &c->abort, p.err)) { ok = false; break; }
+      if (i == 0 && !wait_math(&c->dk_empty, (it & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
       issue_dk(g, i > 0);
-      if (leader) mma_commit(&c->q_empty[g % C::NSQ]);
+      commit(&c->q_empty[g % C::NSQ]);
       if (more) {
         if (!wait_do(g + 1)) { ok = false; break; }
         tc_fence_after();
         if (!issue_dp(g + 1)) { ok = false; break; }
-        if (leader) mma_commit(&c->dp_full);
-        if (i + 2 == f.nt && leader) mma_commit(&c->v_empty);
+        commit(&c->dp_full);
+        if (i + 2 == f.nt) commit(&c->v_empty);
       }
     }
     if (!ok) break;
     gq += f.nt;
-    if (leader) mma_commit(&c->dkdv_full);
+    commit(&c->dkdv_full);
     ++it;
   }
   if (issued && leader) {
-    mma_commit(&c->drain);
+    commit(&c->drain);
     drain_wait(&c->drain, 0, p.err);
   }
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool PAIR>
 __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t tbase) {
   using C = KvCfg<D>;
+  // What the issuer waits for (P^T, dS^T, a freed accumulator): every
+  // thread arrives; in a pair one arrive per warp of either CTA on CTA 0's
+  // barrier, CTA 1's from across the pair (the warp's TMEM accesses are
+  // complete and fenced before it).
+  const bool remote = PAIR && cluster_rank() != 0;
+  auto to_issuer = [&](uint64_t* bar) {
+    if (!PAIR) {
+      mbar_arrive(bar);
+      return;
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+      if (remote)
+        mbar_arrive_remote(smem_in_cta(bar, 0));
+      else
+        mbar_arrive(bar);
+    }
+  };
   const int r = threadIdx.x & 127;    // TMEM lane = key row of the block
   const int qd = threadIdx.x >> 7;    // query columns [32*qd, 32*qd + 32)
   const int cbase = 32 * qd;
@@ -583,7 +704,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(&c->p_full);
+    to_issuer(&c->p_full);
     return true;
   };
   // ---- dS part of tile g: dS^T = P^T (dP^T - Delta): the difference in
@@ -613,7 +734,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(&c->ds_full);
+    to_issuer(&c->ds_full);
     // this warp's reads of the stage's statistics are done
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&c->stat_empty[g % C::NSQ]);
@@ -663,7 +784,7 @@ __device__ void math_role(const BwdParams& p, uint8_t* smem, KvCtl* c, uint32_t 
         w16[i2] = pack_bf16x2(__uint_as_float(a[2 * i2]) * mul, __uint_as_float(a[2 * i2 + 1]) * mul);
     }
     tc_fence_before();
-    mbar_arrive(which == 0 ? &c->dv_empty : &c->dk_empty);
+    to_issuer(which == 0 ? &c->dv_empty : &c->dk_empty);
     constexpr int kCpr = D / 8;       // 16-byte chunks per row
     constexpr int kRpi = 32 / kCpr;   // rows per warp store
     if (which == 1) {  // dV's rows have left the buffer
@@ -799,16 +920,20 @@ __device__ void store_role(const CUtensorMap* tdk, const CUtensorMap* tdv, uint8
   bulk_wait0();
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tq_h,
+                  const __grid_constant__ CUtensorMap tdo_h, const BwdParams p) {
   using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   KvCtl* c = reinterpret_cast<KvCtl*>(smem + C::kCtl);
   const int warp = warp_id(), lane = lane_id();
+  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
+  // Dynamic shared memory starts at the same offset in every CTA of the
+  // kernel, so both CTAs of a pair take this exit together.
   if ((smem_addr(smem) & 1023) != 0) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
     return;
@@ -832,15 +957,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c->stat_full[i], 1);
       mbar_init(&c->stat_empty[i], kMathWarps);  // after each math warp's dS part
       mbar_init(&c->item_full[i], 1);
-      mbar_init(&c->item_empty[i], kMathWarps + 1);  // math warps + the MMA warp
+      // math warps + the MMA warp (a pair's second CTA issues nothing)
+      mbar_init(&c->item_empty[i], kMathWarps + (rank == 0 ? 1 : 0));
     }
+    // Issued products: one commit arrives (on both CTAs of a pair).  Math
+    // results for the issuer: every math thread, or one arrive per warp of
+    // both CTAs of a pair.
+    constexpr uint32_t kToIssuer = PAIR ? 2 * kMathWarps : kMath;
     mbar_init(&c->s_full, 1);
     mbar_init(&c->dp_full, 1);
-    mbar_init(&c->p_full, kMath);
-    mbar_init(&c->ds_full, kMath);
+    mbar_init(&c->p_full, kToIssuer);
+    mbar_init(&c->ds_full, kToIssuer);
     mbar_init(&c->dkdv_full, 1);
-    mbar_init(&c->dv_empty, kMath);
-    mbar_init(&c->dk_empty, kMath);
+    mbar_init(&c->dv_empty, kToIssuer);
+    mbar_init(&c->dk_empty, kToIssuer);
     mbar_init(&c->epi, kMath);
     mbar_init(&c->stg_full[0], kMath);
     mbar_init(&c->stg_full[1], kMath);
@@ -856,46 +986,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tdo);
     tma_prefetch_desc(&tdk);
     tma_prefetch_desc(&tdv);
+    if (PAIR) {
+      tma_prefetch_desc(&tq_h);
+      tma_prefetch_desc(&tdo_h);
+    }
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&c->tmem_base, 512);
-    tmem_relinquish();
+  if (warp == kMmaWarp) {  // a pair: one warp of each CTA, together
+    if (PAIR) {
+      tmem_alloc_pair(&c->tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c->tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair: both CTAs' barriers exist before either signals the other's
+  if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = c->tmem_base;
   if (warp < kMathWarps) {
-    math_role<D, LOCAL, BCAST>(p, smem, c, tbase);
+    math_role<D, LOCAL, BCAST, PAIR>(p, smem, c, tbase);
   } else if (warp == kStoreWarp) {
     if (lane == 0) store_role<D>(&tdk, &tdv, smem, c, p.err);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, LOCAL, BCAST>(&tq, &tk, &tv, &tdo, p, smem, c);
-  } else {
-    mma_role<D, LOCAL>(p, smem, c, tbase);
+    if (lane == 0) producer_role<D, LOCAL, BCAST, PAIR>(&tq, &tk, &tv, &tdo, &tq_h, &tdo_h, p, smem, c);
+  } else if (!PAIR || rank == 0) {
+    mma_role<D, LOCAL, PAIR>(p, smem, c, tbase);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA leaves (or frees TMEM) while the other may still
+  // signal its barriers or read its operands
+  if (PAIR) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tbase, 512);
+    if (PAIR)
+      tmem_dealloc_pair(tbase, 512);
+    else
+      tmem_dealloc(tbase, 512);
   }
 }
 
-template <int D, bool LOCAL, bool BCAST>
+template <int D, bool LOCAL, bool BCAST, bool PAIR = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                     const BwdParams& p, int grid, cudaStream_t s) {
+                     const CUtensorMap& tq_h, const CUtensorMap& tdo_h, const BwdParams& p,
+                     int grid, cudaStream_t s) {
   using C = KvCfg<D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   static_assert(sizeof(KvCtl) <= 512, "control block");
   static_assert(!(LOCAL && BCAST), "causal masking is self-attention only");
-  auto kern = bwd_kv_kernel<D, LOCAL, BCAST>;
+  static_assert(!PAIR || (D == 128 && !LOCAL), "pairs: D = 128 without a local mask");
+  auto kern = bwd_kv_kernel<D, LOCAL, BCAST, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
-  return cudaGetLastError();
+  if (!PAIR) {
+    kern<<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, tq_h, tdo_h, p);
+    return cudaGetLastError();
+  }
+  // Clusters of two CTAs; as many pairs as can be resident at once (each
+  // walks the list in a fixed stride, so fewer resident pairs only cost time).
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int pairs = grid / 2;
+  cfg.gridDim = dim3(2 * pairs);
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0)
+    pairs = std::min(pairs, active);
+  else
+    (void)cudaGetLastError();
+  pairs = std::max(pairs, 1);
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdk, tdv, tq_h, tdo_h, p);
 }
 
 }  // namespace
@@ -903,16 +1077,23 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
-                          int grid, cudaStream_t s) {
+                          int grid, cudaStream_t s, const CUtensorMap* tq_h,
+                          const CUtensorMap* tdo_h) {
   if (bcast && causal) return cudaErrorInvalidValue;
-  if (D == 128) {
-    if (bcast) return launch_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-    if (causal) return launch_t<128, true, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-    return launch_t<128, false, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  if (tq_h != nullptr || tdo_h != nullptr) {  // pairs of CTAs
+    if (D != 128 || causal || tq_h == nullptr || tdo_h == nullptr) return cudaErrorInvalidValue;
+    if (bcast)
+      return launch_t<128, false, true, true>(tq, tk, tv, tdo, tdk, tdv, *tq_h, *tdo_h, p, grid, s);
+    return launch_t<128, false, false, true>(tq, tk, tv, tdo, tdk, tdv, *tq_h, *tdo_h, p, grid, s);
   }
-  if (bcast) return launch_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-  if (causal) return launch_t<64, true, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
-  return launch_t<64, false, false>(tq, tk, tv, tdo, tdk, tdv, p, grid, s);
+  if (D == 128) {
+    if (bcast) return launch_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
+    if (causal) return launch_t<128, true, false>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
+    return launch_t<128, false, false>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
+  }
+  if (bcast) return launch_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
+  if (causal) return launch_t<64, true, false>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
+  return launch_t<64, false, false>(tq, tk, tv, tdo, tdk, tdv, tq, tdo, p, grid, s);
 }
 
 }  // namespace jfa

@@ -142,6 +142,7 @@ struct SchedParams {
   const int32_t* blocks = nullptr;
   const int32_t* counts = nullptr;
   int nqb = 0, kcap = 0;
+  int kpair = 1;  // backward: key blocks per item (2: pairs of CTAs)
 };
 
 // Every parameter block below carries the GQA group G (query heads per K/V
@@ -265,10 +266,14 @@ cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, co
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t s,
                        bool sparse = false);
 // tdk / tdv: the dK / dV outputs as maps like the inputs' (TMA stores).
+// With tq_h and tdo_h (maps of Q and dO with 64-row boxes), the pair
+// variant: clusters of two CTAs over a list of key-block pairs (D = 128,
+// no local mask).
 cudaError_t launch_bwd_kv(int D, bool causal, bool bcast, const CUtensorMap& tq,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
-                          int grid, cudaStream_t s);
+                          int grid, cudaStream_t s, const CUtensorMap* tq_h = nullptr,
+                          const CUtensorMap* tdo_h = nullptr);
 // Broadcast-Q forward for a short dense Q (q_len <= 128), streamed over
 // key-tile chunks (fwd_bs.cu), and the merge of split sequences.
 bool fwd_bs_supported(int Lq);
