@@ -71,6 +71,7 @@ KERNEL_DESC = {
     "sparse_pool": "block-sparse selection: K-block and Q-block means",
     "sparse_select": "block-sparse selection: scores and top-k per Q block",
     "bwd_kv_pair": "backward dK/dV pass on CTA pairs (cta_group::2 products over two key blocks)",
+    "sparse_check": "block-sparse forward: check of every block list",
 }
 
 
@@ -108,6 +109,7 @@ def kernel_model(x):
     # block-sparse selection: K and Q read once (the means are small)
     m["sparse_pool"] = (0.0, T * rkv + T * row)
     m["sparse_select"] = (0.0, 0.0)
+    m["sparse_check"] = (0.0, 0.0)
     return m
 
 
@@ -140,7 +142,7 @@ KERNEL_SOURCES = {
     "fwd": ["fwd.cu"], "bwd_kv": ["bwd_kv.cu"], "bwd_q": ["bwd_q.cu"], "bwd_qb": ["bwd_qb.cu"],
     "prep": ["aux.cu"], "finalize": ["aux.cu"], "sched": ["aux.cu"], "bwd_bs": ["bwd_bs.cu"],
     "fwd_combine": ["fwd_bs.cu"], "sparse_pool": ["sparse.cu"], "sparse_select": ["sparse.cu"],
-    "bwd_kv_pair": ["bwd_kv.cu"],
+    "bwd_kv_pair": ["bwd_kv.cu"], "sparse_check": ["aux.cu"],
 }
 
 

@@ -275,7 +275,8 @@ typedef enum {
   JFA_KERNEL_SPARSE_POOL = 10,   /* block-sparse selection: K-block and Q-block means */
   JFA_KERNEL_SPARSE_SELECT = 11, /* block-sparse selection: scores, top-k */
   JFA_KERNEL_BWD_KV_PAIR = 12,   /* backward dK / dV pass on pairs of CTAs (JFA_KV_PAIR=1) */
-  JFA_KERNEL_KINDS = 13
+  JFA_KERNEL_SPARSE_CHECK = 13,  /* block-sparse forward: check of every block list */
+  JFA_KERNEL_KINDS = 14
 } jfa_kernel_kind;
 
 /* Kernels enqueued by this library since the process started (all threads,

@@ -207,7 +207,8 @@ def jfa_sync_and_check(stream=None):
 
 
 KERNEL_KINDS = ("sched", "fwd", "prep", "bwd_kv", "bwd_q", "bwd_qb", "finalize", "fill",
-                "bwd_bs", "fwd_combine", "sparse_pool", "sparse_select", "bwd_kv_pair")
+                "bwd_bs", "fwd_combine", "sparse_pool", "sparse_select", "bwd_kv_pair",
+                "sparse_check")
 
 
 def launch_count() -> int:

@@ -775,7 +775,7 @@ jfa_status jfa_block_select_ex(const void* q, const void* k, const int32_t* offs
   }
   const size_t kbar_bytes = align256((size_t)B * H_kv * kcap * D * sizeof(float));
   const size_t bytes =
-      kbar_bytes + align256((size_t)(s.broadcast ? 1 : B) * H * nqb * D * sizeof(float));
+      kbar_bytes + align256((size_t)(s.broadcast ? 1 : B) * H * 2 * nqb * D * sizeof(float));
   void* scratch = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, ds->pool, stream);
   if (e != cudaSuccess) return fail(JFA_ERR_WORKSPACE, "scratch allocation: %s", cudaGetErrorString(e));
@@ -798,7 +798,7 @@ jfa_status jfa_block_select_ex(const void* q, const void* k, const int32_t* offs
   sp.wl = s.kwl;
   sp.wr = s.kwr;
   sp.kbar = static_cast<float*>(scratch);
-  sp.qbar = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kbar_bytes);
+  sp.qsum = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kbar_bytes);
   sp.blocks = blocks;
   sp.counts = counts;
   sp.err = ds->err;
@@ -852,8 +852,16 @@ jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const 
   const long long cap = (long long)s.H * s.B * nqb;
   if (cap >= (1LL << 31) || (long long)s.B * s.H * nqb * kcap >= (1LL << 40))
     return fail(JFA_ERR_INVALID_ARG, "work list too large");
+  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.local, s.broadcast, 0, kFwdRows, nullptr,
+                 (int)cap, nullptr, ds->err, s.kwl, s.kwr};
+  sp.blocks = blocks;
+  sp.counts = counts;
+  sp.nqb = (int)nqb;
+  sp.kcap = (int)kcap;
+  sp.n_verdict = list_check_blocks(sp);
   const size_t items_off = 256;
-  const size_t bytes = align256(items_off + cap * sizeof(Item));
+  const size_t verdict_off = align256(items_off + cap * sizeof(Item));
+  const size_t bytes = align256(verdict_off + sp.n_verdict * sizeof(int));
   CUtensorMap tq, tk, tv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
   if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
@@ -864,14 +872,14 @@ jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const 
   uint8_t* base = static_cast<uint8_t*>(scratch);
   WorkHeader* hdr = reinterpret_cast<WorkHeader*>(base);
   Item* items = reinterpret_cast<Item*>(base + items_off);
-  // The scheduler also checks every list before the forward follows it.
-  SchedParams sp{offsets, s.B, s.H, s.Lq, s.max_len, s.local, s.broadcast, 0, kFwdRows, items,
-                 (int)cap, hdr, ds->err, s.kwl, s.kwr};
-  sp.blocks = blocks;
-  sp.counts = counts;
-  sp.nqb = (int)nqb;
-  sp.kcap = (int)kcap;
-  e = run_kernel(JFA_KERNEL_SCHED, stream, [&] { return launch_sched(sp, stream); });
+  sp.items = items;
+  sp.hdr = hdr;
+  sp.verdict = reinterpret_cast<int*>(base + verdict_off);
+  // Every list is checked (many CTAs) before the scheduler reads the
+  // verdicts; a bad list leaves the work list empty, so nothing is written.
+  e = run_kernel(JFA_KERNEL_SPARSE_CHECK, stream, [&] { return launch_list_check(sp, stream); });
+  if (e == cudaSuccess)
+    e = run_kernel(JFA_KERNEL_SCHED, stream, [&] { return launch_sched(sp, stream); });
   if (e == cudaSuccess) {
     FwdParams fp;
     memset(&fp, 0, sizeof(fp));

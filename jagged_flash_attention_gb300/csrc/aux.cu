@@ -130,28 +130,11 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       if (lane == __ffs(peers) - 1) atomicAdd(&hist[key], tot);
     }
   }
-  // Block lists of the sparse forward: per (sequence, head, 256-row query
-  // block) a count of at most the sequence's key tiles and strictly
-  // ascending key tiles below it.
+  // Block lists of the sparse forward: the verdicts list_check_kernel wrote
+  // just before (anything but 1, even a slot never written, is a bad list).
   if (p.blocks != nullptr) {
-    const long long n_lists = static_cast<long long>(p.B) * p.H * p.nqb;
-    for (long long r = tid; r < n_lists; r += blockDim.x) {
-      const int i = static_cast<int>(r % p.nqb);
-      const int b = static_cast<int>(r / p.nqb / p.H);
-      const int L = p.offsets[b + 1] - p.offsets[b];
-      // Q blocks of the sequence (broadcast: of the dense Q, for every sequence)
-      if (L < 0 || L > p.max_len || i * kFwdRows >= (p.broadcast ? p.Lq : L)) continue;
-      const int nk = cdiv(L, kBN);
-      const int c = p.counts[r];
-      bool ok = c >= 0 && c <= nk;
-      const int32_t* lst = p.blocks + r * p.kcap;
-      for (int e = 0, prev = -1; ok && e < c; ++e) {
-        const int v = lst[e];
-        ok = v > prev && v < nk;
-        prev = v;
-      }
-      if (!ok) sm.badblk = 1;
-    }
+    for (int v = tid; v < p.n_verdict; v += blockDim.x)
+      if (p.verdict[v] != 1) sm.badblk = 1;
   }
   __syncthreads();
   if (s_bad || sm.badblk) {
@@ -246,6 +229,52 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
     p.hdr->ticket = 0;
     p.hdr->valid = 1;
   }
+}
+
+// List r of the sparse forward (sequence b, head, 256-row query block i): a
+// count of at most the sequence's key tiles and strictly ascending key tiles
+// below it.  Lists of query blocks past the sequence (broadcast: of every
+// sequence, the dense Q's blocks) are not read, nor those of sequences with
+// bad offsets (which the scheduler itself rejects).
+__device__ bool list_ok(const SchedParams& p, long long r) {
+  const int i = static_cast<int>(r % p.nqb);
+  const int b = static_cast<int>(r / p.nqb / p.H);
+  const int L = p.offsets[b + 1] - p.offsets[b];
+  if (L < 0 || L > p.max_len || i * kFwdRows >= (p.broadcast ? p.Lq : L)) return true;
+  const int nk = cdiv(L, kBN);
+  const int c = p.counts[r];
+  bool ok = c >= 0 && c <= nk;
+  const int32_t* lst = p.blocks + r * p.kcap;
+  const int n = ok ? c : 0;
+  // entries in groups of 8 loaded together (no exit between them, so the
+  // loads of a group are in flight at once)
+  int prev = -1;
+  for (int e0 = 0; e0 < n; e0 += 8) {
+    int v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = e0 + q < n ? lst[e0 + q] : nk + 1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (e0 + q < n) {
+        ok = ok && v[q] > prev && v[q] < nk;
+        prev = v[q];
+      }
+    }
+  }
+  return ok;
+}
+
+// Checks every list of the sparse forward, a thread per list; block x
+// writes verdict[x] = 1 when all its lists are valid, 2 otherwise.
+constexpr int kCheckThreads = 256;
+__global__ void __launch_bounds__(kCheckThreads) list_check_kernel(SchedParams p) {
+  const long long n_lists = static_cast<long long>(p.B) * p.H * p.nqb;
+  bool bad = false;
+  for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < n_lists;
+       r += static_cast<long long>(gridDim.x) * blockDim.x)
+    bad = bad || !list_ok(p, r);
+  bad = __syncthreads_or(bad ? 1 : 0) != 0;
+  if (threadIdx.x == 0) p.verdict[blockIdx.x] = bad ? 2 : 1;
 }
 
 struct QbSmem {
@@ -615,6 +644,16 @@ __global__ void fill_empty_kernel(__nv_bfloat16* out, float* lse, long long rows
 }
 
 }  // namespace
+
+int list_check_blocks(const SchedParams& p) {
+  const long long lists = static_cast<long long>(p.B) * p.H * p.nqb;
+  return static_cast<int>(std::max(1LL, std::min(1024LL, (lists + kCheckThreads - 1) / kCheckThreads)));
+}
+
+cudaError_t launch_list_check(const SchedParams& p, cudaStream_t s) {
+  list_check_kernel<<<p.n_verdict, kCheckThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s) {
   sched_kernel<<<1, kSchedThreads, 0, s>>>(p);

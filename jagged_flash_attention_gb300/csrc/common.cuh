@@ -142,6 +142,9 @@ struct SchedParams {
   const int32_t* blocks = nullptr;
   const int32_t* counts = nullptr;
   int nqb = 0, kcap = 0;
+  // their check, by list_check_kernel: one verdict per block (1: valid)
+  int* verdict = nullptr;
+  int n_verdict = 0;
   int kpair = 1;  // backward: key blocks per item (2: pairs of CTAs)
 };
 
@@ -252,7 +255,7 @@ struct SparseParams {
   int nqb, kcap;  // ceil(max_len / 256) (broadcast: ceil(Lq / 256)), ceil(max_len / 128)
   int wl, wr;     // local mask [i - wl, i + wr] (kNoWindow: unbounded side)
   float* kbar;     // scratch fp32 [B][Hkv][kcap][D]: K-block means
-  float* qbar;     // scratch fp32 [B][H][nqb][D]: Q-block means (broadcast: [1][H][nqb][D])
+  float* qsum;     // scratch fp32 [B][H][2 nqb][D]: sums of 128-row Q halves (broadcast: [1][H][2 nqb][D])
   int32_t* blocks;
   int32_t* counts;
   int* err;
@@ -260,6 +263,10 @@ struct SparseParams {
 
 // Host-side launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
+// Block lists of the sparse forward, checked before the scheduler reads the
+// verdicts: list_check_blocks(p) verdict slots (p.n_verdict of them).
+int list_check_blocks(const SchedParams& p);
+cudaError_t launch_list_check(const SchedParams& p, cudaStream_t s);
 // causal: any local mask (the kernels read wl, wr from the parameters).
 // sparse: the block-sparse forward (self-attention, no mask; p.blocks).
 cudaError_t launch_fwd(int D, bool causal, bool bcast, const CUtensorMap& tq, const CUtensorMap& tk,
