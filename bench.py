@@ -293,7 +293,13 @@ def _l2_note(x):
 
 
 def _workload_def(wname):
-    return W.WORKLOADS[wname] if wname in W.WORKLOADS else W.variant(wname)
+    if wname in W.WORKLOADS:
+        return W.WORKLOADS[wname]
+    if wname in PAIR_VARIANTS:  # the base workload; only the dK/dV pass differs
+        return W.WORKLOADS[PAIR_VARIANTS[wname]]
+    if wname in SPARSE_VARIANTS:
+        return W.WORKLOADS[SPARSE_VARIANTS[wname]]
+    return W.variant(wname)
 
 
 def _config(x, wname, ws=1):

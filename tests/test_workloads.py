@@ -64,3 +64,14 @@ def test_sparse_pair_count_by_enumeration():
                               and (wl is None or c >= r - wl) and (wr is None or c <= r + wr))
                         want += ok
         assert bench._sparse_pairs(lengths, 2, bl, ct, causal, window) == want
+
+
+def test_every_bench_variant_resolves_to_a_workload():
+    """Every name the bench line reports under `variants` maps to a workload
+    definition (the GQA / window variants, the block-sparse and the CTA-pair
+    ones)."""
+    import bench
+    names = list(W.VARIANTS) + list(bench.SPARSE_VARIANTS) + list(bench.PAIR_VARIANTS)
+    for n in names:
+        w = bench._workload_def(n)
+        assert w.name in W.WORKLOADS, n
