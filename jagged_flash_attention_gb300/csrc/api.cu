@@ -858,10 +858,10 @@ jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const 
   sp.counts = counts;
   sp.nqb = (int)nqb;
   sp.kcap = (int)kcap;
-  sp.n_verdict = list_check_blocks(sp);
+  sp.n_check = list_check_blocks(sp);
   const size_t items_off = 256;
-  const size_t verdict_off = align256(items_off + cap * sizeof(Item));
-  const size_t bytes = align256(verdict_off + sp.n_verdict * sizeof(int));
+  const size_t check_off = align256(items_off + cap * sizeof(Item));
+  const size_t bytes = align256(check_off + sp.n_check * sizeof(int));
   CUtensorMap tq, tk, tv;
   if ((st = map_rows(&tq, q, s.D, s.H, s.broadcast ? s.Lq : s.Tcap, "q")) != JFA_OK) return st;
   if ((st = map_rows(&tk, k, s.D, s.Hkv, s.Tcap, "k")) != JFA_OK) return st;
@@ -874,9 +874,9 @@ jfa_status jfa_fwd_sparse_ex(const void* q, const void* k, const void* v, const 
   Item* items = reinterpret_cast<Item*>(base + items_off);
   sp.items = items;
   sp.hdr = hdr;
-  sp.verdict = reinterpret_cast<int*>(base + verdict_off);
+  sp.check = reinterpret_cast<int*>(base + check_off);
   // Every list is checked (many CTAs) before the scheduler reads the
-  // verdicts; a bad list leaves the work list empty, so nothing is written.
+  // results; a bad list leaves the work list empty, so nothing is written.
   e = run_kernel(JFA_KERNEL_SPARSE_CHECK, stream, [&] { return launch_list_check(sp, stream); });
   if (e == cudaSuccess)
     e = run_kernel(JFA_KERNEL_SCHED, stream, [&] { return launch_sched(sp, stream); });

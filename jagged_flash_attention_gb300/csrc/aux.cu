@@ -130,11 +130,11 @@ __device__ void sched_body(const SchedParams& p, SchedSmem& sm) {
       if (lane == __ffs(peers) - 1) atomicAdd(&hist[key], tot);
     }
   }
-  // Block lists of the sparse forward: the verdicts list_check_kernel wrote
+  // Block lists of the sparse forward: the results list_check_kernel wrote
   // just before (anything but 1, even a slot never written, is a bad list).
   if (p.blocks != nullptr) {
-    for (int v = tid; v < p.n_verdict; v += blockDim.x)
-      if (p.verdict[v] != 1) sm.badblk = 1;
+    for (int v = tid; v < p.n_check; v += blockDim.x)
+      if (p.check[v] != 1) sm.badblk = 1;
   }
   __syncthreads();
   if (s_bad || sm.badblk) {
@@ -265,7 +265,7 @@ __device__ bool list_ok(const SchedParams& p, long long r) {
 }
 
 // Checks every list of the sparse forward, a thread per list; block x
-// writes verdict[x] = 1 when all its lists are valid, 2 otherwise.
+// writes check[x] = 1 when all its lists are valid, 2 otherwise.
 constexpr int kCheckThreads = 256;
 __global__ void __launch_bounds__(kCheckThreads) list_check_kernel(SchedParams p) {
   const long long n_lists = static_cast<long long>(p.B) * p.H * p.nqb;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kCheckThreads) list_check_kernel(SchedParams p
        r += static_cast<long long>(gridDim.x) * blockDim.x)
     bad = bad || !list_ok(p, r);
   bad = __syncthreads_or(bad ? 1 : 0) != 0;
-  if (threadIdx.x == 0) p.verdict[blockIdx.x] = bad ? 2 : 1;
+  if (threadIdx.x == 0) p.check[blockIdx.x] = bad ? 2 : 1;
 }
 
 struct QbSmem {
@@ -651,7 +651,7 @@ int list_check_blocks(const SchedParams& p) {
 }
 
 cudaError_t launch_list_check(const SchedParams& p, cudaStream_t s) {
-  list_check_kernel<<<p.n_verdict, kCheckThreads, 0, s>>>(p);
+  list_check_kernel<<<p.n_check, kCheckThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -142,9 +142,9 @@ struct SchedParams {
   const int32_t* blocks = nullptr;
   const int32_t* counts = nullptr;
   int nqb = 0, kcap = 0;
-  // their check, by list_check_kernel: one verdict per block (1: valid)
-  int* verdict = nullptr;
-  int n_verdict = 0;
+  // their check, by list_check_kernel: one result per block (1: valid)
+  int* check = nullptr;
+  int n_check = 0;
   int kpair = 1;  // backward: key blocks per item (2: pairs of CTAs)
 };
 
@@ -264,7 +264,7 @@ struct SparseParams {
 // Host-side launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t s);
 // Block lists of the sparse forward, checked before the scheduler reads the
-// verdicts: list_check_blocks(p) verdict slots (p.n_verdict of them).
+// results: list_check_blocks(p) result slots (p.n_check of them).
 int list_check_blocks(const SchedParams& p);
 cudaError_t launch_list_check(const SchedParams& p, cudaStream_t s);
 // causal: any local mask (the kernels read wl, wr from the parameters).
