@@ -11,6 +11,7 @@ every dK / dV element from the same bf16 operands in the same K order."""
 import numpy as np
 import pytest
 
+import jfa_workloads as W
 from tests.gpu_common import compare, inputs, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -59,3 +60,15 @@ def test_pair_backward_parity(case, monkeypatch):
         scale = float(np.abs(b[fin]).max()) if fin.any() else 1.0
         print(f"  {n}: pair vs single max abs {err:.3g} (of {scale:.3g})")
         assert err <= 1e-2 * max(scale, 1e-6), n
+
+
+@pytest.mark.parametrize("name", ["jagged_self", "broadcast_q"])
+def test_pair_full_size_equals_single(name, monkeypatch):
+    """Full workload sizes, in the launch configuration the benchmark times
+    (its `*_kv_pair` variants): the pair pass's dK and dV equal the
+    single-CTA pass's bit for bit, and the kernel that ran is the pair one."""
+    x = W.make_inputs(W.WORKLOADS[name])
+    g = _run(x, True, monkeypatch)
+    single = _run(x, False, monkeypatch)
+    for n in ("dk", "dv"):
+        assert np.array_equal(g[n], single[n]), n

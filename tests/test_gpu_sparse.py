@@ -348,3 +348,67 @@ def test_local_full_selection_equals_dense_local():
     q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
     out, lse = orc.forward(q, k, v, x["offsets"], x["scale"], True, window=(300, None))
     compare(g, {"out": out, "lse": lse}, ("out", "lse"))
+
+
+# ------------------------------------------------------------- full size
+
+@pytest.mark.parametrize("name", ["jagged_self", "causal_self"])
+def test_sparse_full_size_sampled(name):
+    """Full workload sizes at 500 permille, in the launch configuration the
+    benchmark times (jagged_self_block_sparse500, causal_self_block_sparse500;
+    causal_self with its causal mask): the GPU's lists and forward on every
+    sequence, the oracle on sampled sequences and heads, following the GPU's
+    lists (the forward) and its own (the selection, compared where the
+    oracle's scores separate the boundary, valid everywhere)."""
+    import jagged_flash_attention_gb300 as jfa
+    x = W.make_inputs(W.WORKLOADS[name])
+    causal = bool(x["causal"])
+    (q, k, v), off = _dev(x)
+    blocks, counts = jfa.block_select(q, k, off, x["max_len"], 500, causal=causal)
+    out, lse = jfa.forward_sparse(q, k, v, off, x["max_len"], blocks, counts, scale=x["scale"],
+                                  causal=causal)
+    jfa.jfa_sync_and_check()
+    gb, gc = blocks.cpu().numpy(), counts.cpu().numpy()
+    g_out, g_lse = f64(out), f64(lse)
+    rng = np.random.default_rng(17)
+    L = x["lengths"]
+    order = np.argsort(L)
+    seqs = sorted({int(order[-1]), int(order[len(L) // 2]), int(rng.integers(0, len(L)))})
+    heads = sorted({0, x["H"] - 1})
+    offs = x["offsets"]
+    exact = 0
+    for b in seqs:
+        s0, s1 = int(offs[b]), int(offs[b + 1])
+        sub_off = np.array([0, s1 - s0], dtype=np.int64)
+        for h in heads:
+            hk = h // (x["H"] // x["Hkv"])
+            qs = f64(x["q"][s0:s1, h:h + 1])
+            ks = f64(x["k"][s0:s1, hk:hk + 1])
+            vs = f64(x["v"][s0:s1, hk:hk + 1])
+            bl = gb[b:b + 1, h:h + 1]
+            ct = gc[b:b + 1, h:h + 1]
+            r_out, r_lse = orc.forward_sparse(qs, ks, vs, sub_off, x["scale"], bl, ct, causal=causal)
+            got = {"out": g_out[s0:s1, h:h + 1], "lse": g_lse[h:h + 1, s0:s1]}
+            compare(got, {"out": r_out, "lse": r_lse}, ("out", "lse"))
+            rb, rc, rs = orc.block_select(qs, ks, sub_off, 500, causal=causal)
+            cb, cc, _ = orc.block_select(qs, ks, sub_off, 1000, causal=causal)
+            nq = rc.shape[2]  # the sequence's Q blocks; the GPU's lists past them are empty
+            np.testing.assert_array_equal(ct[:, :, :nq], rc)
+            assert not ct[:, :, nq:].any()
+            for i in range(nq):
+                c = int(ct[0, 0, i])
+                if c == 0:
+                    continue
+                sel = bl[0, 0, i, :c]
+                cand = cb[0, 0, i, :int(cc[0, 0, i])]
+                assert np.all(np.diff(sel) > 0) and np.isin(sel, cand).all()
+                sc = rs[0, 0, i]
+                unsel = np.setdiff1d(cand, sel)
+                if unsel.size:
+                    assert sc[unsel].max() <= sc[sel].min() + GAP
+                srt = np.sort(sc[cand])[::-1]
+                if c == cand.size or srt[c - 1] - srt[c] > GAP:
+                    np.testing.assert_array_equal(sel, rb[0, 0, i, :c])
+                    exact += 1
+    assert exact > 0
+    print(name, seqs, heads, "exact lists:", exact)
