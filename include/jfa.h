@@ -47,6 +47,13 @@
  *   every call synchronises and checks before returning.
  * - Thread safety: calls on different streams may run concurrently, except
  *   jfa_fwd_bq_noalloc, whose calls all share one scratch array (see there).
+ * - With the environment variable JFA_KV_PAIR=1 (read on every call) the
+ *   backward runs its dK/dV pass on CTA pairs ("Optimizing Jagged Flash
+ *   Attention with TLX", "2-CTA collaborative MMA (backward)": clusters of
+ *   two CTAs whose cta_group::2 products cover two adjacent key blocks)
+ *   where that variant exists (D = 128, no causal mask or window; for
+ *   broadcast-Q, the two-pass backward).  Results are bit-identical to the
+ *   default single-CTA pass.
  */
 #ifndef JFA_H_
 #define JFA_H_
