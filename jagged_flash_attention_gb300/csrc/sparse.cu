@@ -32,7 +32,6 @@
 namespace jfa {
 namespace {
 
-constexpr int kPoolThreads = 256;
 constexpr int kPoolBatch = 8;  // row loads a pooling thread issues before adding them
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -55,9 +54,10 @@ __device__ __forceinline__ bool seq_ok(const SparseParams& p, int off0, int L, b
 // [T, Hx, D] tensor: out[h * out_stride + d].  A row of all heads (Hx * D
 // bf16, contiguous) is read as 16-byte chunks: with fewer chunks than
 // threads, thread t takes chunk t % cpr of rows t / cpr, + groups, ... and
-// the row groups are added in shared memory (at most kPoolThreads * 8
-// floats); otherwise every thread owns whole chunks.  A thread issues
-// kPoolBatch row loads before it adds them.
+// the row groups are added in shared memory (at most NT * 8 floats);
+// otherwise every thread owns whole chunks.  A thread issues kPoolBatch row
+// loads before it adds them.
+template <int NT>
 __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0, int n,
                           float scale, float* out, long long out_stride, float* part) {
   const int W = Hx * D;     // elements per row
@@ -87,8 +87,8 @@ __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0,
       for (int q = 0; q < kPoolBatch; ++q) add(acc, u[q]);
     }
   };
-  if (cpr >= kPoolThreads) {
-    for (int c = t; c < cpr; c += kPoolThreads) {
+  if (cpr >= NT) {
+    for (int c = t; c < cpr; c += NT) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       sum_rows(acc, c, 0, 1);
 #pragma unroll
@@ -99,7 +99,7 @@ __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0,
     }
     return;
   }
-  const int groups = kPoolThreads / cpr, c = t % cpr, g = t / cpr;
+  const int groups = NT / cpr, c = t % cpr, g = t / cpr;
   if (g < groups) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     sum_rows(acc, c, g, groups);
@@ -107,7 +107,7 @@ __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0,
     for (int k = 0; k < 8; ++k) part[g * W + c * 8 + k] = acc[k];
   }
   __syncthreads();
-  for (int col = t; col < W; col += kPoolThreads) {
+  for (int col = t; col < W; col += NT) {
     float s = 0.f;
     for (int q = 0; q < groups; ++q) s += part[q * W + col];
     out[(col / D) * out_stride + col % D] = s * scale;
@@ -119,8 +119,12 @@ __device__ void pool_rows(const __nv_bfloat16* x, int Hx, int D, long long row0,
 // [128 j, 128 j + 128) of the sequence, their sum for every query head into
 // qsum [B][H][2 nqb][D] (broadcast-Q: rows of the dense Q, once, by the CTAs
 // of sequence 0, into qsum [H][2 nqb][D]).
-__global__ void __launch_bounds__(kPoolThreads) sparse_pool_kernel(SparseParams p) {
-  __shared__ float part[kPoolThreads * 8];
+// NT threads: 512 for rows of at most 1024 elements (each thread then adds
+// 32 rows of a unit), 256 for wider rows (measured: 66 -> 59 us on H D = 1024;
+// 204 -> 223 us on H D = 2048 with 512).
+template <int NT>
+__global__ void __launch_bounds__(NT) sparse_pool_kernel(SparseParams p) {
+  __shared__ float part[NT * 8];
   const int j = blockIdx.x, b = blockIdx.y;
   const int off0 = p.offsets[b];
   const int L = p.offsets[b + 1] - off0;
@@ -130,16 +134,16 @@ __global__ void __launch_bounds__(kPoolThreads) sparse_pool_kernel(SparseParams 
   if (blockIdx.z == 0) {
     if (j >= p.kcap || r0 >= L) return;
     const int n = min(kUnit, L - r0);
-    pool_rows(p.k, p.Hkv, p.D, off0 + r0, n, 1.f / n,
+    pool_rows<NT>(p.k, p.Hkv, p.D, off0 + r0, n, 1.f / n,
               p.kbar + (static_cast<long long>(b) * p.Hkv * p.kcap + j) * p.D,
               static_cast<long long>(p.kcap) * p.D, part);
   } else if (p.broadcast) {
     if (b != 0 || j >= nh || r0 >= p.Lq) return;
-    pool_rows(p.q, p.H, p.D, r0, min(kUnit, p.Lq - r0), 1.f,
+    pool_rows<NT>(p.q, p.H, p.D, r0, min(kUnit, p.Lq - r0), 1.f,
               p.qsum + static_cast<long long>(j) * p.D, static_cast<long long>(nh) * p.D, part);
   } else {
     if (j >= nh || r0 >= L) return;
-    pool_rows(p.q, p.H, p.D, off0 + r0, min(kUnit, L - r0), 1.f,
+    pool_rows<NT>(p.q, p.H, p.D, off0 + r0, min(kUnit, L - r0), 1.f,
               p.qsum + (static_cast<long long>(b) * p.H * nh + j) * p.D,
               static_cast<long long>(nh) * p.D, part);
   }
@@ -347,7 +351,11 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseParams
 }  // namespace
 
 cudaError_t launch_sparse_pool(const SparseParams& p, cudaStream_t s) {
-  sparse_pool_kernel<<<dim3(max(p.kcap, 2 * p.nqb), p.B, 2), kPoolThreads, 0, s>>>(p);
+  const dim3 grid(max(p.kcap, 2 * p.nqb), p.B, 2);
+  if (p.H * p.D <= 1024)
+    sparse_pool_kernel<512><<<grid, 512, 0, s>>>(p);
+  else
+    sparse_pool_kernel<256><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
