@@ -32,7 +32,7 @@
  * - causal (self-attention only): query i attends to key j iff j <= i, both
  *   counted from the start of their own sequence.
  * - scale: positive finite softmax scale (normally 1/sqrt(D)).
- * - D must be 64 or 128.
+ * - D must be 64 or 128; 1 <= H <= 32767.
  * - Inputs must be finite.  Rows of neighbouring sequences are read into a
  *   tile's padding and then multiplied by an exact zero, so a non-finite
  *   value in one sequence can leak into its neighbours.

@@ -24,6 +24,9 @@ __device__ int g_device_error;
 
 namespace {
 
+// Largest head count: work items hold (head << 16) | tile in an int32.
+constexpr int kMaxHeads = 32767;
+
 using namespace jfa;
 
 thread_local std::string t_last_error;
@@ -202,7 +205,9 @@ void set_variant(P& p, const Shape& s) {
 jfa_status check_common(const Shape& s, const void* q, const void* k, const void* v,
                         const int32_t* offsets) {
   if (s.B < 1) return fail(JFA_ERR_INVALID_ARG, "B must be >= 1 (got %d)", s.B);
-  if (s.H < 1 || s.H > 65535) return fail(JFA_ERR_INVALID_ARG, "H must be in [1, 65535] (got %d)", s.H);
+  // Work items carry the head in bits 16-30 of a signed 32-bit word.
+  if (s.H < 1 || s.H > kMaxHeads)
+    return fail(JFA_ERR_INVALID_ARG, "H must be in [1, %d] (got %d)", kMaxHeads, s.H);
   if (s.D != 64 && s.D != 128) return fail(JFA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", s.D);
   if (s.max_len < 0) return fail(JFA_ERR_INVALID_ARG, "max_len must be >= 0");
   if (cdivll(s.max_len, kBN) > 65535 || cdivll(s.Lq, kBM) > 65535)
@@ -912,8 +917,9 @@ jfa_status jfa_worklist(const int32_t* offsets, int B, int H, int max_len, int q
                         int broadcast_q, int causal, int list, int32_t* items, int capacity,
                         int32_t* count, cudaStream_t stream) {
   t_last_error.clear();
-  if (B < 1 || H < 1 || H > 65535 || max_len < 0 || capacity < 0)
-    return fail(JFA_ERR_INVALID_ARG, "worklist: B, H >= 1, max_len, capacity >= 0");
+  if (B < 1 || H < 1 || H > kMaxHeads || max_len < 0 || capacity < 0)
+    return fail(JFA_ERR_INVALID_ARG, "worklist: B >= 1, 1 <= H <= %d, max_len, capacity >= 0",
+                kMaxHeads);
   if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 3u) || !count ||
       (reinterpret_cast<uintptr_t>(count) & 3u) || (capacity > 0 && !aligned16(items)))
     return fail(JFA_ERR_INVALID_ARG, "worklist: offsets, count 4-byte and items 16-byte aligned");

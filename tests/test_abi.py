@@ -47,6 +47,8 @@ def _fwd(L, **kw):
     (dict(bq=1), 1, "jfa_fwd_bq"),
     (dict(B=0), 1, "B must be"),
     (dict(H=0), 1, "H must be"),
+    # work items hold the head in bits 16-30 of an int32
+    (dict(H=32768), 1, "H must be in [1, 32767]"),
     (dict(scale=float("nan")), 1, "scale"),
     (dict(scale=-1.0), 1, "scale"),
     (dict(q=0), 1, "non-null"),
@@ -127,6 +129,8 @@ def test_worklist_argument_errors(L):
     assert fn(16, 4, 2, 100, 64, 1, 1, 1, 16, 100, 16, 0) == 1
     assert fn(16, 4, 2, 100, 0, 0, 0, 0, 8, 100, 16, 0) == 1  # items not 16-byte aligned
     assert b"16-byte" in L.jfa_last_error()
+    assert fn(16, 4, 32768, 100, 0, 0, 0, 0, 16, 100, 16, 0) == 1  # head beyond the item encoding
+    assert b"32767" in L.jfa_last_error()
 
 
 def _fwd_ex(L, **kw):
