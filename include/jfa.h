@@ -296,6 +296,12 @@ long long jfa_launch_count(void);
  * Always returns JFA_OK. */
 jfa_status jfa_profile_enable(int on);
 
+/* Kernel kinds that profiling brackets: bit k of `kinds` selects kind k
+ * (1u << JFA_KERNEL_BWD_KV: the dK/dV pass alone); other launches are
+ * counted by jfa_launch_count but get no events.  Default: every kind
+ * (~0u).  Process-wide; read at each launch.  Always returns JFA_OK. */
+jfa_status jfa_profile_select(unsigned int kinds);
+
 /* Waits for every event pair recorded so far, writes per kernel kind the
  * summed device time in milliseconds (ms[kind]) and the number of launches
  * (launches[kind]) for kinds < n, and releases the records.  ms and

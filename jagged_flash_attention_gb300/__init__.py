@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.jfa_profile_enable.restype = _I
         L.jfa_profile_read.argtypes = [_P, _P, _I]
         L.jfa_profile_read.restype = _I
+        L.jfa_profile_select.argtypes = [ctypes.c_uint]
+        L.jfa_profile_select.restype = _I
         L.jfa_version.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -218,6 +220,13 @@ def launch_count() -> int:
 
 def profile_enable(on: bool):
     _check(lib().jfa_profile_enable(1 if on else 0))
+
+
+def profile_select(kinds=None):
+    """Kernel kinds profiling brackets with events (names of KERNEL_KINDS;
+    None: every kind)."""
+    mask = 0xFFFFFFFF if kinds is None else sum(1 << KERNEL_KINDS.index(k) for k in kinds)
+    _check(lib().jfa_profile_select(mask))
 
 
 def profile_read():

@@ -36,6 +36,7 @@ thread_local std::string t_last_error;
 // the launch's own stream (read back by jfa_profile_read).
 std::atomic<long long> g_launch_count{0};
 std::atomic<int> g_profile_on{0};
+std::atomic<unsigned> g_profile_kinds{~0u};  // bit k: record kind k
 struct ProfRecord {
   int kind;
   cudaEvent_t start, stop;
@@ -47,6 +48,7 @@ template <class F>
 cudaError_t run_kernel(jfa_kernel_kind kind, cudaStream_t stream, F&& launch) {
   cudaEvent_t a = nullptr, b = nullptr;
   const bool prof = g_profile_on.load(std::memory_order_relaxed) != 0 &&
+                    ((g_profile_kinds.load(std::memory_order_relaxed) >> kind) & 1u) != 0 &&
                     cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess;
   if (prof) cudaEventRecord(a, stream);
   const cudaError_t e = launch();
@@ -982,6 +984,11 @@ long long jfa_launch_count(void) { return g_launch_count.load(std::memory_order_
 
 jfa_status jfa_profile_enable(int on) {
   g_profile_on.store(on ? 1 : 0, std::memory_order_relaxed);
+  return JFA_OK;
+}
+
+jfa_status jfa_profile_select(unsigned int kinds) {
+  g_profile_kinds.store(kinds, std::memory_order_relaxed);
   return JFA_OK;
 }
 

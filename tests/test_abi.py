@@ -112,6 +112,10 @@ def test_launch_count_without_launches():
     prof = jfa.profile_read()
     assert set(prof) == set(jfa.KERNEL_KINDS)
     assert jfa.launch_count() == n0
+    jfa.profile_select(["bwd_kv", "fwd"])
+    jfa.profile_select(None)
+    with pytest.raises(ValueError):
+        jfa.profile_select(["no_such_kernel"])
 
 
 def test_worklist_argument_errors(L):

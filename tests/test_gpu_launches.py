@@ -32,8 +32,24 @@ def test_self_attention_launches_and_kernel_times():
     prof = jfa.profile_read()
     counts = {k: n for k, (t, n) in prof.items() if n}
     assert counts == {"sched": 1, "fwd": 1, "prep": 1, "bwd_kv": 1, "bwd_q": 1}
-    for k in counts:
-        assert prof[k][0] > 0.0, k
+    for kind in counts:
+        assert prof[kind][0] > 0.0, kind
+    # With a kind selection only the selected launches get events; every
+    # launch is still counted.
+    n0 = jfa.launch_count()
+    jfa.profile_select(["bwd_kv"])
+    jfa.profile_enable(True)
+    try:
+        out, lse = jfa.forward(q, k, v, off, x["max_len"])
+        jfa.backward(q, k, v, off, x["max_len"], out, lse, do)
+        torch.cuda.synchronize()
+    finally:
+        jfa.profile_enable(False)
+        jfa.profile_select(None)
+    assert jfa.launch_count() - n0 == 5
+    prof = jfa.profile_read()
+    assert {kind: n for kind, (t, n) in prof.items() if n} == {"bwd_kv": 1}
+    assert prof["bwd_kv"][0] > 0.0
     jfa.jfa_sync_and_check()
 
 
