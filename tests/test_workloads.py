@@ -75,3 +75,28 @@ def test_every_bench_variant_resolves_to_a_workload():
     for n in names:
         w = bench._workload_def(n)
         assert w.name in W.WORKLOADS, n
+
+
+def test_breakdown_selects_the_dominant_flop_kernel():
+    """bench's breakdown window: every kind profiled, then events only around
+    the kernel with the most device time among those with algorithmic FLOPs
+    (the pre-pass, FLOP-free, is never chosen even when it is slow)."""
+    import types
+
+    import bench
+
+    calls = []
+    prof = {"sched": (0.1, 3), "fwd": (0.9, 3), "prep": (5.0, 3), "bwd_kv": (1.6, 3),
+            "bwd_q": (1.3, 3)}
+    reads = iter([{}, prof])
+    fake = types.SimpleNamespace(
+        profile_read=lambda: next(reads),
+        profile_select=lambda kinds=None: calls.append(("select", kinds)),
+        profile_enable=lambda on: calls.append(("enable", on)))
+    torch_ = types.SimpleNamespace(cuda=types.SimpleNamespace(synchronize=lambda: None))
+    ran = []
+    x = W.make_inputs(W.WORKLOADS["tiny_self"])
+    got = bench._breakdown(fake, torch_, x, ran.append, 4)
+    assert got == prof and ran == [4]
+    assert calls == [("select", None), ("enable", True), ("enable", False),
+                     ("select", ["bwd_kv"])]
