@@ -100,3 +100,40 @@ def test_breakdown_selects_the_dominant_flop_kernel():
     assert got == prof and ran == [4]
     assert calls == [("select", None), ("enable", True), ("enable", False),
                      ("select", ["bwd_kv"])]
+
+
+def test_window_pairs_by_brute_force():
+    """The useful-work count behind every TFLOPS figure, against an explicit
+    mask: query i keeps key j iff i - left <= j <= i + right (causal: right
+    = 0; -1: unbounded)."""
+    lengths = [1, 7, 20, 0, 33]
+    for causal, win in [(False, (3, 2)), (False, (0, -1)), (False, (-1, 4)), (True, (5, -1)),
+                        (True, (-1, -1)), (False, (-1, -1)), (False, (0, 0))]:
+        want = 0
+        for n in lengths:
+            for i in range(n):
+                for j in range(n):
+                    lo = i - win[0] if win[0] >= 0 else -10**9
+                    hi = i + (0 if causal else (win[1] if win[1] >= 0 else 10**9))
+                    if causal and win[1] >= 0:
+                        hi = min(hi, i + win[1])
+                    want += lo <= j <= hi
+        assert W.pairs(lengths, causal=causal, window=win) == want, (causal, win)
+
+
+def test_bench_work_model_products():
+    """Tensor FLOPs per launch in the bench's model: 2*D per pair and
+    product (forward 2 products, dK/dV pass 4, dQ pass 3: S and dP again,
+    then dS K); the method's backward counts 5."""
+    import bench
+    for name, lengths in (("tiny_self", None), ("broadcast_q", [0, 5, 300])):
+        x = W.make_inputs(W.WORKLOADS[name], lengths=lengths)
+        p = bench._pairs(x)
+        unit = 2.0 * x["H"] * x["D"] * p
+        m = bench.kernel_model(x)
+        fwd_f, bwd_f, _ = bench._flops(x)
+        assert m["fwd"][0] == 2 * unit and fwd_f == 2 * unit
+        assert m["bwd_kv"][0] == 4 * unit and bwd_f == 5 * unit
+        assert m["bwd_qb" if x["broadcast_q"] else "bwd_q"][0] == 3 * unit
+    frac, bound = bench._roof(1e12, 1e9, 1e-3, 1000.0, 1000.0)
+    assert bound == "tensor" and abs(frac - 1.0) < 1e-12
